@@ -1,0 +1,501 @@
+"""Pins of the float64 oracle against things other than itself: brute force on
+tiny inputs, closed forms, invariants, library routines that the oracle does
+not call (torch CPU float64), the counts the Luminal blog prints for a
+Flux.2 Klein step, and planted mistakes that a pin must catch."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import mmdit_oracle as O
+from diffusion_transformer_image_mmdit_gb300 import synthetic as S
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+torch.set_default_dtype(torch.float64)
+
+
+def rel(a, b):
+    return float(np.linalg.norm(np.asarray(a) - np.asarray(b)) / max(np.linalg.norm(np.asarray(b)), 1e-300))
+
+
+def rnd(name, shape, std=1.0):
+    return S.normal(name, shape, std)
+
+
+# ------------------------------------------------------------------ attention
+def _attention_brute(q, k, v):
+    B, Lq, H, d = q.shape
+    Lk = k.shape[1]
+    out = np.zeros_like(q)
+    for b in range(B):
+        for h in range(H):
+            for i in range(Lq):
+                sc = [sum(q[b, i, h, c] * k[b, j, h, c] for c in range(d)) / math.sqrt(d) for j in range(Lk)]
+                m = max(sc)
+                e = [math.exp(s - m) for s in sc]
+                z = sum(e)
+                for c in range(d):
+                    out[b, i, h, c] = sum(e[j] * v[b, j, h, c] for j in range(Lk)) / z
+    return out
+
+
+def test_attention_brute_force():
+    q, k, v = (rnd(n, (1, 5, 2, 4)) for n in ("aq", "ak", "av"))
+    assert rel(O.attention(q, k, v), _attention_brute(q, k, v)) < 1e-13
+
+
+def test_attention_rectangular_brute_force():
+    q = rnd("rq", (2, 3, 1, 8))
+    k = rnd("rk", (2, 7, 1, 8)) * 2
+    v = rnd("rv", (2, 7, 1, 8))
+    assert rel(O.attention(q, k, v), _attention_brute(q, k, v)) < 1e-13
+
+
+def test_attention_vs_torch_sdpa():
+    q, k, v = (rnd(n, (2, 37, 3, 16)) * 3 for n in ("tq", "tk", "tv"))
+    ref = F.scaled_dot_product_attention(*(torch.from_numpy(t).transpose(1, 2) for t in (q, k, v))).transpose(1, 2)
+    assert rel(O.attention(q, k, v), ref.numpy()) < 1e-13
+
+
+def test_attention_one_key_returns_v():
+    q = rnd("oq", (1, 6, 2, 8))
+    k = rnd("ok", (1, 1, 2, 8))
+    v = rnd("ov", (1, 1, 2, 8))
+    out = O.attention(q, k, v)
+    assert np.array_equal(out, np.broadcast_to(v, out.shape))
+
+
+def test_attention_zero_query_is_mean_of_v():
+    q = np.zeros((1, 3, 2, 8))
+    k, v = rnd("zk", (1, 9, 2, 8)), rnd("zv", (1, 9, 2, 8))
+    out = O.attention(q, k, v)
+    assert np.abs(out - v.mean(axis=1, keepdims=True)).max() < 1e-15
+
+
+def test_attention_key_permutation_invariance():
+    q, k, v = (rnd(n, (1, 11, 2, 8)) for n in ("pq", "pk", "pv"))
+    perm = np.random.default_rng(0).permutation(11)
+    assert np.abs(O.attention(q, k, v) - O.attention(q, k[:, perm], v[:, perm])).max() < 1e-14
+
+
+# ------------------------------------------------------------------ RoPE
+def test_rope_ids_layout():
+    ids = O.rope_ids(2, 2, 3)
+    expect = [[0, 0, 0], [0, 0, 0], [0, 0, 0], [0, 0, 1], [0, 0, 2], [0, 1, 0], [0, 1, 1], [0, 1, 2]]
+    assert ids.dtype == np.int32 and ids.tolist() == expect
+
+
+def test_latent_token_counts_golden():
+    g = json.load(open(os.path.join(GOLD, "latent_tokens.json")))
+    for c in g["cases"]:
+        gh, gw = c["height"] // 16, c["width"] // 16
+        assert (gh, gw) == (c["grid_h"], c["grid_w"])
+        ids = O.rope_ids(c["text_tokens"], gh, gw)
+        assert ids.shape == (c["tokens"], 3)
+        assert (ids[c["text_tokens"]:, 1:] != 0).any(axis=1).sum() == c["image_tokens"] - 1
+
+
+def test_rope_angles_closed_form():
+    ids = O.rope_ids(3, 5, 7)
+    ang = O.rope_angles(ids, (16, 24, 24), 10000.0)
+    assert ang.shape == (3 + 35, 32)
+    assert np.all(ang[:, :8] == 0) and np.all(ang[:3] == 0)
+    # pair 0 of each spatial axis turns at frequency 1: the angle is the coordinate itself
+    assert np.array_equal(ang[:, 8], ids[:, 1].astype(float))
+    assert np.array_equal(ang[:, 20], ids[:, 2].astype(float))
+    assert ang[3 + 7 * 4 + 5, 9] == pytest.approx(4 * 10000.0 ** (-2 / 24), rel=1e-15)
+
+
+def test_rope_preserves_pair_norms():
+    x = rnd("rx", (1, 38, 2, 64))
+    c, s = O.rope_tables(O.rope_ids(3, 5, 7), (16, 24, 24), 10000.0)
+    y = O.rope_apply(x, c, s)
+    nx = x[..., 0::2] ** 2 + x[..., 1::2] ** 2
+    ny = y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    assert np.abs(nx - ny).max() < 1e-13
+
+
+def test_rope_text_tokens_untouched():
+    x = rnd("rt", (1, 38, 2, 64))
+    c, s = O.rope_tables(O.rope_ids(3, 5, 7), (16, 24, 24), 10000.0)
+    y = O.rope_apply(x, c, s)
+    assert np.array_equal(y[:, :3], x[:, :3])
+    assert np.array_equal(y[..., :16], x[..., :16])
+
+
+def test_rope_relative_position_identity():
+    """<R_m q, R_n k> depends only on m - n (per axis)."""
+    d = 128
+    q = rnd("rrq", (d,))
+    k = rnd("rrk", (d,))
+    axes = (16, 56, 56)
+
+    def rot(vec, pos):
+        ids = np.array([pos], dtype=np.int32)
+        c, s = O.rope_tables(ids, axes, 10000.0)
+        return O.rope_apply(vec[None, None, :], c, s)[0, 0]
+
+    rng = np.random.default_rng(1)
+    for _ in range(20):
+        delta = rng.integers(-40, 40, size=3)
+        delta[0] = 0
+        m = rng.integers(0, 60, size=3); m[0] = 0
+        n = rng.integers(0, 60, size=3); n[0] = 0
+        a = rot(q, m + delta) @ rot(k, m)
+        b = rot(q, n + delta) @ rot(k, n)
+        assert abs(a - b) < 1e-11 * (1 + abs(a))
+
+
+def test_rope_matches_complex_multiplication():
+    """Independent restatement: adjacent channel pairs as complex numbers times e^{i angle}."""
+    x = rnd("rc", (2, 38, 3, 64))
+    ids = O.rope_ids(3, 5, 7)
+    c, s = O.rope_tables(ids, (16, 24, 24), 10000.0)
+    ang = np.arctan2(s, c)
+    z = torch.view_as_complex(torch.from_numpy(x).reshape(2, 38, 3, 32, 2).contiguous())
+    ref = torch.view_as_real(z * torch.polar(torch.ones(38, 1, 32), torch.from_numpy(ang)[:, None, :])).reshape(x.shape)
+    assert rel(O.rope_apply(x, c, s), ref.numpy()) < 1e-14
+
+
+# ------------------------------------------------------------------ norms / activations
+def test_layer_norm_moments_and_torch():
+    x = rnd("ln", (4, 7, 96)) * 3 + 1.5
+    y = O.layer_norm(x, 1e-6)
+    assert np.abs(y.mean(-1)).max() < 1e-13
+    assert np.abs((y ** 2).mean(-1) - 1).max() < 1e-5
+    assert rel(y, F.layer_norm(torch.from_numpy(x), (96,), eps=1e-6).numpy()) < 1e-14
+
+
+def test_rms_norm_unit_rms_and_torch():
+    x = rnd("rms", (5, 3, 128)) * 2
+    g = S.norm_gain("g", 128)
+    y = O.rms_norm(x, np.ones(128), 0.0)
+    assert np.abs(np.sqrt((y ** 2).mean(-1)) - 1).max() < 1e-14
+    ref = F.rms_norm(torch.from_numpy(x), (128,), weight=torch.from_numpy(g), eps=1e-6)
+    assert rel(O.rms_norm(x, g, 1e-6), ref.numpy()) < 1e-14
+
+
+def test_gelu_tanh():
+    x = np.linspace(-8, 8, 1001)
+    y = O.gelu_tanh(x)
+    assert O.gelu_tanh(np.array([0.0]))[0] == 0.0
+    assert np.abs((y - O.gelu_tanh(-x)) - x).max() < 1e-14
+    assert rel(y, F.gelu(torch.from_numpy(x), approximate="tanh").numpy()) < 1e-15
+
+
+def test_silu_and_linear():
+    x = rnd("sx", (3, 5))
+    assert rel(O.silu(x), F.silu(torch.from_numpy(x)).numpy()) < 1e-15
+    w, b = rnd("lw", (4, 5)), rnd("lb", (4,))
+    brute = np.array([[sum(x[i, k] * w[n, k] for k in range(5)) + b[n] for n in range(4)] for i in range(3)])
+    assert rel(O.linear(x, w, b), brute) < 1e-15
+
+
+# ------------------------------------------------------------------ blocks
+TINY = O.Shape(B=2, L_txt=5, grid_h=3, grid_w=4, D=64, H=2, d_head=32, D_mlp=96, rope_axes=(8, 12, 12))
+
+
+def _tables(sh):
+    return O.rope_tables(O.rope_ids(sh.L_txt, sh.grid_h, sh.grid_w), sh.rope_axes, sh.rope_theta)
+
+
+def _torch_rope(x, sh):
+    ids = O.rope_ids(sh.L_txt, sh.grid_h, sh.grid_w)
+    ang = []
+    for a, d_a in enumerate(sh.rope_axes):
+        om = torch.tensor(sh.rope_theta) ** (-torch.arange(0, d_a, 2) / d_a)
+        ang.append(torch.from_numpy(ids[:, a]).double()[:, None] * om[None, :])
+    ang = torch.cat(ang, 1)
+    B, L, H, d = x.shape
+    z = torch.view_as_complex(x.reshape(B, L, H, d // 2, 2).contiguous())
+    return torch.view_as_real(z * torch.polar(torch.ones_like(ang), ang)[:, None, :]).reshape(B, L, H, d)
+
+
+def _torch_double(x_txt, x_img, vec, wt, sh):
+    T = torch.from_numpy
+    D, H, d = sh.D, sh.H, sh.d_head
+    st = {}
+    for s, x in (("txt", T(x_txt)), ("img", T(x_img))):
+        w = {k: T(v) for k, v in wt[s].items()}
+        m = F.linear(F.silu(T(vec)), w["mod_w"], w["mod_b"]).unsqueeze(1).chunk(6, dim=-1)
+        y = F.layer_norm(x, (D,), eps=sh.eps_ln) * (1 + m[1]) + m[0]
+        q, k, v = F.linear(y, w["qkv_w"], w["qkv_b"]).split(D, dim=-1)
+        B, L, _ = q.shape
+        q = F.rms_norm(q.reshape(B, L, H, d), (d,), weight=w["q_norm"], eps=sh.eps_rms)
+        k = F.rms_norm(k.reshape(B, L, H, d), (d,), weight=w["k_norm"], eps=sh.eps_rms)
+        st[s] = (x, w, m, q, k, v.reshape(B, L, H, d))
+    q = _torch_rope(torch.cat([st["txt"][3], st["img"][3]], 1), sh)
+    k = _torch_rope(torch.cat([st["txt"][4], st["img"][4]], 1), sh)
+    v = torch.cat([st["txt"][5], st["img"][5]], 1)
+    o = F.scaled_dot_product_attention(q.transpose(1, 2), k.transpose(1, 2), v.transpose(1, 2)).transpose(1, 2)
+    o = o.reshape(o.shape[0], o.shape[1], D)
+    outs = []
+    for s, sl in (("txt", slice(0, sh.L_txt)), ("img", slice(sh.L_txt, None))):
+        x, w, m, *_ = st[s]
+        x = x + m[2] * F.linear(o[:, sl], w["proj_w"], w["proj_b"])
+        y = F.layer_norm(x, (D,), eps=sh.eps_ln) * (1 + m[4]) + m[3]
+        x = x + m[5] * F.linear(F.gelu(F.linear(y, w["mlp_in_w"], w["mlp_in_b"]), approximate="tanh"), w["mlp_out_w"], w["mlp_out_b"])
+        outs.append(x.numpy())
+    return outs
+
+
+def _torch_single(x, vec, wt, sh):
+    T = torch.from_numpy
+    D, H, d = sh.D, sh.H, sh.d_head
+    w = {k: T(v) for k, v in wt.items()}
+    x = T(x)
+    m = F.linear(F.silu(T(vec)), w["mod_w"], w["mod_b"]).unsqueeze(1).chunk(3, dim=-1)
+    y = F.layer_norm(x, (D,), eps=sh.eps_ln) * (1 + m[1]) + m[0]
+    h = F.linear(y, w["lin1_w"], w["lin1_b"])
+    q, k, v, mlp = h.split([D, D, D, sh.D_mlp], dim=-1)
+    B, L, _ = q.shape
+    q = _torch_rope(F.rms_norm(q.reshape(B, L, H, d), (d,), weight=w["q_norm"], eps=sh.eps_rms), sh)
+    k = _torch_rope(F.rms_norm(k.reshape(B, L, H, d), (d,), weight=w["k_norm"], eps=sh.eps_rms), sh)
+    o = F.scaled_dot_product_attention(q.transpose(1, 2), k.transpose(1, 2), v.reshape(B, L, H, d).transpose(1, 2))
+    o = o.transpose(1, 2).reshape(B, L, D)
+    return (x + m[2] * F.linear(torch.cat([o, F.gelu(mlp, approximate="tanh")], -1), w["lin2_w"], w["lin2_b"])).numpy()
+
+
+def _double_inputs(sh, scale_w=1.0):
+    wt = S.double_block_params("pin.dbl", sh.D, sh.d_head, sh.D_mlp)
+    if scale_w != 1.0:
+        for s in wt.values():
+            for k in s:
+                if k.endswith("_w"):
+                    s[k] = s[k] * scale_w
+    a = S.activations(sh.B, sh.L_txt, sh.L_img, sh.D)
+    return wt, a
+
+
+def test_double_block_vs_torch_restatement():
+    sh = TINY
+    wt, a = _double_inputs(sh, scale_w=25.0)  # larger weights so every branch matters
+    c, s = _tables(sh)
+    got = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s)
+    ref = _torch_double(a["x_txt"], a["x_img"], a["vec"], wt, sh)
+    assert rel(got[0], ref[0]) < 1e-12 and rel(got[1], ref[1]) < 1e-12
+    # the branches really move the residual stream
+    assert rel(got[1], a["x_img"]) > 0.1
+
+
+def test_double_block_row_subset_matches_full():
+    sh = TINY
+    wt, a = _double_inputs(sh, scale_w=25.0)
+    c, s = _tables(sh)
+    full = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s)
+    part = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s, rows_txt=[0, 4], rows_img=[1, 11])
+    assert rel(part[0], full[0][:, [0, 4]]) < 1e-14
+    assert rel(part[1], full[1][:, [1, 11]]) < 1e-14
+
+
+def test_single_block_vs_torch_restatement():
+    sh = TINY
+    w = S.single_block_params("pin.sgl", sh.D, sh.d_head, sh.D_mlp)
+    for k in w:
+        if k.endswith("_w"):
+            w[k] = w[k] * 25.0
+    x = S.normal_f32("pin.x", (sh.B, sh.L, sh.D))
+    vec = S.normal_f32("pin.vec", (sh.B, sh.D))
+    c, s = _tables(sh)
+    got = O.single_block(x, vec, w, sh, c, s)
+    assert rel(got, _torch_single(x, vec, w, sh)) < 1e-12
+    part = O.single_block(x, vec, w, sh, c, s, rows=[0, 7, 16])
+    assert rel(part, got[:, [0, 7, 16]]) < 1e-14
+
+
+def _zero_gates(mod_w, mod_b, n_chunks, gate_chunks):
+    D = mod_w.shape[0] // n_chunks
+    mod_w, mod_b = mod_w.copy(), mod_b.copy()
+    for g in gate_chunks:
+        mod_w[g * D:(g + 1) * D] = 0
+        mod_b[g * D:(g + 1) * D] = 0
+    return mod_w, mod_b
+
+
+def test_zero_gates_make_blocks_identity():
+    sh = TINY
+    wt, a = _double_inputs(sh)
+    c, s = _tables(sh)
+    for st in wt.values():
+        st["mod_w"], st["mod_b"] = _zero_gates(st["mod_w"], st["mod_b"], 6, (2, 5))
+    t, i = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s)
+    assert np.array_equal(t, a["x_txt"]) and np.array_equal(i, a["x_img"])
+    w = S.single_block_params("pin.sgl", sh.D, sh.d_head, sh.D_mlp)
+    w["mod_w"], w["mod_b"] = _zero_gates(w["mod_w"], w["mod_b"], 3, (2,))
+    x = np.concatenate([a["x_txt"], a["x_img"]], 1)
+    assert np.array_equal(O.single_block(x, a["vec"], w, sh, c, s), x)
+
+
+def test_zero_branch_weights_leave_gated_biases():
+    """With proj and MLP-out weights zero, each stream gets exactly
+    x + gate1 * b_proj + gate2 * b_mlp_out."""
+    sh = TINY
+    wt, a = _double_inputs(sh)
+    c, s = _tables(sh)
+    for st in wt.values():
+        st["proj_w"] = np.zeros_like(st["proj_w"])
+        st["mlp_out_w"] = np.zeros_like(st["mlp_out_w"])
+    t, i = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s)
+    for name, x, out in (("txt", a["x_txt"], t), ("img", a["x_img"], i)):
+        w = wt[name]
+        m = O.silu(a["vec"]) @ w["mod_w"].T + w["mod_b"]
+        D = sh.D
+        g1, g2 = m[:, None, 2 * D:3 * D], m[:, None, 5 * D:6 * D]
+        assert np.abs(out - (x + g1 * w["proj_b"] + g2 * w["mlp_out_b"])).max() < 1e-14
+
+
+def test_klein_step_counts_golden():
+    """One step of a Klein-shaped stack calls LN+modulate 57 times and
+    RMSNorm (fused with RoPE on the pages) 80 times, with 32 attention sites."""
+    g = json.load(open(os.path.join(GOLD, "klein_step_counts.json")))
+    sh = O.Shape(B=1, L_txt=2, grid_h=2, grid_w=2, D=32, H=2, d_head=16, D_mlp=32, rope_axes=(4, 6, 6), C_lat=8, t_dim=16)
+    W = S.embed_params(sh.D, sh.C_lat, sh.t_dim)
+    W["double"] = [S.double_block_params(f"k.d{i}", sh.D, sh.d_head, sh.D_mlp) for i in range(g["n_double"])]
+    W["single"] = [S.single_block_params(f"k.s{i}", sh.D, sh.d_head, sh.D_mlp) for i in range(g["n_single"])]
+    counts = {"ln": 0, "rms": 0, "attn": 0}
+    ln, rms, att = O.layer_norm, O.rms_norm, O.attention
+
+    def c_ln(*a, **k):
+        counts["ln"] += 1
+        return ln(*a, **k)
+
+    def c_rms(*a, **k):
+        counts["rms"] += 1
+        return rms(*a, **k)
+
+    def c_att(*a, **k):
+        counts["attn"] += 1
+        return att(*a, **k)
+
+    O.layer_norm, O.rms_norm, O.attention = c_ln, c_rms, c_att
+    try:
+        x_lat = S.normal_f32("k.lat", (1, 4, 8))
+        x_txt = S.normal_f32("k.txt", (1, 2, 32))
+        O.denoise_step(x_lat, x_txt, 1.0, 0.75, W, sh)
+    finally:
+        O.layer_norm, O.rms_norm, O.attention = ln, rms, att
+    assert counts["ln"] == g["layernorm_modulate_per_step"]
+    assert counts["rms"] == g["rmsnorm_rope_per_step"]
+    assert counts["attn"] == 2 * g["n_double"] + g["n_single"]  # double blocks: one call per stream's query rows
+    assert g["n_double"] + g["n_single"] == g["attention_sites_per_step"]
+
+
+# ------------------------------------------------------------------ step pieces
+def test_timestep_sinusoid_closed_forms():
+    e = O.timestep_sinusoid([0.0, 3.0], 256)
+    assert np.array_equal(e[0, :128], np.ones(128)) and np.array_equal(e[0, 128:], np.zeros(128))
+    assert e[1, 0] == math.cos(3.0) and e[1, 128] == math.sin(3.0)
+    assert e[1, 64] == pytest.approx(math.cos(3.0 * 10000.0 ** -0.5), rel=1e-14)
+
+
+def test_sigma_schedule():
+    s = O.sigma_schedule(4, 0.0)
+    assert np.allclose(s, [1, 0.75, 0.5, 0.25, 0], rtol=0, atol=1e-16)
+    s = O.sigma_schedule(2, math.log(3.0))
+    assert np.allclose(s, [1.0, 0.75, 0.0], rtol=0, atol=1e-15)
+    s = O.sigma_schedule(50, O.shift_mu(6889))
+    assert s[0] == 1.0 and s[-1] == 0.0 and np.all(np.diff(s) < 0)
+    assert O.shift_mu(4096) == pytest.approx(1.15) and O.shift_mu(256) == pytest.approx(0.5)
+
+
+def test_euler_constant_velocity_telescopes():
+    x0 = rnd("ex", (3, 10))
+    v = rnd("ev", (3, 10))
+    sig = O.sigma_schedule(28, O.shift_mu(4096))
+    x = x0
+    for i in range(28):
+        x = O.euler_step(x, v, sig[i], sig[i + 1])
+    assert np.abs(x - (x0 - v)).max() < 1e-13
+    assert np.array_equal(O.euler_step(x0, v, 0.5, 0.5), x0)
+
+
+def test_time_embed_and_final_layer_vs_torch():
+    sh = O.Shape(B=2, L_txt=3, grid_h=2, grid_w=3, D=32, H=2, d_head=16, D_mlp=32, C_lat=8, t_dim=16)
+    W = S.embed_params(sh.D, sh.C_lat, sh.t_dim)
+    T = {k: torch.from_numpy(v) for k, v in W.items()}
+    vec = O.time_embed(0.6, W, sh)
+    half = 8
+    f = torch.exp(-math.log(10000.0) * torch.arange(half) / half)
+    a = torch.full((2, 1), 600.0) * f[None]
+    ref = F.linear(F.silu(F.linear(torch.cat([a.cos(), a.sin()], 1), T["t_w1"], T["t_b1"])), T["t_w2"], T["t_b2"])
+    assert rel(vec, ref.numpy()) < 1e-14
+    x = S.normal_f32("fl.x", (2, 6, 32))
+    m = F.linear(F.silu(torch.from_numpy(vec)), T["final_mod_w"], T["final_mod_b"]).unsqueeze(1).chunk(2, -1)
+    y = F.layer_norm(torch.from_numpy(x), (32,), eps=1e-6) * (1 + m[1]) + m[0]
+    assert rel(O.final_layer(x, vec, W, sh), F.linear(y, T["final_w"], T["final_b"]).numpy()) < 1e-14
+
+
+# ------------------------------------------------------------------ int8 quantiser
+def test_quantize_w8_invariants():
+    w = S.normal_bf16("q.w", (64, 96), 0.02)
+    w[5] = 0.0
+    q, s = O.quantize_w8(w)
+    assert q.dtype == np.int8 and s.dtype == np.float32
+    assert np.abs(q.astype(int)).max() <= 127
+    nz = np.abs(w).max(1) > 0
+    assert np.all(np.abs(q[nz].astype(int)).max(1) == 127)
+    assert s[5] == 1.0 and np.all(q[5] == 0)
+    # |w - q s| <= s/2, widened by the float32 rounding of the quotient w/s (|w/s| <= 127)
+    assert np.all(np.abs(w - O.dequantize_w8(q, s)) <= s[:, None].astype(np.float64) * (0.5 + 128 * 2.0 ** -24))
+
+
+def test_quantize_w8_ties_and_float32_decisions():
+    w = np.array([[127.0, 63.5, -0.5, 2.5, -2.5, 1.4999999]], dtype=np.float64)
+    q, s = O.quantize_w8(w)
+    assert s[0] == np.float32(1.0)
+    assert q[0].tolist() == [127, 64, 0, 2, -2, 1]
+
+
+# ------------------------------------------------------------------ planted mistakes
+def _planted(monkeypatch, name, fn, test):
+    monkeypatch.setattr(O, name, fn)
+    with pytest.raises(AssertionError):
+        test()
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    orig = {n: getattr(O, n) for n in ("attention", "rope_apply", "layer_norm", "gelu_tanh", "modulate", "rms_norm")}
+
+    def att_noscale(q, k, v):
+        return orig["attention"](q * math.sqrt(q.shape[-1]), k, v)
+
+    def rope_half(x, c, s):  # rotate-half pairing instead of adjacent pairs
+        h = x.shape[-1] // 2
+        y = np.empty_like(x)
+        y[..., :h] = x[..., :h] * c[:, None] - x[..., h:] * s[:, None]
+        y[..., h:] = x[..., :h] * s[:, None] + x[..., h:] * c[:, None]
+        return y
+
+    def rope_sign(x, c, s):
+        return orig["rope_apply"](x, c, -s)
+
+    def ln_unbiased(x, eps):
+        mu = x.mean(-1, keepdims=True)
+        return (x - mu) / np.sqrt(x.var(-1, ddof=1, keepdims=True) + eps)
+
+    def gelu_erf(x):
+        return 0.5 * x * (1 + np.vectorize(math.erf)(x / math.sqrt(2)))
+
+    def mod_noone(y, shift, scale):
+        return y * scale + shift
+
+    def rms_nog(x, g, eps):
+        return orig["rms_norm"](x, np.ones_like(g), eps)
+
+    cases = [
+        ("attention", att_noscale, test_attention_brute_force),
+        ("rope_apply", rope_half, test_rope_matches_complex_multiplication),
+        ("rope_apply", rope_sign, test_rope_matches_complex_multiplication),
+        ("layer_norm", ln_unbiased, test_layer_norm_moments_and_torch),
+        ("gelu_tanh", gelu_erf, test_gelu_tanh),
+        ("modulate", mod_noone, test_double_block_vs_torch_restatement),
+        ("rms_norm", rms_nog, test_single_block_vs_torch_restatement),
+        ("rope_apply", rope_half, test_double_block_vs_torch_restatement),
+    ]
+    for name, fn, t in cases:
+        _planted(monkeypatch, name, fn, t)
+        monkeypatch.setattr(O, name, orig[name])
