@@ -1,0 +1,779 @@
+// C ABI of libmmdit: argument checks, workspace carving, tensor maps and the
+// kernel sequence of each block and of a whole denoising step.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "elementwise.h"
+#include "mmdit.h"
+#include "mmdit_internal.h"
+
+namespace mmdit {
+
+// ----------------------------------------------------------------- process state
+static __device__ unsigned g_status_word;
+static std::atomic<long long> g_launches{0};
+
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+static int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev < 0 ? 0 : (dev > 63 ? 63 : dev);
+}
+
+unsigned* device_status_ptr() {
+  static unsigned* ptrs[64] = {};
+  const int dev = current_device();
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptrs[dev] = static_cast<unsigned*>(p);
+  }
+  return ptrs[dev];
+}
+
+int num_sms() {
+  static int sms[64] = {};
+  const int dev = current_device();
+  if (!sms[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 1;
+  }
+  return sms[dev];
+}
+
+// 1 = sm_103, -1 = other device, 0 = unknown yet.
+static int device_ok() {
+  static int ok[64] = {};
+  const int dev = current_device();
+  if (!ok[dev]) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return 0;
+    ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return ok[dev] > 0;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t inner,
+                  uint64_t rows, uint64_t batch, uint64_t row_stride_bytes, uint64_t batch_stride_bytes,
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  (void)elem_bytes;
+  cuuint64_t dims[3] = {inner, rows, batch};
+  cuuint64_t strides[2] = {row_stride_bytes, batch_stride_bytes};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------------------- helpers
+static inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+static inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MMDIT_OK : MMDIT_ERR_CUDA; }
+
+#define MMDIT_TRY(expr)            \
+  do {                             \
+    const int _st = (expr);        \
+    if (_st != MMDIT_OK) return _st; \
+  } while (0)
+#define MMDIT_CUDA(expr) MMDIT_TRY(cuda_status(expr))
+
+// Bump allocator over the caller's workspace (or a size query with base == 0).
+struct Carve {
+  uint8_t* base;
+  size_t off;
+  template <class T>
+  T* take(size_t n) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += n * sizeof(T);
+    return p;
+  }
+};
+
+struct Dims {
+  int B, Lt, Li, L, Lpad, D, H, d, Dm;
+};
+
+static int check_shape(const mmdit_shape_t* s, Dims* out) {
+  if (!s) return MMDIT_ERR_ARG;
+  if (s->B < 1 || s->L_txt < 0 || s->grid_h < 1 || s->grid_w < 1) return MMDIT_ERR_SHAPE;
+  if (s->D <= 0 || s->D % 256 || s->D > 4096) return MMDIT_ERR_SHAPE;
+  if (s->d_head != 64 && s->d_head != 128) return MMDIT_ERR_SHAPE;
+  if (s->H * s->d_head != s->D) return MMDIT_ERR_SHAPE;
+  if (s->D_mlp <= 0 || s->D_mlp % 64) return MMDIT_ERR_SHAPE;
+  const int a0 = s->rope_axes[0], a1 = s->rope_axes[1], a2 = s->rope_axes[2];
+  if (a0 < 0 || a1 < 0 || a2 < 0 || (a0 | a1 | a2) & 1 || a0 + a1 + a2 != s->d_head) return MMDIT_ERR_SHAPE;
+  if (s->w_dtype != MMDIT_BF16 && s->w_dtype != MMDIT_I8W) return MMDIT_ERR_ARG;
+  const long long L = (long long)s->L_txt + (long long)s->grid_h * s->grid_w;
+  if (L > (1 << 24)) return MMDIT_ERR_SHAPE;
+  if (out) {
+    out->B = s->B, out->Lt = s->L_txt, out->Li = s->grid_h * s->grid_w, out->L = (int)L;
+    out->Lpad = (int)((L + 7) / 8 * 8);
+    out->D = s->D, out->H = s->H, out->d = s->d_head, out->Dm = s->D_mlp;
+  }
+  return MMDIT_OK;
+}
+
+static int check_device() {
+  if (!device_ok()) return MMDIT_ERR_UNSUPPORTED;
+  if (!encode_fn()) return MMDIT_ERR_UNSUPPORTED;
+  if (!device_status_ptr()) return MMDIT_ERR_CUDA;
+  return MMDIT_OK;
+}
+
+static bool lin_ok(const mmdit_linear_t& l, bool want_i8) {
+  if (!l.w || !al16(l.w)) return false;
+  if (l.b && !al16(l.b)) return false;
+  if (want_i8 != (l.scale != nullptr)) return false;
+  if (l.scale && !al16(l.scale)) return false;
+  return true;
+}
+
+// ----------------------------------------------------------------- GEMM
+// A row r of segment s at A + (s * a_seg_rows + r) * a_ld (bf16 elements).
+static int run_gemm(const void* A, long long a_ld, long long a_seg_rows, int M_seg, int n_seg, int K,
+                    const mmdit_linear_t& lin, int N, GemmParams p, uint16_t* wdeq, cudaStream_t st) {
+  if (K % kBK || N % 32 || M_seg < 1 || n_seg < 1) return MMDIT_ERR_SHAPE;
+  if (!al16(A) || (a_ld * 2) % 16) return MMDIT_ERR_ALIGN;
+  const void* W = lin.w;
+  p.wscale = nullptr;
+  if (lin.scale) {
+    if (!wdeq) return MMDIT_ERR_WORKSPACE;
+    MMDIT_CUDA(launch_dequant_i8(static_cast<const int8_t*>(lin.w), wdeq, (long long)N * K, st));
+    W = wdeq;
+    p.wscale = lin.scale;
+  }
+  p.bias = lin.b;
+  CUtensorMap ta, tb;
+  if (!make_tmap_3d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M_seg, (uint64_t)n_seg,
+                    (uint64_t)a_ld * 2, (uint64_t)a_seg_rows * a_ld * 2, kBK, kBM, true))
+    return MMDIT_ERR_ALIGN;
+  if (!make_tmap_3d(&tb, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, 1, (uint64_t)K * 2,
+                    (uint64_t)N * K * 2, kBK, kBN, true))
+    return MMDIT_ERR_ALIGN;
+  p.M_seg = M_seg;
+  p.n_seg = n_seg;
+  p.N = N;
+  p.K = K;
+  p.tiles_m = (M_seg + kBM - 1) / kBM;
+  p.tiles_n = (N + kBN - 1) / kBN;
+  p.num_tiles = p.tiles_m * p.tiles_n * n_seg;
+  p.group_m = 16;
+  p.status = device_status_ptr();
+  return cuda_status(launch_gemm(ta, tb, p, st));
+}
+
+static GemmParams gemm_params(int mode) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.mode = mode;
+  p.gelu_from = 1 << 30;
+  return p;
+}
+
+// ----------------------------------------------------------------- attention
+static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, uint16_t* out, long long out_ld,
+                         cudaStream_t st) {
+  CUtensorMap tq, tv;
+  const uint64_t D2 = 2ull * d.D;
+  if (!make_tmap_3d(&tq, qk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D2, (uint64_t)d.L, (uint64_t)d.B, D2 * 2,
+                    D2 * 2 * d.L, 64, kAttnBM, true))
+    return MMDIT_ERR_ALIGN;
+  if (!make_tmap_3d(&tv, vT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.L, (uint64_t)d.D, (uint64_t)d.B,
+                    (uint64_t)d.Lpad * 2, (uint64_t)d.Lpad * 2 * d.D, 64, (uint32_t)d.d, true))
+    return MMDIT_ERR_ALIGN;
+  AttnParams p;
+  p.L = d.L;
+  p.H = d.H;
+  p.B = d.B;
+  p.n_q_tiles = (d.L + kAttnBM - 1) / kAttnBM;
+  p.n_kv_tiles = (d.L + kAttnBN - 1) / kAttnBN;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.d));
+  p.out = out;
+  p.out_ld = out_ld;
+  p.status = device_status_ptr();
+  return cuda_status(launch_attention(tq, tv, p, d.d, st));
+}
+
+// ----------------------------------------------------------------- workspace layouts
+struct DoubleWS {
+  float* mod;
+  uint16_t *y, *qk, *vT, *O, *h, *wdeq;
+};
+static void layout_double(const Dims& d, bool i8, bool need_mod, Carve& c, DoubleWS& w) {
+  w.mod = need_mod ? c.take<float>((size_t)2 * d.B * 6 * d.D) : nullptr;
+  w.y = c.take<uint16_t>((size_t)d.B * d.L * d.D);
+  w.qk = c.take<uint16_t>((size_t)d.B * d.L * 2 * d.D);
+  w.vT = c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
+  w.O = c.take<uint16_t>((size_t)d.B * d.L * d.D);
+  w.h = c.take<uint16_t>((size_t)d.B * (d.Lt > d.Li ? d.Lt : d.Li) * d.Dm);
+  w.wdeq = i8 ? c.take<uint16_t>((size_t)(3 * d.D > d.Dm ? 3 * d.D : d.Dm) * d.D) : nullptr;
+}
+
+struct SingleWS {
+  float* mod;
+  uint16_t *y, *qk, *vT, *cat, *wdeq;
+};
+static void layout_single(const Dims& d, bool i8, bool need_mod, Carve& c, SingleWS& w) {
+  w.mod = need_mod ? c.take<float>((size_t)d.B * 3 * d.D) : nullptr;
+  w.y = c.take<uint16_t>((size_t)d.B * d.L * d.D);
+  w.qk = c.take<uint16_t>((size_t)d.B * d.L * 2 * d.D);
+  w.vT = c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
+  w.cat = c.take<uint16_t>((size_t)d.B * d.L * (d.D + d.Dm));
+  w.wdeq = i8 ? c.take<uint16_t>((size_t)(3 * d.D + d.Dm) * d.D) : nullptr;
+}
+
+struct StepWS {
+  float *vec, *temb, *mods, *x, *v, *cs, *sn;
+  uint16_t* xlat;
+  uint8_t* block;
+  size_t block_bytes;
+};
+static size_t mods_floats(const Dims& d, int n_double, int n_single) {
+  return (size_t)n_double * 2 * d.B * 6 * d.D + (size_t)n_single * d.B * 3 * d.D + (size_t)d.B * 2 * d.D;
+}
+static void layout_step(const Dims& d, const mmdit_shape_t& s, int n_double, int n_single, Carve& c, StepWS& w) {
+  const bool i8 = s.w_dtype == MMDIT_I8W;
+  w.vec = c.take<float>((size_t)d.B * d.D);
+  w.temb = c.take<float>((size_t)d.B * (s.t_dim + d.D));
+  w.mods = c.take<float>(mods_floats(d, n_double, n_single));
+  w.x = c.take<float>((size_t)d.B * d.L * d.D);
+  w.v = c.take<float>((size_t)d.B * d.Li * s.C_lat);
+  w.xlat = c.take<uint16_t>((size_t)d.B * d.Li * s.C_lat);
+  w.cs = c.take<float>((size_t)d.L * (d.d / 2));
+  w.sn = c.take<float>((size_t)d.L * (d.d / 2));
+  Carve c1{nullptr, 0}, c2{nullptr, 0};
+  DoubleWS dw;
+  SingleWS sw;
+  layout_double(d, i8, false, c1, dw);
+  layout_single(d, i8, false, c2, sw);
+  w.block_bytes = (c1.off > c2.off ? c1.off : c2.off) + 256;
+  w.block = c.take<uint8_t>(w.block_bytes);
+}
+
+// ----------------------------------------------------------------- blocks
+static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_double_w_t& w, const float* vec,
+                             const float* mod_pre, float* x_txt, long long xt_seg_rows, float* x_img,
+                             long long xi_seg_rows, const float* cs, const float* sn, const DoubleWS& ws,
+                             cudaStream_t st) {
+  const int D = d.D;
+  const float* mod = mod_pre;
+  if (!mod) {
+    for (int i = 0; i < 2; ++i)
+      MMDIT_CUDA(launch_gemv(w.mod[i].w, w.mod[i].scale != nullptr, w.mod[i].scale, w.mod[i].b, vec, d.B, 6 * D, D,
+                             1, ws.mod + (size_t)i * d.B * 6 * D, st));
+    mod = ws.mod;
+  }
+  float* xs[2] = {x_txt, x_img};
+  const long long xseg[2] = {xt_seg_rows, xi_seg_rows};
+  const int Ls[2] = {d.Lt, d.Li};
+  const int off[2] = {0, d.Lt};
+  // LN + modulate and the fused QKV / RMSNorm / RoPE GEMM per stream
+  for (int i = 0; i < 2; ++i) {
+    if (Ls[i] == 0) continue;
+    const float* m = mod + (size_t)i * d.B * 6 * D;
+    uint16_t* y = ws.y + (size_t)off[i] * d.B * D;
+    MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, m, m + D, 6 * D, s.eps_ln, y, st));
+    GemmParams p = gemm_params(GM_QKV);
+    p.out_seg_rows = d.L;
+    p.out_row_off = off[i];
+    p.qkv_D = D;
+    p.d_head = d.d;
+    p.gq = w.q_norm[i];
+    p.gk = w.k_norm[i];
+    p.eps = s.eps_rms;
+    p.rope_cos = cs;
+    p.rope_sin = sn;
+    p.qk = ws.qk;
+    p.qk_ld = 2 * D;
+    p.vT = ws.vT;
+    p.vT_ld = d.Lpad;
+    MMDIT_TRY(run_gemm(y, D, Ls[i], Ls[i], d.B, D, w.qkv[i], 3 * D, p, ws.wdeq, st));
+  }
+  MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.O, D, st));
+  for (int i = 0; i < 2; ++i) {
+    if (Ls[i] == 0) continue;
+    const float* m = mod + (size_t)i * d.B * 6 * D;
+    // x += gate1 * (o Wp^T + bp)
+    GemmParams p = gemm_params(GM_RESID);
+    p.resid = xs[i];
+    p.resid_ld = D;
+    p.resid_seg_rows = xseg[i];
+    p.gate = m + 2 * D;
+    p.gate_seg_stride = 6 * D;
+    MMDIT_TRY(run_gemm(ws.O + (size_t)off[i] * D, D, d.L, Ls[i], d.B, D, w.proj[i], D, p, ws.wdeq, st));
+    // y2 = LN(x)(1 + scale2) + shift2; h = GELU(y2 W1^T + b1); x += gate2 (h W2^T + b2)
+    MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, m + 3 * D, m + 4 * D, 6 * D, s.eps_ln, ws.y, st));
+    GemmParams p1 = gemm_params(GM_STORE_BF16);
+    p1.gelu_from = 0;
+    p1.out = ws.h;
+    p1.out_ld = d.Dm;
+    p1.out_seg_rows = Ls[i];
+    MMDIT_TRY(run_gemm(ws.y, D, Ls[i], Ls[i], d.B, D, w.mlp_in[i], d.Dm, p1, ws.wdeq, st));
+    GemmParams p2 = gemm_params(GM_RESID);
+    p2.resid = xs[i];
+    p2.resid_ld = D;
+    p2.resid_seg_rows = xseg[i];
+    p2.gate = m + 5 * D;
+    p2.gate_seg_stride = 6 * D;
+    MMDIT_TRY(run_gemm(ws.h, d.Dm, Ls[i], Ls[i], d.B, d.Dm, w.mlp_out[i], D, p2, ws.wdeq, st));
+  }
+  return MMDIT_OK;
+}
+
+static int single_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_single_w_t& w, const float* vec,
+                             const float* mod_pre, float* x, const float* cs, const float* sn, const SingleWS& ws,
+                             cudaStream_t st) {
+  const int D = d.D;
+  const float* mod = mod_pre;
+  if (!mod) {
+    MMDIT_CUDA(launch_gemv(w.mod.w, w.mod.scale != nullptr, w.mod.scale, w.mod.b, vec, d.B, 3 * D, D, 1, ws.mod, st));
+    mod = ws.mod;
+  }
+  MMDIT_CUDA(launch_ln_modulate(x, d.L, d.L, d.B, D, mod, mod + D, 3 * D, s.eps_ln, ws.y, st));
+  const long long cat_ld = D + d.Dm;
+  GemmParams p = gemm_params(GM_QKV);
+  p.out_seg_rows = d.L;
+  p.out_row_off = 0;
+  p.qkv_D = D;
+  p.d_head = d.d;
+  p.gq = w.q_norm;
+  p.gk = w.k_norm;
+  p.eps = s.eps_rms;
+  p.rope_cos = cs;
+  p.rope_sin = sn;
+  p.qk = ws.qk;
+  p.qk_ld = 2 * D;
+  p.vT = ws.vT;
+  p.vT_ld = d.Lpad;
+  p.aux = ws.cat;
+  p.aux_ld = cat_ld;
+  p.aux_col_off = D;
+  MMDIT_TRY(run_gemm(ws.y, D, d.L, d.L, d.B, D, w.lin1, 3 * D + d.Dm, p, ws.wdeq, st));
+  MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.cat, cat_ld, st));
+  GemmParams p2 = gemm_params(GM_RESID);
+  p2.resid = x;
+  p2.resid_ld = D;
+  p2.resid_seg_rows = d.L;
+  p2.gate = mod + 2 * D;
+  p2.gate_seg_stride = 3 * D;
+  MMDIT_TRY(run_gemm(ws.cat, cat_ld, d.L, d.L, d.B, (int)cat_ld, w.lin2, D, p2, ws.wdeq, st));
+  return MMDIT_OK;
+}
+
+static bool double_w_ok(const mmdit_double_w_t* w, bool i8) {
+  if (!w) return false;
+  for (int i = 0; i < 2; ++i) {
+    if (!lin_ok(w->mod[i], i8) || !lin_ok(w->qkv[i], i8) || !lin_ok(w->proj[i], i8) || !lin_ok(w->mlp_in[i], i8) ||
+        !lin_ok(w->mlp_out[i], i8))
+      return false;
+    if (!w->q_norm[i] || !w->k_norm[i] || !al16(w->q_norm[i]) || !al16(w->k_norm[i])) return false;
+  }
+  return true;
+}
+
+static bool single_w_ok(const mmdit_single_w_t* w, bool i8) {
+  if (!w) return false;
+  if (!lin_ok(w->mod, i8) || !lin_ok(w->lin1, i8) || !lin_ok(w->lin2, i8)) return false;
+  return w->q_norm && w->k_norm && al16(w->q_norm) && al16(w->k_norm);
+}
+
+}  // namespace mmdit
+
+using namespace mmdit;
+
+// =================================================================== exports
+extern "C" {
+
+const char* mmdit_status_string(int status) {
+  switch (status) {
+    case MMDIT_OK: return "ok";
+    case MMDIT_ERR_ARG: return "invalid argument (null pointer or bad enum)";
+    case MMDIT_ERR_SHAPE: return "shape outside the supported limits";
+    case MMDIT_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case MMDIT_ERR_WORKSPACE: return "workspace too small";
+    case MMDIT_ERR_CUDA: return "CUDA runtime error";
+    case MMDIT_ERR_TIMEOUT: return "a kernel abandoned a bounded wait";
+    case MMDIT_ERR_UNSUPPORTED: return "device is not sm_103 or a driver entry point is missing";
+    default: return "unknown status";
+  }
+}
+
+int mmdit_sync_status(void* stream) {
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MMDIT_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return MMDIT_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return MMDIT_ERR_CUDA;
+    return MMDIT_ERR_TIMEOUT;
+  }
+  return MMDIT_OK;
+}
+
+long long mmdit_launch_count(void) { return g_launches.load(); }
+
+int mmdit_workspace_size(const mmdit_shape_t* shape, int op, size_t* bytes) {
+  if (!bytes) return MMDIT_ERR_ARG;
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  const bool i8 = shape->w_dtype == MMDIT_I8W;
+  Carve c{nullptr, 0};
+  switch (op) {
+    case MMDIT_OP_DOUBLE: {
+      DoubleWS w;
+      layout_double(d, i8, true, c, w);
+      break;
+    }
+    case MMDIT_OP_SINGLE: {
+      SingleWS w;
+      layout_single(d, i8, true, c, w);
+      break;
+    }
+    case MMDIT_OP_ATTENTION:
+      c.take<uint16_t>((size_t)d.B * d.L * 2 * d.D);
+      c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
+      break;
+    default:
+      return MMDIT_ERR_ARG;
+  }
+  *bytes = c.off + 256;
+  return MMDIT_OK;
+}
+
+int mmdit_step_workspace_size(const mmdit_shape_t* shape, int n_double, int n_single, size_t* bytes) {
+  if (!bytes || n_double < 0 || n_single < 0) return MMDIT_ERR_ARG;
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  if (shape->C_lat <= 0 || shape->C_lat % 64 || shape->t_dim <= 0 || shape->t_dim % 16) return MMDIT_ERR_SHAPE;
+  Carve c{nullptr, 0};
+  StepWS w;
+  layout_step(d, *shape, n_double, n_single, c, w);
+  *bytes = c.off + 256;
+  return MMDIT_OK;
+}
+
+int mmdit_rope2d_build(const mmdit_shape_t* shape, int32_t* ids, float* cos_, float* sin_, void* stream) {
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  if (!cos_ || !sin_) return MMDIT_ERR_ARG;
+  if (!al16(cos_) || !al16(sin_) || (ids && (reinterpret_cast<uintptr_t>(ids) & 3))) return MMDIT_ERR_ALIGN;
+  MMDIT_TRY(check_device());
+  return cuda_status(
+      launch_rope_build(d.Lt, shape->grid_w, d.L, shape->rope_axes, shape->rope_theta, ids, cos_, sin_, S(stream)));
+}
+
+int rope2d_apply(const mmdit_shape_t* shape, const float* cos_, const float* sin_, void* x, int row_stride,
+                 void* stream) {
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  if (!cos_ || !sin_ || !x) return MMDIT_ERR_ARG;
+  if (row_stride < d.D || row_stride % 8) return MMDIT_ERR_SHAPE;
+  if (!al16(cos_) || !al16(sin_) || !al16(x)) return MMDIT_ERR_ALIGN;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_rope_apply(static_cast<uint16_t*>(x), (long long)d.B * d.L, d.L, d.H, d.d, row_stride,
+                                       cos_, sin_, S(stream)));
+}
+
+int joint_attention_fwd(const mmdit_shape_t* shape, const void* qkv, int qkv_row_stride, const float* const q_norm[2],
+                        const float* const k_norm[2], const float* cos_, const float* sin_, void* out,
+                        int out_row_stride, void* ws, size_t ws_bytes, void* stream) {
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  if (!qkv || !out || !ws) return MMDIT_ERR_ARG;
+  if ((cos_ == nullptr) != (sin_ == nullptr)) return MMDIT_ERR_ARG;
+  if (qkv_row_stride < 3 * d.D || qkv_row_stride % 8 || out_row_stride < d.D || out_row_stride % 8)
+    return MMDIT_ERR_SHAPE;
+  if (!al16(qkv) || !al16(out) || !al16(ws)) return MMDIT_ERR_ALIGN;
+  const float* gq0 = q_norm ? q_norm[0] : nullptr;
+  const float* gq1 = q_norm ? q_norm[1] : nullptr;
+  const float* gk0 = k_norm ? k_norm[0] : nullptr;
+  const float* gk1 = k_norm ? k_norm[1] : nullptr;
+  if (gq0 && (!gq1 || !gk0 || !gk1)) return MMDIT_ERR_ARG;
+  size_t need = 0;
+  MMDIT_TRY(mmdit_workspace_size(shape, MMDIT_OP_ATTENTION, &need));
+  if (ws_bytes < need) return MMDIT_ERR_WORKSPACE;
+  MMDIT_TRY(check_device());
+  Carve c{static_cast<uint8_t*>(ws), 0};
+  uint16_t* qk = c.take<uint16_t>((size_t)d.B * d.L * 2 * d.D);
+  uint16_t* vT = c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
+  MMDIT_CUDA(launch_attn_prep(static_cast<const uint16_t*>(qkv), qkv_row_stride, d.B, d.L, d.Lt, d.H, d.d, gq0, gq1,
+                              gk0, gk1, shape->eps_rms, cos_, sin_, qk, vT, d.Lpad, S(stream)));
+  return run_attention(d, qk, vT, static_cast<uint16_t*>(out), out_row_stride, S(stream));
+}
+
+int mmdit_double_block_fwd(const mmdit_shape_t* shape, const mmdit_double_w_t* w, const float* vec,
+                           const float* mod_precomputed, float* x_txt, float* x_img, const float* cos_,
+                           const float* sin_, void* ws, size_t ws_bytes, void* stream) {
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  const bool i8 = shape->w_dtype == MMDIT_I8W;
+  if (!double_w_ok(w, i8)) return MMDIT_ERR_ARG;
+  if ((vec == nullptr) == (mod_precomputed == nullptr)) return MMDIT_ERR_ARG;
+  if (!x_img || (d.Lt > 0 && !x_txt) || !cos_ || !sin_ || !ws) return MMDIT_ERR_ARG;
+  if ((x_txt && !al16(x_txt)) || !al16(x_img) || !al16(cos_) || !al16(sin_) || !al16(ws) ||
+      (vec && !al16(vec)) || (mod_precomputed && !al16(mod_precomputed)))
+    return MMDIT_ERR_ALIGN;
+  Carve c{static_cast<uint8_t*>(ws), 0};
+  DoubleWS dw;
+  {
+    Carve q{nullptr, 0};
+    layout_double(d, i8, vec != nullptr, q, dw);
+    if (ws_bytes < q.off) return MMDIT_ERR_WORKSPACE;
+  }
+  MMDIT_TRY(check_device());
+  layout_double(d, i8, vec != nullptr, c, dw);
+  return double_block_impl(*shape, d, *w, vec, mod_precomputed, x_txt, d.Lt, x_img, d.Li, cos_, sin_, dw, S(stream));
+}
+
+int mmdit_single_block_fwd(const mmdit_shape_t* shape, const mmdit_single_w_t* w, const float* vec,
+                           const float* mod_precomputed, float* x, const float* cos_, const float* sin_, void* ws,
+                           size_t ws_bytes, void* stream) {
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  const bool i8 = shape->w_dtype == MMDIT_I8W;
+  if (!single_w_ok(w, i8)) return MMDIT_ERR_ARG;
+  if ((vec == nullptr) == (mod_precomputed == nullptr)) return MMDIT_ERR_ARG;
+  if (!x || !cos_ || !sin_ || !ws) return MMDIT_ERR_ARG;
+  if (!al16(x) || !al16(cos_) || !al16(sin_) || !al16(ws) || (vec && !al16(vec)) ||
+      (mod_precomputed && !al16(mod_precomputed)))
+    return MMDIT_ERR_ALIGN;
+  SingleWS sw;
+  {
+    Carve q{nullptr, 0};
+    layout_single(d, i8, vec != nullptr, q, sw);
+    if (ws_bytes < q.off) return MMDIT_ERR_WORKSPACE;
+  }
+  MMDIT_TRY(check_device());
+  Carve c{static_cast<uint8_t*>(ws), 0};
+  layout_single(d, i8, vec != nullptr, c, sw);
+  return single_block_impl(*shape, d, *w, vec, mod_precomputed, x, cos_, sin_, sw, S(stream));
+}
+
+int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_txt_in,
+                   double sigma, double sigma_next, float* v_out, void* ws, size_t ws_bytes, void* stream) {
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  if (!w || !x_lat || (d.Lt > 0 && !x_txt_in) || !ws) return MMDIT_ERR_ARG;
+  if (w->n_double < 0 || w->n_single < 0 || (w->n_double && !w->doubles) || (w->n_single && !w->singles))
+    return MMDIT_ERR_ARG;
+  const bool i8 = shape->w_dtype == MMDIT_I8W;
+  if (!lin_ok(w->time1, i8) || !lin_ok(w->time2, i8) || !lin_ok(w->img_in, i8) || !lin_ok(w->final_mod, i8) ||
+      !lin_ok(w->final, i8))
+    return MMDIT_ERR_ARG;
+  for (int i = 0; i < w->n_double; ++i)
+    if (!double_w_ok(&w->doubles[i], i8)) return MMDIT_ERR_ARG;
+  for (int i = 0; i < w->n_single; ++i)
+    if (!single_w_ok(&w->singles[i], i8)) return MMDIT_ERR_ARG;
+  if (!al16(x_lat) || (x_txt_in && !al16(x_txt_in)) || !al16(ws) || (v_out && !al16(v_out))) return MMDIT_ERR_ALIGN;
+  size_t need = 0;
+  MMDIT_TRY(mmdit_step_workspace_size(shape, w->n_double, w->n_single, &need));
+  if (ws_bytes < need) return MMDIT_ERR_WORKSPACE;
+  MMDIT_TRY(check_device());
+  cudaStream_t st = S(stream);
+  const int D = d.D, C = shape->C_lat;
+  Carve c{static_cast<uint8_t*>(ws), 0};
+  StepWS sw;
+  layout_step(d, *shape, w->n_double, w->n_single, c, sw);
+  MMDIT_CUDA(launch_rope_build(d.Lt, shape->grid_w, d.L, shape->rope_axes, shape->rope_theta, nullptr, sw.cs, sw.sn,
+                               st));
+  // timestep embedding: vec = time2 SiLU(time1 sinusoid(1000 sigma))
+  MMDIT_CUDA(launch_sinusoid(1000.0 * sigma, d.B, shape->t_dim, sw.temb, st));
+  float* th = sw.temb + (size_t)d.B * shape->t_dim;
+  MMDIT_CUDA(launch_gemv(w->time1.w, w->time1.scale != nullptr, w->time1.scale, w->time1.b, sw.temb, d.B, D,
+                         shape->t_dim, 0, th, st));
+  MMDIT_CUDA(launch_gemv(w->time2.w, w->time2.scale != nullptr, w->time2.scale, w->time2.b, th, d.B, D, D, 1,
+                         sw.vec, st));
+  // modulation vectors of every block (they depend on vec only)
+  float* mp = sw.mods;
+  for (int i = 0; i < w->n_double; ++i)
+    for (int s = 0; s < 2; ++s) {
+      const mmdit_linear_t& l = w->doubles[i].mod[s];
+      MMDIT_CUDA(launch_gemv(l.w, l.scale != nullptr, l.scale, l.b, sw.vec, d.B, 6 * D, D, 1, mp, st));
+      mp += (size_t)d.B * 6 * D;
+    }
+  for (int i = 0; i < w->n_single; ++i) {
+    const mmdit_linear_t& l = w->singles[i].mod;
+    MMDIT_CUDA(launch_gemv(l.w, l.scale != nullptr, l.scale, l.b, sw.vec, d.B, 3 * D, D, 1, mp, st));
+    mp += (size_t)d.B * 3 * D;
+  }
+  float* mod_final = mp;
+  MMDIT_CUDA(launch_gemv(w->final_mod.w, w->final_mod.scale != nullptr, w->final_mod.scale, w->final_mod.b, sw.vec,
+                         d.B, 2 * D, D, 1, mod_final, st));
+  // residual stream x = [text; image] per sample: text copied in, image from img_in
+  if (d.Lt > 0)
+    MMDIT_CUDA(cudaMemcpy2DAsync(sw.x, (size_t)d.L * D * 4, x_txt_in, (size_t)d.Lt * D * 4, (size_t)d.Lt * D * 4, d.B,
+                                 cudaMemcpyDeviceToDevice, st));
+  MMDIT_CUDA(launch_cast_bf16(x_lat, sw.xlat, (long long)d.B * d.Li * C, st));
+  {
+    GemmParams p = gemm_params(GM_STORE_F32);
+    p.out = sw.x;
+    p.out_ld = D;
+    p.out_seg_rows = d.L;
+    p.out_row_off = d.Lt;
+    Carve bc{sw.block, 0};
+    uint16_t* wdeq = i8 ? bc.take<uint16_t>((size_t)D * C) : nullptr;
+    MMDIT_TRY(run_gemm(sw.xlat, C, d.Li, d.Li, d.B, C, w->img_in, D, p, wdeq, st));
+  }
+  // blocks
+  mp = sw.mods;
+  {
+    Carve bc{sw.block, 0};
+    DoubleWS dw;
+    layout_double(d, i8, false, bc, dw);
+    for (int i = 0; i < w->n_double; ++i) {
+      MMDIT_TRY(double_block_impl(*shape, d, w->doubles[i], nullptr, mp, sw.x, d.L, sw.x + (size_t)d.Lt * D, d.L,
+                                  sw.cs, sw.sn, dw, st));
+      mp += (size_t)2 * d.B * 6 * D;
+    }
+  }
+  {
+    Carve bc{sw.block, 0};
+    SingleWS ssw;
+    layout_single(d, i8, false, bc, ssw);
+    for (int i = 0; i < w->n_single; ++i) {
+      MMDIT_TRY(single_block_impl(*shape, d, w->singles[i], nullptr, mp, sw.x, sw.cs, sw.sn, ssw, st));
+      mp += (size_t)d.B * 3 * D;
+    }
+  }
+  // final layer on the image tokens and the Euler update
+  {
+    Carve bc{sw.block, 0};
+    uint16_t* y = bc.take<uint16_t>((size_t)d.B * d.Li * D);
+    uint16_t* wdeq = i8 ? bc.take<uint16_t>((size_t)D * C) : nullptr;
+    MMDIT_CUDA(launch_ln_modulate(sw.x + (size_t)d.Lt * D, d.L, d.Li, d.B, D, mod_final, mod_final + D, 2 * D,
+                                  shape->eps_ln, y, st));
+    GemmParams p = gemm_params(GM_STORE_F32);
+    float* v = v_out ? v_out : sw.v;
+    p.out = v;
+    p.out_ld = C;
+    p.out_seg_rows = d.Li;
+    MMDIT_TRY(run_gemm(y, D, d.Li, d.Li, d.B, D, w->final, C, p, wdeq, st));
+    MMDIT_CUDA(launch_euler(x_lat, v, false, (float)(sigma_next - sigma), (long long)d.B * d.Li * C, st));
+  }
+  return MMDIT_OK;
+}
+
+int euler_step(float* x, const void* v, int v_dtype, double sigma, double sigma_next, int64_t n, void* stream) {
+  if (!x || !v || n < 0) return MMDIT_ERR_ARG;
+  if (v_dtype != MMDIT_F32 && v_dtype != MMDIT_BF16) return MMDIT_ERR_ARG;
+  if (!al16(x) || !al16(v)) return MMDIT_ERR_ALIGN;
+  if (n == 0) return MMDIT_OK;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_euler(x, v, v_dtype == MMDIT_BF16, (float)(sigma_next - sigma), n, S(stream)));
+}
+
+int mmdit_quantize_w8(const void* w, int w_dtype, int N, int K, int8_t* q, float* scale, void* stream) {
+  if (!w || !q || !scale) return MMDIT_ERR_ARG;
+  if (w_dtype != MMDIT_F32 && w_dtype != MMDIT_BF16) return MMDIT_ERR_ARG;
+  if (N < 1 || K < 1) return MMDIT_ERR_SHAPE;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_quantize(w, w_dtype == MMDIT_BF16, N, K, q, scale, S(stream)));
+}
+
+int mmdit_linear_fwd(const mmdit_linear_t* lin, int M, int N, int K, const void* x, void* y, int epilogue,
+                     const float* gate, void* ws, size_t ws_bytes, void* stream) {
+  if (!lin || !x || !y) return MMDIT_ERR_ARG;
+  if (!lin_ok(*lin, lin->scale != nullptr)) return MMDIT_ERR_ARG;
+  if (M < 1 || N < 32 || N % 32 || K < 64 || K % 64) return MMDIT_ERR_SHAPE;
+  if (!al16(x) || !al16(y) || (gate && !al16(gate))) return MMDIT_ERR_ALIGN;
+  uint16_t* wdeq = nullptr;
+  if (lin->scale) {
+    if (!ws || ws_bytes < (size_t)N * K * 2) return MMDIT_ERR_WORKSPACE;
+    if (!al16(ws)) return MMDIT_ERR_ALIGN;
+    wdeq = static_cast<uint16_t*>(ws);
+  }
+  MMDIT_TRY(check_device());
+  GemmParams p;
+  switch (epilogue) {
+    case MMDIT_EPI_BF16:
+    case MMDIT_EPI_BF16_GELU:
+      p = gemm_params(GM_STORE_BF16);
+      if (epilogue == MMDIT_EPI_BF16_GELU) p.gelu_from = 0;
+      p.out = y;
+      p.out_ld = N;
+      p.out_seg_rows = M;
+      break;
+    case MMDIT_EPI_F32:
+      p = gemm_params(GM_STORE_F32);
+      p.out = y;
+      p.out_ld = N;
+      p.out_seg_rows = M;
+      break;
+    case MMDIT_EPI_RESID:
+      p = gemm_params(GM_RESID);
+      p.resid = static_cast<float*>(y);
+      p.resid_ld = N;
+      p.resid_seg_rows = M;
+      p.gate = gate;
+      p.gate_seg_stride = 0;
+      break;
+    default:
+      return MMDIT_ERR_ARG;
+  }
+  return run_gemm(x, K, M, M, 1, K, *lin, N, p, wdeq, S(stream));
+}
+
+int mmdit_ln_modulate(const float* x, int B, int rows, int D, const float* shift, const float* scale,
+                      int64_t mod_stride, float eps, void* y, void* stream) {
+  if (!x || !shift || !scale || !y) return MMDIT_ERR_ARG;
+  if (B < 1 || rows < 1 || D < 256 || D % 256 || D > 4096) return MMDIT_ERR_SHAPE;
+  if (!al16(x) || !al16(shift) || !al16(scale) || !al16(y) || (mod_stride % 4)) return MMDIT_ERR_ALIGN;
+  MMDIT_TRY(check_device());
+  return cuda_status(
+      launch_ln_modulate(x, rows, rows, B, D, shift, scale, mod_stride, eps, static_cast<uint16_t*>(y), S(stream)));
+}
+
+int mmdit_gemv(const mmdit_linear_t* lin, int B, int N, int K, const float* x, int act, float* y, void* stream) {
+  if (!lin || !x || !y || (act != 0 && act != 1)) return MMDIT_ERR_ARG;
+  if (!lin_ok(*lin, lin->scale != nullptr)) return MMDIT_ERR_ARG;
+  if (B < 1 || B > 8 || N < 1 || K < 16 || K % 16) return MMDIT_ERR_SHAPE;
+  if ((size_t)B * K * 4 > 200 * 1024) return MMDIT_ERR_SHAPE;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_gemv(lin->w, lin->scale != nullptr, lin->scale, lin->b, x, B, N, K, act, y, S(stream)));
+}
+
+int mmdit_time_embed(const mmdit_shape_t* shape, const mmdit_linear_t* time1, const mmdit_linear_t* time2,
+                     double sigma, float* vec, float* ws, void* stream) {
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  if (!time1 || !time2 || !vec || !ws) return MMDIT_ERR_ARG;
+  if (shape->t_dim <= 0 || shape->t_dim % 16) return MMDIT_ERR_SHAPE;
+  if (!lin_ok(*time1, time1->scale != nullptr) || !lin_ok(*time2, time2->scale != nullptr)) return MMDIT_ERR_ARG;
+  if (!al16(vec) || !al16(ws)) return MMDIT_ERR_ALIGN;
+  MMDIT_TRY(check_device());
+  cudaStream_t st = S(stream);
+  MMDIT_CUDA(launch_sinusoid(1000.0 * sigma, d.B, shape->t_dim, ws, st));
+  float* th = ws + (size_t)d.B * shape->t_dim;
+  MMDIT_CUDA(launch_gemv(time1->w, time1->scale != nullptr, time1->scale, time1->b, ws, d.B, d.D, shape->t_dim, 0,
+                         th, st));
+  return cuda_status(
+      launch_gemv(time2->w, time2->scale != nullptr, time2->scale, time2->b, th, d.B, d.D, d.D, 1, vec, st));
+}
+
+}  // extern "C"

@@ -1,0 +1,450 @@
+// Bandwidth-bound kernels of the step: LayerNorm + adaLN modulate, the
+// modulation / timestep GEMVs, RoPE tables and rotation, the Euler update,
+// the int8 quantiser and dequantiser, and the attention input prep.
+// Vectorised 16-byte global accesses, one warp per row where a row reduces.
+#include "common.cuh"
+#include "elementwise.h"
+
+namespace mmdit {
+
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------ LN + modulate
+// y = (x - mean) / sqrt(var + eps) * (1 + scale) + shift over one row of D
+// floats per CTA of D/8 threads (8 consecutive floats each); statistics in
+// fp32, two passes over registers.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int i = 0; i < nw; ++i) t += red[i];
+  return t;
+}
+
+__global__ void __launch_bounds__(512) ln_mod_kernel(const float* __restrict__ x, long long x_seg_rows, int rows,
+                                                     int D, const float* __restrict__ shift,
+                                                     const float* __restrict__ scale, long long mod_stride, float eps,
+                                                     uint16_t* __restrict__ y) {
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  const int seg = row / rows, i = row - seg * rows;
+  const int t = threadIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + ((long long)seg * x_seg_rows + i) * D) + 2 * t;
+  const float4 a = __ldg(xr), b = __ldg(xr + 1);
+  const float inv_d = 1.0f / (float)D;
+  const float mean = block_sum((a.x + a.y) + (a.z + a.w) + (b.x + b.y) + (b.z + b.w), red) * inv_d;
+  float v[8] = {a.x - mean, a.y - mean, a.z - mean, a.w - mean, b.x - mean, b.y - mean, b.z - mean, b.w - mean};
+  float q = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) q = fmaf(v[j], v[j], q);
+  const float rstd = rsqrtf(block_sum(q, red) * inv_d + eps);
+  const float4* sc4 = reinterpret_cast<const float4*>(scale + (long long)seg * mod_stride) + 2 * t;
+  const float4* sh4 = reinterpret_cast<const float4*>(shift + (long long)seg * mod_stride) + 2 * t;
+  const float4 s0 = __ldg(sc4), s1 = __ldg(sc4 + 1), h0 = __ldg(sh4), h1 = __ldg(sh4 + 1);
+  const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  const float sh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    o[j] = pack_bf16x2(v[2 * j] * rstd * (1.f + sc[2 * j]) + sh[2 * j],
+                       v[2 * j + 1] * rstd * (1.f + sc[2 * j + 1]) + sh[2 * j + 1]);
+  reinterpret_cast<uint4*>(y + (long long)row * D)[t] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ------------------------------------------------------------------ GEMV
+// y[b, n] = sum_k W[n, k] act(x[b, k]) (* scale[n]) + bias[n] for B <= 8 rows
+// of x: one warp per output row, 16-byte weight loads along K, x staged in
+// shared memory after the activation.
+constexpr int kGemvRowsPerWarp = 4;
+constexpr int kGemvWarps = 8;
+
+template <bool I8>
+__global__ void __launch_bounds__(256) gemv_kernel(const void* __restrict__ W, const float* __restrict__ wscale,
+                                                   const float* __restrict__ bias, const float* __restrict__ x, int B,
+                                                   int N, int K, int act, float* __restrict__ y) {
+  extern __shared__ float xs[];
+  for (int i = threadIdx.x; i < B * K; i += blockDim.x) {
+    const float t = x[i];
+    xs[i] = act ? silu_f(t) : t;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp;
+  constexpr int EPV = I8 ? 16 : 8;  // elements per 16-byte vector
+  const int nvec = K / EPV;
+#pragma unroll 1
+  for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
+    const int n = row0 + rr;
+    if (n >= N) break;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint4* wr = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(W) + (long long)n * K * (I8 ? 1 : 2));
+#pragma unroll 4
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 wv = __ldg(wr + v);
+      float w[EPV];
+      if (I8) {
+        const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = (float)(int8_t)((u[j >> 2] >> (8 * (j & 3))) & 0xFF);
+      } else {
+        const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[2 * j] = bf16_lo(u[j]), w[2 * j + 1] = bf16_hi(u[j]);
+      }
+      const int k0 = v * EPV;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (b < B) {
+          const float* xb = xs + b * K + k0;
+          float a = acc[b];
+#pragma unroll
+          for (int j = 0; j < EPV; ++j) a = fmaf(w[j], xb[j], a);
+          acc[b] = a;
+        }
+      }
+    }
+    const float sc = wscale ? wscale[n] : 1.0f;
+    const float bi = bias ? bias[n] : 0.0f;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (b < B) {
+        const float t = warp_sum(acc[b]);
+        if (lane == 0) y[(long long)b * N + n] = t * sc + bi;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ timestep sinusoid
+__global__ void sinusoid_kernel(double t, int B, int dim, float* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int half = dim / 2;
+  if (i >= B * dim) return;
+  const int j = i % dim;
+  const int jj = j < half ? j : j - half;
+  const double f = exp(-log(10000.0) * (double)jj / (double)half);
+  const double a = t * f;
+  out[i] = (float)(j < half ? cos(a) : sin(a));
+}
+
+// ------------------------------------------------------------------ RoPE
+// ids [L,3] and cos/sin [L, d/2]: angle = pos_axis * theta^(-2i/d_axis), fp64.
+__global__ void rope_build_kernel(int L_txt, int grid_w, int L, int a0, int a1, int a2, double theta,
+                                  int32_t* __restrict__ ids, float* __restrict__ cs, float* __restrict__ sn) {
+  const int npairs = (a0 + a1 + a2) / 2;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)L * npairs) return;
+  const int tok = (int)(idx / npairs), p = (int)(idx - (long long)tok * npairs);
+  int pos[3] = {0, 0, 0};
+  if (tok >= L_txt) {
+    const int img = tok - L_txt;
+    pos[1] = img / grid_w;
+    pos[2] = img - pos[1] * grid_w;
+  }
+  if (p == 0 && ids) {
+    ids[3 * tok + 0] = pos[0];
+    ids[3 * tok + 1] = pos[1];
+    ids[3 * tok + 2] = pos[2];
+  }
+  int axis, i, da;
+  if (p < a0 / 2) {
+    axis = 0, i = p, da = a0;
+  } else if (p < (a0 + a1) / 2) {
+    axis = 1, i = p - a0 / 2, da = a1;
+  } else {
+    axis = 2, i = p - (a0 + a1) / 2, da = a2;
+  }
+  const double omega = pow(theta, (-2.0 * (double)i) / (double)da);
+  const double ang = (double)pos[axis] * omega;
+  cs[idx] = (float)cos(ang);
+  sn[idx] = (float)sin(ang);
+}
+
+// x [rows][row_stride] bf16, each row H*d channels; one thread per 8 channels.
+__global__ void rope_apply_kernel(uint16_t* __restrict__ x, long long rows, int L, int H, int d, int row_stride,
+                                  const float* __restrict__ cs, const float* __restrict__ sn) {
+  const int chunks = H * d / 8;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * chunks) return;
+  const long long row = idx / chunks;
+  const int c = (int)(idx - row * chunks);
+  const int tok = (int)(row % L);
+  const int p0 = (c % (d / 8)) * 4;
+  uint4* ptr = reinterpret_cast<uint4*>(x + row * row_stride + c * 8);
+  uint4 v = *ptr;
+  const float4 co = __ldg(reinterpret_cast<const float4*>(cs + (long long)tok * (d / 2) + p0));
+  const float4 si = __ldg(reinterpret_cast<const float4*>(sn + (long long)tok * (d / 2) + p0));
+  const float cc[4] = {co.x, co.y, co.z, co.w}, ss[4] = {si.x, si.y, si.z, si.w};
+  uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float x0 = bf16_lo(u[j]), x1 = bf16_hi(u[j]);
+    u[j] = pack_bf16x2(x0 * cc[j] - x1 * ss[j], x0 * ss[j] + x1 * cc[j]);
+  }
+  *ptr = make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+// ------------------------------------------------------------------ Euler
+__global__ void euler_f32_kernel(float* __restrict__ x, const float* __restrict__ v, float dt, long long n) {
+  const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i + 3 < n) {
+    float4 a = *reinterpret_cast<float4*>(x + i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(v + i));
+    a.x = fmaf(dt, b.x, a.x), a.y = fmaf(dt, b.y, a.y), a.z = fmaf(dt, b.z, a.z), a.w = fmaf(dt, b.w, a.w);
+    *reinterpret_cast<float4*>(x + i) = a;
+  } else {
+    for (long long k = i; k < n; ++k) x[k] = fmaf(dt, v[k], x[k]);
+  }
+}
+
+__global__ void euler_bf16_kernel(float* __restrict__ x, const uint16_t* __restrict__ v, float dt, long long n) {
+  const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i + 3 < n) {
+    float4 a = *reinterpret_cast<float4*>(x + i);
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(v + i));
+    a.x = fmaf(dt, bf16_lo(b.x), a.x), a.y = fmaf(dt, bf16_hi(b.x), a.y);
+    a.z = fmaf(dt, bf16_lo(b.y), a.z), a.w = fmaf(dt, bf16_hi(b.y), a.w);
+    *reinterpret_cast<float4*>(x + i) = a;
+  } else {
+    for (long long k = i; k < n; ++k) x[k] = fmaf(dt, __uint_as_float((uint32_t)v[k] << 16), x[k]);
+  }
+}
+
+// ------------------------------------------------------------------ int8
+template <typename T>
+__device__ __forceinline__ float load_w(const T* w, long long i);
+template <>
+__device__ __forceinline__ float load_w<float>(const float* w, long long i) {
+  return w[i];
+}
+template <>
+__device__ __forceinline__ float load_w<uint16_t>(const uint16_t* w, long long i) {
+  return __uint_as_float((uint32_t)w[i] << 16);
+}
+
+// One CTA per output row: s = max|w| / 127 (fp32), q = clamp(rint(w / s)).
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_kernel(const T* __restrict__ w, int K, int8_t* __restrict__ q,
+                                                       float* __restrict__ scale) {
+  __shared__ float red[8];
+  const long long base = (long long)blockIdx.x * K;
+  float m = 0.f;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) m = fmaxf(m, fabsf(load_w<T>(w, base + k)));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_max(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float amax = red[0];
+  const float s = amax == 0.f ? 1.0f : __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) scale[blockIdx.x] = s;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    float r = rintf(__fdiv_rn(load_w<T>(w, base + k), s));
+    r = fminf(fmaxf(r, -127.f), 127.f);
+    q[base + k] = (int8_t)r;
+  }
+}
+
+// int8 -> bf16 (exact: |q| <= 127 has at most 7 significant bits); 16 per thread.
+__global__ void dequant_i8_kernel(const int8_t* __restrict__ q, uint16_t* __restrict__ out, long long n16) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(q) + i);
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float lo = (float)(int8_t)((u[j >> 1] >> (16 * (j & 1))) & 0xFF);
+    const float hi = (float)(int8_t)((u[j >> 1] >> (16 * (j & 1) + 8)) & 0xFF);
+    o[j] = pack_bf16x2(lo, hi);
+  }
+  uint4* d = reinterpret_cast<uint4*>(out) + 2 * i;
+  d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__global__ void cast_f32_bf16_kernel(const float* __restrict__ x, uint16_t* __restrict__ y, long long n4) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = __ldg(reinterpret_cast<const float4*>(x) + i);
+  reinterpret_cast<uint2*>(y)[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+// ------------------------------------------------------------------ attention prep
+// One warp per (sample, token, head): q and k get RMSNorm (gain by stream)
+// and RoPE, written to qk [B][L][2D]; v is written transposed to vT [B][D][Lpad].
+template <int HD>
+__global__ void attn_prep_kernel(const uint16_t* __restrict__ qkv, long long qkv_ld, int B, int L, int L_txt, int H,
+                                 const float* gq0, const float* gq1, const float* gk0, const float* gk1, float eps,
+                                 const float* __restrict__ cs, const float* __restrict__ sn, uint16_t* __restrict__ qk,
+                                 uint16_t* __restrict__ vT, long long vT_ld) {
+  constexpr int PER = HD / 32;  // channels per lane (2 or 4), consecutive
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)B * L * H) return;
+  const int h = (int)(gw % H);
+  const long long bt = gw / H;
+  const int tok = (int)(bt % L);
+  const int b = (int)(bt / L);
+  const int D = H * HD;
+  const uint16_t* row = qkv + bt * qkv_ld;
+  const bool txt = tok < L_txt;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const float* g = which == 0 ? (txt ? gq0 : gq1) : (txt ? gk0 : gk1);
+    const uint16_t* src = row + which * D + h * HD + lane * PER;
+    float v[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) v[j] = __uint_as_float((uint32_t)src[j] << 16);
+    if (g) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) ss = fmaf(v[j], v[j], ss);
+      const float rs = rsqrtf(warp_sum(ss) * (1.0f / HD) + eps);
+#pragma unroll
+      for (int j = 0; j < PER; ++j) v[j] = v[j] * rs * g[lane * PER + j];
+    }
+    if (cs) {
+#pragma unroll
+      for (int j = 0; j < PER; j += 2) {
+        const int pr = (lane * PER + j) / 2;
+        const float c = cs[(long long)tok * (HD / 2) + pr], s = sn[(long long)tok * (HD / 2) + pr];
+        const float x0 = v[j], x1 = v[j + 1];
+        v[j] = x0 * c - x1 * s;
+        v[j + 1] = x0 * s + x1 * c;
+      }
+    }
+    uint16_t* dst = qk + bt * (2LL * D) + which * D + h * HD + lane * PER;
+#pragma unroll
+    for (int j = 0; j < PER; j += 2) *reinterpret_cast<uint32_t*>(dst + j) = pack_bf16x2(v[j], v[j + 1]);
+  }
+  const uint16_t* vs = row + 2 * D + h * HD + lane * PER;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) vT[((long long)b * D + h * HD + lane * PER + j) * vT_ld + tok] = vs[j];
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
+                               const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st) {
+  if (D % 256 || D > 4096) return cudaErrorInvalidValue;
+  ln_mod_kernel<<<rows * n_seg, D / 8, 0, st>>>(x, x_seg_rows, rows, D, shift, scale, mod_stride, eps, y);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
+                        int K, int act, float* y, cudaStream_t st) {
+  const size_t smem = (size_t)B * K * sizeof(float);
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaFuncSetAttribute(gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaFuncSetAttribute(gemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr_done[dev] = true;
+  }
+  const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
+  const int blocks = (N + rows_per_cta - 1) / rows_per_cta;
+  if (i8)
+    gemv_kernel<true><<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
+  else
+    gemv_kernel<false><<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st) {
+  const int n = B * dim;
+  sinusoid_kernel<<<(n + 255) / 256, 256, 0, st>>>(t, B, dim, out);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_build(int L_txt, int grid_w, int L, const int axes[3], double theta, int32_t* ids, float* cs,
+                              float* sn, cudaStream_t st) {
+  const long long n = (long long)L * ((axes[0] + axes[1] + axes[2]) / 2);
+  rope_build_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(L_txt, grid_w, L, axes[0], axes[1], axes[2], theta,
+                                                                 ids, cs, sn);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_apply(uint16_t* x, long long rows, int L, int H, int d, int row_stride, const float* cs,
+                              const float* sn, cudaStream_t st) {
+  const long long n = rows * (H * d / 8);
+  rope_apply_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(x, rows, L, H, d, row_stride, cs, sn);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long long n, cudaStream_t st) {
+  const long long threads = (n + 3) / 4;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (v_bf16)
+    euler_bf16_kernel<<<blocks, 256, 0, st>>>(x, reinterpret_cast<const uint16_t*>(v), dt, n);
+  else
+    euler_f32_kernel<<<blocks, 256, 0, st>>>(x, reinterpret_cast<const float*>(v), dt, n);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const void* w, bool w_bf16, int N, int K, int8_t* q, float* scale, cudaStream_t st) {
+  if (w_bf16)
+    quantize_kernel<uint16_t><<<N, 256, 0, st>>>(reinterpret_cast<const uint16_t*>(w), K, q, scale);
+  else
+    quantize_kernel<float><<<N, 256, 0, st>>>(reinterpret_cast<const float*>(w), K, q, scale);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_i8(const int8_t* q, uint16_t* out, long long n, cudaStream_t st) {
+  const long long n16 = n / 16;
+  dequant_i8_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(q, out, n16);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_bf16(const float* x, uint16_t* y, long long n, cudaStream_t st) {
+  const long long n4 = n / 4;
+  cast_f32_bf16_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(x, y, n4);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_prep(const uint16_t* qkv, long long qkv_ld, int B, int L, int L_txt, int H, int d,
+                             const float* gq0, const float* gq1, const float* gk0, const float* gk1, float eps,
+                             const float* cs, const float* sn, uint16_t* qk, uint16_t* vT, long long vT_ld,
+                             cudaStream_t st) {
+  const long long warps = (long long)B * L * H;
+  const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+  if (d == 128)
+    attn_prep_kernel<128><<<blocks, 256, 0, st>>>(qkv, qkv_ld, B, L, L_txt, H, gq0, gq1, gk0, gk1, eps, cs, sn, qk,
+                                                  vT, vT_ld);
+  else
+    attn_prep_kernel<64><<<blocks, 256, 0, st>>>(qkv, qkv_ld, B, L, L_txt, H, gq0, gq1, gk0, gk1, eps, cs, sn, qk, vT,
+                                                 vT_ld);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace mmdit

@@ -1,0 +1,28 @@
+// Launchers of the bandwidth-bound kernels (elementwise.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mmdit {
+
+// y[seg][i] = LN(x[seg*x_seg_rows + i]) (1 + scale[seg]) + shift[seg]; D % 256 == 0, D <= 4096.
+cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
+                               const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st);
+cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
+                        int K, int act, float* y, cudaStream_t st);
+cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st);
+cudaError_t launch_rope_build(int L_txt, int grid_w, int L, const int axes[3], double theta, int32_t* ids, float* cs,
+                              float* sn, cudaStream_t st);
+cudaError_t launch_rope_apply(uint16_t* x, long long rows, int L, int H, int d, int row_stride, const float* cs,
+                              const float* sn, cudaStream_t st);
+cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long long n, cudaStream_t st);
+cudaError_t launch_quantize(const void* w, bool w_bf16, int N, int K, int8_t* q, float* scale, cudaStream_t st);
+cudaError_t launch_dequant_i8(const int8_t* q, uint16_t* out, long long n, cudaStream_t st);
+cudaError_t launch_cast_bf16(const float* x, uint16_t* y, long long n, cudaStream_t st);
+cudaError_t launch_attn_prep(const uint16_t* qkv, long long qkv_ld, int B, int L, int L_txt, int H, int d,
+                             const float* gq0, const float* gq1, const float* gk0, const float* gk1, float eps,
+                             const float* cs, const float* sn, uint16_t* qk, uint16_t* vT, long long vT_ld,
+                             cudaStream_t st);
+
+}  // namespace mmdit

@@ -1,0 +1,91 @@
+// Internal declarations shared by the translation units of libmmdit.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mmdit {
+
+// ----------------------------------------------------------------- GEMM
+// Tile shape of the tcgen05 GEMM: 128 x 256 output tile per CTA, K blocks of
+// 64 bf16 (one 128-byte swizzle row), a 4-stage TMA ring.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+
+enum GemmMode : int {
+  GM_STORE_BF16 = 0,  // out bf16, GELU on columns >= gelu_from
+  GM_STORE_F32 = 1,   // out fp32
+  GM_RESID = 2,       // resid fp32 += gate * value
+  GM_QKV = 3,         // q,k: RMSNorm + RoPE -> qk; v -> transposed vT; rest: GELU -> aux
+};
+
+// Rows are grouped in `n_seg` segments (samples) of M_seg rows each; the A
+// operand's row r of segment s is read through a 3D tensor map (K, M_seg,
+// n_seg).  Output row of (s, m) = s * out_seg_rows + out_row_off + m.
+struct GemmParams {
+  int M_seg, n_seg, N, K;
+  int tiles_m, tiles_n, num_tiles, group_m;
+  int mode;
+  int gelu_from;
+  const float* bias;    // [N] or null
+  const float* wscale;  // [N] or null (int8 weights)
+  void* out;            // bf16 or fp32 output
+  long long out_ld;
+  long long out_seg_rows;
+  int out_row_off;
+  // GM_RESID
+  float* resid;
+  long long resid_ld;
+  long long resid_seg_rows;
+  const float* gate;  // [n_seg][gate_seg_stride] or null
+  long long gate_seg_stride;
+  // GM_QKV
+  int qkv_D;   // H * d_head
+  int d_head;  // 64 or 128
+  const float* gq;
+  const float* gk;
+  float eps;
+  const float* rope_cos;  // [L, d_head/2]; table row = out_row_off + m
+  const float* rope_sin;
+  uint16_t* qk;  // [seg][out_seg_rows][qk_ld]: q at col n, k at col n
+  long long qk_ld;
+  uint16_t* vT;  // [seg][H*d][vT_ld]
+  long long vT_ld;
+  uint16_t* aux;  // rest columns n >= 3D -> aux[row][aux_col_off + n - 3D], GELU
+  long long aux_ld;
+  int aux_col_off;
+  unsigned* status;
+};
+
+// ----------------------------------------------------------------- attention
+constexpr int kAttnBM = 128;  // queries per CTA
+constexpr int kAttnBN = 128;  // keys per KV tile
+
+struct AttnParams {
+  int L, H, B, n_q_tiles, n_kv_tiles;
+  float scale_log2;              // log2(e) / sqrt(d_head)
+  uint16_t* out;        // [B][L][out_ld], head h at column h*d
+  long long out_ld;
+  unsigned* status;
+};
+
+// ----------------------------------------------------------------- host helpers
+unsigned* device_status_ptr();  // device address of the status word (current device)
+void count_launch(int n = 1);
+
+// Encodes a 3D bf16 tensor map with a 64-element (128-byte) inner box and the
+// 128-byte swizzle: dims (inner, rows, batch), byte strides of rows and batch.
+bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t inner,
+                  uint64_t rows, uint64_t batch, uint64_t row_stride_bytes, uint64_t batch_stride_bytes,
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, cudaStream_t s);
+cudaError_t launch_attention(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, int d_head,
+                             cudaStream_t s);
+int num_sms();
+
+}  // namespace mmdit

@@ -1,0 +1,265 @@
+/*
+ * mmdit.h - C ABI of a GB300 (sm_103a) library for the forward pass of one
+ * Flux-style multi-modal diffusion transformer (MMDiT) denoising step.
+ *
+ * Sources.  The operations follow the primitive definitions in the Luminal
+ * blog post "Reducing image generation cost with ..." (section "What the
+ * compiler found on its own": matmul, attention as scores/scale/max/exp/
+ * sum/divide, RMSNorm, LayerNorm, adaLN scale-and-shift, RoPE as a partner
+ * gather with cosine/sine tables, gate-and-residual add, text/image
+ * concatenation, timestep embedding), the block structure of its section
+ * "Flux.2 Klein 9B" (double-stream and single-stream blocks, 16x latent
+ * patches with 128 channels), the host-side Euler sampler of its section
+ * "The AMD MI300X pipeline", and the int8 weight-only setting of the
+ * flux-amd-rocm BENCHMARKS.md page (torchao Int8WeightOnlyConfig).  Readings
+ * of steps the pages leave open are stated at each declaration.
+ *
+ * Conventions shared by every entry point:
+ *  - Return value: MMDIT_OK (0) or a negative MMDIT_ERR_* code.  On an
+ *    argument error nothing is launched.  Launches are asynchronous on the
+ *    given stream (a cudaStream_t passed as void*; NULL = legacy default).
+ *    A kernel that gives up a bounded wait records MMDIT_ERR_TIMEOUT in a
+ *    device status word that mmdit_sync_status() reads and clears.
+ *  - Pointers marked "device" must be device memory, owned by the caller,
+ *    and 16-byte aligned.  The library allocates no device memory: scratch
+ *    comes from the caller's workspace, sized by mmdit_workspace_size().
+ *  - Tensors are dense row-major.  bf16 = IEEE bfloat16 bits (uint16).
+ *    Linear weights are [N_out, K_in] row-major (y = x W^T + b), bias fp32
+ *    [N_out].  Int8 weights are int8 [N_out, K_in] with an fp32 per-row
+ *    scale: W = q * scale[n].
+ *  - Token layout: per sample, the L_txt text tokens come first, then the
+ *    L_img = grid_h * grid_w image tokens in row-major (h, w) order; the
+ *    batch index is outermost.
+ *  - The residual streams are fp32 and are updated in place.  GEMM and
+ *    attention operands are bf16 with fp32 accumulation; norms, softmax and
+ *    modulation are computed in fp32.
+ *  - Limits: D a multiple of 256, d_head 64 or 128, H * d_head == D,
+ *    D_mlp a multiple of 64, rope_axes summing to d_head with even entries,
+ *    1 <= B, L_txt >= 0, L_img >= 1.
+ */
+#ifndef MMDIT_H_
+#define MMDIT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+#define MMDIT_OK 0
+#define MMDIT_ERR_ARG (-1)         /* null pointer or bad enum value */
+#define MMDIT_ERR_SHAPE (-2)       /* shape outside the limits above */
+#define MMDIT_ERR_ALIGN (-3)       /* pointer or stride not 16-byte aligned */
+#define MMDIT_ERR_WORKSPACE (-4)   /* workspace smaller than required */
+#define MMDIT_ERR_CUDA (-5)        /* a CUDA runtime call failed */
+#define MMDIT_ERR_TIMEOUT (-6)     /* a kernel abandoned a bounded wait */
+#define MMDIT_ERR_UNSUPPORTED (-7) /* device is not sm_103 / feature absent */
+
+/* ---------------------------------------------------------------- dtypes */
+#define MMDIT_BF16 0
+#define MMDIT_F32 1
+#define MMDIT_I8W 2 /* int8 weight with fp32 per-output-channel scale */
+
+/* ---------------------------------------------------------------- shapes */
+typedef struct {
+  int B;            /* batch (independent samples) */
+  int L_txt;        /* text tokens per sample */
+  int grid_h;       /* latent grid rows */
+  int grid_w;       /* latent grid columns; L_img = grid_h * grid_w */
+  int D;            /* hidden width */
+  int H;            /* attention heads */
+  int d_head;       /* head width (64 or 128) */
+  int D_mlp;        /* MLP hidden width */
+  int rope_axes[3]; /* channels per RoPE axis (id, row, column) */
+  double rope_theta;
+  float eps_ln;     /* LayerNorm epsilon */
+  float eps_rms;    /* q/k RMSNorm epsilon */
+  int w_dtype;      /* MMDIT_BF16 or MMDIT_I8W for all linear weights */
+  int C_lat;        /* latent channels per image token (step only) */
+  int t_dim;        /* timestep sinusoid width (step only) */
+} mmdit_shape_t;
+
+/* One linear layer.  w: device [N, K] (bf16, or int8 when scale != NULL);
+ * b: device fp32 [N] or NULL; scale: device fp32 [N] for int8 weights. */
+typedef struct {
+  const void* w;
+  const float* b;
+  const float* scale;
+} mmdit_linear_t;
+
+/* Double-stream block weights; index 0 = text stream, 1 = image stream.
+ * mod: D -> 6D, chunks (shift1, scale1, gate1, shift2, scale2, gate2).
+ * qkv: D -> 3D (q | k | v, head-major inside each).  proj: D -> D.
+ * mlp_in: D -> D_mlp (GELU-tanh).  mlp_out: D_mlp -> D.
+ * q_norm / k_norm: device fp32 [d_head] RMSNorm gains. */
+typedef struct {
+  mmdit_linear_t mod[2], qkv[2], proj[2], mlp_in[2], mlp_out[2];
+  const float* q_norm[2];
+  const float* k_norm[2];
+} mmdit_double_w_t;
+
+/* Single-stream block weights.  mod: D -> 3D (shift, scale, gate).
+ * lin1: D -> 3D + D_mlp (q | k | v | mlp).  lin2: D + D_mlp -> D over
+ * [attention output | GELU-tanh(mlp)]. */
+typedef struct {
+  mmdit_linear_t mod, lin1, lin2;
+  const float* q_norm;
+  const float* k_norm;
+} mmdit_single_w_t;
+
+/* Whole-step weights.  time1: t_dim -> D, time2: D -> D (SiLU between);
+ * img_in: C_lat -> D; final_mod: D -> 2D (shift, scale); final: D -> C_lat. */
+typedef struct {
+  mmdit_linear_t time1, time2, img_in, final_mod, final;
+  const mmdit_double_w_t* doubles; /* host array of n_double */
+  int n_double;
+  const mmdit_single_w_t* singles; /* host array of n_single */
+  int n_single;
+} mmdit_step_w_t;
+
+/* ------------------------------------------------------------ utilities */
+const char* mmdit_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * the current device.  Returns MMDIT_ERR_TIMEOUT if a kernel abandoned a
+ * bounded wait since the last call, MMDIT_ERR_CUDA on a sticky CUDA error. */
+int mmdit_sync_status(void* stream);
+
+/* Number of kernels this library has launched in this process. */
+long long mmdit_launch_count(void);
+
+/* Workspace bytes the named operation needs for `shape` (vec given, i.e.
+ * the block computes its own modulation).
+ * op: MMDIT_OP_DOUBLE, MMDIT_OP_SINGLE or MMDIT_OP_ATTENTION. */
+#define MMDIT_OP_DOUBLE 1
+#define MMDIT_OP_SINGLE 2
+#define MMDIT_OP_ATTENTION 3
+int mmdit_workspace_size(const mmdit_shape_t* shape, int op, size_t* bytes);
+
+/* Workspace bytes of mmdit_step_fwd for n_double + n_single blocks
+ * (C_lat a multiple of 64, t_dim a multiple of 16). */
+int mmdit_step_workspace_size(const mmdit_shape_t* shape, int n_double, int n_single, size_t* bytes);
+
+/* ------------------------------------------------------------ RoPE */
+/* Position ids and rotation tables for 2D axial RoPE.
+ * The Luminal blog (section "What the compiler found on its own") describes
+ * RoPE as pairing each channel with a partner channel and combining the two
+ * with cosine and sine tables; it fixes nothing else.  Reading taken: text
+ * token i sits at (0, 0, 0); image
+ * token (h, w) at (0, h, w).  Channel pairs are adjacent, (2i, 2i+1); the
+ * first rope_axes[0]/2 pairs follow axis 0, the next rope_axes[1]/2 axis 1,
+ * the rest axis 2.  Pair i of axis a turns by pos_a * theta^(-2i/rope_axes[a]),
+ * computed in fp64 and rounded once to fp32.
+ * ids: device int32 [L, 3]; cos_, sin_: device fp32 [L, d_head/2]. */
+int mmdit_rope2d_build(const mmdit_shape_t* shape, int32_t* ids, float* cos_, float* sin_, void* stream);
+
+/* Rotates x in place: x device bf16 [B, L, H, d_head] with token row stride
+ * `row_stride` elements (>= H*d_head, multiple of 8):
+ * (x0, x1) -> (x0 c - x1 s, x0 s + x1 c) per pair, in fp32. */
+int rope2d_apply(const mmdit_shape_t* shape, const float* cos_, const float* sin_, void* x, int row_stride,
+                 void* stream);
+
+/* ------------------------------------------------------------ attention */
+/* Joint softmax attention over the concatenated [text; image] sequence of
+ * each sample, one softmax per (sample, head, query), scale 1/sqrt(d_head),
+ * no mask (Luminal blog: attention = scores, scale, max, exp, sum, divide).
+ * qkv: device bf16 [B, L, 3, H, d_head] with token row stride
+ * `qkv_row_stride` elements (>= 3*D, multiple of 8).
+ * q_norm / k_norm: device fp32 [d_head] gains; entry [0] applies to text
+ * tokens, [1] to image tokens (pass the same pointer twice for one stream).
+ * If q_norm[0] is NULL no RMSNorm is applied; if cos_ is NULL no RoPE.
+ * Otherwise q and k get RMSNorm (eps_rms) and then RoPE before the scores.
+ * out: device bf16 [B, L, H*d_head], token row stride out_row_stride.
+ * ws: device workspace of mmdit_workspace_size(MMDIT_OP_ATTENTION) bytes. */
+int joint_attention_fwd(const mmdit_shape_t* shape, const void* qkv, int qkv_row_stride, const float* const q_norm[2],
+                        const float* const k_norm[2], const float* cos_, const float* sin_, void* out,
+                        int out_row_stride, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ blocks */
+/* Double-stream block, in place on x_txt (device fp32 [B, L_txt, D]) and
+ * x_img (device fp32 [B, L_img, D]).  vec: device fp32 [B, D] conditioning
+ * vector; or pass vec = NULL and mod_precomputed = device fp32 [2, B, 6D]
+ * (stream, sample, chunk) already equal to mod.W SiLU(vec) + mod.b.
+ * Per stream: y = LN(x)(1 + scale1) + shift1; q, k, v = y Wqkv^T + b;
+ * q, k <- RMSNorm then RoPE; o = joint attention; x += gate1 (o Wp^T + bp);
+ * y2 = LN(x)(1 + scale2) + shift2; x += gate2 (GELU(y2 W1^T + b1) W2^T + b2).
+ * cos_/sin_: tables from mmdit_rope2d_build. */
+int mmdit_double_block_fwd(const mmdit_shape_t* shape, const mmdit_double_w_t* w, const float* vec,
+                           const float* mod_precomputed, float* x_txt, float* x_img, const float* cos_,
+                           const float* sin_, void* ws, size_t ws_bytes, void* stream);
+
+/* Single-stream block, in place on x (device fp32 [B, L, D], text first).
+ * mod_precomputed, if used: device fp32 [B, 3D].
+ * y = LN(x)(1 + scale) + shift; [q k v m] = y W1^T + b1; q, k <- RMSNorm,
+ * RoPE; x += gate ([attention(q,k,v) | GELU(m)] W2^T + b2). */
+int mmdit_single_block_fwd(const mmdit_shape_t* shape, const mmdit_single_w_t* w, const float* vec,
+                           const float* mod_precomputed, float* x, const float* cos_, const float* sin_, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ step */
+/* One denoising step: vec = time2 SiLU(time1 sinusoid(1000 sigma) + b) + b;
+ * x_img = img_in(x_lat); the n_double double blocks on (x_txt_in, x_img);
+ * the n_single single blocks on [x_txt; x_img]; v = final(LN(x_img)(1 +
+ * scale) + shift); x_lat += (sigma_next - sigma) v.
+ * The sinusoid has t_dim/2 frequencies 10000^(-j/(t_dim/2)), order [cos | sin].
+ * x_lat: device fp32 [B, L_img, C_lat], updated in place.
+ * x_txt_in: device fp32 [B, L_txt, D], read only.
+ * v_out: device fp32 [B, L_img, C_lat] or NULL. */
+int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_txt_in,
+                   double sigma, double sigma_next, float* v_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Flow-matching Euler update (Luminal blog, "The AMD MI300X pipeline": the
+ * sampler integrates the latent in fp32): x[i] += (sigma_next - sigma) v[i].
+ * x: device fp32 [n]; v: device [n], v_dtype MMDIT_F32 or MMDIT_BF16.
+ * The step size is rounded once to fp32. */
+int euler_step(float* x, const void* v, int v_dtype, double sigma, double sigma_next, int64_t n, void* stream);
+
+/* ------------------------------------------------------------ int8 */
+/* Per-output-channel symmetric int8 quantiser (flux-amd-rocm BENCHMARKS.md:
+ * torchao Int8WeightOnlyConfig).  Reading: s_n = max_k |w_nk| / 127 in fp32
+ * (1 for an all-zero row); q = clamp(rint(w / s_n), -127, 127), division
+ * in fp32, ties to even.  w: device [N, K] of w_dtype (MMDIT_BF16 or
+ * MMDIT_F32); q: device int8 [N, K]; scale: device fp32 [N]. */
+int mmdit_quantize_w8(const void* w, int w_dtype, int N, int K, int8_t* q, float* scale, void* stream);
+
+/* ------------------------------------------------------------ pieces */
+/* Building blocks of the step, exported for tests and for callers that
+ * compose their own loop. */
+
+/* y = x W^T (+ b), x device bf16 [M, K]; epilogue:
+ *   MMDIT_EPI_BF16:        y device bf16 [M, N]
+ *   MMDIT_EPI_BF16_GELU:   y device bf16 [M, N], GELU-tanh applied
+ *   MMDIT_EPI_F32:         y device fp32 [M, N]
+ *   MMDIT_EPI_RESID:       y device fp32 [M, N] += gate[n] * (x W^T + b),
+ *                          gate device fp32 [N] (NULL = 1)
+ * Int8 weights when lin->scale != NULL (y = (x q^T) * scale + b); they are
+ * widened to bf16 (exactly) in `ws`, which then needs N*K*2 bytes.
+ * K a multiple of 64, N a multiple of 32. */
+#define MMDIT_EPI_BF16 0
+#define MMDIT_EPI_BF16_GELU 1
+#define MMDIT_EPI_F32 2
+#define MMDIT_EPI_RESID 3
+int mmdit_linear_fwd(const mmdit_linear_t* lin, int M, int N, int K, const void* x, void* y, int epilogue,
+                     const float* gate, void* ws, size_t ws_bytes, void* stream);
+
+/* y = LN(x)(1 + scale) + shift per row, x device fp32 [B, rows, D],
+ * shift/scale device fp32 with sample stride mod_stride elements,
+ * y device bf16 [B, rows, D]. */
+int mmdit_ln_modulate(const float* x, int B, int rows, int D, const float* shift, const float* scale,
+                      int64_t mod_stride, float eps, void* y, void* stream);
+
+/* y[b, n] = W act(x[b, :]) + bias, x device fp32 [B, K] (B <= 8),
+ * act 0 = identity, 1 = SiLU; y device fp32 [B, N]. */
+int mmdit_gemv(const mmdit_linear_t* lin, int B, int N, int K, const float* x, int act, float* y, void* stream);
+
+/* vec = time2(SiLU(time1(sinusoid(1000 sigma)))) for all B samples:
+ * device fp32 [B, D]; ws: device fp32 scratch of B*(t_dim + D) floats. */
+int mmdit_time_embed(const mmdit_shape_t* shape, const mmdit_linear_t* time1, const mmdit_linear_t* time2,
+                     double sigma, float* vec, float* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MMDIT_H_ */

@@ -1,0 +1,205 @@
+"""Block- and step-level parity of the CUDA path against the float64 oracle,
+through the C ABI: double- and single-stream blocks at small shapes (several
+tiles, ragged tails, batch 2), the zero-gate identity (bit-exact), the int8
+weight-only variant, a short full step, and Flux-sized blocks checked on
+sampled output rows."""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_image_mmdit_gb300 import api, synthetic as S, weights as Wt
+from oracle import mmdit_oracle as O
+from tests.gpu_common import (CONFIGS, FULL, REL_L2_INT8_SCHEME, api_shape, assert_close, check_status, f32,
+                              gpu_tables, host, need_gpu, oracle_shape, rel_l2, tables)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    need_gpu()
+    yield
+    check_status()
+
+
+def _zero_gates(mod_w, mod_b, n_chunks, gates):
+    D = mod_w.shape[0] // n_chunks
+    mod_w, mod_b = mod_w.copy(), mod_b.copy()
+    for g in gates:
+        mod_w[g * D:(g + 1) * D] = 0
+        mod_b[g * D:(g + 1) * D] = 0
+    return mod_w, mod_b
+
+
+def run_double(cfg, params, acts, i8=False):
+    shape = api_shape(cfg, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_BF16)
+    w = Wt.double_from_host(params)
+    if i8:
+        w = w.quantized()
+    _, cs, sn = gpu_tables(shape)
+    xt, xi = f32(acts["x_txt"]), f32(acts["x_img"])
+    ws = api.alloc_workspace(api.workspace_size(shape, api.MMDIT_OP_DOUBLE))
+    api.mmdit_double_block_fwd(shape, w, f32(acts["vec"]), None, xt, xi, cs, sn, ws)
+    return host(xt), host(xi), w
+
+
+def run_single(cfg, params, x, vec, i8=False):
+    shape = api_shape(cfg, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_BF16)
+    w = Wt.single_from_host(params)
+    if i8:
+        w = w.quantized()
+    _, cs, sn = gpu_tables(shape)
+    xg = f32(x)
+    ws = api.alloc_workspace(api.workspace_size(shape, api.MMDIT_OP_SINGLE))
+    api.mmdit_single_block_fwd(shape, w, f32(vec), None, xg, cs, sn, ws)
+    return host(xg), w
+
+
+def _dequantised_double(params, wq):
+    out = {}
+    for i, s in enumerate(("txt", "img")):
+        d = dict(params[s])
+        for name in ("mod", "qkv", "proj", "mlp_in", "mlp_out"):
+            lin = getattr(wq, name)[i]
+            d[name + "_w"] = O.dequantize_w8(lin.w.cpu().numpy(), lin.scale.cpu().numpy())
+        out[s] = d
+    return out
+
+
+# ------------------------------------------------------------------ double block
+@pytest.mark.parametrize("name", ["c1", "d128", "ragged", "tail"])
+def test_double_block(name):
+    cfg = CONFIGS[name]
+    sh = oracle_shape(cfg)
+    p = S.double_block_params(f"db.{name}", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    a = S.activations(cfg["B"], cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, _ = run_double(cfg, p, a)
+    c, s = tables(cfg)
+    rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s)
+    if cfg["L_txt"]:
+        assert_close(gt, rt, what=f"double {name} x_txt")
+    assert_close(gi, ri, what=f"double {name} x_img")
+
+
+@pytest.mark.parametrize("name", ["c1", "d128", "ragged", "tail"])
+def test_single_block(name):
+    cfg = CONFIGS[name]
+    sh = oracle_shape(cfg)
+    p = S.single_block_params(f"sb.{name}", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    x = S.normal_f32("sb.x", (cfg["B"], sh.L, cfg["D"]))
+    vec = S.normal_f32("sb.vec", (cfg["B"], cfg["D"]))
+    g, _ = run_single(cfg, p, x, vec)
+    c, s = tables(cfg)
+    assert_close(g, O.single_block(x, vec, p, sh, c, s), what=f"single {name}")
+
+
+def test_zero_gates_identity_bit_exact():
+    cfg = CONFIGS["d128"]
+    sh = oracle_shape(cfg)
+    p = S.double_block_params("zg", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    for st in p.values():
+        st["mod_w"], st["mod_b"] = _zero_gates(st["mod_w"], st["mod_b"], 6, (2, 5))
+    a = S.activations(cfg["B"], cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, _ = run_double(cfg, p, a)
+    assert np.array_equal(gt, a["x_txt"]) and np.array_equal(gi, a["x_img"])
+    q = S.single_block_params("zg1", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    q["mod_w"], q["mod_b"] = _zero_gates(q["mod_w"], q["mod_b"], 3, (2,))
+    x = np.concatenate([a["x_txt"], a["x_img"]], axis=1)
+    g, _ = run_single(cfg, q, x, a["vec"])
+    assert np.array_equal(g, x)
+
+
+# ------------------------------------------------------------------ int8 weight-only
+def test_double_block_int8():
+    cfg = CONFIGS["d128"]
+    sh = oracle_shape(cfg)
+    p = S.double_block_params("i8", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    a = S.activations(cfg["B"], cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, wq = run_double(cfg, p, a, i8=True)
+    c, s = tables(cfg)
+    rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], _dequantised_double(p, wq), sh, c, s)
+    assert_close(gt, rt, what="int8 double x_txt vs dequantised")
+    assert_close(gi, ri, what="int8 double x_img vs dequantised")
+    bt, bi = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s)
+    # the scheme itself: the residual update against the bf16-weight block
+    assert rel_l2(gi - a["x_img"], bi - a["x_img"]) <= REL_L2_INT8_SCHEME
+    assert rel_l2(gt - a["x_txt"], bt - a["x_txt"]) <= REL_L2_INT8_SCHEME
+
+
+def test_single_block_int8():
+    cfg = CONFIGS["tail"]
+    sh = oracle_shape(cfg)
+    p = S.single_block_params("i8s", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    x = S.normal_f32("i8s.x", (1, sh.L, cfg["D"]))
+    vec = S.normal_f32("i8s.vec", (1, cfg["D"]))
+    g, wq = run_single(cfg, p, x, vec, i8=True)
+    c, s = tables(cfg)
+    pd = dict(p)
+    for name in ("mod", "lin1", "lin2"):
+        lin = getattr(wq, name)
+        pd[name + "_w"] = O.dequantize_w8(lin.w.cpu().numpy(), lin.scale.cpu().numpy())
+    assert_close(g, O.single_block(x, vec, pd, sh, c, s), what="int8 single vs dequantised")
+    ref = O.single_block(x, vec, p, sh, c, s)
+    assert rel_l2(g - x, ref - x) <= REL_L2_INT8_SCHEME
+
+
+# ------------------------------------------------------------------ whole step
+@pytest.mark.parametrize("i8", [False, True])
+def test_step_small(i8):
+    cfg = dict(CONFIGS["d128"])
+    cfg["B"] = 2
+    sh = oracle_shape(cfg)
+    sh.C_lat, sh.t_dim = 64, 256
+    W = S.embed_params(cfg["D"], sh.C_lat, sh.t_dim, seed=3)
+    W["double"] = [S.double_block_params(f"st.d{i}", cfg["D"], cfg["d_head"], cfg["D_mlp"]) for i in range(2)]
+    W["single"] = [S.single_block_params(f"st.s{i}", cfg["D"], cfg["d_head"], cfg["D_mlp"]) for i in range(2)]
+    x_lat = S.normal_f32("st.lat", (cfg["B"], sh.L_img, sh.C_lat))
+    x_txt = S.normal_f32("st.txt", (cfg["B"], cfg["L_txt"], cfg["D"]))
+    sig = O.sigma_schedule(50, O.shift_mu(sh.L_img))
+    shape = api_shape(cfg, C_lat=sh.C_lat, t_dim=sh.t_dim, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_BF16)
+    w = Wt.step_from_host(W)
+    if i8:
+        w = w.quantized()
+    ws = api.alloc_workspace(api.step_workspace_size(shape, 2, 2))
+    xl = f32(x_lat)
+    v = torch.empty_like(xl)
+    api.mmdit_step_fwd(shape, w, xl, f32(x_txt), sig[0], sig[1], v, ws)
+    ref_x, ref_v = O.denoise_step(x_lat, x_txt, sig[0], sig[1], W, sh)
+    tol = REL_L2_INT8_SCHEME if i8 else 1e-2
+    assert rel_l2(host(v), ref_v) <= tol, rel_l2(host(v), ref_v)
+    assert_close(host(xl), ref_x, rel=tol, what="step x_lat")
+
+
+# ------------------------------------------------------------------ Flux-sized blocks, sampled rows
+def _sample_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.choice(n, size=k, replace=False)]))
+    return rows
+
+
+@pytest.mark.parametrize("name", ["c2"])
+def test_double_block_flux_sampled(name):
+    cfg = FULL[name]
+    sh = oracle_shape(cfg)
+    p = S.double_block_params(f"full.{name}", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    a = S.activations(1, cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, _ = run_double(cfg, p, a)
+    rt_rows = _sample_rows(cfg["L_txt"], 6, 1)
+    ri_rows = _sample_rows(sh.L_img, 10, 2)
+    c, s = tables(cfg)
+    rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows)
+    assert_close(gt[:, rt_rows], rt, what=f"{name} double x_txt rows")
+    assert_close(gi[:, ri_rows], ri, what=f"{name} double x_img rows")
+
+
+@pytest.mark.parametrize("name", ["c3"])
+def test_single_block_flux_sampled(name):
+    cfg = FULL[name]
+    sh = oracle_shape(cfg)
+    p = S.single_block_params(f"full.s.{name}", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    x = S.normal_f32("full.x", (1, sh.L, cfg["D"]))
+    vec = S.normal_f32("full.vec", (1, cfg["D"]))
+    g, _ = run_single(cfg, p, x, vec)
+    rows = _sample_rows(sh.L, 12, 3)
+    c, s = tables(cfg)
+    assert_close(g[:, rows], O.single_block(x, vec, p, sh, c, s, rows=rows), what=f"{name} single rows")

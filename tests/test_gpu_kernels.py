@@ -1,0 +1,213 @@
+"""Kernel-level parity of the CUDA path against the float64 oracle, called
+through the C ABI: RoPE tables (bit-exact), RoPE rotation, Euler, the int8
+quantiser (bit-exact), LN+modulate, the GEMV, the tcgen05 GEMM with every
+epilogue, and joint attention."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_image_mmdit_gb300 import api, synthetic as S
+from diffusion_transformer_image_mmdit_gb300.api import LinearDev
+from oracle import mmdit_oracle as O
+from tests.gpu_common import (CONFIGS, FULL, api_shape, assert_close, bf16, check_status, f32, gpu_tables, host,
+                              need_gpu, rel_l2, tables)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    need_gpu()
+    yield
+    check_status()
+
+
+# ------------------------------------------------------------------ RoPE
+@pytest.mark.parametrize("cfg", [CONFIGS["c1"], CONFIGS["d128"], CONFIGS["tail"], FULL["c3"], FULL["c4"]])
+def test_rope_tables_bit_exact(cfg):
+    shape = api_shape(cfg)
+    ids, cs, sn = gpu_tables(shape)
+    torch.cuda.synchronize()
+    ref_ids = O.rope_ids(cfg["L_txt"], cfg["grid_h"], cfg["grid_w"])
+    c, s = tables(cfg)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    gc, gs = cs.cpu().numpy(), sn.cpu().numpy()
+    mis_c = int((gc.view(np.uint32) != c.astype(np.float32).view(np.uint32)).sum())
+    mis_s = int((gs.view(np.uint32) != s.astype(np.float32).view(np.uint32)).sum())
+    assert mis_c == 0 and mis_s == 0, f"fp32 table entries differing: cos {mis_c}, sin {mis_s} of {gc.size}"
+
+
+@pytest.mark.parametrize("cfg", [CONFIGS["c1"], CONFIGS["d128"]])
+def test_rope_apply(cfg):
+    shape = api_shape(cfg)
+    _, cs, sn = gpu_tables(shape)
+    B, L, H, d = cfg["B"], api.seq_len(shape), cfg["H"], cfg["d_head"]
+    x = S.normal_bf16("ra.x", (B, L, H, d))
+    row_stride = H * d + 64  # a padded row
+    xp = np.zeros((B, L, row_stride))
+    xp[..., :H * d] = x.reshape(B, L, H * d)
+    xt = bf16(xp)
+    api.rope2d_apply(shape, cs, sn, xt, row_stride)
+    c, s = tables(cfg)
+    ref = O.rope_apply(x, c, s).reshape(B, L, H * d)
+    got = host(xt)
+    assert_close(got[..., :H * d], ref, what="rope2d_apply")
+    assert np.array_equal(got[..., H * d:], xp[..., H * d:]), "padding touched"
+
+
+# ------------------------------------------------------------------ Euler
+@pytest.mark.parametrize("n", [1, 7, 4096 + 3])
+@pytest.mark.parametrize("vdt", [torch.float32, torch.bfloat16])
+def test_euler(n, vdt):
+    x = S.normal_f32("eu.x", (n,))
+    v = S.normal_f32("eu.v", (n,)) if vdt == torch.float32 else S.normal_bf16("eu.v", (n,))
+    xt, vt = f32(x), f32(v).to(vdt)
+    sig = O.sigma_schedule(50, O.shift_mu(6889))
+    api.euler_step(xt, vt, sig[0], sig[1])
+    ref = O.euler_step(x, v, sig[0], sig[1])
+    assert np.abs(host(xt) - ref).max() <= 1e-6 * (1 + np.abs(ref).max())
+
+
+# ------------------------------------------------------------------ int8 quantiser
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_quantize_bit_exact(dt):
+    w = S.normal_bf16("qz.w", (70, 320), 0.02) if dt == torch.bfloat16 else S.normal_f32("qz.w", (70, 320), 0.02)
+    w[3] = 0.0
+    w[4, :6] = [127.0, 63.5, -0.5, 2.5, -2.5, 1.5]
+    w[4, 6:] = 0.0
+    wt = f32(w).to(dt)
+    q = torch.empty((70, 320), dtype=torch.int8, device="cuda")
+    s = torch.empty((70,), dtype=torch.float32, device="cuda")
+    api.mmdit_quantize_w8(wt, q, s)
+    rq, rs = O.quantize_w8(host(wt))
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+# ------------------------------------------------------------------ LN + modulate, GEMV
+@pytest.mark.parametrize("D", [256, 3072])
+def test_ln_modulate(D):
+    B, rows = 2, 37
+    x = S.normal_f32("ln.x", (B, rows, D)) * 2 + 0.5
+    mod = S.normal_f32("ln.m", (B, 3 * D)) * 0.3
+    xt, mt = f32(x), f32(mod)
+    y = torch.empty((B, rows, D), dtype=torch.bfloat16, device="cuda")
+    # shift at column 0, scale at column D of each sample's 3D-wide modulation row
+    api.mmdit_ln_modulate(xt, mt[:, :D], mt[:, D:2 * D], 3 * D, 1e-6, y)
+    ref = O.modulate(O.layer_norm(x, 1e-6), mod[:, None, :D], mod[:, None, D:2 * D])
+    assert_close(host(y), ref, what="ln_modulate")
+
+
+@pytest.mark.parametrize("i8", [False, True])
+@pytest.mark.parametrize("act", [0, 1])
+def test_gemv(i8, act):
+    B, N, K = 3, 1000, 3072
+    w, b = S.linear_params("gv", N, K)
+    x = S.normal_f32("gv.x", (B, K))
+    lin = LinearDev(bf16(w), f32(b))
+    wref = w
+    if i8:
+        lin = api.quantize_linear(lin)
+        wref = O.dequantize_w8(lin.w.cpu().numpy(), lin.scale.cpu().numpy())
+    y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+    api.mmdit_gemv(lin, f32(x), act, y)
+    ref = O.linear(O.silu(x) if act else x, wref, b)
+    assert_close(host(y), ref, rel=1e-4, what="gemv")
+
+
+# ------------------------------------------------------------------ GEMM
+GEMM_SHAPES = [(1, 256, 64), (100, 512, 320), (300, 768, 256), (257, 128, 1024), (129, 1056, 192)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("epi", ["bf16", "gelu", "f32", "resid"])
+def test_linear_epilogues(M, N, K, epi):
+    w, b = S.linear_params(f"gm{M}.{N}.{K}", N, K)
+    w = w * 10  # unit-scale outputs
+    w = S.round_bf16(w)
+    x = S.normal_bf16("gm.x", (M, K))
+    lin = LinearDev(bf16(w), f32(b))
+    ref = O.linear(x, w, b)
+    if epi in ("bf16", "gelu"):
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_BF16 if epi == "bf16" else api.MMDIT_EPI_BF16_GELU)
+        if epi == "gelu":
+            ref = O.gelu_tanh(ref)
+        assert_close(host(y), ref, what=f"gemm {epi}")
+    elif epi == "f32":
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_F32)
+        assert_close(host(y), ref, rel=1e-4, max_abs=1e-2, what="gemm f32")
+    else:
+        r0 = S.normal_f32("gm.r", (M, N))
+        gate = S.normal_f32("gm.g", (N,))
+        y = f32(r0)
+        api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_RESID, gate=f32(gate))
+        assert_close(host(y), r0 + gate * ref, rel=1e-4, max_abs=1e-2, what="gemm resid")
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 768, 256), (1, 256, 64)])
+def test_linear_int8(M, N, K):
+    w, b = S.linear_params("g8", N, K)
+    x = S.normal_bf16("g8.x", (M, K))
+    lin8 = api.quantize_linear(LinearDev(bf16(w), f32(b)))
+    ws = api.alloc_workspace(N * K * 2)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    api.mmdit_linear_fwd(lin8, bf16(x), y, api.MMDIT_EPI_F32, ws=ws)
+    wq = O.dequantize_w8(lin8.w.cpu().numpy(), lin8.scale.cpu().numpy())
+    assert_close(host(y), O.linear(x, wq, b), rel=1e-4, max_abs=1e-3, what="int8 gemm vs dequantised")
+    assert rel_l2(host(y), O.linear(x, w, b)) <= 3e-2
+
+
+def test_gemm_large_tiles_and_ragged():
+    """Several waves of persistent tiles, M tail of 9 rows, K = 3072."""
+    M, N, K = 128 * 20 + 9, 1024, 3072
+    w, b = S.linear_params("gbig", N, K)
+    x = S.normal_bf16("gbig.x", (M, K))
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    api.mmdit_linear_fwd(LinearDev(bf16(w), f32(b)), bf16(x), y, api.MMDIT_EPI_F32)
+    assert_close(host(y), O.linear(x, w, b), rel=1e-4, max_abs=1e-2, what="gemm large")
+
+
+# ------------------------------------------------------------------ attention
+@pytest.mark.parametrize("name", ["c1", "d128", "ragged", "tail"])
+@pytest.mark.parametrize("norm", [True, False])
+def test_joint_attention(name, norm):
+    cfg = CONFIGS[name]
+    shape = api_shape(cfg)
+    B, L, H, d, D = cfg["B"], api.seq_len(shape), cfg["H"], cfg["d_head"], cfg["D"]
+    Lt = cfg["L_txt"]
+    qkv = S.normal_bf16(f"at.{name}", (B, L, 3, H, d))
+    if not norm:
+        qkv[:, :, :2] *= 0.3  # keep raw scores moderate
+    g = [S.norm_gain(f"at.g{i}", d) for i in range(4)]
+    _, cs, sn = gpu_tables(shape)
+    row_stride = 3 * D
+    out_stride = D + 64
+    out = torch.zeros((B, L, out_stride), dtype=torch.bfloat16, device="cuda")
+    ws = api.alloc_workspace(api.workspace_size(shape, api.MMDIT_OP_ATTENTION))
+    qn = [f32(g[0]), f32(g[1])] if norm else None
+    kn = [f32(g[2]), f32(g[3])] if norm else None
+    api.joint_attention_fwd(shape, bf16(qkv.reshape(B, L, 3 * D)), row_stride, qn, kn, cs, sn, out, out_stride, ws)
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    if norm:
+        q = np.concatenate([O.rms_norm(q[:, :Lt], g[0], 1e-6), O.rms_norm(q[:, Lt:], g[1], 1e-6)], axis=1)
+        k = np.concatenate([O.rms_norm(k[:, :Lt], g[2], 1e-6), O.rms_norm(k[:, Lt:], g[3], 1e-6)], axis=1)
+    c, s = tables(cfg)
+    ref = O.attention(O.rope_apply(q, c, s), O.rope_apply(k, c, s), v).reshape(B, L, D)
+    got = host(out)
+    assert_close(got[..., :D], ref, what=f"attention {name}")
+    assert np.all(got[..., D:] == 0)
+
+
+def test_attention_single_key_returns_v():
+    cfg = dict(B=1, L_txt=0, grid_h=1, grid_w=1, D=256, H=2, d_head=128, D_mlp=256, rope_axes=(16, 56, 56))
+    shape = api_shape(cfg)
+    qkv = S.normal_bf16("one", (1, 1, 3, 2, 128))
+    out = torch.empty((1, 1, 256), dtype=torch.bfloat16, device="cuda")
+    ws = api.alloc_workspace(api.workspace_size(shape, api.MMDIT_OP_ATTENTION))
+    _, cs, sn = gpu_tables(shape)
+    api.joint_attention_fwd(shape, bf16(qkv.reshape(1, 1, 768)), 768, None, None, cs, sn, out, 256, ws)
+    assert np.array_equal(host(out).reshape(2, 128), qkv[0, 0, 2])
