@@ -1,0 +1,369 @@
+#!/usr/bin/env python3
+"""Benchmark of one MMDiT denoising step on GB300 (sm_103a kernels via the C ABI).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4|c5|c3|c2] [--impl ours|reference]
+
+One step = the whole hot path: timestep embedding, the modulation GEMVs of
+every block, img_in, 19 double-stream + 38 single-stream blocks, the final
+layer and the Euler update, on one batch of synthetic inputs resident in HBM.
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MMDiT block fwd ms & TFLOP/s (% bf16 tensor peak); ms per 1024² denoise step"
+
+FLUX = dict(D=3072, H=24, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56), C_lat=128, t_dim=256)
+CONFIGS = {
+    # full denoising step stack at 1328^2: 512 text + 83x83 image tokens, batch 1, bf16
+    "c4": dict(B=1, L_txt=512, grid_h=83, grid_w=83, n_double=19, n_single=38, int8=False, n_steps=50, **FLUX),
+    # int8 weight-only step at 1024^2, batch 4 (28-step schedule)
+    "c5": dict(B=4, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=True, n_steps=28, **FLUX),
+    # bf16 step at 1024^2, batch 1 (57 blocks, 512 + 4096 tokens)
+    "step1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=False, n_steps=50, **FLUX),
+}
+WORKLOAD_NAME = {
+    "c4": "full denoising step, 19 double + 38 single blocks, D=3072, 24x128 heads, MLP 12288, 512 text + 83x83 "
+          "image tokens (1328^2), batch 1, bf16, Euler update, step 0 of a 50-step shifted schedule",
+    "c5": "int8 weight-only denoising step, 19 double + 38 single blocks, 512 text + 64x64 image tokens (1024^2), "
+          "batch 4, step 0 of a 28-step shifted schedule",
+    "step1024": "bf16 denoising step, 19 double + 38 single blocks, 512 text + 64x64 image tokens (1024^2), batch 1",
+}
+
+
+def step_flops(c: dict) -> dict:
+    """Algorithmic FLOPs of one step: 2*M*N*K per linear, 4*L^2*D per joint attention."""
+    B, D, Dm, C, T = c["B"], c["D"], c["D_mlp"], c["C_lat"], c["t_dim"]
+    Lt, Li = c["L_txt"], c["grid_h"] * c["grid_w"]
+    L = Lt + Li
+    lin_double = 2 * L * (3 * D * D + D * D + 2 * D * Dm)
+    lin_single = 2 * L * (D * (3 * D + Dm) + (D + Dm) * D)
+    attn = 4 * L * L * D
+    blocks = c["n_double"] * (lin_double + attn) + c["n_single"] * (lin_single + attn)
+    small = 2 * (T * D + D * D) + c["n_double"] * 2 * 2 * D * 6 * D + c["n_single"] * 2 * D * 3 * D + 2 * D * 2 * D
+    io = 2 * Li * C * D * 2
+    gemm = B * (c["n_double"] * lin_double + c["n_single"] * lin_single + io)
+    return {"total": B * (blocks + io) + B * small, "gemm": gemm, "attention": B * (c["n_double"] + c["n_single"]) * attn,
+            "block_flops": 24 * L * D * D + 4 * L * L * D, "L": L}
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def summary(self) -> dict:
+        rows = getattr(self, "rows", [])
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------------ CPU baseline (the oracle)
+def cpu_baseline_sample(c: dict, seconds_hint: float = 15.0) -> dict:
+    """Times the float64 oracle on a bounded sample of the workload: one
+    double block at the workload's shape, outputs restricted to a few query
+    rows per stream (all keys and values are still computed)."""
+    import numpy as np
+    from oracle import mmdit_oracle as O
+    rng = np.random.default_rng(0)
+    D, Dm = c["D"], c["D_mlp"]
+    sh = O.Shape(B=1, L_txt=c["L_txt"], grid_h=c["grid_h"], grid_w=c["grid_w"], D=D, H=c["H"], d_head=c["d_head"],
+                 D_mlp=Dm, rope_axes=tuple(c["rope_axes"]))
+    L = sh.L
+
+    def lin(n, k):
+        return rng.standard_normal((n, k)) * 0.02, rng.standard_normal(n) * 0.02
+
+    wt = {}
+    for s in ("txt", "img"):
+        w = {}
+        for name, (n, k) in {"mod": (6 * D, D), "qkv": (3 * D, D), "proj": (D, D), "mlp_in": (Dm, D),
+                             "mlp_out": (D, Dm)}.items():
+            w[name + "_w"], w[name + "_b"] = lin(n, k)
+        w["q_norm"] = 1 + 0.02 * rng.standard_normal(c["d_head"])
+        w["k_norm"] = 1 + 0.02 * rng.standard_normal(c["d_head"])
+        wt[s] = w
+    x_txt = rng.standard_normal((1, sh.L_txt, D))
+    x_img = rng.standard_normal((1, sh.L_img, D))
+    vec = rng.standard_normal((1, D))
+    cs, sn = O.rope_tables(O.rope_ids(sh.L_txt, sh.grid_h, sh.grid_w), sh.rope_axes, sh.rope_theta)
+    rows_t, rows_i = np.arange(4), np.arange(0, sh.L_img, max(1, sh.L_img // 28))[:28]
+    t0 = time.perf_counter()
+    O.double_block(x_txt, x_img, vec, wt, sh, cs, sn, rows_txt=rows_t, rows_img=rows_i)
+    dt = time.perf_counter() - t0
+    r = len(rows_t) + len(rows_i)
+    flops = 2 * L * D * 3 * D + r * (4 * L * D + 2 * D * D + 4 * D * Dm) + 2 * 2 * D * 6 * D
+    return {"seconds": dt, "flops": flops,
+            "sample": f"oracle double block at the workload shape (L={L}), K/V for all {L} tokens, outputs for "
+                      f"{r} query rows ({flops / 1e9:.0f} GFLOP of fp64 work)"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, c: dict, rank: int, world: int, local_rank: int):
+    import torch
+    from diffusion_transformer_image_mmdit_gb300 import api, build, schedule
+    from diffusion_transformer_image_mmdit_gb300.weights import DeviceDraw
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(build.LIB):
+        build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    api._lib.load()
+    fl = step_flops(c)
+    shape = api.make_shape(B=c["B"], L_txt=c["L_txt"], grid_h=c["grid_h"], grid_w=c["grid_w"], D=c["D"], H=c["H"],
+                           d_head=c["d_head"], D_mlp=c["D_mlp"], rope_axes=c["rope_axes"],
+                           w_dtype=api.MMDIT_I8W if c["int8"] else api.MMDIT_BF16, C_lat=c["C_lat"],
+                           t_dim=c["t_dim"])
+    draw = DeviceDraw(seed=1000 + rank, device=dev)
+    w = draw.step(c["D"], c["d_head"], c["D_mlp"], c["C_lat"], c["t_dim"], c["n_double"], c["n_single"])
+    if c["int8"]:
+        wq = w.quantized()
+        del w
+        w = wq
+    torch.cuda.synchronize()
+    wstruct = w.struct()
+    Li = c["grid_h"] * c["grid_w"]
+    x_lat = draw.normal((c["B"], Li, c["C_lat"]))
+    x_txt = draw.normal((c["B"], c["L_txt"], c["D"]))
+    v = torch.empty_like(x_lat)
+    ws = api.alloc_workspace(api.step_workspace_size(shape, c["n_double"], c["n_single"]), device=dev)
+    sig = schedule.sigmas(c["n_steps"], schedule.mu_for_tokens(Li))
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j = i % c["n_steps"]
+        api.mmdit_step_fwd(shape, w, x_lat, x_txt, sig[j], sig[j + 1], v, ws, stream, step_struct=wstruct)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st = api.sync_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    # ---- timed region: K steps, inputs resident in HBM (weights 2x larger than L2 each step)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = api.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        e0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = api.launch_count() - n0
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    st = api.sync_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after timed region")
+
+    # ---- traced step: per-kernel durations with CUDA events on the launch stream
+    api.trace_begin(4096)
+    step(0)
+    n_tr = api.trace_end()
+    trace = api.trace_read(n_tr)
+    per = {}
+    for name, t_ms in trace:
+        a = per.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += t_ms
+    traced_total = sum(a[1] for a in per.values())
+    gemm_n, gemm_ms = per.get("gemm_bf16_tc", [0, 0.0])
+    attn_n, attn_ms = per.get("attn_fwd", [0, 0.0])
+    pk = peaks()
+    gemm_tflops = fl["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
+    attn_tflops = fl["attention"] / (attn_ms * 1e-3) / 1e12 if attn_ms else None
+
+    # ---- end to end through the public API: host buffers, copies inside the timed region
+    xl_h = torch.empty(x_lat.shape, dtype=torch.float32, pin_memory=True)
+    xt_h = torch.empty(x_txt.shape, dtype=torch.float32, pin_memory=True)
+    out_h = torch.empty(x_lat.shape, dtype=torch.float32, pin_memory=True)
+    xl_h.copy_(x_lat.cpu())
+    xt_h.copy_(x_txt.cpu())
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(args.steps):
+        x_lat.copy_(xl_h, non_blocking=True)
+        x_txt.copy_(xt_h, non_blocking=True)
+        step(i)
+        out_h.copy_(x_lat, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    res = {
+        "ms_step": ms_step, "launches_per_step": launches / args.steps, "clocks": clk.summary(),
+        "e2e_ms": e2e_ms, "h2d": xl_h.numel() * 4 + xt_h.numel() * 4, "d2h": out_h.numel() * 4,
+        "per_kernel": {k: {"launches": a[0], "ms": round(a[1], 4), "share": round(a[1] / traced_total, 4)}
+                       for k, a in sorted(per.items(), key=lambda kv: -kv[1][1])},
+        "gemm_tflops": gemm_tflops, "attn_tflops": attn_tflops, "gemm_launches": gemm_n, "gemm_ms": gemm_ms,
+        "attn_ms": attn_ms, "attn_launches": attn_n, "peaks": pk, "traced_ms": traced_total,
+        "peak_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+    }
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="c4", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    c = CONFIGS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    fl = step_flops(c)
+    cfg_json = {"workload": WORKLOAD_NAME[args.config], "model": "flux-shaped MMDiT (random init)",
+                "global_batch": c["B"] * max(world, args.gpus if world == 1 else world), "seq_len": fl["L"],
+                "parallelism": f"replicas x{world}", "l2": "inputs larger than L2: 23.7 GB of bf16 weights read per step"
+                if not c["int8"] else "inputs larger than L2: 11.8 GB of int8 weights read per step"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        samples = []
+        for i in range(args.warmup + args.steps):
+            r = cpu_baseline_sample(c)
+            if i >= args.warmup:
+                samples.append(r)
+        secs = sum(s["seconds"] for s in samples)
+        flops = sum(s["flops"] for s in samples)
+        value = flops / secs / 1e12
+        cores = os.cpu_count()
+        out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * fl["total"] / (value * 1e12),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic", "config": cfg_json,
+               "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": samples[0]["sample"]},
+               "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(out))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    r = run_ours(args, c, rank, world, local_rank)
+    if rank != 0:
+        return
+    pk = r["peaks"]
+    value = fl["total"] * world / (r["ms_step"] * 1e-3) / 1e12
+    e2e_value = fl["total"] * world / (r["e2e_ms"] * 1e-3) / 1e12
+    gemm_peak = pk["bf16_tflops_sustained"]
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8w-bf16" if c["int8"] else "bf16",
+        "data": "synthetic: seeded GPU draws, weights N(0,0.02), latents and text tokens N(0,1); random init",
+        "config": cfg_json,
+        "clocks": r["clocks"],
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 3)},
+        "gpu_launches": int(round(r["launches_per_step"] * args.steps)),
+        "roofline": {"kernel": "gemm_bf16_tc", "bound": "tensor",
+                     "achieved": round(r["gemm_tflops"], 1) if r["gemm_tflops"] else None, "peak": gemm_peak,
+                     "unit": "TFLOP/s",
+                     "frac": round(r["gemm_tflops"] / gemm_peak, 3) if r["gemm_tflops"] else None,
+                     "traffic": None,
+                     "peak_source": f"{pk['source']} bf16 sustained (kernel timed inside the step)",
+                     "launches_per_step": r["gemm_launches"],
+                     "flops_per_launch": round(fl["gemm"] / max(1, r["gemm_launches"]))},
+        "attention": {"achieved": round(r["attn_tflops"], 1) if r["attn_tflops"] else None, "unit": "TFLOP/s",
+                      "frac": round(r["attn_tflops"] / gemm_peak, 3) if r["attn_tflops"] else None,
+                      "launches_per_step": r["attn_launches"]},
+        "per_kernel": r["per_kernel"],
+        "block_tflop": round(fl["block_flops"] / 1e12, 4),
+        "step_tflop": round(fl["total"] / 1e12, 3),
+        "peak_mem_gb": round(r["peak_mem_gb"], 2),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        s = cpu_baseline_sample(c)
+        out["cpu_baseline"] = {"value": s["flops"] / s["seconds"] / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                               "kind": "oracle", "sample": s["sample"], "seconds": round(s["seconds"], 2)}
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -48,6 +48,10 @@ SIGNATURES = {
     "mmdit_status_string": (ctypes.c_char_p, [c_int]),
     "mmdit_sync_status": (c_int, [c_void_p]),
     "mmdit_launch_count": (c_longlong, []),
+    "mmdit_kernel_name": (ctypes.c_char_p, [c_int]),
+    "mmdit_trace_begin": (c_int, [c_int]),
+    "mmdit_trace_end": (c_int, [POINTER(c_int)]),
+    "mmdit_trace_read": (c_int, [POINTER(c_int), POINTER(c_float), c_int, POINTER(c_int)]),
     "mmdit_workspace_size": (c_int, [POINTER(Shape), c_int, POINTER(c_size_t)]),
     "mmdit_step_workspace_size": (c_int, [POINTER(Shape), c_int, c_int, POINTER(c_size_t)]),
     "mmdit_rope2d_build": (c_int, [POINTER(Shape), c_void_p, c_void_p, c_void_p, c_void_p]),

@@ -181,6 +181,26 @@ def launch_count() -> int:
     return int(_lib.load().mmdit_launch_count())
 
 
+def trace_begin(capacity: int) -> None:
+    call("mmdit_trace_begin", capacity)
+
+
+def trace_end() -> int:
+    n = ctypes.c_int(0)
+    call("mmdit_trace_end", ctypes.byref(n))
+    return n.value
+
+
+def trace_read(capacity: int):
+    """[(kernel name, milliseconds)] of the launches recorded by the trace."""
+    ids = (ctypes.c_int * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = ctypes.c_int(0)
+    call("mmdit_trace_read", ids, ms, capacity, ctypes.byref(n))
+    lib = _lib.load()
+    return [(lib.mmdit_kernel_name(ids[i]).decode(), float(ms[i])) for i in range(n.value)]
+
+
 def mmdit_rope2d_build(shape: Shape, ids: Optional[torch.Tensor], cos: torch.Tensor, sin: torch.Tensor, stream=None):
     call("mmdit_rope2d_build", ctypes.byref(shape), ptr(ids), ptr(cos), ptr(sin), stream_handle(stream))
 

@@ -286,8 +286,9 @@ cudaError_t launch_attn_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, cons
     attr_done[dev] = true;
   }
   dim3 grid(p.n_q_tiles, p.H, p.B);
+  launch_begin(KID_ATTENTION, s);
   attn_fwd_kernel<HD><<<grid, kAttnThreads, AttnSmem<HD>::total, s>>>(tmQK, tmV, p);
-  count_launch();
+  launch_end(s);
   return cudaGetLastError();
 }
 

@@ -14,7 +14,39 @@ namespace mmdit {
 static __device__ unsigned g_status_word;
 static std::atomic<long long> g_launches{0};
 
-void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+// Launch trace: a pool of CUDA events created by mmdit_trace_begin; while it
+// is on, each launch records one event before and one after its kernel.
+struct Trace {
+  bool on = false;
+  int cap = 0, n = 0;
+  cudaEvent_t* ev = nullptr;  // 2 * cap
+  int* ids = nullptr;         // cap
+};
+static Trace g_trace;
+
+void launch_begin(int kernel_id, cudaStream_t s) {
+  if (g_trace.on && g_trace.n < g_trace.cap) {
+    g_trace.ids[g_trace.n] = kernel_id;
+    cudaEventRecord(g_trace.ev[2 * g_trace.n], s);
+  }
+}
+
+void launch_end(cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_trace.on && g_trace.n < g_trace.cap) {
+    cudaEventRecord(g_trace.ev[2 * g_trace.n + 1], s);
+    ++g_trace.n;
+  }
+}
+
+static void trace_free() {
+  if (g_trace.ev) {
+    for (int i = 0; i < 2 * g_trace.cap; ++i) cudaEventDestroy(g_trace.ev[i]);
+    delete[] g_trace.ev;
+    delete[] g_trace.ids;
+  }
+  g_trace = Trace();
+}
 
 static int current_device() {
   int dev = 0;
@@ -437,6 +469,52 @@ int mmdit_sync_status(void* stream) {
 }
 
 long long mmdit_launch_count(void) { return g_launches.load(); }
+
+const char* mmdit_kernel_name(int kernel_id) {
+  static const char* names[KID_COUNT] = {"gemm_bf16_tc",  "attn_fwd",  "ln_modulate", "gemv",
+                                         "sinusoid",      "rope_build", "rope_apply", "euler",
+                                         "quantize_w8",   "dequant_i8", "cast_bf16",  "attn_prep"};
+  return (kernel_id >= 0 && kernel_id < KID_COUNT) ? names[kernel_id] : "unknown";
+}
+
+int mmdit_trace_begin(int capacity) {
+  if (capacity < 1) return MMDIT_ERR_ARG;
+  trace_free();
+  g_trace.ev = new cudaEvent_t[2 * (size_t)capacity];
+  g_trace.ids = new int[capacity];
+  for (int i = 0; i < 2 * capacity; ++i) {
+    if (cudaEventCreate(&g_trace.ev[i]) != cudaSuccess) {
+      g_trace.cap = i / 2;
+      trace_free();
+      return MMDIT_ERR_CUDA;
+    }
+    g_trace.cap = (i + 1) / 2;
+  }
+  g_trace.cap = capacity;
+  g_trace.n = 0;
+  g_trace.on = true;
+  return MMDIT_OK;
+}
+
+int mmdit_trace_end(int* count) {
+  g_trace.on = false;
+  if (count) *count = g_trace.n;
+  return MMDIT_OK;
+}
+
+int mmdit_trace_read(int* kernel_ids, float* ms, int capacity, int* count) {
+  if (!kernel_ids || !ms || !count || capacity < 0) return MMDIT_ERR_ARG;
+  const int n = g_trace.n < capacity ? g_trace.n : capacity;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(g_trace.ev[2 * i + 1]) != cudaSuccess) return MMDIT_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, g_trace.ev[2 * i], g_trace.ev[2 * i + 1]) != cudaSuccess) return MMDIT_ERR_CUDA;
+    kernel_ids[i] = g_trace.ids[i];
+    ms[i] = t;
+  }
+  *count = n;
+  return MMDIT_OK;
+}
 
 int mmdit_workspace_size(const mmdit_shape_t* shape, int op, size_t* bytes) {
   if (!bytes) return MMDIT_ERR_ARG;

@@ -347,8 +347,9 @@ __global__ void attn_prep_kernel(const uint16_t* __restrict__ qkv, long long qkv
 cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
                                const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st) {
   if (D % 256 || D > 4096) return cudaErrorInvalidValue;
+  launch_begin(KID_LN_MODULATE, st);
   ln_mod_kernel<<<rows * n_seg, D / 8, 0, st>>>(x, x_seg_rows, rows, D, shift, scale, mod_stride, eps, y);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
@@ -365,69 +366,77 @@ cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float
   }
   const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
   const int blocks = (N + rows_per_cta - 1) / rows_per_cta;
+  launch_begin(KID_GEMV, st);
   if (i8)
     gemv_kernel<true><<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
   else
     gemv_kernel<false><<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st) {
   const int n = B * dim;
+  launch_begin(KID_SINUSOID, st);
   sinusoid_kernel<<<(n + 255) / 256, 256, 0, st>>>(t, B, dim, out);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rope_build(int L_txt, int grid_w, int L, const int axes[3], double theta, int32_t* ids, float* cs,
                               float* sn, cudaStream_t st) {
   const long long n = (long long)L * ((axes[0] + axes[1] + axes[2]) / 2);
+  launch_begin(KID_ROPE_BUILD, st);
   rope_build_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(L_txt, grid_w, L, axes[0], axes[1], axes[2], theta,
                                                                  ids, cs, sn);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rope_apply(uint16_t* x, long long rows, int L, int H, int d, int row_stride, const float* cs,
                               const float* sn, cudaStream_t st) {
   const long long n = rows * (H * d / 8);
+  launch_begin(KID_ROPE_APPLY, st);
   rope_apply_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(x, rows, L, H, d, row_stride, cs, sn);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long long n, cudaStream_t st) {
   const long long threads = (n + 3) / 4;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
+  launch_begin(KID_EULER, st);
   if (v_bf16)
     euler_bf16_kernel<<<blocks, 256, 0, st>>>(x, reinterpret_cast<const uint16_t*>(v), dt, n);
   else
     euler_f32_kernel<<<blocks, 256, 0, st>>>(x, reinterpret_cast<const float*>(v), dt, n);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const void* w, bool w_bf16, int N, int K, int8_t* q, float* scale, cudaStream_t st) {
+  launch_begin(KID_QUANTIZE, st);
   if (w_bf16)
     quantize_kernel<uint16_t><<<N, 256, 0, st>>>(reinterpret_cast<const uint16_t*>(w), K, q, scale);
   else
     quantize_kernel<float><<<N, 256, 0, st>>>(reinterpret_cast<const float*>(w), K, q, scale);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dequant_i8(const int8_t* q, uint16_t* out, long long n, cudaStream_t st) {
   const long long n16 = n / 16;
+  launch_begin(KID_DEQUANT, st);
   dequant_i8_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(q, out, n16);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cast_bf16(const float* x, uint16_t* y, long long n, cudaStream_t st) {
   const long long n4 = n / 4;
+  launch_begin(KID_CAST, st);
   cast_f32_bf16_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(x, y, n4);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 
@@ -437,13 +446,14 @@ cudaError_t launch_attn_prep(const uint16_t* qkv, long long qkv_ld, int B, int L
                              cudaStream_t st) {
   const long long warps = (long long)B * L * H;
   const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+  launch_begin(KID_ATTN_PREP, st);
   if (d == 128)
     attn_prep_kernel<128><<<blocks, 256, 0, st>>>(qkv, qkv_ld, B, L, L_txt, H, gq0, gq1, gk0, gk1, eps, cs, sn, qk,
                                                   vT, vT_ld);
   else
     attn_prep_kernel<64><<<blocks, 256, 0, st>>>(qkv, qkv_ld, B, L, L_txt, H, gq0, gq1, gk0, gk1, eps, cs, sn, qk, vT,
                                                  vT_ld);
-  count_launch();
+  launch_end(st);
   return cudaGetLastError();
 }
 

@@ -347,8 +347,9 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
     attr_done[dev] = true;
   }
   const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  launch_begin(KID_GEMM, s);
   gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(tmA, tmB, p);
-  count_launch();
+  launch_end(s);
   return cudaGetLastError();
 }
 

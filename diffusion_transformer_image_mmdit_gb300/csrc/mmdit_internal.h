@@ -74,7 +74,27 @@ struct AttnParams {
 
 // ----------------------------------------------------------------- host helpers
 unsigned* device_status_ptr();  // device address of the status word (current device)
-void count_launch(int n = 1);
+
+// Kernel ids reported by the launch trace.
+enum KernelId : int {
+  KID_GEMM = 0,
+  KID_ATTENTION,
+  KID_LN_MODULATE,
+  KID_GEMV,
+  KID_SINUSOID,
+  KID_ROPE_BUILD,
+  KID_ROPE_APPLY,
+  KID_EULER,
+  KID_QUANTIZE,
+  KID_DEQUANT,
+  KID_CAST,
+  KID_ATTN_PREP,
+  KID_COUNT
+};
+// Bracket every kernel launch: counts launches and, while a trace is on,
+// records a CUDA event on the launch stream before and after the kernel.
+void launch_begin(int kernel_id, cudaStream_t s);
+void launch_end(cudaStream_t s);
 
 // Encodes a 3D bf16 tensor map with a 64-element (128-byte) inner box and the
 // 128-byte swizzle: dims (inner, rows, batch), byte strides of rows and batch.

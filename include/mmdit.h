@@ -130,6 +130,17 @@ int mmdit_sync_status(void* stream);
 /* Number of kernels this library has launched in this process. */
 long long mmdit_launch_count(void);
 
+/* Launch trace.  mmdit_trace_begin creates 2*capacity CUDA events (call it
+ * outside stream capture) and turns tracing on: each of the next `capacity`
+ * kernel launches is bracketed by an event pair on its own stream.
+ * mmdit_trace_end turns it off and reports how many launches were recorded;
+ * mmdit_trace_read waits for them and returns each launch's kernel id and
+ * duration in milliseconds.  mmdit_kernel_name maps an id to a name. */
+int mmdit_trace_begin(int capacity);
+int mmdit_trace_end(int* count);
+int mmdit_trace_read(int* kernel_ids, float* ms, int capacity, int* count);
+const char* mmdit_kernel_name(int kernel_id);
+
 /* Workspace bytes the named operation needs for `shape` (vec given, i.e.
  * the block computes its own modulation).
  * op: MMDIT_OP_DOUBLE, MMDIT_OP_SINGLE or MMDIT_OP_ATTENTION. */

@@ -135,7 +135,8 @@ def test_linear_epilogues(M, N, K, epi):
         api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_BF16 if epi == "bf16" else api.MMDIT_EPI_BF16_GELU)
         if epi == "gelu":
             ref = O.gelu_tanh(ref)
-        assert_close(host(y), ref, what=f"gemm {epi}")
+        # bf16 output: one rounding of at most 2^-9 relative on top of fp32 accumulation
+        assert_close(host(y), ref, max_abs=2.0 ** -8 * max(1.0, np.abs(ref).max()), what=f"gemm {epi}")
     elif epi == "f32":
         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
         api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_F32)

@@ -1,0 +1,27 @@
+"""Host logic of the product path checked against the oracle on CPU: the
+sigma schedule, and the benchmark's FLOP accounting against the per-block
+formula 24 L D^2 + 4 L^2 D."""
+import numpy as np
+
+from diffusion_transformer_image_mmdit_gb300 import schedule
+from oracle import mmdit_oracle as O
+
+
+def test_schedule_matches_oracle():
+    for n, tokens in ((50, 6889), (28, 4096), (4, 1024)):
+        got = np.array(schedule.sigmas(n, schedule.mu_for_tokens(tokens)))
+        ref = O.sigma_schedule(n, O.shift_mu(tokens))
+        assert np.abs(got - ref).max() < 1e-15
+    assert schedule.sigmas(4, 0.0) == [1.0, 0.75, 0.5, 0.25, 0.0]
+
+
+def test_bench_flop_accounting():
+    import bench
+    c4 = bench.step_flops(bench.CONFIGS["c4"])
+    L, D = 7401, 3072
+    per_block = 24 * L * D * D + 4 * L * L * D
+    assert c4["block_flops"] == per_block
+    assert abs(c4["total"] - 57 * per_block) / c4["total"] < 2e-3  # + img_in, final, modulation, timestep
+    assert abs(57 * per_block / 1e12 - 133.9) < 0.05
+    c5 = bench.step_flops(bench.CONFIGS["c5"])
+    assert abs(c5["total"] / 1e12 - 297.4) / 297.4 < 3e-3
