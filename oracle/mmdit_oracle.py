@@ -145,11 +145,14 @@ def rope_apply(x, cos, sin):
 
 # --------------------------------------------------------------------------
 # attention
-def attention(q, k, v):
+def attention(q, k, v, rnd=None):
     """Softmax attention per sample and head with no mask.
     q [B, Lq, H, d], k, v [B, Lk, H, d] -> [B, Lq, H, d].
     Scores = q k^T / sqrt(d); subtract the row max; exponentiate; divide by
-    the row sum; weight v."""
+    the row sum; weight v.
+
+    rnd (optional, precision model only): applied to the exponentials that
+    weight v, while the row sum keeps them unrounded."""
     B, Lq, H, d = q.shape
     out = np.empty((B, Lq, H, d))
     for b in range(B):
@@ -157,8 +160,11 @@ def attention(q, k, v):
             s = q[b, :, h, :] @ k[b, :, h, :].T / math.sqrt(d)
             s = s - s.max(axis=1, keepdims=True)
             p = np.exp(s)
-            p = p / p.sum(axis=1, keepdims=True)
-            out[b, :, h, :] = p @ v[b, :, h, :]
+            if rnd is None:
+                p = p / p.sum(axis=1, keepdims=True)
+                out[b, :, h, :] = p @ v[b, :, h, :]
+            else:
+                out[b, :, h, :] = (rnd(p) @ v[b, :, h, :]) / p.sum(axis=1, keepdims=True)
     return out
 
 
@@ -177,7 +183,11 @@ def _heads(x, H):
     return x.reshape(B, L, H, D // H)
 
 
-def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows_img=None):
+def _ident(x):
+    return x
+
+
+def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows_img=None, rnd=None):
     """Double-stream block.  x_txt [B, L_txt, D], x_img [B, L_img, D], vec
     [B, D]; wt['txt'] / wt['img'] hold each stream's weights.  Per stream:
     adaLN-Zero modulation from vec, LN+modulate, QKV linear, per-head RMSNorm
@@ -186,7 +196,13 @@ def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows
     residual, LN+modulate, GELU-tanh MLP with gated residual.
 
     rows_txt / rows_img (optional index arrays) restrict the outputs to those
-    query rows; keys and values always cover the whole sequence."""
+    query rows; keys and values always cover the whole sequence.
+
+    rnd (optional) is a precision model, not part of the definition: when
+    given, it is applied where a bf16 implementation stores a matmul operand
+    (LN+modulate outputs, q/k after RoPE, v, softmax weights, attention
+    output, MLP hidden).  Left as None the block is the plain definition."""
+    R = _ident if rnd is None else rnd
     H = sh.H
     streams = (("txt", x_txt, rows_txt, 0), ("img", x_img, rows_img, sh.L_txt))
     qs, ks, vs, mods = [], [], [], {}
@@ -194,44 +210,47 @@ def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows
         w = wt[name]
         sh1, sc1, g1, sh2, sc2, g2 = modulation(vec, w["mod_w"], w["mod_b"], 6)
         mods[name] = (sh1, sc1, g1, sh2, sc2, g2)
-        y = modulate(layer_norm(x, sh.eps_ln), sh1, sc1)
+        y = R(modulate(layer_norm(x, sh.eps_ln), sh1, sc1))
         qkv = linear(y, w["qkv_w"], w["qkv_b"])
         D = sh.D
         q = rms_norm(_heads(qkv[..., :D], H), w["q_norm"], sh.eps_rms)
         k = rms_norm(_heads(qkv[..., D:2 * D], H), w["k_norm"], sh.eps_rms)
-        v = _heads(qkv[..., 2 * D:], H)
+        v = R(_heads(qkv[..., 2 * D:], H))
         qs.append(q), ks.append(k), vs.append(v)
-    q = rope_apply(np.concatenate(qs, axis=1), cos, sin)
-    k = rope_apply(np.concatenate(ks, axis=1), cos, sin)
+    q = R(rope_apply(np.concatenate(qs, axis=1), cos, sin))
+    k = R(rope_apply(np.concatenate(ks, axis=1), cos, sin))
     v = np.concatenate(vs, axis=1)
     outs = []
     for name, x, rows, off in streams:
         w = wt[name]
         sh1, sc1, g1, sh2, sc2, g2 = mods[name]
         idx = np.arange(x.shape[1]) if rows is None else np.asarray(rows)
-        o = attention(q[:, off + idx], k, v).reshape(x.shape[0], len(idx), -1)
+        o = R(attention(q[:, off + idx], k, v, rnd).reshape(x.shape[0], len(idx), sh.D))
         xr = x[:, idx] + g1 * linear(o, w["proj_w"], w["proj_b"])
-        y2 = modulate(layer_norm(xr, sh.eps_ln), sh2, sc2)
-        xr = xr + g2 * linear(gelu_tanh(linear(y2, w["mlp_in_w"], w["mlp_in_b"])), w["mlp_out_w"], w["mlp_out_b"])
+        y2 = R(modulate(layer_norm(xr, sh.eps_ln), sh2, sc2))
+        hid = R(gelu_tanh(linear(y2, w["mlp_in_w"], w["mlp_in_b"])))
+        xr = xr + g2 * linear(hid, w["mlp_out_w"], w["mlp_out_b"])
         outs.append(xr)
     return outs[0], outs[1]
 
 
-def single_block(x, vec, w, sh: Shape, cos, sin, rows=None):
+def single_block(x, vec, w, sh: Shape, cos, sin, rows=None, rnd=None):
     """Single-stream block on x = [text; image] [B, L, D]: LN+modulate, one
     linear D -> 3D + D_mlp, RMSNorm of q and k, RoPE, joint attention in
     parallel with GELU-tanh on the MLP columns, one linear over the
-    concatenation [attention output | GELU(mlp)], gated residual."""
+    concatenation [attention output | GELU(mlp)], gated residual.
+    rnd: optional precision model, as in double_block."""
+    R = _ident if rnd is None else rnd
     D, H = sh.D, sh.H
     shift, scale, gate = modulation(vec, w["mod_w"], w["mod_b"], 3)
-    y = modulate(layer_norm(x, sh.eps_ln), shift, scale)
+    y = R(modulate(layer_norm(x, sh.eps_ln), shift, scale))
     h = linear(y, w["lin1_w"], w["lin1_b"])
-    q = rope_apply(rms_norm(_heads(h[..., :D], H), w["q_norm"], sh.eps_rms), cos, sin)
-    k = rope_apply(rms_norm(_heads(h[..., D:2 * D], H), w["k_norm"], sh.eps_rms), cos, sin)
-    v = _heads(h[..., 2 * D:3 * D], H)
+    q = R(rope_apply(rms_norm(_heads(h[..., :D], H), w["q_norm"], sh.eps_rms), cos, sin))
+    k = R(rope_apply(rms_norm(_heads(h[..., D:2 * D], H), w["k_norm"], sh.eps_rms), cos, sin))
+    v = R(_heads(h[..., 2 * D:3 * D], H))
     idx = np.arange(x.shape[1]) if rows is None else np.asarray(rows)
-    o = attention(q[:, idx], k, v).reshape(x.shape[0], len(idx), D)
-    cat = np.concatenate([o, gelu_tanh(h[:, idx, 3 * D:])], axis=-1)
+    o = R(attention(q[:, idx], k, v, rnd).reshape(x.shape[0], len(idx), D))
+    cat = np.concatenate([o, R(gelu_tanh(h[:, idx, 3 * D:]))], axis=-1)
     return x[:, idx] + gate * linear(cat, w["lin2_w"], w["lin2_b"])
 
 

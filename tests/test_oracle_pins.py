@@ -316,6 +316,20 @@ def _zero_gates(mod_w, mod_b, n_chunks, gate_chunks):
     return mod_w, mod_b
 
 
+def test_precision_hook_is_inert_by_default_and_bf16_sized():
+    """rnd=None is the plain definition; rnd=bf16 rounding moves the block
+    output by the size of one bf16 rounding (2^-9) carried through."""
+    sh = TINY
+    wt, a = _double_inputs(sh)
+    c, s = _tables(sh)
+    plain = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s)
+    ident = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s, rnd=lambda x: x)
+    assert rel(ident[1], plain[1]) < 1e-14  # only the softmax normalisation order differs
+    emu = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s, rnd=S.round_bf16)
+    r = rel(emu[1] - a["x_img"], plain[1] - a["x_img"])
+    assert 1e-4 < r < 2e-2
+
+
 def test_zero_gates_make_blocks_identity():
     sh = TINY
     wt, a = _double_inputs(sh)
