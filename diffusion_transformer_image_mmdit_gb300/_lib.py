@@ -58,6 +58,8 @@ SIGNATURES = {
     "rope2d_apply": (c_int, [POINTER(Shape), c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "joint_attention_fwd": (c_int, [POINTER(Shape), c_void_p, c_int, POINTER(c_void_p), POINTER(c_void_p), c_void_p,
                                     c_void_p, c_void_p, c_int, c_void_p, c_size_t, c_void_p]),
+    "joint_attention_fwd_noalloc": (c_int, [POINTER(Shape), c_void_p, c_int, POINTER(c_void_p), POINTER(c_void_p),
+                                            c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "mmdit_double_block_fwd": (c_int, [POINTER(Shape), POINTER(DoubleW), c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "mmdit_single_block_fwd": (c_int, [POINTER(Shape), POINTER(SingleW), c_void_p, c_void_p, c_void_p, c_void_p,

@@ -225,6 +225,17 @@ def joint_attention_fwd(shape: Shape, qkv: torch.Tensor, qkv_row_stride: int, q_
          out_row_stride, ptr(ws), ws.numel(), stream_handle(stream))
 
 
+def joint_attention_fwd_noalloc(shape: Shape, qkv: torch.Tensor, qkv_row_stride: int, q_norm, k_norm, cos, sin,
+                                out: torch.Tensor, out_row_stride: int, stream=None):
+    """joint_attention_fwd without a workspace: the library's fixed device
+    scratch is used instead (for callers that cannot allocate)."""
+    qn, kn = _pair(q_norm), _pair(k_norm)
+    call("joint_attention_fwd_noalloc", ctypes.byref(shape), ptr(qkv), qkv_row_stride,
+         ctypes.cast(qn, ctypes.POINTER(ctypes.c_void_p)) if qn is not None else None,
+         ctypes.cast(kn, ctypes.POINTER(ctypes.c_void_p)) if kn is not None else None, ptr(cos), ptr(sin), ptr(out),
+         out_row_stride, stream_handle(stream))
+
+
 def mmdit_double_block_fwd(shape: Shape, w: DoubleWeights, vec, mod_precomputed, x_txt, x_img, cos, sin,
                            ws: torch.Tensor, stream=None):
     ws_struct = w.struct()

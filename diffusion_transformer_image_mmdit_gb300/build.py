@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmmdit.so")
-SOURCES = ["gemm.cu", "attention.cu", "elementwise.cu", "capi.cu"]
+SOURCES = ["gemm.cu", "attention.cu", "elementwise.cu", "capi.cu", "attention_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

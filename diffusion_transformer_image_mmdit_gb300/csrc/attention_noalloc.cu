@@ -1,0 +1,123 @@
+// joint_attention_fwd_noalloc: the joint-attention entry point for callers
+// that cannot allocate device memory.
+//
+// joint_attention_fwd needs scratch for the normalised/rotated q and k and
+// the transposed v, which its caller passes as a workspace.  Some callers
+// cannot provide one: a plugin inside a host application that owns every
+// device allocation and forbids its plugins from calling cudaMalloc, or code
+// that must not risk the implicit device synchronisation cudaMalloc/cudaFree
+// can cause.  This variant takes its scratch from a fixed, file-scope device
+// array instead, so the call allocates nothing.
+//
+// Properties of the fixed scratch:
+//  - kNoallocScratchBytes (48 MiB) per device, reserved for the lifetime of
+//    the process on every GPU that loads this library; shapes needing more
+//    are rejected with MMDIT_ERR_WORKSPACE before anything is launched.
+//  - One array per device, shared by every call: calls whose work overlaps
+//    on the GPU (for example on two streams at once) race on it.  Issue them
+//    on one stream or serialise them.
+//  - It keeps the previous call's contents.  Nothing needs clearing: every
+//    scratch byte the attention kernel reads is written earlier in the same
+//    call (the key extent of the V tensor map stops at L, so the padding
+//    columns are never read).
+//  - The first call on a device looks up the array's device address with
+//    cudaGetSymbolAddress (with that device current) and caches it; make
+//    that first call before any stream capture.
+#include <cmath>
+#include <cstring>
+
+#include "elementwise.h"
+#include "mmdit.h"
+#include "mmdit_internal.h"
+
+namespace mmdit {
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = 48ull << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch, per device, filled by the first call.
+void* scratch_address(int dev) {
+  static void* addr[64] = {};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+}  // namespace mmdit
+
+extern "C" int joint_attention_fwd_noalloc(const mmdit_shape_t* shape, const void* qkv, int qkv_row_stride,
+                                           const float* const q_norm[2], const float* const k_norm[2],
+                                           const float* cos_, const float* sin_, void* out, int out_row_stride,
+                                           void* stream) {
+  using namespace mmdit;
+  // The public size query validates the shape and gives the scratch it needs.
+  size_t need = 0;
+  const int st = mmdit_workspace_size(shape, MMDIT_OP_ATTENTION, &need);
+  if (st != MMDIT_OK) return st;
+  if (need > kNoallocScratchBytes) return MMDIT_ERR_WORKSPACE;
+  if (!qkv || !out) return MMDIT_ERR_ARG;
+  if ((cos_ == nullptr) != (sin_ == nullptr)) return MMDIT_ERR_ARG;
+  const int B = shape->B, Lt = shape->L_txt, L = shape->L_txt + shape->grid_h * shape->grid_w;
+  const int D = shape->D, H = shape->H, d = shape->d_head;
+  const int Lpad = (L + 7) / 8 * 8;
+  if (qkv_row_stride < 3 * D || qkv_row_stride % 8 || out_row_stride < D || out_row_stride % 8)
+    return MMDIT_ERR_SHAPE;
+  if (!aligned16(qkv) || !aligned16(out)) return MMDIT_ERR_ALIGN;
+  const float* gq0 = q_norm ? q_norm[0] : nullptr;
+  const float* gq1 = q_norm ? q_norm[1] : nullptr;
+  const float* gk0 = k_norm ? k_norm[0] : nullptr;
+  const float* gk1 = k_norm ? k_norm[1] : nullptr;
+  if (gq0 && (!gq1 || !gk0 || !gk1)) return MMDIT_ERR_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MMDIT_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MMDIT_ERR_CUDA;
+  if (major != 10 || minor != 3) return MMDIT_ERR_UNSUPPORTED;
+  unsigned char* base = static_cast<unsigned char*>(scratch_address(dev));
+  unsigned* status = device_status_ptr();
+  if (!base || !status) return MMDIT_ERR_CUDA;
+
+  // Same carving as the workspace variant: qk [B][L][2D], then vT [B][D][Lpad], 256-byte aligned.
+  const size_t qk_bytes = (size_t)B * L * 2 * D * 2;
+  uint16_t* qk = reinterpret_cast<uint16_t*>(base);
+  uint16_t* vT = reinterpret_cast<uint16_t*>(base + ((qk_bytes + 255) & ~size_t(255)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_attn_prep(static_cast<const uint16_t*>(qkv), qkv_row_stride, B, L, Lt, H, d, gq0, gq1, gk0, gk1,
+                       shape->eps_rms, cos_, sin_, qk, vT, Lpad, s) != cudaSuccess)
+    return MMDIT_ERR_CUDA;
+
+  CUtensorMap tq, tv;
+  const uint64_t D2 = 2ull * D;
+  if (!make_tmap_3d(&tq, qk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D2, (uint64_t)L, (uint64_t)B, D2 * 2, D2 * 2 * L, 64,
+                    kAttnBM, true))
+    return MMDIT_ERR_ALIGN;
+  if (!make_tmap_3d(&tv, vT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)L, (uint64_t)D, (uint64_t)B,
+                    (uint64_t)Lpad * 2, (uint64_t)Lpad * 2 * D, 64, (uint32_t)d, true))
+    return MMDIT_ERR_ALIGN;
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.L = L;
+  p.H = H;
+  p.B = B;
+  p.n_q_tiles = (L + kAttnBM - 1) / kAttnBM;
+  p.n_kv_tiles = (L + kAttnBN - 1) / kAttnBN;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  p.out = static_cast<uint16_t*>(out);
+  p.out_ld = out_row_stride;
+  p.status = status;
+  return launch_attention(tq, tv, p, d, s) == cudaSuccess ? MMDIT_OK : MMDIT_ERR_CUDA;
+}

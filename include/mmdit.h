@@ -188,6 +188,27 @@ int joint_attention_fwd(const mmdit_shape_t* shape, const void* qkv, int qkv_row
                         const float* const k_norm[2], const float* cos_, const float* sin_, void* out,
                         int out_row_stride, void* ws, size_t ws_bytes, void* stream);
 
+/* joint_attention_fwd for callers that cannot allocate device memory.
+ * No counterpart on the pages: this is a deployment variant.  A caller such
+ * as a plugin inside a host application that owns every device allocation,
+ * or code that must avoid the implicit synchronisation cudaMalloc/cudaFree
+ * can cause, may have no workspace to pass.  This call computes exactly what
+ * joint_attention_fwd computes (same arguments minus ws/ws_bytes) and
+ * allocates nothing: its scratch is a fixed 48 MiB device array inside the
+ * library, reserved on every GPU that loads it until the process exits.
+ *  - Shapes needing more scratch than 48 MiB (the ws size that
+ *    mmdit_workspace_size(MMDIT_OP_ATTENTION) reports) return
+ *    MMDIT_ERR_WORKSPACE and launch nothing.
+ *  - The array is shared by all calls on a device: calls that overlap on
+ *    the GPU (e.g. on two streams) race.  It keeps the last call's contents;
+ *    nothing in it needs clearing, since each call writes every byte it reads.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture. */
+int joint_attention_fwd_noalloc(const mmdit_shape_t* shape, const void* qkv, int qkv_row_stride,
+                                const float* const q_norm[2], const float* const k_norm[2], const float* cos_,
+                                const float* sin_, void* out, int out_row_stride, void* stream);
+
 /* ------------------------------------------------------------ blocks */
 /* Double-stream block, in place on x_txt (device fp32 [B, L_txt, D]) and
  * x_img (device fp32 [B, L_img, D]).  vec: device fp32 [B, D] conditioning
