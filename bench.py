@@ -32,6 +32,10 @@ CONFIGS = {
     "c5": dict(B=4, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=True, n_steps=28, **FLUX),
     # bf16 step at 1024^2, batch 1 (57 blocks, 512 + 4096 tokens)
     "step1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=False, n_steps=50, **FLUX),
+    # one double + one single block at 1024^2 (the block-pair workload; small case for full profiles)
+    "c3pair": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=1, n_single=1, int8=False, n_steps=50, **FLUX),
+    # one double block at 512^2 (512 + 1024 tokens)
+    "c2": dict(B=1, L_txt=512, grid_h=32, grid_w=32, n_double=1, n_single=0, int8=False, n_steps=50, **FLUX),
 }
 WORKLOAD_NAME = {
     "c4": "full denoising step, 19 double + 38 single blocks, D=3072, 24x128 heads, MLP 12288, 512 text + 83x83 "
@@ -39,6 +43,9 @@ WORKLOAD_NAME = {
     "c5": "int8 weight-only denoising step, 19 double + 38 single blocks, 512 text + 64x64 image tokens (1024^2), "
           "batch 4, step 0 of a 28-step shifted schedule",
     "step1024": "bf16 denoising step, 19 double + 38 single blocks, 512 text + 64x64 image tokens (1024^2), batch 1",
+    "c3pair": "one double + one single block (with embedding, img_in, final layer, Euler) at 512 text + 64x64 image "
+              "tokens, batch 1, bf16",
+    "c2": "one double block (with embedding, img_in, final layer, Euler) at 512 text + 32x32 image tokens, batch 1",
 }
 
 
@@ -56,6 +63,14 @@ def step_flops(c: dict) -> dict:
     gemm = B * (c["n_double"] * lin_double + c["n_single"] * lin_single + io)
     return {"total": B * (blocks + io) + B * small, "gemm": gemm, "attention": B * (c["n_double"] + c["n_single"]) * attn,
             "block_flops": 24 * L * D * D + 4 * L * L * D, "L": L}
+
+
+def step_weight_bytes(c: dict) -> float:
+    D, Dm, C, T = c["D"], c["D_mlp"], c["C_lat"], c["t_dim"]
+    per_double = 2 * (6 * D * D + 3 * D * D + D * D + 2 * D * Dm)
+    per_single = 3 * D * D + D * (3 * D + Dm) + (D + Dm) * D
+    n = c["n_double"] * per_double + c["n_single"] * per_single + T * D + D * D + 2 * C * D + 2 * D * D
+    return n * (1 if c["int8"] else 2)
 
 
 def peaks() -> dict:
@@ -295,8 +310,8 @@ def main():
     fl = step_flops(c)
     cfg_json = {"workload": WORKLOAD_NAME[args.config], "model": "flux-shaped MMDiT (random init)",
                 "global_batch": c["B"] * max(world, args.gpus if world == 1 else world), "seq_len": fl["L"],
-                "parallelism": f"replicas x{world}", "l2": "inputs larger than L2: 23.7 GB of bf16 weights read per step"
-                if not c["int8"] else "inputs larger than L2: 11.8 GB of int8 weights read per step"}
+                "parallelism": f"replicas x{world}",
+                "l2": f"inputs larger than L2: {step_weight_bytes(c) / 1e9:.2f} GB of weights read per step"}
 
     if args.impl == "reference":
         if rank != 0:
