@@ -13,62 +13,69 @@
 // (q at column h*d, k at column D + h*d), v transposed as [B][D][Lpad] so
 // that both MMAs read K-major operands.
 //
-// CTA = 128 queries of one (sample, head); 192 threads:
-//   warp 0      TMA: Q once, then K and V^T tiles of 128 keys, 2-stage ring.
-//   warp 1      TMEM (512 columns: S double buffer 2x128, O d columns) and
-//               the MMAs S = Q K^T (M=128, N=128, K=d) and O += P V
-//               (M=128, N=d, K=128) from one thread.
-//   warps 2-5   softmax, one query row per thread: tcgen05.ld of the S row,
-//               running max in the log2 domain, exp2 on the MUFU, P written
-//               to shared memory in the swizzled K-major layout, O rescaled
-//               in TMEM only when the running max grows by more than 2^8,
-//               final O / l and bf16 store.
+// MMA shapes: S = Q K^T is M=128, N=128 keys, K=d (both operands K-major
+// in shared memory, 128-byte swizzle); O += P V is M=128, N=d, K=128 keys
+// with P read from tensor memory.  The running max lives in the log2
+// domain; O is rescaled in TMEM only when the running max grows by more
+// than 2^8, which stays exact because the same reference is used for the
+// numerator and the row sum.
 #include "common.cuh"
 
 namespace mmdit {
 
 namespace {
 
-constexpr int kAttnThreads = 192;
 constexpr uint32_t kHalf = 128 * 128;  // one 128-row x 128-byte swizzled half tile
 constexpr float kRescaleThreshold = 8.0f;
 
+// Two query tiles per CTA (256 rows of one (sample, head)), K/V tiles shared.
+//   warp 0      TMA: both Q tiles once, then K and V^T tiles, 2-stage ring.
+//   warp 1      TMEM (S0 | S1 | O0 | O1, 128 columns each) and the MMAs, in
+//               the order S0(j), S1(j), then per j: PV0(j), S0(j+1), PV1(j),
+//               S1(j+1), so the tensor pipe works on one tile while the
+//               other tile's softmax runs.  P(j) is written by the softmax
+//               over the first 64 columns of S(j) as packed bf16 and read by
+//               the P V MMA straight from TMEM; S(j+1) reuses the columns
+//               only after PV(j), which precedes it in the MMA issue order.
+//   warps 2-5   softmax of tile 0; warps 6-9 softmax of tile 1 (one query
+//               row per thread): tree max/sum, exp2 on the MUFU for 3 of
+//               every 4 column pairs and a cubic on the FMA pipe for the
+//               4th, lazy O rescale in TMEM, final O / l and bf16 store.
+constexpr int kAttn2Threads = 320;
+
 template <int HD>
-struct AttnSmem {
-  static constexpr uint32_t Q = (HD / 64) * kHalf;
+struct Attn2Smem {
+  static constexpr uint32_t QT = (HD / 64) * kHalf;  // one 128-row Q tile
   static constexpr uint32_t K = (HD / 64) * kHalf;
-  static constexpr uint32_t V = 2 * HD * 128;  // two 64-key halves of HD rows x 128 B
-  static constexpr uint32_t P = 2 * kHalf;
-  static constexpr uint32_t total = 1024 + Q + 2 * K + 2 * V + P + 256;
+  static constexpr uint32_t V = 2 * HD * 128;
+  static constexpr uint32_t total = 1024 + 2 * QT + 2 * K + 2 * V + 256;
 };
 
 template <int HD>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttn2Threads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ AttnParams p) {
-  using SM = AttnSmem<HD>;
+  using SM = Attn2Smem<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = sQ + SM::Q;
+  uint8_t* sK = sQ + 2 * SM::QT;
   uint8_t* sV = sK + 2 * SM::K;
-  uint8_t* sP = sV + 2 * SM::V;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + SM::P);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * SM::V);
   const uint32_t q_full = smem_u32(bars + 0);
-  const uint32_t k_full0 = smem_u32(bars + 1);   // [2]
-  const uint32_t v_full0 = smem_u32(bars + 3);   // [2]
-  const uint32_t kv_empty0 = smem_u32(bars + 5); // [2]
-  const uint32_t s_full0 = smem_u32(bars + 7);   // [2]
-  const uint32_t s_empty0 = smem_u32(bars + 9);  // [2]
-  const uint32_t p_full = smem_u32(bars + 11);
-  const uint32_t pv_done = smem_u32(bars + 12);
+  const uint32_t k_full0 = smem_u32(bars + 1);    // [2] per stage
+  const uint32_t v_full0 = smem_u32(bars + 3);    // [2] per stage
+  const uint32_t kv_empty0 = smem_u32(bars + 5);  // [2] per stage
+  const uint32_t s_full0 = smem_u32(bars + 7);    // [2] per tile
+  const uint32_t p_full0 = smem_u32(bars + 9);    // [2] per tile
+  const uint32_t pv_done0 = smem_u32(bars + 11);  // [2] per tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int q0 = qt * kAttnBM;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int q0 = blockIdx.x * (2 * kAttnBM);
   const int D = p.H * HD;
   const int nkv = p.n_kv_tiles;
 
@@ -79,10 +86,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(v_full0 + 8 * i, 1);
       mbar_init(kv_empty0 + 8 * i, 1);
       mbar_init(s_full0 + 8 * i, 1);
-      mbar_init(s_empty0 + 8 * i, 4);
+      mbar_init(p_full0 + 8 * i, 4);
+      mbar_init(pv_done0 + 8 * i, 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -98,14 +104,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_O = tmem + 256;
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_expect_tx(q_full, SM::Q);
+      mbar_expect_tx(q_full, 2 * SM::QT);
 #pragma unroll
-      for (int hf = 0; hf < HD / 64; ++hf)
-        tma_load_3d(smem_u32(sQ + hf * kHalf), &tmQK, q_full, h * HD + hf * 64, q0, b);
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int hf = 0; hf < HD / 64; ++hf)
+          tma_load_3d(smem_u32(sQ + t * SM::QT + hf * kHalf), &tmQK, q_full, h * HD + hf * 64, q0 + t * kAttnBM, b);
       for (int j = 0; j < nkv; ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
@@ -126,75 +133,78 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(128, kAttnBN);
       const uint32_t idesc_o = idesc_bf16(128, HD);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, ST_TIMEOUT_MMA);
       const uint32_t aQ = smem_u32(sQ);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i & 1;
-        if (!mbar_wait(p_full, i & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
-        if (!mbar_wait(v_full0 + 8 * st, (i >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
-        tc_fence_after();
-        const uint32_t aP = smem_u32(sP);
-        const uint32_t bV = smem_u32(sV + st * SM::V);
-#pragma unroll
-        for (int k = 0; k < kAttnBN / 16; ++k) {
-          const int kh = k >> 2, off = (k & 3) * 32;
-          umma_bf16(tmem_O, sdesc_k128(aP + kh * kHalf + off), sdesc_k128(bV + kh * (HD * 128) + off), idesc_o,
-                    (i > 0 || k > 0) ? 1u : 0u);
-        }
-        umma_commit(pv_done);
-        umma_commit(kv_empty0 + 8 * st);
-        return true;
-      };
-      for (int j = 0; ok && j < nkv; ++j) {
+      auto issue_s = [&](int t, int j) -> bool {
         const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(k_full0 + 8 * st, ph, abort_flag, p.status, ST_TIMEOUT_MMA)) { ok = false; break; }
-        if (!mbar_wait(s_empty0 + 8 * st, ph ^ 1, abort_flag, p.status, ST_TIMEOUT_MMA)) { ok = false; break; }
+        if (t == 0 && !mbar_wait(k_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
         tc_fence_after();
         const uint32_t bK = smem_u32(sK + st * SM::K);
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const int hf = k >> 2, off = (k & 3) * 32;
-          umma_bf16(tmem + st * kAttnBN, sdesc_k128(aQ + hf * kHalf + off), sdesc_k128(bK + hf * kHalf + off),
-                    idesc_s, k > 0 ? 1u : 0u);
+          umma_bf16(tmem + t * 128, sdesc_k128(aQ + t * SM::QT + hf * kHalf + off),
+                    sdesc_k128(bK + hf * kHalf + off), idesc_s, k > 0 ? 1u : 0u);
         }
-        umma_commit(s_full0 + 8 * st);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        umma_commit(s_full0 + 8 * t);
+        return true;
+      };
+      auto issue_pv = [&](int t, int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(p_full0 + 8 * t, j & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
+        if (t == 0 && !mbar_wait(v_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
+        tc_fence_after();
+        const uint32_t bV = smem_u32(sV + st * SM::V);
+#pragma unroll
+        for (int k = 0; k < kAttnBN / 16; ++k) {
+          const int kh = k >> 2, off = (k & 3) * 32;
+          umma_bf16_ta(tmem + 256 + t * 128, tmem + t * 128 + k * 8, sdesc_k128(bV + kh * (HD * 128) + off), idesc_o,
+                       (j > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(pv_done0 + 8 * t);
+        if (t == 1) umma_commit(kv_empty0 + 8 * st);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, ST_TIMEOUT_MMA) && issue_s(0, 0) && issue_s(1, 0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        ok = issue_pv(0, j) && (j + 1 >= nkv || issue_s(0, j + 1)) && issue_pv(1, j) &&
+             (j + 1 >= nkv || issue_s(1, j + 1));
       }
-      if (ok) issue_pv(nkv - 1);
     }
   } else {
+    const int t = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + 256 + t * 128;
+    const uint32_t s_full = s_full0 + 8 * t, p_full = p_full0 + 8 * t, pv_done = pv_done0 + 8 * t;
     float m_run = -INFINITY, l_run = 0.f;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int st = j & 1;
-      if (!mbar_wait(s_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
+      if (!mbar_wait(s_full, j & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
       tc_fence_after();
-      float s[kAttnBN];
+      const int kv0 = j * kAttnBN;
+      const bool tail = kv0 + kAttnBN > p.L;
+      // pass 1: row max over the 128 scores, 64 columns at a time, 8 independent partial maxima
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < kAttnBN / 32; ++c) {
-        uint32_t raw[32];
-        MMDIT_TMEM_LD32(tmem + lane_base + st * kAttnBN + c * 32, raw);
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        uint32_t raw[64];
+        MMDIT_TMEM_LD32(tS + hlf * 64, raw);
+        MMDIT_TMEM_LD32(tS + hlf * 64 + 32, (raw + 32));
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
+        for (int c = 0; c < 64; ++c) {
+          float v = __uint_as_float(raw[c]);
+          if (tail && kv0 + hlf * 64 + c >= p.L) v = -INFINITY;
+          mx8[c & 7] = fmaxf(mx8[c & 7], v);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty0 + 8 * st);
-      const int kv0 = j * kAttnBN;
-      if (kv0 + kAttnBN > p.L) {
-#pragma unroll
-        for (int c = 0; c < kAttnBN; ++c)
-          if (kv0 + c >= p.L) s[c] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < kAttnBN; ++c) mx = fmaxf(mx, s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_run, mx * sl2);
       if (j > 0) {
         if (!mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
@@ -206,39 +216,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t raw[32];
-            MMDIT_TMEM_LD32(tmem_O + lane_base + c * 32, raw);
+            MMDIT_TMEM_LD32(tO + c * 32, raw);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
-            MMDIT_TMEM_ST32(tmem_O + lane_base + c * 32, raw);
+            MMDIT_TMEM_ST32(tO + c * 32, raw);
           }
           tmem_wait_st();
         }
         l_run *= alpha;
         m_run = m_new;
       }
-      float lsum = 0.f;
-      uint32_t pk[kAttnBN / 2];
+      // pass 2: exponentials, row sum (8 partial sums), bf16 P over the first 64 columns of S
+      float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kAttnBN / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(s[2 * c], sl2, -m_run));
-        const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m_run));
-        lsum += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      l_run += lsum;
-      // P row r into the two 64-key halves, 16-byte chunks swizzled by r & 7.
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        uint32_t raw[64];
+        MMDIT_TMEM_LD32(tS + hlf * 64, raw);
+        MMDIT_TMEM_LD32(tS + hlf * 64 + 32, (raw + 32));
+        tmem_wait_ld();
+        uint32_t pk[32];
 #pragma unroll
-      for (int kh = 0; kh < 2; ++kh) {
-        uint8_t* rowp = sP + kh * kHalf + r * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int base = kh * 32 + ch * 4;
-          *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(pk[base], pk[base + 1], pk[base + 2], pk[base + 3]);
+        for (int c = 0; c < 32; ++c) {
+          float v0 = __uint_as_float(raw[2 * c]), v1 = __uint_as_float(raw[2 * c + 1]);
+          if (tail) {
+            if (kv0 + hlf * 64 + 2 * c >= p.L) v0 = -INFINITY;
+            if (kv0 + hlf * 64 + 2 * c + 1 >= p.L) v1 = -INFINITY;
+          }
+          const float x0 = fmaf(v0, sl2, -m_run);
+          const float x1 = fmaf(v1, sl2, -m_run);
+          float p0, p1;
+          if ((c & 3) == 3) {
+            p0 = ex2_poly(x0);
+            p1 = ex2_poly(x1);
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
+          ls8[c & 7] += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
         }
+        MMDIT_TMEM_ST32(tS + hlf * 32, pk);
       }
-      fence_proxy_async_smem();
+      l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
@@ -246,12 +267,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (ok && mbar_wait(pv_done, (nkv - 1) & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) {
       tc_fence_after();
       const float inv_l = 1.0f / l_run;
-      const int row = q0 + r;
+      const int row = q0 + t * kAttnBM + r;
       uint16_t* dst = p.out + ((long long)b * p.L + row) * p.out_ld + h * HD;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t raw[32];
-        MMDIT_TMEM_LD32(tmem_O + lane_base + c * 32, raw);
+        MMDIT_TMEM_LD32(tO + c * 32, raw);
         tmem_wait_ld();
         float v[32];
 #pragma unroll
@@ -275,19 +296,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 template <int HD>
-cudaError_t launch_attn_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, cudaStream_t s) {
+cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)AttnSmem<HD>::total);
+                                         (int)Attn2Smem<HD>::total);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  dim3 grid(p.n_q_tiles, p.H, p.B);
+  dim3 grid((p.n_q_tiles + 1) / 2, p.H, p.B);
   launch_begin(KID_ATTENTION, s);
-  attn_fwd_kernel<HD><<<grid, kAttnThreads, AttnSmem<HD>::total, s>>>(tmQK, tmV, p);
+  attn_fwd_kernel<HD><<<grid, kAttn2Threads, Attn2Smem<HD>::total, s>>>(tmQK, tmV, p);
   launch_end(s);
   return cudaGetLastError();
 }
@@ -296,8 +317,8 @@ cudaError_t launch_attn_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, cons
 
 cudaError_t launch_attention(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, int d_head,
                              cudaStream_t s) {
-  if (d_head == 128) return launch_attn_hd<128>(tmQK, tmV, p, s);
-  return launch_attn_hd<64>(tmQK, tmV, p, s);
+  if (d_head == 128) return launch_attn2_hd<128>(tmQK, tmV, p, s);
+  return launch_attn2_hd<64>(tmQK, tmV, p, s);
 }
 
 }  // namespace mmdit

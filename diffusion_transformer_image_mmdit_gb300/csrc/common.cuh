@@ -128,6 +128,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16; A is read from tensor memory
+// (row i in lane i, two 16-bit elements per 32-bit column).
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -179,6 +190,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA pipe, for x <= 126 (inputs below -125 are clamped; the
+// result there is below 2^-124, negligible next to the 2^0 terms it is summed
+// with).  Cody-Waite style split x = n + f, n = round(x) obtained by adding
+// 1.5 * 2^23 (the integer lands in the low mantissa bits), |f| <= 1/2; 2^f
+// from a cubic whose coefficients were fitted here by least squares on the
+// relative error at 2000 Chebyshev nodes of [-1/2, 1/2] (max relative error
+// 7.7e-5, far below the 2^-9 of the bf16 weights it feeds); n is added to the
+// exponent field.
+__device__ __forceinline__ float ex2_poly(float x) {
+  x = fmaxf(x, -125.0f);
+  const float r = x + 12582912.0f;
+  const float n = r - 12582912.0f;
+  const float f = x - n;
+  const float p = fmaf(fmaf(fmaf(0.05508868396282196f, f, 0.24260404706001282f), f, 0.6932762265205383f), f,
+                       0.9999289512634277f);
+  return __int_as_float(__float_as_int(p) + ((__float_as_int(r) - 0x4B400000) << 23));
 }
 
 __device__ __forceinline__ float gelu_tanh_f(float x) {
