@@ -29,19 +29,28 @@ constexpr uint32_t kHalf = 128 * 128;  // one 128-row x 128-byte swizzled half t
 constexpr float kRescaleThreshold = 8.0f;
 
 // Two query tiles per CTA (256 rows of one (sample, head)), K/V tiles shared.
-//   warp 0      TMA: both Q tiles once, then K and V^T tiles, 2-stage ring.
-//   warp 1      TMEM (S0 | S1 | O0 | O1, 128 columns each) and the MMAs, in
+//   warps 0-3   softmax of tile 0; warps 4-7 softmax of tile 1 (one query
+//               row per thread, 216 registers each after setmaxnreg so a
+//               whole 128-score row stays in registers).
+//   warp 8      TMA: both Q tiles once, then K and V^T tiles, 2-stage ring.
+//   warp 9      TMEM (S0 | S1 | O0 | O1, 128 columns each) and the MMAs, in
 //               the order S0(j), S1(j), then per j: PV0(j), S0(j+1), PV1(j),
 //               S1(j+1), so the tensor pipe works on one tile while the
 //               other tile's softmax runs.  P(j) is written by the softmax
 //               over the first 64 columns of S(j) as packed bf16 and read by
 //               the P V MMA straight from TMEM; S(j+1) reuses the columns
 //               only after PV(j), which precedes it in the MMA issue order.
-//   warps 2-5   softmax of tile 0; warps 6-9 softmax of tile 1 (one query
-//               row per thread): tree max/sum, exp2 on the MUFU for 3 of
+//   warps 10-11 idle (they complete the third warpgroup, which gives its
+//               registers to the softmax warpgroups).
+// Softmax per KV tile: one TMEM load of the S row, tree max/sum, exp2 on the MUFU for 3 of
 //               every 4 column pairs and a cubic on the FMA pipe for the
 //               4th, lazy O rescale in TMEM, final O / l and bf16 store.
-constexpr int kAttn2Threads = 320;
+constexpr int kAttn2Threads = 384;
+// Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512);
+// warpgroup 2 drops to 72 and the two softmax warpgroups rise to 216:
+// 128 x 72 + 256 x 216 = 64512.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 72;
 
 template <int HD>
 struct Attn2Smem {
@@ -92,11 +101,11 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -105,73 +114,9 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      mbar_expect_tx(q_full, 2 * SM::QT);
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int hf = 0; hf < HD / 64; ++hf)
-          tma_load_3d(smem_u32(sQ + t * SM::QT + hf * kHalf), &tmQK, q_full, h * HD + hf * 64, q0 + t * kAttnBM, b);
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(kv_empty0 + 8 * st, ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) break;
-        mbar_expect_tx(k_full0 + 8 * st, SM::K);
-#pragma unroll
-        for (int hf = 0; hf < HD / 64; ++hf)
-          tma_load_3d(smem_u32(sK + st * SM::K + hf * kHalf), &tmQK, k_full0 + 8 * st, D + h * HD + hf * 64,
-                      j * kAttnBN, b);
-        mbar_expect_tx(v_full0 + 8 * st, SM::V);
-#pragma unroll
-        for (int kh = 0; kh < 2; ++kh)
-          tma_load_3d(smem_u32(sV + st * SM::V + kh * (HD * 128)), &tmV, v_full0 + 8 * st, j * kAttnBN + kh * 64,
-                      h * HD, b);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc_s = idesc_bf16(128, kAttnBN);
-      const uint32_t idesc_o = idesc_bf16(128, HD);
-      const uint32_t aQ = smem_u32(sQ);
-      auto issue_s = [&](int t, int j) -> bool {
-        const int st = j & 1;
-        if (t == 0 && !mbar_wait(k_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
-        tc_fence_after();
-        const uint32_t bK = smem_u32(sK + st * SM::K);
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const int hf = k >> 2, off = (k & 3) * 32;
-          umma_bf16(tmem + t * 128, sdesc_k128(aQ + t * SM::QT + hf * kHalf + off),
-                    sdesc_k128(bK + hf * kHalf + off), idesc_s, k > 0 ? 1u : 0u);
-        }
-        umma_commit(s_full0 + 8 * t);
-        return true;
-      };
-      auto issue_pv = [&](int t, int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(p_full0 + 8 * t, j & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
-        if (t == 0 && !mbar_wait(v_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
-        tc_fence_after();
-        const uint32_t bV = smem_u32(sV + st * SM::V);
-#pragma unroll
-        for (int k = 0; k < kAttnBN / 16; ++k) {
-          const int kh = k >> 2, off = (k & 3) * 32;
-          umma_bf16_ta(tmem + 256 + t * 128, tmem + t * 128 + k * 8, sdesc_k128(bV + kh * (HD * 128) + off), idesc_o,
-                       (j > 0 || k > 0) ? 1u : 0u);
-        }
-        umma_commit(pv_done0 + 8 * t);
-        if (t == 1) umma_commit(kv_empty0 + 8 * st);
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, ST_TIMEOUT_MMA) && issue_s(0, 0) && issue_s(1, 0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        ok = issue_pv(0, j) && (j + 1 >= nkv || issue_s(0, j + 1)) && issue_pv(1, j) &&
-             (j + 1 >= nkv || issue_s(1, j + 1));
-      }
-    }
-  } else {
-    const int t = (warp - 2) >> 2;
+  if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int t = warp >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -185,24 +130,25 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       if (!mbar_wait(s_full, j & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
       tc_fence_after();
       const int kv0 = j * kAttnBN;
-      const bool tail = kv0 + kAttnBN > p.L;
-      // pass 1: row max over the 128 scores, 64 columns at a time, 8 independent partial maxima
-      float mx8[8];
+      float sv[kAttnBN];
+      {
+        uint32_t raw[kAttnBN];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-#pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        uint32_t raw[64];
-        MMDIT_TMEM_LD32(tS + hlf * 64, raw);
-        MMDIT_TMEM_LD32(tS + hlf * 64 + 32, (raw + 32));
+        for (int c = 0; c < kAttnBN / 32; ++c) MMDIT_TMEM_LD32(tS + c * 32, (raw + c * 32));
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float v = __uint_as_float(raw[c]);
-          if (tail && kv0 + hlf * 64 + c >= p.L) v = -INFINITY;
-          mx8[c & 7] = fmaxf(mx8[c & 7], v);
-        }
+        for (int c = 0; c < kAttnBN; ++c) sv[c] = __uint_as_float(raw[c]);
       }
+      if (kv0 + kAttnBN > p.L) {
+#pragma unroll
+        for (int c = 0; c < kAttnBN; ++c)
+          if (kv0 + c >= p.L) sv[c] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+      for (int c = 8; c < kAttnBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_run, mx * sl2);
@@ -227,37 +173,26 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         l_run *= alpha;
         m_run = m_new;
       }
-      // pass 2: exponentials, row sum (8 partial sums), bf16 P over the first 64 columns of S
+      // exponentials, row sum (8 partial sums), bf16 P over the first 64 columns of S
       float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[kAttnBN / 2];
 #pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
-        uint32_t raw[64];
-        MMDIT_TMEM_LD32(tS + hlf * 64, raw);
-        MMDIT_TMEM_LD32(tS + hlf * 64 + 32, (raw + 32));
-        tmem_wait_ld();
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float v0 = __uint_as_float(raw[2 * c]), v1 = __uint_as_float(raw[2 * c + 1]);
-          if (tail) {
-            if (kv0 + hlf * 64 + 2 * c >= p.L) v0 = -INFINITY;
-            if (kv0 + hlf * 64 + 2 * c + 1 >= p.L) v1 = -INFINITY;
-          }
-          const float x0 = fmaf(v0, sl2, -m_run);
-          const float x1 = fmaf(v1, sl2, -m_run);
-          float p0, p1;
-          if ((c & 3) == 3) {
-            p0 = ex2_poly(x0);
-            p1 = ex2_poly(x1);
-          } else {
-            p0 = ex2_approx(x0);
-            p1 = ex2_approx(x1);
-          }
-          ls8[c & 7] += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
+      for (int c = 0; c < kAttnBN / 2; ++c) {
+        const float x0 = fmaf(sv[2 * c], sl2, -m_run);
+        const float x1 = fmaf(sv[2 * c + 1], sl2, -m_run);
+        float p0, p1;
+        if ((c & 3) == 3) {
+          p0 = ex2_poly(x0);
+          p1 = ex2_poly(x1);
+        } else {
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
         }
-        MMDIT_TMEM_ST32(tS + hlf * 32, pk);
+        ls8[c & 7] += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
       }
+      MMDIT_TMEM_ST32(tS, pk);
+      MMDIT_TMEM_ST32(tS + 32, (pk + 32));
       l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       tmem_wait_st();
       tc_fence_before();
@@ -286,10 +221,78 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         }
       }
     }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+    if (warp == 8) {
+      if (lane == 0) {
+        mbar_expect_tx(q_full, 2 * SM::QT);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int hf = 0; hf < HD / 64; ++hf)
+            tma_load_3d(smem_u32(sQ + t * SM::QT + hf * kHalf), &tmQK, q_full, h * HD + hf * 64, q0 + t * kAttnBM, b);
+        for (int j = 0; j < nkv; ++j) {
+          const int st = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!mbar_wait(kv_empty0 + 8 * st, ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) break;
+          mbar_expect_tx(k_full0 + 8 * st, SM::K);
+#pragma unroll
+          for (int hf = 0; hf < HD / 64; ++hf)
+            tma_load_3d(smem_u32(sK + st * SM::K + hf * kHalf), &tmQK, k_full0 + 8 * st, D + h * HD + hf * 64,
+                        j * kAttnBN, b);
+          mbar_expect_tx(v_full0 + 8 * st, SM::V);
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh)
+            tma_load_3d(smem_u32(sV + st * SM::V + kh * (HD * 128)), &tmV, v_full0 + 8 * st, j * kAttnBN + kh * 64,
+                        h * HD, b);
+        }
+      }
+    } else if (warp == 9) {
+      if (lane == 0) {
+        const uint32_t idesc_s = idesc_bf16(128, kAttnBN);
+        const uint32_t idesc_o = idesc_bf16(128, HD);
+        const uint32_t aQ = smem_u32(sQ);
+        auto issue_s = [&](int t, int j) -> bool {
+          const int st = j & 1;
+          if (t == 0 && !mbar_wait(k_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
+          tc_fence_after();
+          const uint32_t bK = smem_u32(sK + st * SM::K);
+#pragma unroll
+          for (int k = 0; k < HD / 16; ++k) {
+            const int hf = k >> 2, off = (k & 3) * 32;
+            umma_bf16(tmem + t * 128, sdesc_k128(aQ + t * SM::QT + hf * kHalf + off),
+                      sdesc_k128(bK + hf * kHalf + off), idesc_s, k > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full0 + 8 * t);
+          return true;
+        };
+        auto issue_pv = [&](int t, int j) -> bool {
+          const int st = j & 1;
+          if (!mbar_wait(p_full0 + 8 * t, j & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
+          if (t == 0 && !mbar_wait(v_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
+          tc_fence_after();
+          const uint32_t bV = smem_u32(sV + st * SM::V);
+#pragma unroll
+          for (int k = 0; k < kAttnBN / 16; ++k) {
+            const int kh = k >> 2, off = (k & 3) * 32;
+            umma_bf16_ta(tmem + 256 + t * 128, tmem + t * 128 + k * 8, sdesc_k128(bV + kh * (HD * 128) + off), idesc_o,
+                         (j > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(pv_done0 + 8 * t);
+          if (t == 1) umma_commit(kv_empty0 + 8 * st);
+          return true;
+        };
+        bool ok = mbar_wait(q_full, 0, abort_flag, p.status, ST_TIMEOUT_MMA) && issue_s(0, 0) && issue_s(1, 0);
+        for (int j = 0; ok && j < nkv; ++j) {
+          ok = issue_pv(0, j) && (j + 1 >= nkv || issue_s(0, j + 1)) && issue_pv(1, j) &&
+               (j + 1 >= nkv || issue_s(1, j + 1));
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

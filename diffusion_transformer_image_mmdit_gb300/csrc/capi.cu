@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <vector>
 
 #include "elementwise.h"
 #include "mmdit.h"
@@ -215,7 +216,11 @@ static int run_gemm(const void* A, long long a_ld, long long a_seg_rows, int M_s
   p.tiles_m = (M_seg + kBM - 1) / kBM;
   p.tiles_n = (N + kBN - 1) / kBN;
   p.num_tiles = p.tiles_m * p.tiles_n * n_seg;
-  p.group_m = 16;
+  // Raster: when the whole A operand fits comfortably in L2, sweep all M
+  // tiles for each N tile (A stays resident, W streams once); otherwise
+  // groups of 16 M tiles bound the A footprint of a wave.
+  const double a_bytes = (double)n_seg * M_seg * K * 2.0;
+  p.group_m = a_bytes <= 48.0 * 1024 * 1024 ? p.tiles_m * n_seg : 16;
   p.status = device_status_ptr();
   return cuda_status(launch_gemm(ta, tb, p, st));
 }
@@ -687,22 +692,23 @@ int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x
                          shape->t_dim, 0, th, st));
   MMDIT_CUDA(launch_gemv(w->time2.w, w->time2.scale != nullptr, w->time2.scale, w->time2.b, th, d.B, D, D, 1,
                          sw.vec, st));
-  // modulation vectors of every block (they depend on vec only)
+  // modulation vectors of every block and of the final layer (they depend on vec only): one batched launch
+  std::vector<GemvJob> jobs;
   float* mp = sw.mods;
   for (int i = 0; i < w->n_double; ++i)
     for (int s = 0; s < 2; ++s) {
       const mmdit_linear_t& l = w->doubles[i].mod[s];
-      MMDIT_CUDA(launch_gemv(l.w, l.scale != nullptr, l.scale, l.b, sw.vec, d.B, 6 * D, D, 1, mp, st));
+      jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 6 * D});
       mp += (size_t)d.B * 6 * D;
     }
   for (int i = 0; i < w->n_single; ++i) {
     const mmdit_linear_t& l = w->singles[i].mod;
-    MMDIT_CUDA(launch_gemv(l.w, l.scale != nullptr, l.scale, l.b, sw.vec, d.B, 3 * D, D, 1, mp, st));
+    jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 3 * D});
     mp += (size_t)d.B * 3 * D;
   }
   float* mod_final = mp;
-  MMDIT_CUDA(launch_gemv(w->final_mod.w, w->final_mod.scale != nullptr, w->final_mod.scale, w->final_mod.b, sw.vec,
-                         d.B, 2 * D, D, 1, mod_final, st));
+  jobs.push_back(GemvJob{w->final_mod.w, w->final_mod.scale, w->final_mod.b, mod_final, 2 * D});
+  MMDIT_CUDA(launch_gemv_batched(jobs.data(), (int)jobs.size(), i8, sw.vec, d.B, D, 1, st));
   // residual stream x = [text; image] per sample: text copied in, image from img_in
   if (d.Lt > 0)
     MMDIT_CUDA(cudaMemcpy2DAsync(sw.x, (size_t)d.L * D * 4, x_txt_in, (size_t)d.Lt * D * 4, (size_t)d.Lt * D * 4, d.B,

@@ -129,6 +129,75 @@ __global__ void __launch_bounds__(256) gemv_kernel(const void* __restrict__ W, c
   }
 }
 
+// Batched form: the jobs' output rows are numbered consecutively; each warp
+// finds the job of its row in the kernel-parameter table.
+constexpr int kMaxGemvJobs = 96;
+struct GemvBatch {
+  GemvJob job[kMaxGemvJobs];
+  int row0[kMaxGemvJobs + 1];
+  int n_jobs;
+};
+
+template <bool I8>
+__global__ void __launch_bounds__(256) gemv_batched_kernel(const __grid_constant__ GemvBatch jb,
+                                                           const float* __restrict__ x, int B, int K, int act) {
+  extern __shared__ float xs[];
+  for (int i = threadIdx.x; i < B * K; i += blockDim.x) {
+    const float t = x[i];
+    xs[i] = act ? silu_f(t) : t;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row_base = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp;
+  constexpr int EPV = I8 ? 16 : 8;
+  const int nvec = K / EPV;
+  int j = 0;
+#pragma unroll 1
+  for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
+    const int R = row_base + rr;
+    if (R >= jb.row0[jb.n_jobs]) break;
+    while (R >= jb.row0[j + 1]) ++j;
+    const GemvJob& job = jb.job[j];
+    const int n = R - jb.row0[j];
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint4* wr =
+        reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(job.W) + (long long)n * K * (I8 ? 1 : 2));
+#pragma unroll 4
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 wv = __ldg(wr + v);
+      float w[EPV];
+      const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
+      if (I8) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = (float)(int8_t)((u[e >> 2] >> (8 * (e & 3))) & 0xFF);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[2 * e] = bf16_lo(u[e]), w[2 * e + 1] = bf16_hi(u[e]);
+      }
+      const int k0 = v * EPV;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (b < B) {
+          const float* xb = xs + b * K + k0;
+          float a = acc[b];
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) a = fmaf(w[e], xb[e], a);
+          acc[b] = a;
+        }
+      }
+    }
+    const float sc = job.scale ? job.scale[n] : 1.0f;
+    const float bi = job.bias ? job.bias[n] : 0.0f;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (b < B) {
+        const float t = warp_sum(acc[b]);
+        if (lane == 0) job.out[(long long)b * job.N + n] = t * sc + bi;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ timestep sinusoid
 __global__ void sinusoid_kernel(double t, int B, int dim, float* __restrict__ out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -373,6 +442,43 @@ cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float
     gemv_kernel<false><<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
   launch_end(st);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const float* x, int B, int K, int act,
+                                cudaStream_t st) {
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    cudaFuncSetAttribute(gemv_batched_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaFuncSetAttribute(gemv_batched_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr_done[dev] = true;
+  }
+  const size_t smem = (size_t)B * K * sizeof(float);
+  for (int first = 0; first < n_jobs; first += kMaxGemvJobs) {
+    GemvBatch jb;
+    jb.n_jobs = n_jobs - first < kMaxGemvJobs ? n_jobs - first : kMaxGemvJobs;
+    jb.row0[0] = 0;
+    for (int i = 0; i < jb.n_jobs; ++i) {
+      jb.job[i] = jobs[first + i];
+      jb.row0[i + 1] = jb.row0[i] + jobs[first + i].N;
+    }
+    for (int i = jb.n_jobs; i < kMaxGemvJobs; ++i) {
+      jb.job[i] = GemvJob{nullptr, nullptr, nullptr, nullptr, 0};
+      jb.row0[i + 1] = jb.row0[jb.n_jobs];
+    }
+    const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
+    const int blocks = (jb.row0[jb.n_jobs] + rows_per_cta - 1) / rows_per_cta;
+    launch_begin(KID_GEMV, st);
+    if (i8)
+      gemv_batched_kernel<true><<<blocks, 256, smem, st>>>(jb, x, B, K, act);
+    else
+      gemv_batched_kernel<false><<<blocks, 256, smem, st>>>(jb, x, B, K, act);
+    launch_end(st);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st) {

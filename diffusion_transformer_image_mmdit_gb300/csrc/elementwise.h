@@ -11,6 +11,18 @@ cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, i
                                const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st);
 cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
                         int K, int act, float* y, cudaStream_t st);
+// Many GEMVs sharing one input vector set x [B, K] (after the activation):
+// job j computes out_j[b, n] = W_j act(x[b]) (* scale_j[n]) + bias_j[n] for
+// n < N_j.  All jobs use the same weight type.
+struct GemvJob {
+  const void* W;
+  const float* scale;
+  const float* bias;
+  float* out;
+  int N;
+};
+cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const float* x, int B, int K, int act,
+                                cudaStream_t st);
 cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st);
 cudaError_t launch_rope_build(int L_txt, int grid_w, int L, const int axes[3], double theta, int32_t* ids, float* cs,
                               float* sn, cudaStream_t st);
