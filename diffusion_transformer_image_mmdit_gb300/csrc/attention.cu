@@ -144,13 +144,15 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         for (int c = 0; c < kAttnBN; ++c)
           if (kv0 + c >= p.L) sv[c] = -INFINITY;
       }
+      // row max: 8 independent chains of three-input max
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-      for (int c = 8; c < kAttnBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int c = 8; c < kAttnBN; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       const float m_new = fmaxf(m_run, mx * sl2);
       if (j > 0) {
         if (!mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
@@ -173,27 +175,32 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         l_run *= alpha;
         m_run = m_new;
       }
-      // exponentials, row sum (8 partial sums), bf16 P over the first 64 columns of S
-      float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // exponentials on column pairs (f32x2 arithmetic), row sum in 4 packed
+      // partial sums, bf16 P over the first 64 columns of S
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_run, -m_run);
+      uint64_t ls2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ls2[i] = f2_pack(0.f, 0.f);
       uint32_t pk[kAttnBN / 2];
 #pragma unroll
       for (int c = 0; c < kAttnBN / 2; ++c) {
-        const float x0 = fmaf(sv[2 * c], sl2, -m_run);
-        const float x1 = fmaf(sv[2 * c + 1], sl2, -m_run);
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sl2x2, negm2), x0, x1);
+        uint64_t p2;
+        if ((c & 3) == 3)
+          p2 = ex2_poly2(x0, x1);
+        else
+          p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
+        ls2[c & 3] = f2_add(ls2[c & 3], p2);
         float p0, p1;
-        if ((c & 3) == 3) {
-          p0 = ex2_poly(x0);
-          p1 = ex2_poly(x1);
-        } else {
-          p0 = ex2_approx(x0);
-          p1 = ex2_approx(x1);
-        }
-        ls8[c & 7] += p0 + p1;
+        f2_unpack(p2, p0, p1);
         pk[c] = pack_bf16x2(p0, p1);
       }
+      float ls[2];
+      f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), ls[0], ls[1]);
       MMDIT_TMEM_ST32(tS, pk);
       MMDIT_TMEM_ST32(tS + 32, (pk + 32));
-      l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      l_run += ls[0] + ls[1];
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

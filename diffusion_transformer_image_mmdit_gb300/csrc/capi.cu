@@ -188,9 +188,17 @@ static bool lin_ok(const mmdit_linear_t& l, bool want_i8) {
 }
 
 // ----------------------------------------------------------------- GEMM
+// One problem of a GEMM launch: its tensor maps and epilogue parameters.
+struct GemmProblem {
+  CUtensorMap ta, tb;
+  GemmParams p;
+};
+
 // A row r of segment s at A + (s * a_seg_rows + r) * a_ld (bf16 elements).
-static int run_gemm(const void* A, long long a_ld, long long a_seg_rows, int M_seg, int n_seg, int K,
-                    const mmdit_linear_t& lin, int N, GemmParams p, uint16_t* wdeq, cudaStream_t st) {
+// Int8 weights are first widened into wdeq (exact), their scale goes to the epilogue.
+static int prepare_gemm(const void* A, long long a_ld, long long a_seg_rows, int M_seg, int n_seg, int K,
+                        const mmdit_linear_t& lin, int N, GemmParams p, uint16_t* wdeq, cudaStream_t st,
+                        GemmProblem& out) {
   if (K % kBK || N % 32 || M_seg < 1 || n_seg < 1) return MMDIT_ERR_SHAPE;
   if (!al16(A) || (a_ld * 2) % 16) return MMDIT_ERR_ALIGN;
   const void* W = lin.w;
@@ -202,11 +210,10 @@ static int run_gemm(const void* A, long long a_ld, long long a_seg_rows, int M_s
     p.wscale = lin.scale;
   }
   p.bias = lin.b;
-  CUtensorMap ta, tb;
-  if (!make_tmap_3d(&ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M_seg, (uint64_t)n_seg,
+  if (!make_tmap_3d(&out.ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M_seg, (uint64_t)n_seg,
                     (uint64_t)a_ld * 2, (uint64_t)a_seg_rows * a_ld * 2, kBK, kBM, true))
     return MMDIT_ERR_ALIGN;
-  if (!make_tmap_3d(&tb, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, 1, (uint64_t)K * 2,
+  if (!make_tmap_3d(&out.tb, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, 1, (uint64_t)K * 2,
                     (uint64_t)N * K * 2, kBK, kBN, true))
     return MMDIT_ERR_ALIGN;
   p.M_seg = M_seg;
@@ -222,7 +229,35 @@ static int run_gemm(const void* A, long long a_ld, long long a_seg_rows, int M_s
   const double a_bytes = (double)n_seg * M_seg * K * 2.0;
   p.group_m = a_bytes <= 48.0 * 1024 * 1024 ? p.tiles_m * n_seg : 16;
   p.status = device_status_ptr();
-  return cuda_status(launch_gemm(ta, tb, p, st));
+  out.p = p;
+  return MMDIT_OK;
+}
+
+// One persistent launch over the tiles of one or two problems.
+static int launch_problems(const GemmProblem* a, const GemmProblem* b, cudaStream_t st) {
+  GemmGroup g;
+  std::memset(&g, 0, sizeof(g));
+  g.tmA[0] = a->ta;
+  g.tmB[0] = a->tb;
+  g.p[0] = a->p;
+  g.n_prob = 1;
+  g.tiles0 = a->p.num_tiles;
+  g.total_tiles = g.tiles0;
+  if (b) {
+    g.tmA[1] = b->ta;
+    g.tmB[1] = b->tb;
+    g.p[1] = b->p;
+    g.n_prob = 2;
+    g.total_tiles += b->p.num_tiles;
+  }
+  return cuda_status(launch_gemm(g, st));
+}
+
+static int run_gemm(const void* A, long long a_ld, long long a_seg_rows, int M_seg, int n_seg, int K,
+                    const mmdit_linear_t& lin, int N, GemmParams p, uint16_t* wdeq, cudaStream_t st) {
+  GemmProblem pr;
+  MMDIT_TRY(prepare_gemm(A, a_ld, a_seg_rows, M_seg, n_seg, K, lin, N, p, wdeq, st, pr));
+  return launch_problems(&pr, nullptr, st);
 }
 
 static GemmParams gemm_params(int mode) {
@@ -260,16 +295,21 @@ static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, 
 // ----------------------------------------------------------------- workspace layouts
 struct DoubleWS {
   float* mod;
-  uint16_t *y, *qk, *vT, *O, *h, *wdeq;
+  uint16_t *y, *qk, *vT, *O, *h, *wdeq[2];
 };
+// y and h hold both streams at once (text rows first), so that each linear
+// of the two streams runs as one grouped launch; int8 weights need one
+// widening buffer per stream.
 static void layout_double(const Dims& d, bool i8, bool need_mod, Carve& c, DoubleWS& w) {
   w.mod = need_mod ? c.take<float>((size_t)2 * d.B * 6 * d.D) : nullptr;
   w.y = c.take<uint16_t>((size_t)d.B * d.L * d.D);
   w.qk = c.take<uint16_t>((size_t)d.B * d.L * 2 * d.D);
   w.vT = c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
   w.O = c.take<uint16_t>((size_t)d.B * d.L * d.D);
-  w.h = c.take<uint16_t>((size_t)d.B * (d.Lt > d.Li ? d.Lt : d.Li) * d.Dm);
-  w.wdeq = i8 ? c.take<uint16_t>((size_t)(3 * d.D > d.Dm ? 3 * d.D : d.Dm) * d.D) : nullptr;
+  w.h = c.take<uint16_t>((size_t)d.B * d.L * d.Dm);
+  const size_t wmax = (size_t)(3 * d.D > d.Dm ? 3 * d.D : d.Dm) * d.D;
+  w.wdeq[0] = i8 ? c.take<uint16_t>(wmax) : nullptr;
+  w.wdeq[1] = i8 ? c.take<uint16_t>(wmax) : nullptr;
 }
 
 struct SingleWS {
@@ -330,12 +370,19 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
   const long long xseg[2] = {xt_seg_rows, xi_seg_rows};
   const int Ls[2] = {d.Lt, d.Li};
   const int off[2] = {0, d.Lt};
-  // LN + modulate and the fused QKV / RMSNorm / RoPE GEMM per stream
-  for (int i = 0; i < 2; ++i) {
-    if (Ls[i] == 0) continue;
-    const float* m = mod + (size_t)i * d.B * 6 * D;
-    uint16_t* y = ws.y + (size_t)off[i] * d.B * D;
-    MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, m, m + D, 6 * D, s.eps_ln, y, st));
+  const int first = d.Lt > 0 ? 0 : 1;  // streams with tokens: [first, 2)
+  auto modp = [&](int i) { return mod + (size_t)i * d.B * 6 * D; };
+  auto yp = [&](int i) { return ws.y + (size_t)off[i] * d.B * D; };
+  auto hp = [&](int i) { return ws.h + (size_t)off[i] * d.B * d.Dm; };
+  // Runs one linear of both streams as one grouped launch (text tiles first).
+  auto grouped = [&](const GemmProblem* pr) -> int {
+    return launch_problems(&pr[first], first == 0 ? &pr[1] : nullptr, st);
+  };
+  GemmProblem pr[2];
+  // LN + modulate, then the fused QKV / RMSNorm / RoPE GEMM
+  for (int i = first; i < 2; ++i)
+    MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, modp(i), modp(i) + D, 6 * D, s.eps_ln, yp(i), st));
+  for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(GM_QKV);
     p.out_seg_rows = d.L;
     p.out_row_off = off[i];
@@ -350,36 +397,45 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     p.qk_ld = 2 * D;
     p.vT = ws.vT;
     p.vT_ld = d.Lpad;
-    MMDIT_TRY(run_gemm(y, D, Ls[i], Ls[i], d.B, D, w.qkv[i], 3 * D, p, ws.wdeq, st));
+    MMDIT_TRY(prepare_gemm(yp(i), D, Ls[i], Ls[i], d.B, D, w.qkv[i], 3 * D, p, ws.wdeq[i], st, pr[i]));
   }
+  MMDIT_TRY(grouped(pr));
   MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.O, D, st));
-  for (int i = 0; i < 2; ++i) {
-    if (Ls[i] == 0) continue;
-    const float* m = mod + (size_t)i * d.B * 6 * D;
-    // x += gate1 * (o Wp^T + bp)
+  // x += gate1 * (o Wp^T + bp)
+  for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(GM_RESID);
     p.resid = xs[i];
     p.resid_ld = D;
     p.resid_seg_rows = xseg[i];
-    p.gate = m + 2 * D;
+    p.gate = modp(i) + 2 * D;
     p.gate_seg_stride = 6 * D;
-    MMDIT_TRY(run_gemm(ws.O + (size_t)off[i] * D, D, d.L, Ls[i], d.B, D, w.proj[i], D, p, ws.wdeq, st));
-    // y2 = LN(x)(1 + scale2) + shift2; h = GELU(y2 W1^T + b1); x += gate2 (h W2^T + b2)
-    MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, m + 3 * D, m + 4 * D, 6 * D, s.eps_ln, ws.y, st));
-    GemmParams p1 = gemm_params(GM_STORE_BF16);
-    p1.gelu_from = 0;
-    p1.out = ws.h;
-    p1.out_ld = d.Dm;
-    p1.out_seg_rows = Ls[i];
-    MMDIT_TRY(run_gemm(ws.y, D, Ls[i], Ls[i], d.B, D, w.mlp_in[i], d.Dm, p1, ws.wdeq, st));
-    GemmParams p2 = gemm_params(GM_RESID);
-    p2.resid = xs[i];
-    p2.resid_ld = D;
-    p2.resid_seg_rows = xseg[i];
-    p2.gate = m + 5 * D;
-    p2.gate_seg_stride = 6 * D;
-    MMDIT_TRY(run_gemm(ws.h, d.Dm, Ls[i], Ls[i], d.B, d.Dm, w.mlp_out[i], D, p2, ws.wdeq, st));
+    MMDIT_TRY(prepare_gemm(ws.O + (size_t)off[i] * D, D, d.L, Ls[i], d.B, D, w.proj[i], D, p, ws.wdeq[i], st, pr[i]));
   }
+  MMDIT_TRY(grouped(pr));
+  // y2 = LN(x)(1 + scale2) + shift2; h = GELU(y2 W1^T + b1)
+  for (int i = first; i < 2; ++i)
+    MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, modp(i) + 3 * D, modp(i) + 4 * D, 6 * D, s.eps_ln,
+                                  yp(i), st));
+  for (int i = first; i < 2; ++i) {
+    GemmParams p = gemm_params(GM_STORE_BF16);
+    p.gelu_from = 0;
+    p.out = hp(i);
+    p.out_ld = d.Dm;
+    p.out_seg_rows = Ls[i];
+    MMDIT_TRY(prepare_gemm(yp(i), D, Ls[i], Ls[i], d.B, D, w.mlp_in[i], d.Dm, p, ws.wdeq[i], st, pr[i]));
+  }
+  MMDIT_TRY(grouped(pr));
+  // x += gate2 * (h W2^T + b2)
+  for (int i = first; i < 2; ++i) {
+    GemmParams p = gemm_params(GM_RESID);
+    p.resid = xs[i];
+    p.resid_ld = D;
+    p.resid_seg_rows = xseg[i];
+    p.gate = modp(i) + 5 * D;
+    p.gate_seg_stride = 6 * D;
+    MMDIT_TRY(prepare_gemm(hp(i), d.Dm, Ls[i], Ls[i], d.B, d.Dm, w.mlp_out[i], D, p, ws.wdeq[i], st, pr[i]));
+  }
+  MMDIT_TRY(grouped(pr));
   return MMDIT_OK;
 }
 

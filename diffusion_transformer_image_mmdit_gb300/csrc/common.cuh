@@ -210,6 +210,49 @@ __device__ __forceinline__ float ex2_poly(float x) {
   return __int_as_float(__float_as_int(p) + ((__float_as_int(r) - 0x4B400000) << 23));
 }
 
+// ---- packed fp32 pairs (one 64-bit register, two lanes of f32x2 arithmetic)
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// ex2_poly on a pair, the float steps as f32x2 arithmetic.
+__device__ __forceinline__ uint64_t ex2_poly2(float x0, float x1) {
+  const uint64_t x = f2_pack(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
+  const uint64_t r = f2_add(x, f2_pack(12582912.0f, 12582912.0f));
+  const uint64_t n = f2_add(r, f2_pack(-12582912.0f, -12582912.0f));
+  float n0, n1;
+  f2_unpack(n, n0, n1);
+  const uint64_t f = f2_add(x, f2_pack(-n0, -n1));
+  uint64_t q = f2_fma(f2_pack(0.05508868396282196f, 0.05508868396282196f), f,
+                      f2_pack(0.24260404706001282f, 0.24260404706001282f));
+  q = f2_fma(q, f, f2_pack(0.6932762265205383f, 0.6932762265205383f));
+  q = f2_fma(q, f, f2_pack(0.9999289512634277f, 0.9999289512634277f));
+  float p0, p1, r0, r1;
+  f2_unpack(q, p0, p1);
+  f2_unpack(r, r0, r1);
+  return f2_pack(__int_as_float(__float_as_int(p0) + ((__float_as_int(r0) - 0x4B400000) << 23)),
+                 __int_as_float(__float_as_int(p1) + ((__float_as_int(r1) - 0x4B400000) << 23)));
+}
+
 __device__ __forceinline__ float gelu_tanh_f(float x) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
   const float k1 = 0.044715f;

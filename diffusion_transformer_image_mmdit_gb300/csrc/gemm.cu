@@ -223,9 +223,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   }
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmGroup g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -254,8 +252,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    for (int q = 0; q < g.n_prob; ++q) {
+      tma_prefetch_desc(&g.tmA[q]);
+      tma_prefetch_desc(&g.tmB[q]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -265,20 +265,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nk = p.K / kBK;
+  unsigned* const status = g.p[0].status;
 
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        const TileCoord c = tile_coord(p, t);
+      for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+        const int q = t < g.tiles0 ? 0 : 1;
+        const GemmParams& p = g.p[q];
+        const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0));
         const int m0 = c.tm * kBM, n0 = c.tn * kBN;
+        const int nk = p.K / kBK;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) goto done;
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, status, ST_TIMEOUT_PRODUCER)) goto done;
           mbar_expect_tx(full0 + 8 * stage, kStageA + kStageB);
-          tma_load_3d(smem_u32(sA + stage * kStageA), &tmA, full0 + 8 * stage, kb * kBK, m0, c.seg);
-          tma_load_3d(smem_u32(sB + stage * kStageB), &tmB, full0 + 8 * stage, kb * kBK, n0, 0);
+          tma_load_3d(smem_u32(sA + stage * kStageA), &g.tmA[q], full0 + 8 * stage, kb * kBK, m0, c.seg);
+          tma_load_3d(smem_u32(sB + stage * kStageB), &g.tmB[q], full0 + 8 * stage, kb * kBK, n0, 0);
           if (++stage == kStages) stage = 0, phase ^= 1;
         }
       }
@@ -290,12 +293,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status, ST_TIMEOUT_MMA)) goto done;
+      for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+        const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kBK;
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
         tc_fence_after();
         const uint32_t d = tmem + acc * kBN;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, ST_TIMEOUT_MMA)) goto done;
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
           tc_fence_after();
           const uint32_t a = smem_u32(sA + stage * kStageA);
           const uint32_t b = smem_u32(sB + stage * kStageB);
@@ -314,9 +318,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int r = quad * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const TileCoord c = tile_coord(p, t);
-      if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.status, ST_TIMEOUT_EPILOGUE)) break;
+    for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+      const int q = t < g.tiles0 ? 0 : 1;
+      const GemmParams& p = g.p[q];
+      const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0));
+      if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, status, ST_TIMEOUT_EPILOGUE)) break;
       tc_fence_after();
       epilogue_tile(p, c, tmem + ((uint32_t)(quad * 32) << 16) + acc * kBN, r);
       tc_fence_before();
@@ -336,7 +342,7 @@ done:
 
 }  // namespace
 
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s) {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -346,9 +352,9 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int grid = p.num_tiles < num_sms() ? p.num_tiles : num_sms();
+  const int grid = g.total_tiles < num_sms() ? g.total_tiles : num_sms();
   launch_begin(KID_GEMM, s);
-  gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(tmA, tmB, p);
+  gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(g);
   launch_end(s);
   return cudaGetLastError();
 }

@@ -60,6 +60,18 @@ struct GemmParams {
   unsigned* status;
 };
 
+// One launch of the persistent GEMM serves up to two problems with the same
+// tile shape (e.g. the text and image streams of a double block): tiles
+// [0, tiles0) belong to problem 0, the rest to problem 1.
+struct GemmGroup {
+  CUtensorMap tmA[2];
+  CUtensorMap tmB[2];
+  GemmParams p[2];
+  int n_prob;
+  int tiles0;
+  int total_tiles;
+};
+
 // ----------------------------------------------------------------- attention
 constexpr int kAttnBM = 128;  // queries per CTA
 constexpr int kAttnBN = 128;  // keys per KV tile
@@ -103,7 +115,7 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
                   uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 
 // Launchers (return cudaError_t of the launch).
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, cudaStream_t s);
+cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s);
 cudaError_t launch_attention(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, int d_head,
                              cudaStream_t s);
 int num_sms();
