@@ -82,6 +82,59 @@ def peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# ------------------------------------------------------------------ ncu traffic of the GEMM
+GEMM_SOURCES = ["diffusion_transformer_image_mmdit_gb300/csrc/gemm.cu",
+                "diffusion_transformer_image_mmdit_gb300/csrc/common.cuh",
+                "diffusion_transformer_image_mmdit_gb300/csrc/mmdit_internal.h"]
+
+
+def gemm_sources_sha256() -> str:
+    """Hash of the GEMM kernel's sources and of the host code that shapes its
+    launches (tile counts, raster, grouping) in capi.cu."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    capi = open(os.path.join(ROOT, "diffusion_transformer_image_mmdit_gb300/csrc/capi.cu")).read()
+    a = capi.find("// ----------------------------------------------------------------- GEMM")
+    b = capi.find("static GemmParams gemm_params(int mode)")
+    h.update(capi[a:b].encode())
+    return h.hexdigest()
+
+
+def gemm_traffic_per_launch(config: str):
+    """DRAM bytes per GEMM launch from the committed ncu summary of this
+    workload, or None when absent or when the GEMM changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"gemm_traffic_{config}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        for key in ("traffic_per_launch_bytes", "sources_sha256"):
+            if line.strip().startswith(key + ":"):
+                vals[key] = line.split(":", 1)[1].strip().strip("`")
+    if vals.get("sources_sha256") != gemm_sources_sha256() or "traffic_per_launch_bytes" not in vals:
+        return None
+    return int(float(vals["traffic_per_launch_bytes"]))
+
+
+# ------------------------------------------------------------------ multi-rank helpers
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank timing over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(step_flop: float, world: int, ms_per_step: float) -> float:
+    """Replicas: every rank runs the full workload, so the job does world x the work per step time."""
+    return step_flop * world / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -231,11 +284,7 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int):
     if world > 1:
         dist.barrier()
     launches = api.launch_count() - n0
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
     ms_step = ms / args.steps
     st = api.sync_status()
     if st != 0:
@@ -274,11 +323,7 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int):
         out_h.copy_(x_lat, non_blocking=True)
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, dev)
 
     res = {
         "ms_step": ms_step, "launches_per_step": launches / args.steps, "clocks": clk.summary(),
@@ -344,8 +389,8 @@ def main():
     if rank != 0:
         return
     pk = r["peaks"]
-    value = fl["total"] * world / (r["ms_step"] * 1e-3) / 1e12
-    e2e_value = fl["total"] * world / (r["e2e_ms"] * 1e-3) / 1e12
+    value = whole_job_tflops(fl["total"], world, r["ms_step"])
+    e2e_value = whole_job_tflops(fl["total"], world, r["e2e_ms"])
     gemm_peak = pk["bf16_tflops_sustained"]
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -361,7 +406,8 @@ def main():
                      "achieved": round(r["gemm_tflops"], 1) if r["gemm_tflops"] else None, "peak": gemm_peak,
                      "unit": "TFLOP/s",
                      "frac": round(r["gemm_tflops"] / gemm_peak, 3) if r["gemm_tflops"] else None,
-                     "traffic": None,
+                     "traffic": gemm_traffic_per_launch(args.config),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "peak_source": f"{pk['source']} bf16 sustained (kernel timed inside the step)",
                      "launches_per_step": r["gemm_launches"],
                      "flops_per_launch": round(fl["gemm"] / max(1, r["gemm_launches"]))},

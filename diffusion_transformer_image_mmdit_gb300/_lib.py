@@ -48,6 +48,7 @@ SIGNATURES = {
     "mmdit_status_string": (ctypes.c_char_p, [c_int]),
     "mmdit_sync_status": (c_int, [c_void_p]),
     "mmdit_launch_count": (c_longlong, []),
+    "mmdit_selftest_wait_timeout": (c_int, [ctypes.c_uint, c_void_p]),
     "mmdit_kernel_name": (ctypes.c_char_p, [c_int]),
     "mmdit_trace_begin": (c_int, [c_int]),
     "mmdit_trace_end": (c_int, [POINTER(c_int)]),

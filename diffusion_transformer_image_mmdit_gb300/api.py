@@ -177,6 +177,10 @@ def sync_status(stream=None) -> int:
     return _lib.load().mmdit_sync_status(stream_handle(stream))
 
 
+def selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    call("mmdit_selftest_wait_timeout", limit_us, stream_handle(stream))
+
+
 def launch_count() -> int:
     return int(_lib.load().mmdit_launch_count())
 

@@ -532,9 +532,9 @@ int mmdit_sync_status(void* stream) {
 long long mmdit_launch_count(void) { return g_launches.load(); }
 
 const char* mmdit_kernel_name(int kernel_id) {
-  static const char* names[KID_COUNT] = {"gemm_bf16_tc",  "attn_fwd",  "ln_modulate", "gemv",
-                                         "sinusoid",      "rope_build", "rope_apply", "euler",
-                                         "quantize_w8",   "dequant_i8", "cast_bf16",  "attn_prep"};
+  static const char* names[KID_COUNT] = {"gemm_bf16_tc", "attn_fwd",   "ln_modulate", "gemv",      "sinusoid",
+                                         "rope_build",   "rope_apply", "euler",       "quantize_w8", "dequant_i8",
+                                         "cast_bf16",    "attn_prep",  "wait_selftest"};
   return (kernel_id >= 0 && kernel_id < KID_COUNT) ? names[kernel_id] : "unknown";
 }
 
@@ -817,6 +817,12 @@ int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x
     MMDIT_CUDA(launch_euler(x_lat, v, false, (float)(sigma_next - sigma), (long long)d.B * d.Li * C, st));
   }
   return MMDIT_OK;
+}
+
+int mmdit_selftest_wait_timeout(unsigned limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return MMDIT_ERR_ARG;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_wait_selftest(1000ull * limit_us, device_status_ptr(), S(stream)));
 }
 
 int euler_step(float* x, const void* v, int v_dtype, double sigma, double sigma_next, int64_t n, void* stream) {

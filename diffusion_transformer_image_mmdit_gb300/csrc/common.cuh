@@ -18,6 +18,7 @@ enum : unsigned {
   ST_TIMEOUT_EPILOGUE = 4u,
   ST_TIMEOUT_SOFTMAX = 8u,
   ST_BAD_LAUNCH = 16u,
+  ST_SELFTEST = 32u,
 };
 
 // A bounded wait gives up after this many nanoseconds of global time.
@@ -66,7 +67,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // (returns false, records `code` in *status and raises *abort) after
 // kWaitLimitNs, or as soon as another role of the CTA raised *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status,
-                                          unsigned code) {
+                                          unsigned code, unsigned long long limit_ns = kWaitLimitNs) {
 #pragma unroll 1
   for (int i = 0; i < 32; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -75,7 +76,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort = 1;
       if (status) atomicOr(status, code);
       return false;

@@ -410,9 +410,32 @@ __global__ void attn_prep_kernel(const uint16_t* __restrict__ qkv, long long qkv
   for (int j = 0; j < PER; ++j) vT[((long long)b * D + h * HD + lane * PER + j) * vT_ld + tok] = vs[j];
 }
 
+// ------------------------------------------------------------------ wait self-test
+// Waits on an mbarrier that nothing ever completes, with the given limit:
+// exercises the bounded-wait path (status bit, abort flag, orderly exit).
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, unsigned* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  mbar_wait(smem_u32(&bar), 0, &abort_flag, status, ST_SELFTEST, limit_ns);
+  __syncthreads();
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned* status, cudaStream_t st) {
+  launch_begin(KID_SELFTEST, st);
+  wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, status);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
                                const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st) {
   if (D % 256 || D > 4096) return cudaErrorInvalidValue;

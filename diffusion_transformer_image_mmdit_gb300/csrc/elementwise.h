@@ -32,6 +32,7 @@ cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long lo
 cudaError_t launch_quantize(const void* w, bool w_bf16, int N, int K, int8_t* q, float* scale, cudaStream_t st);
 cudaError_t launch_dequant_i8(const int8_t* q, uint16_t* out, long long n, cudaStream_t st);
 cudaError_t launch_cast_bf16(const float* x, uint16_t* y, long long n, cudaStream_t st);
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned* status, cudaStream_t st);
 cudaError_t launch_attn_prep(const uint16_t* qkv, long long qkv_ld, int B, int L, int L_txt, int H, int d,
                              const float* gq0, const float* gq1, const float* gk0, const float* gk1, float eps,
                              const float* cs, const float* sn, uint16_t* qk, uint16_t* vT, long long vT_ld,

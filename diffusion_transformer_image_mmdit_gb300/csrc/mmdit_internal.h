@@ -101,6 +101,7 @@ enum KernelId : int {
   KID_DEQUANT,
   KID_CAST,
   KID_ATTN_PREP,
+  KID_SELFTEST,
   KID_COUNT
 };
 // Bracket every kernel launch: counts launches and, while a trace is on,

@@ -127,6 +127,13 @@ const char* mmdit_status_string(int status);
  * bounded wait since the last call, MMDIT_ERR_CUDA on a sticky CUDA error. */
 int mmdit_sync_status(void* stream);
 
+/* Failure-detection self-test: launches one tiny kernel that waits on a
+ * barrier nothing ever completes, with a limit of limit_us microseconds
+ * (1 .. 1e6).  The wait gives up, records its bit in the device status word
+ * and the kernel returns normally; the next mmdit_sync_status() reports
+ * MMDIT_ERR_TIMEOUT and clears the word.  No fault, trap or hang. */
+int mmdit_selftest_wait_timeout(unsigned limit_us, void* stream);
+
 /* Number of kernels this library has launched in this process. */
 long long mmdit_launch_count(void);
 

@@ -185,7 +185,7 @@ def _sample_rows(n, k, seed):
     return rows
 
 
-@pytest.mark.parametrize("name", ["c2"])
+@pytest.mark.parametrize("name", ["c2", "c4"])
 def test_double_block_flux_sampled(name):
     cfg = FULL[name]
     sh = oracle_shape(cfg)
@@ -202,7 +202,7 @@ def test_double_block_flux_sampled(name):
     assert_close(gi[:, ri_rows], ri, max_abs=flux_max_abs(ei, ri), what=f"{name} double x_img rows")
 
 
-@pytest.mark.parametrize("name", ["c3"])
+@pytest.mark.parametrize("name", ["c3", "c4"])
 def test_single_block_flux_sampled(name):
     cfg = FULL[name]
     sh = oracle_shape(cfg)
@@ -215,3 +215,37 @@ def test_single_block_flux_sampled(name):
     ref = O.single_block(x, vec, p, sh, c, s, rows=rows)
     emu = O.single_block(x, vec, p, sh, c, s, rows=rows, rnd=S.round_bf16)
     assert_close(g[:, rows], ref, max_abs=flux_max_abs(emu, ref), what=f"{name} single rows")
+
+
+def test_double_block_int8_flux_batch4_sampled():
+    """Int8 weight-only double block at 1024^2, batch 4 (512 + 64x64 tokens
+    per sample): sampled rows of the first and last sample against the
+    oracle on the dequantised weights (bf16 bar) and on the bf16 weights
+    (the quantisation scheme's 3e-2 bar on the residual update)."""
+    cfg = dict(FULL["c3"])
+    cfg["B"] = 4
+    sh = oracle_shape(cfg)
+    p = S.double_block_params("full.i8", cfg["D"], cfg["d_head"], cfg["D_mlp"])
+    a = S.activations(4, cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, wq = run_double(cfg, p, a, i8=True)
+    pd = _dequantised_double(p, wq)
+    rt_rows = _sample_rows(cfg["L_txt"], 3, 5)
+    ri_rows = _sample_rows(sh.L_img, 5, 6)
+    c, s = tables(cfg)
+    for b in (0, 3):
+        sub = {k: v[b:b + 1] for k, v in a.items()}
+        rt, ri = O.double_block(sub["x_txt"], sub["x_img"], sub["vec"], pd, sh_b1(sh), c, s, rows_txt=rt_rows,
+                                rows_img=ri_rows)
+        et, ei = O.double_block(sub["x_txt"], sub["x_img"], sub["vec"], pd, sh_b1(sh), c, s, rows_txt=rt_rows,
+                                rows_img=ri_rows, rnd=S.round_bf16)
+        assert_close(gt[b:b + 1, rt_rows], rt, max_abs=flux_max_abs(et, rt), what=f"int8 b={b} x_txt rows")
+        assert_close(gi[b:b + 1, ri_rows], ri, max_abs=flux_max_abs(ei, ri), what=f"int8 b={b} x_img rows")
+        bt, bi = O.double_block(sub["x_txt"], sub["x_img"], sub["vec"], p, sh_b1(sh), c, s, rows_txt=rt_rows,
+                                rows_img=ri_rows)
+        x0 = sub["x_img"][:, ri_rows]
+        assert rel_l2(gi[b:b + 1, ri_rows] - x0, bi - x0) <= REL_L2_INT8_SCHEME
+
+
+def sh_b1(sh):
+    import dataclasses
+    return dataclasses.replace(sh, B=1)
