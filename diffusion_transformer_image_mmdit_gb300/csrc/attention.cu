@@ -74,11 +74,12 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
   const uint32_t q_full = smem_u32(bars + 0);
   const uint32_t k_full0 = smem_u32(bars + 1);    // [2] per stage
   const uint32_t v_full0 = smem_u32(bars + 3);    // [2] per stage
-  const uint32_t kv_empty0 = smem_u32(bars + 5);  // [2] per stage
+  const uint32_t k_empty0 = smem_u32(bars + 5);   // [2] per stage: freed after both S MMAs of the K tile
   const uint32_t s_full0 = smem_u32(bars + 7);    // [2] per tile
   const uint32_t p_full0 = smem_u32(bars + 9);    // [2] per tile
   const uint32_t pv_done0 = smem_u32(bars + 11);  // [2] per tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  const uint32_t v_empty0 = smem_u32(bars + 13);  // [2] per stage: freed after both P V MMAs of the V tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -93,7 +94,8 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(k_full0 + 8 * i, 1);
       mbar_init(v_full0 + 8 * i, 1);
-      mbar_init(kv_empty0 + 8 * i, 1);
+      mbar_init(k_empty0 + 8 * i, 1);
+      mbar_init(v_empty0 + 8 * i, 1);
       mbar_init(s_full0 + 8 * i, 1);
       mbar_init(p_full0 + 8 * i, 4);
       mbar_init(pv_done0 + 8 * i, 1);
@@ -238,62 +240,85 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
 #pragma unroll
           for (int hf = 0; hf < HD / 64; ++hf)
             tma_load_3d(smem_u32(sQ + t * SM::QT + hf * kHalf), &tmQK, q_full, h * HD + hf * 64, q0 + t * kAttnBM, b);
-        for (int j = 0; j < nkv; ++j) {
+        // Loads in the order the MMAs need them: K(j + 1) (for S(j + 1)) before
+        // V(j) (for P V(j)).  K and V rings are freed independently, so a K
+        // slot is refilled as soon as both S MMAs that read it complete.
+        auto load_k = [&](int j) -> bool {
           const int st = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait(kv_empty0 + 8 * st, ph ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) break;
+          if (!mbar_wait(k_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER))
+            return false;
           mbar_expect_tx(k_full0 + 8 * st, SM::K);
 #pragma unroll
           for (int hf = 0; hf < HD / 64; ++hf)
             tma_load_3d(smem_u32(sK + st * SM::K + hf * kHalf), &tmQK, k_full0 + 8 * st, D + h * HD + hf * 64,
                         j * kAttnBN, b);
+          return true;
+        };
+        auto load_v = [&](int j) -> bool {
+          const int st = j & 1;
+          if (!mbar_wait(v_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER))
+            return false;
           mbar_expect_tx(v_full0 + 8 * st, SM::V);
 #pragma unroll
           for (int kh = 0; kh < 2; ++kh)
             tma_load_3d(smem_u32(sV + st * SM::V + kh * (HD * 128)), &tmV, v_full0 + 8 * st, j * kAttnBN + kh * 64,
                         h * HD, b);
-        }
+          return true;
+        };
+        bool okp = load_k(0);
+        for (int j = 0; okp && j < nkv; ++j) okp = (j + 1 >= nkv || load_k(j + 1)) && load_v(j);
       }
     } else if (warp == 9) {
-      if (lane == 0) {
-        const uint32_t idesc_s = idesc_bf16(128, kAttnBN);
-        const uint32_t idesc_o = idesc_bf16(128, HD);
-        const uint32_t aQ = smem_u32(sQ);
-        auto issue_s = [&](int t, int j) -> bool {
-          const int st = j & 1;
-          if (t == 0 && !mbar_wait(k_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
-          tc_fence_after();
-          const uint32_t bK = smem_u32(sK + st * SM::K);
+      // The whole warp runs the issue loop (warp-uniform operands); the
+      // elected lane issues the MMAs and commits.
+      const uint32_t leader = elect_one_sync();
+      const uint32_t idesc_s = idesc_bf16(128, kAttnBN);
+      const uint32_t idesc_o = idesc_bf16(128, HD);
+      // Descriptors of both Q tiles and both K / V stages are built once;
+      // each MMA adds a compile-time offset in 16-byte units.
+      const uint64_t dQ0 = sdesc_k128(smem_u32(sQ)), dQ1 = sdesc_k128(smem_u32(sQ + SM::QT));
+      const uint64_t dK0 = sdesc_k128(smem_u32(sK)), dK1 = sdesc_k128(smem_u32(sK + SM::K));
+      const uint64_t dV0 = sdesc_k128(smem_u32(sV)), dV1 = sdesc_k128(smem_u32(sV + SM::V));
+      auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        return mbar_wait_warp(bar, parity, abort_flag, p.status, ST_TIMEOUT_MMA);
+      };
+      auto issue_s = [&](int t, int j) -> bool {
+        const int st = j & 1;
+        if (t == 0 && !wait(k_full0 + 8 * st, (j >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t aQ = t ? dQ1 : dQ0;
+        const uint64_t bK = st ? dK1 : dK0;
+        const uint32_t dS = tmem + t * 128;
 #pragma unroll
-          for (int k = 0; k < HD / 16; ++k) {
-            const int hf = k >> 2, off = (k & 3) * 32;
-            umma_bf16(tmem + t * 128, sdesc_k128(aQ + t * SM::QT + hf * kHalf + off),
-                      sdesc_k128(bK + hf * kHalf + off), idesc_s, k > 0 ? 1u : 0u);
-          }
-          umma_commit(s_full0 + 8 * t);
-          return true;
-        };
-        auto issue_pv = [&](int t, int j) -> bool {
-          const int st = j & 1;
-          if (!mbar_wait(p_full0 + 8 * t, j & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
-          if (t == 0 && !mbar_wait(v_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.status, ST_TIMEOUT_MMA)) return false;
-          tc_fence_after();
-          const uint32_t bV = smem_u32(sV + st * SM::V);
-#pragma unroll
-          for (int k = 0; k < kAttnBN / 16; ++k) {
-            const int kh = k >> 2, off = (k & 3) * 32;
-            umma_bf16_ta(tmem + 256 + t * 128, tmem + t * 128 + k * 8, sdesc_k128(bV + kh * (HD * 128) + off), idesc_o,
-                         (j > 0 || k > 0) ? 1u : 0u);
-          }
-          umma_commit(pv_done0 + 8 * t);
-          if (t == 1) umma_commit(kv_empty0 + 8 * st);
-          return true;
-        };
-        bool ok = mbar_wait(q_full, 0, abort_flag, p.status, ST_TIMEOUT_MMA) && issue_s(0, 0) && issue_s(1, 0);
-        for (int j = 0; ok && j < nkv; ++j) {
-          ok = issue_pv(0, j) && (j + 1 >= nkv || issue_s(0, j + 1)) && issue_pv(1, j) &&
-               (j + 1 >= nkv || issue_s(1, j + 1));
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
+          umma_bf16_if(leader, dS, aQ + off, bK + off, idesc_s, k > 0 ? 1u : 0u);
         }
+        umma_commit_if(leader, s_full0 + 8 * t);
+        if (t == 1) umma_commit_if(leader, k_empty0 + 8 * st);
+        return true;
+      };
+      auto issue_pv = [&](int t, int j) -> bool {
+        const int st = j & 1;
+        if (!wait(p_full0 + 8 * t, j & 1)) return false;
+        if (t == 0 && !wait(v_full0 + 8 * st, (j >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t bV = st ? dV1 : dV0;
+        const uint32_t dO = tmem + 256 + t * 128, aP = tmem + t * 128;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+        for (int k = 0; k < kAttnBN / 16; ++k) {
+          const uint32_t off = ((k >> 2) * (HD * 128) + (k & 3) * 32) >> 4;
+          umma_bf16_ta_if(leader, dO, aP + k * 8, bV + off, idesc_o, k > 0 ? 1u : acc0);
+        }
+        umma_commit_if(leader, pv_done0 + 8 * t);
+        if (t == 1) umma_commit_if(leader, v_empty0 + 8 * st);
+        return true;
+      };
+      bool ok = wait(q_full, 0) && issue_s(0, 0) && issue_s(1, 0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        ok = issue_pv(0, j) && (j + 1 >= nkv || issue_s(0, j + 1)) && issue_pv(1, j) &&
+             (j + 1 >= nkv || issue_s(1, j + 1));
       }
     }
   }

@@ -145,6 +145,50 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Warp-wide issue.  An MMA warp runs its issue loop with all 32 lanes so
+// that every operand (TMEM address, shared-memory descriptor) is
+// warp-uniform; `issue` is 1 in the one lane chosen by elect.sync (computed
+// once, in converged code) and 0 elsewhere, and predicates the tcgen05
+// instruction itself.
+__device__ __forceinline__ uint32_t elect_one_sync() {
+  uint32_t pred;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+  return pred;
+}
+
+__device__ __forceinline__ void umma_bf16_if(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16_ta_if(uint32_t issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_if(uint32_t issue, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(issue)
+      : "memory");
+}
+
+// mbar_wait by every lane of a converged warp; true in all lanes only if
+// every lane saw the phase complete (a time-out in any lane fails them all).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status,
+                                               unsigned code) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status, code)) != 0;
+}
+
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
 // layout written by TMA with CU_TENSOR_MAP_SWIZZLE_128B: 8-row x 128-byte
 // atoms stacked every 1024 bytes along M/N.  Fields: start address >> 4

@@ -287,31 +287,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kBM, kBN);
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
-        const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kBK;
-        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
+    // The whole warp runs the issue loop (warp-uniform operands); the
+    // elected lane issues the MMAs and commits.  Descriptors are built once;
+    // per MMA only a compile-time offset (in 16-byte units of the
+    // start-address field) is added.
+    const uint32_t leader = elect_one_sync();
+    const uint32_t idesc = idesc_bf16(kBM, kBN);
+    const uint64_t dA0 = sdesc_k128(smem_u32(sA)), dB0 = sdesc_k128(smem_u32(sB));
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+      const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kBK;
+      if (!mbar_wait_warp(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
+      tc_fence_after();
+      const uint32_t d = tmem + acc * kBN;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_warp(full0 + 8 * stage, phase, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
         tc_fence_after();
-        const uint32_t d = tmem + acc * kBN;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
-          tc_fence_after();
-          const uint32_t a = smem_u32(sA + stage * kStageA);
-          const uint32_t b = smem_u32(sB + stage * kStageB);
+        const uint64_t da = dA0 + (uint64_t)(stage * (kStageA >> 4));
+        const uint64_t db = dB0 + (uint64_t)(stage * (kStageB >> 4));
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            umma_bf16(d, sdesc_k128(a + 32 * k), sdesc_k128(b + 32 * k), idesc, (kb | k) != 0);
-          umma_commit(empty0 + 8 * stage);
-          if (++stage == kStages) stage = 0, phase ^= 1;
-        }
-        umma_commit(tfull0 + 8 * acc);
-        if (++acc == 2) acc = 0, acc_phase ^= 1;
+        for (int k = 0; k < kBK / 16; ++k) umma_bf16_if(leader, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+        umma_commit_if(leader, empty0 + 8 * stage);
+        if (++stage == kStages) stage = 0, phase ^= 1;
       }
+      umma_commit_if(leader, tfull0 + 8 * acc);
+      if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
   } else {
     const int quad = warp & 3;
