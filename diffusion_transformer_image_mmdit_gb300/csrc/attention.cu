@@ -17,8 +17,9 @@
 // in shared memory, 128-byte swizzle); O += P V is M=128, N=d, K=128 keys
 // with P read from tensor memory.  The running max lives in the log2
 // domain; O is rescaled in TMEM only when the running max grows by more
-// than 2^8, which stays exact because the same reference is used for the
-// numerator and the row sum.
+// than 16 (a factor 2^16), which stays exact because the same reference is
+// used for the numerator and the row sum: P entries stay below 2^16 (bf16
+// keeps its relative precision there) and the fp32 sums far from overflow.
 #include "common.cuh"
 
 namespace mmdit {
@@ -26,7 +27,7 @@ namespace mmdit {
 namespace {
 
 constexpr uint32_t kHalf = 128 * 128;  // one 128-row x 128-byte swizzled half tile
-constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRescaleThreshold = 16.0f;
 
 // Two query tiles per CTA (256 rows of one (sample, head)), K/V tiles shared.
 //   warps 0-3   softmax of tile 0; warps 4-7 softmax of tile 1 (one query
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait(s_full, j & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
+      if (!mbar_wait_warp(s_full, j & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
       tc_fence_after();
       const int kv0 = j * kAttnBN;
       float sv[kAttnBN];
@@ -156,12 +157,16 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
       const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       const float m_new = fmaxf(m_run, mx * sl2);
-      if (j > 0) {
-        if (!mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
-        tc_fence_after();
-      }
-      if (m_new > m_run + kRescaleThreshold) {
-        const float alpha = ex2_approx(m_run - m_new);
+      // P V(j - 1) has completed here: S(j) was issued after it and the
+      // commit behind s_full covers every earlier MMA of the issuing thread.
+      // So O may be rescaled, and P(j) may overwrite P(j - 1), without a
+      // further wait.
+      // Lazy rescale: the TMEM accesses are warp-wide, so the warp rescales
+      // when any of its rows needs it (alpha = 1, an exact no-op, for the
+      // others).
+      const bool grow = m_new > m_run + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float alpha = grow ? ex2_approx(m_run - m_new) : 1.0f;
         if (j > 0) {
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
@@ -174,11 +179,14 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
           }
           tmem_wait_st();
         }
-        l_run *= alpha;
-        m_run = m_new;
+        if (grow) {
+          l_run *= alpha;
+          m_run = m_new;
+        }
       }
       // exponentials on column pairs (f32x2 arithmetic), row sum in 4 packed
-      // partial sums, bf16 P over the first 64 columns of S
+      // partial sums, bf16 P over the first 64 columns of S.  1 of every 4
+      // pairs uses the FMA-pipe polynomial, the rest the MUFU ex2.
       const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_run, -m_run);
       uint64_t ls2[4];
 #pragma unroll
@@ -208,7 +216,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (ok && mbar_wait(pv_done, (nkv - 1) & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) {
+    if (ok && mbar_wait_warp(pv_done, 0, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) {  // the last P V only
       tc_fence_after();
       const float inv_l = 1.0f / l_run;
       const int row = q0 + t * kAttnBM + r;
@@ -311,7 +319,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
           const uint32_t off = ((k >> 2) * (HD * 128) + (k & 3) * 32) >> 4;
           umma_bf16_ta_if(leader, dO, aP + k * 8, bV + off, idesc_o, k > 0 ? 1u : acc0);
         }
-        umma_commit_if(leader, pv_done0 + 8 * t);
+        if (j + 1 == nkv) umma_commit_if(leader, pv_done0 + 8 * t);  // for the final O / l
         if (t == 1) umma_commit_if(leader, v_empty0 + 8 * st);
         return true;
       };

@@ -213,8 +213,9 @@ static int prepare_gemm(const void* A, long long a_ld, long long a_seg_rows, int
   if (!make_tmap_3d(&out.ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M_seg, (uint64_t)n_seg,
                     (uint64_t)a_ld * 2, (uint64_t)a_seg_rows * a_ld * 2, kBK, kBM, true))
     return MMDIT_ERR_ALIGN;
+  // W is loaded in 128-row halves of the 256-row tile, one by each CTA of a cluster pair.
   if (!make_tmap_3d(&out.tb, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, 1, (uint64_t)K * 2,
-                    (uint64_t)N * K * 2, kBK, kBN, true))
+                    (uint64_t)N * K * 2, kBK, kBN / 2, true))
     return MMDIT_ERR_ALIGN;
   p.M_seg = M_seg;
   p.n_seg = n_seg;
@@ -222,12 +223,15 @@ static int prepare_gemm(const void* A, long long a_ld, long long a_seg_rows, int
   p.K = K;
   p.tiles_m = (M_seg + kBM - 1) / kBM;
   p.tiles_n = (N + kBN - 1) / kBN;
-  p.num_tiles = p.tiles_m * p.tiles_n * n_seg;
+  // Work units are pairs of vertically adjacent M tiles (one per CTA of a
+  // cluster) at one N tile.
+  const int pairs_m = (p.tiles_m * n_seg + 1) / 2;
+  p.num_tiles = pairs_m * p.tiles_n;
   // Raster: when the whole A operand fits comfortably in L2, sweep all M
   // tiles for each N tile (A stays resident, W streams once); otherwise
-  // groups of 16 M tiles bound the A footprint of a wave.
+  // groups of 8 pairs (16 M tiles) bound the A footprint of a wave.
   const double a_bytes = (double)n_seg * M_seg * K * 2.0;
-  p.group_m = a_bytes <= 48.0 * 1024 * 1024 ? p.tiles_m * n_seg : 16;
+  p.group_m = a_bytes <= 48.0 * 1024 * 1024 ? pairs_m : 8;
   p.status = device_status_ptr();
   out.p = p;
   return MMDIT_OK;

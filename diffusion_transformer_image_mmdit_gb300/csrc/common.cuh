@@ -66,6 +66,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Waits until the phase with the given parity has completed.  Gives up
 // (returns false, records `code` in *status and raises *abort) after
 // kWaitLimitNs, or as soon as another role of the CTA raised *abort.
+// `abort` and `status` may be null (a plain bounded wait).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status,
                                           unsigned code, unsigned long long limit_ns = kWaitLimitNs) {
 #pragma unroll 1
@@ -75,9 +76,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 #pragma unroll 1
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
+    if (abort && *abort) return false;
     if (global_ns() - t0 > limit_ns) {
-      *abort = 1;
+      if (abort) *abort = 1;
       if (status) atomicOr(status, code);
       return false;
     }
@@ -179,6 +180,43 @@ __device__ __forceinline__ void umma_commit_if(uint32_t issue, uint32_t bar) {
       "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
       "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
       "r"(issue)
+      : "memory");
+}
+
+// Multicast commit: arrives on the mbarrier at the same shared-memory offset
+// in every CTA of the cluster named by `mask`, once this thread's prior MMAs
+// complete.
+__device__ __forceinline__ void umma_commit_mc_if(uint32_t issue, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          bar),
+      "h"(mask), "r"(issue)
+      : "memory");
+}
+
+// ----------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA in the cluster; release/acquire orders shared
+// memory (and mbarrier initialisation) across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA tile load written to the same shared-memory offset in every CTA of
+// `mask`; each destination CTA's mbarrier at offset `bar` receives the bytes
+// it got.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* map, uint32_t bar, int x, int y, int z,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
       : "memory");
 }
 
@@ -298,10 +336,16 @@ __device__ __forceinline__ uint64_t ex2_poly2(float x0, float x1) {
                  __int_as_float(__float_as_int(p1) + ((__float_as_int(r1) - 0x4B400000) << 23)));
 }
 
+// GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3),
+// evaluated through the identity 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)):
+// one exp2 and one fast divide.  For u -> -inf the denominator overflows to
+// +inf and the result is the correct -0 limit; relative error is a few fp32
+// ulps, far below the bf16 rounding of the outputs.
 __device__ __forceinline__ float gelu_tanh_f(float x) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
   const float k1 = 0.044715f;
-  return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
+  const float u = k0 * fmaf(k1 * x, x * x, x);
+  return __fdividef(x, 1.0f + ex2_approx(-2.8853900817779268f * u));  // -2 log2(e) u
 }
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }

@@ -5,9 +5,17 @@
 // bf16 contractions with fp32 accumulation (Luminal blog, section "The AMD
 // MI300X pipeline": all bf16 GEMMs accumulate in fp32, with bias epilogues).
 //
-// Structure (one CTA per SM, 192 threads):
-//   warp 0      TMA producer: A tile 128x64 and B tile 256x64 per K block
-//               into a 4-stage ring (128-byte swizzle).
+// Structure (one CTA per SM, 192 threads, clusters of two CTAs):
+//   The two CTAs of a cluster compute the vertically adjacent 128x256 output
+//   tiles (m, n) and (m + 1, n), which share their 256x64 W tile for every K
+//   block: each CTA loads one 128-row half of it and multicasts it into both
+//   CTAs' shared memory, so the pair reads W from L2 once (32 KB per CTA and
+//   K block instead of 48 KB).
+//   warp 0      TMA producer: its A tile 128x64 and its W half 128x64
+//               (multicast) per K block into a 4-stage ring (128-byte
+//               swizzle).  A stage is refilled only when the MMAs of both
+//               CTAs have released it (the empty barrier counts two
+//               multicast commits).
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
 //               and issues tcgen05.mma (M=128, N=256, K=16) from one thread.
 //   warps 2-5   epilogue: tcgen05.ld of the finished accumulator (one TMEM
@@ -24,23 +32,32 @@ constexpr int kGemmThreads = 192;
 constexpr uint32_t kStageA = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kStageB = kBN * kBK * 2;  // 32 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr size_t kGemmSmem = 1024 + kStages * (kStageA + kStageB) + 256;
+constexpr uint32_t kEpiStageBytes = 4096;  // staging area of one epilogue warp
+constexpr size_t kGemmSmem = 1024 + kStages * (kStageA + kStageB) + 256 + 4 * kEpiStageBytes;
 
 struct TileCoord {
   int seg, tm, tn;
+  bool valid;  // false for the second tile of a pair past the last M tile
 };
 
-// Grouped raster: runs of group_m M tiles (over all segments) sweep all N
-// tiles with M fastest, so the CTAs of one wave share A and B tiles in L2.
-__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int t) {
+// Work unit t of a problem is a pair of M tiles (2 pm, 2 pm + 1) over all
+// segments, at one N tile; CTA `rank` of the cluster takes M tile 2 pm + rank.
+// Grouped raster: runs of group_m pairs sweep all N tiles with M fastest, so
+// the clusters of one wave share A and W tiles in L2.  A missing second tile
+// (odd M tile count) repeats the last real tile with its stores switched off,
+// so both CTAs run the same K loop.
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int t, int rank) {
   const int total_m = p.n_seg * p.tiles_m;
+  const int pairs_m = (total_m + 1) >> 1;
   const int per_group = p.group_m * p.tiles_n;
   const int g = t / per_group;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.group_m, total_m - first_m);
+  const int first = g * p.group_m;
+  const int gm = min(p.group_m, pairs_m - first);
   const int r = t - g * per_group;
-  const int mi = first_m + r % gm;
+  int mi = 2 * (first + r % gm) + rank;
   TileCoord c;
+  c.valid = mi < total_m;
+  if (!c.valid) mi = total_m - 1;
   c.seg = mi / p.tiles_m;
   c.tm = mi - c.seg * p.tiles_m;
   c.tn = r / gm;
@@ -78,24 +95,78 @@ __device__ __forceinline__ void acc_chunk(uint32_t taddr, const GemmParams& p, i
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+// ------------------------------------------------------------ epilogue I/O
+// Each epilogue thread owns one output row (its TMEM lane) and produces 32
+// consecutive columns at a time.  Stored directly, one warp instruction
+// would touch 32 rows with 16 bytes each (half sectors).  Instead the warp
+// passes the 32 x 32 chunk through its own 4 KB staging area in shared
+// memory (16-byte slots XOR-swizzled by row, so both the row-wise writes and
+// the column-wise reads are free of bank conflicts) and every global
+// instruction covers whole 32-byte sectors: 8 rows x 64 bytes for bf16, 4
+// rows x 128 bytes for fp32.  `row0` points at column n of the warp's first
+// row; rows at or beyond `nrows` are not touched.
+__device__ __forceinline__ void warp_store_bf16x32(uint8_t* stg, int lane, const float* v, uint16_t* row0,
+                                                   long long ld, int nrows) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+    w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+    w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+    w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+    *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = w;
+  }
+  __syncwarp();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-    w.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-    w.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-    w.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-    d4[i] = w;
+    const int rr = i * 8 + (lane >> 2), c = lane & 3;
+    const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
+    if (rr < nrows) *reinterpret_cast<uint4*>(row0 + rr * ld + c * 8) = w;
   }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void warp_store_f32x32(uint8_t* stg, int lane, const float* v, float* row0, long long ld,
+                                                  int nrows) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = i * 4 + (lane >> 3), c = lane & 7;
+    const float4 w = *reinterpret_cast<const float4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+    if (rr < nrows) *reinterpret_cast<float4*>(row0 + rr * ld + c * 4) = w;
+  }
+  __syncwarp();
+}
+
+// The transpose of warp_store_f32x32: coalesced loads of 32 rows x 32 fp32,
+// each thread gets its own row (zeros for rows at or beyond nrows).
+__device__ __forceinline__ void warp_load_f32x32(uint8_t* stg, int lane, float* v, const float* row0, long long ld,
+                                                 int nrows) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = i * 4 + (lane >> 3), c = lane & 7;
+    const float4 w = rr < nrows ? *reinterpret_cast<const float4*>(row0 + rr * ld + c * 4) : make_float4(0, 0, 0, 0);
+    *reinterpret_cast<float4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4)) = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 w = *reinterpret_cast<const float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4));
+    v[4 * c] = w.x, v[4 * c + 1] = w.y, v[4 * c + 2] = w.z, v[4 * c + 3] = w.w;
+  }
+  __syncwarp();
 }
 
 // q/k head of HD columns: bias, RMSNorm with gain g, adjacent-pair RoPE at
-// table row `tok`, bf16 store of the whole head row.
+// table row `tok`, bf16 store of the whole head row (HD / 32 staged chunks).
 template <int HD>
 __device__ __forceinline__ void epi_qk_head(uint32_t taddr, const GemmParams& p, int n, const float* __restrict__ g,
-                                            int tok, bool valid, uint16_t* dst) {
+                                            int tok, uint8_t* stg, int lane, uint16_t* row0, long long ld,
+                                            int nrows) {
   float v[HD];
 #pragma unroll
   for (int c = 0; c < HD / 32; ++c) acc_chunk(taddr + c * 32, p, n + c * 32, v + c * 32);
@@ -103,11 +174,9 @@ __device__ __forceinline__ void epi_qk_head(uint32_t taddr, const GemmParams& p,
 #pragma unroll
   for (int i = 0; i < HD; ++i) ss = fmaf(v[i], v[i], ss);
   const float rs = rsqrtf(ss * (1.0f / HD) + p.eps);
-  if (!valid) return;
   const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cos + (long long)tok * (HD / 2));
   const float4* sn4 = reinterpret_cast<const float4*>(p.rope_sin + (long long)tok * (HD / 2));
   const float4* g4 = reinterpret_cast<const float4*>(g);
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < HD / 8; ++q) {  // 8 channels = 4 pairs per iteration
     const float4 c = __ldg(cs4 + q);
@@ -117,46 +186,56 @@ __device__ __forceinline__ void epi_qk_head(uint32_t taddr, const GemmParams& p,
     const float cc[4] = {c.x, c.y, c.z, c.w};
     const float sc[4] = {s.x, s.y, s.z, s.w};
     const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-    uint32_t w[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float x0 = v[8 * q + 2 * j] * rs * gg[2 * j];
       const float x1 = v[8 * q + 2 * j + 1] * rs * gg[2 * j + 1];
-      w[j] = pack_bf16x2(x0 * cc[j] - x1 * sc[j], x0 * sc[j] + x1 * cc[j]);
+      v[8 * q + 2 * j] = x0 * cc[j] - x1 * sc[j];
+      v[8 * q + 2 * j + 1] = x0 * sc[j] + x1 * cc[j];
     }
-    d4[q] = make_uint4(w[0], w[1], w[2], w[3]);
   }
+#pragma unroll
+  for (int c = 0; c < HD / 32; ++c) warp_store_bf16x32(stg, lane, v + 32 * c, row0 + 32 * c, ld, nrows);
 }
 
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& c, uint32_t tbase, int r) {
+// One 128 x 256 accumulator tile; thread r of the four epilogue warps owns
+// tile row r (TMEM lane r).  All 32 lanes of each warp take part in every
+// staged store; rows past M_seg are computed but not written.
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& c, uint32_t tbase, int r,
+                                              uint8_t* stg) {
+  const int lane = r & 31;
   const int m = c.tm * kBM + r;
-  const bool valid = m < p.M_seg;
-  const long long orow = (long long)c.seg * p.out_seg_rows + p.out_row_off + m;
+  const int wm0 = m - lane;                                // the warp's first row
+  const int nrows = min(32, p.M_seg - wm0);                // rows of this warp inside the problem (may be <= 0)
+  const long long orow0 = (long long)c.seg * p.out_seg_rows + p.out_row_off + wm0;
   const int n0 = c.tn * kBN;
 
   if (p.mode == GM_QKV) {
     const int D = p.qkv_D;
-    const int tok = p.out_row_off + m;
     if (n0 < 2 * D) {
       const float* g = n0 < D ? p.gq : p.gk;
-      uint16_t* dst = p.qk + orow * p.qk_ld;
+      // table row of this token; rows past the problem read row 0 (not stored)
+      const int tok = m < p.M_seg ? p.out_row_off + m : 0;
+      uint16_t* row0 = p.qk + orow0 * p.qk_ld + n0;
       if (p.d_head == 128) {
 #pragma unroll 1
         for (int h = 0; h < kBN / 128; ++h)
-          epi_qk_head<128>(tbase + h * 128, p, n0 + h * 128, g, tok, valid, dst + n0 + h * 128);
+          epi_qk_head<128>(tbase + h * 128, p, n0 + h * 128, g, tok, stg, lane, row0 + h * 128, p.qk_ld, nrows);
       } else {
 #pragma unroll 1
         for (int h = 0; h < kBN / 64; ++h)
-          epi_qk_head<64>(tbase + h * 64, p, n0 + h * 64, g, tok, valid, dst + n0 + h * 64);
+          epi_qk_head<64>(tbase + h * 64, p, n0 + h * 64, g, tok, stg, lane, row0 + h * 64, p.qk_ld, nrows);
       }
     } else if (n0 < 3 * D) {
+      // v^T: for each channel, the 32 lanes write 32 consecutive tokens (64 bytes)
+      const int tok = p.out_row_off + m;
       uint16_t* vt = p.vT + (long long)c.seg * D * p.vT_ld + tok;
 #pragma unroll 1
       for (int j = 0; j < kBN / 32; ++j) {
         const int n = n0 + j * 32;
         float v[32];
         acc_chunk(tbase + j * 32, p, n, v);
-        if (valid) {
+        if (lane < nrows) {
           const long long col = n - 2 * D;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -166,7 +245,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         }
       }
     } else {
-      uint16_t* dst = p.aux + orow * p.aux_ld + p.aux_col_off - 3 * D;
+      uint16_t* row0 = p.aux + orow0 * p.aux_ld + p.aux_col_off - 3 * D;
 #pragma unroll 1
       for (int j = 0; j < kBN / 32; ++j) {
         const int n = n0 + j * 32;
@@ -175,7 +254,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         acc_chunk(tbase + j * 32, p, n, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_f(v[i]);
-        if (valid) store_bf16x32(dst + n, v);
+        warp_store_bf16x32(stg, lane, v, row0 + n, p.aux_ld, nrows);
       }
     }
     return;
@@ -192,14 +271,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_f(v[i]);
       }
-      if (valid) store_bf16x32(reinterpret_cast<uint16_t*>(p.out) + orow * p.out_ld + n, v);
+      warp_store_bf16x32(stg, lane, v, reinterpret_cast<uint16_t*>(p.out) + orow0 * p.out_ld + n, p.out_ld, nrows);
     } else if (p.mode == GM_STORE_F32) {
-      if (valid) {
-        float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * p.out_ld + n);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-      }
-    } else {  // GM_RESID
+      warp_store_f32x32(stg, lane, v, reinterpret_cast<float*>(p.out) + orow0 * p.out_ld + n, p.out_ld, nrows);
+    } else {  // GM_RESID: x += gate * v
       float gt[32];
       if (p.gate) {
         load_vec32(p.gate + (long long)c.seg * p.gate_seg_stride + n, gt);
@@ -207,18 +282,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 #pragma unroll
         for (int i = 0; i < 32; ++i) gt[i] = 1.0f;
       }
-      if (valid) {
-        float4* x4 = reinterpret_cast<float4*>(p.resid + ((long long)c.seg * p.resid_seg_rows + m) * p.resid_ld + n);
+      float* x0 = p.resid + ((long long)c.seg * p.resid_seg_rows + wm0) * p.resid_ld + n;
+      float x[32];
+      warp_load_f32x32(stg, lane, x, x0, p.resid_ld, nrows);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float4 x = x4[i];
-          x.x = fmaf(gt[4 * i], v[4 * i], x.x);
-          x.y = fmaf(gt[4 * i + 1], v[4 * i + 1], x.y);
-          x.z = fmaf(gt[4 * i + 2], v[4 * i + 2], x.z);
-          x.w = fmaf(gt[4 * i + 3], v[4 * i + 3], x.w);
-          x4[i] = x;
-        }
-      }
+      for (int i = 0; i < 32; ++i) x[i] = fmaf(gt[i], v[i], x[i]);
+      warp_store_f32x32(stg, lane, x, x0, p.resid_ld, nrows);
     }
   }
 }
@@ -238,11 +307,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();
+  const int cluster = blockIdx.x >> 1;
+  const int n_clusters = gridDim.x >> 1;
+  constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 2);  // one multicast commit from each CTA of the pair
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -262,26 +335,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // Both CTAs' barriers are initialised before either CTA's multicast loads
+  // or commits can reach them.
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   unsigned* const status = g.p[0].status;
+  int n_fill = 0;  // stages this CTA's producer has filled (for the drain on exit)
 
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+      for (int t = cluster; t < g.total_tiles; t += n_clusters) {
         const int q = t < g.tiles0 ? 0 : 1;
         const GemmParams& p = g.p[q];
-        const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0));
+        const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0), rank);
         const int m0 = c.tm * kBM, n0 = c.tn * kBN;
         const int nk = p.K / kBK;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, status, ST_TIMEOUT_PRODUCER)) goto done;
+          // 16 KB of A from this CTA, 2 x 16 KB of W (one half from each CTA)
           mbar_expect_tx(full0 + 8 * stage, kStageA + kStageB);
           tma_load_3d(smem_u32(sA + stage * kStageA), &g.tmA[q], full0 + 8 * stage, kb * kBK, m0, c.seg);
-          tma_load_3d(smem_u32(sB + stage * kStageB), &g.tmB[q], full0 + 8 * stage, kb * kBK, n0, 0);
+          tma_load_3d_mc(smem_u32(sB + stage * kStageB + rank * (kStageB / 2)), &g.tmB[q], full0 + 8 * stage,
+                         kb * kBK, n0 + rank * (kBN / 2), 0, kPair);
+          ++n_fill;
           if (++stage == kStages) stage = 0, phase ^= 1;
         }
       }
@@ -298,7 +377,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+    for (int t = cluster; t < g.total_tiles; t += n_clusters) {
       const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kBK;
       if (!mbar_wait_warp(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
       tc_fence_after();
@@ -310,7 +389,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         const uint64_t db = dB0 + (uint64_t)(stage * (kStageB >> 4));
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) umma_bf16_if(leader, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-        umma_commit_if(leader, empty0 + 8 * stage);
+        umma_commit_mc_if(leader, empty0 + 8 * stage, kPair);  // frees the stage in both CTAs
         if (++stage == kStages) stage = 0, phase ^= 1;
       }
       umma_commit_if(leader, tfull0 + 8 * acc);
@@ -319,15 +398,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
   } else {
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
+    uint8_t* stg = reinterpret_cast<uint8_t*>(bars) + 256 + quad * kEpiStageBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < g.total_tiles; t += gridDim.x) {
+    for (int t = cluster; t < g.total_tiles; t += n_clusters) {
       const int q = t < g.tiles0 ? 0 : 1;
       const GemmParams& p = g.p[q];
-      const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0));
+      const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0), rank);
       if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, status, ST_TIMEOUT_EPILOGUE)) break;
       tc_fence_after();
-      epilogue_tile(p, c, tmem + ((uint32_t)(quad * 32) << 16) + acc * kBN, r);
+      if (c.valid) epilogue_tile(p, c, tmem + ((uint32_t)(quad * 32) << 16) + acc * kBN, r, stg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
@@ -335,8 +415,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     }
   }
 done:
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // After a time-out: wait (bounded) until this CTA's own fills of the
+    // last ring round have landed before its shared memory goes away.
+    for (int i = max(0, n_fill - kStages); i < n_fill; ++i)
+      mbar_wait(full0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1, nullptr, nullptr, 0, 100000000ull);
+  }
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  // Neither CTA leaves while the other can still multicast into it or
+  // arrive on its barriers.
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -347,19 +436,40 @@ done:
 
 cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s) {
   static bool attr_done[64] = {};
+  static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
+    // Clusters of two that fit on the device at once (one CTA per SM).
+    cfg.gridDim = dim3(2 * (num_sms() / 2));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_clusters[dev] = n;
     attr_done[dev] = true;
   }
-  const int grid = g.total_tiles < num_sms() ? g.total_tiles : num_sms();
+  const int clusters = g.total_tiles < max_clusters[dev] ? g.total_tiles : max_clusters[dev];
+  cfg.gridDim = dim3(2 * clusters);
   launch_begin(KID_GEMM, s);
-  gemm_bf16_tc_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(g);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel, g);
   launch_end(s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mmdit
