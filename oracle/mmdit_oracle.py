@@ -301,13 +301,17 @@ def euler_step(x, v, sigma, sigma_next):
     return x + (sigma_next - sigma) * v
 
 
-def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape):
+def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape, vec_add=None):
     """One full step: timestep embedding, img_in, the double blocks, the
     single blocks on [text; image], the final layer on the image tokens, the
-    Euler update.  Returns (x_lat_next, v)."""
+    Euler update.  vec_add ([B, D] or None) is added to the timestep
+    embedding (the step-independent conditioning of the sampling loop).
+    Returns (x_lat_next, v)."""
     ids = rope_ids(sh.L_txt, sh.grid_h, sh.grid_w)
     cos, sin = rope_tables(ids, sh.rope_axes, sh.rope_theta)
     vec = time_embed(sigma, W, sh)
+    if vec_add is not None:
+        vec = vec + vec_add
     h_img = img_in(x_lat, W)
     h_txt = x_txt
     for blk in W["double"]:
@@ -317,6 +321,47 @@ def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape):
         x = single_block(x, vec, blk, sh, cos, sin)
     v = final_layer(x[:, sh.L_txt:], vec, W, sh)
     return euler_step(x_lat, v, sigma, sigma_next), v
+
+
+# --------------------------------------------------------------------------
+# conditioning and the sampling loop
+#
+# The pages name the pieces around the denoiser without defining them: a text
+# encoder produces the conditioning embeddings that the DiT denoises against
+# over 20-50 steps (SGLang blog, "Architecture"), and FLUX.1-dev is sampled
+# with 28 steps at guidance 3.5 (flux-amd-rocm benchmark notes).  Readings
+# taken, the plainest that fit: the text-encoder output enters through one
+# linear projection to width D; the guidance scale goes through the same
+# sinusoid (of 1000 g) and two-layer SiLU MLP shape as the timestep; the
+# pooled text vector through a two-layer SiLU MLP; both are added to the
+# timestep embedding, and neither depends on the step.
+def txt_in(txt, w):
+    """Text-token projection C_txt -> D: x_txt = txt W^T + b."""
+    return linear(txt, w["txt_in_w"], w["txt_in_b"])
+
+
+def guidance_embed(guidance, w, sh: Shape):
+    """W_b SiLU(W_a sinusoid(1000 g) + b_a) + b_b, [B, D]."""
+    s = timestep_sinusoid(np.full(sh.B, 1000.0 * guidance), sh.t_dim)
+    return linear(silu(linear(s, w["g_w1"], w["g_b1"])), w["g_w2"], w["g_b2"])
+
+
+def pooled_embed(pooled, w):
+    """W_b SiLU(W_a y + b_a) + b_b on the pooled text vector y [B, C_pool]."""
+    return linear(silu(linear(pooled, w["y_w1"], w["y_b1"])), w["y_w2"], w["y_b2"])
+
+
+def sample(x_lat, txt, pooled, guidance, sigmas, W, sh: Shape):
+    """The sampling loop over the schedule sigmas[0..n]: the text stream
+    x_txt = txt_in(txt) and the conditioning vec_cond = guidance_embed(g) +
+    pooled_embed(y) are formed once; step i runs denoise_step with sigma_i,
+    sigma_{i+1} and vec_add = vec_cond.  Returns the final latent."""
+    x_txt = txt_in(txt, W)
+    vec_cond = guidance_embed(guidance, W, sh) + pooled_embed(pooled, W)
+    x = np.asarray(x_lat, np.float64)
+    for i in range(len(sigmas) - 1):
+        x, _ = denoise_step(x, x_txt, sigmas[i], sigmas[i + 1], W, sh, vec_add=vec_cond)
+    return x
 
 
 # --------------------------------------------------------------------------

@@ -443,6 +443,101 @@ def test_time_embed_and_final_layer_vs_torch():
     assert rel(O.final_layer(x, vec, W, sh), F.linear(y, T["final_w"], T["final_b"]).numpy()) < 1e-14
 
 
+# ------------------------------------------------------------------ conditioning and the sampling loop
+def _cond_params(sh, C_txt, C_pool):
+    W = S.embed_params(sh.D, sh.C_lat, sh.t_dim, seed=5)
+    W["txt_in_w"], W["txt_in_b"] = S.linear_params("cond.txt_in", sh.D, C_txt, 5)
+    W["g_w1"], W["g_b1"] = S.linear_params("cond.guid1", sh.D, sh.t_dim, 5)
+    W["g_w2"], W["g_b2"] = S.linear_params("cond.guid2", sh.D, sh.D, 5)
+    W["y_w1"], W["y_b1"] = S.linear_params("cond.vec1", sh.D, C_pool, 5)
+    W["y_w2"], W["y_b2"] = S.linear_params("cond.vec2", sh.D, sh.D, 5)
+    return W
+
+
+def _tiny_step_model(sh, seed=5):
+    W = _cond_params(sh, 24, 12)
+    W["double"] = [S.double_block_params(f"smp.d{i}", sh.D, sh.d_head, sh.D_mlp, seed) for i in range(sh.n_double)]
+    W["single"] = [S.single_block_params(f"smp.s{i}", sh.D, sh.d_head, sh.D_mlp, seed) for i in range(sh.n_single)]
+    return W
+
+
+def _sample_inputs(sh):
+    return (rnd("smp.x", (sh.B, sh.L_img, sh.C_lat)), rnd("smp.txt", (sh.B, sh.L_txt, 24)), rnd("smp.y", (sh.B, 12)))
+
+
+SH_SAMPLE = O.Shape(B=2, L_txt=3, grid_h=2, grid_w=2, D=32, H=2, d_head=16, D_mlp=64, rope_axes=(4, 6, 6),
+                    C_lat=8, t_dim=16, n_double=1, n_single=1)
+
+
+def test_conditioning_embeddings_vs_torch():
+    sh = O.Shape(B=2, L_txt=3, grid_h=2, grid_w=3, D=32, H=2, d_head=16, D_mlp=32, C_lat=8, t_dim=16)
+    W = _cond_params(sh, 24, 12)
+    T = {k: torch.from_numpy(v) for k, v in W.items()}
+    half = 8
+    f = torch.exp(-math.log(10000.0) * torch.arange(half) / half)
+    a = torch.full((2, 1), 3500.0) * f[None]
+    ref = F.linear(F.silu(F.linear(torch.cat([a.cos(), a.sin()], 1), T["g_w1"], T["g_b1"])), T["g_w2"], T["g_b2"])
+    assert rel(O.guidance_embed(3.5, W, sh), ref.numpy()) < 1e-14
+    y = rnd("cond.y", (2, 12))
+    ref = F.linear(F.silu(F.linear(torch.from_numpy(y), T["y_w1"], T["y_b1"])), T["y_w2"], T["y_b2"])
+    assert rel(O.pooled_embed(y, W), ref.numpy()) < 1e-14
+    txt = rnd("cond.txt", (2, 3, 24))
+    assert rel(O.txt_in(txt, W), F.linear(torch.from_numpy(txt), T["txt_in_w"], T["txt_in_b"]).numpy()) < 1e-14
+
+
+def test_sample_constant_velocity_closed_form():
+    """With a zero final projection the velocity is its bias b at every step,
+    whatever the blocks and the conditioning do, so the loop telescopes to
+    x_N = x_0 + (sigma_N - sigma_0) b = x_0 - b."""
+    sh = SH_SAMPLE
+    W = _tiny_step_model(sh)
+    W["final_w"] = np.zeros_like(W["final_w"])
+    x0, txt, y = _sample_inputs(sh)
+    sig = O.sigma_schedule(3, O.shift_mu(sh.L_img))
+    x = O.sample(x0, txt, y, 3.5, sig, W, sh)
+    assert np.abs(x - (x0 - W["final_b"])).max() < 1e-12
+
+
+def test_vec_add_is_a_shift_of_the_time_embedding_bias():
+    """Adding a constant vector a to the timestep embedding is the same model
+    as adding a to the output bias of the time MLP (B = 1)."""
+    sh = O.Shape(B=1, L_txt=3, grid_h=2, grid_w=2, D=32, H=2, d_head=16, D_mlp=64, rope_axes=(4, 6, 6),
+                 C_lat=8, t_dim=16, n_double=1, n_single=1)
+    W = _tiny_step_model(sh)
+    x0 = rnd("va.x", (1, sh.L_img, sh.C_lat))
+    xt = rnd("va.t", (1, sh.L_txt, sh.D))
+    a = rnd("va.a", (1, sh.D))
+    got, _ = O.denoise_step(x0, xt, 0.8, 0.6, W, sh, vec_add=a)
+    W2 = dict(W)
+    W2["t_b2"] = W["t_b2"] + a[0]
+    want, _ = O.denoise_step(x0, xt, 0.8, 0.6, W2, sh)
+    assert rel(got, want) < 1e-13
+    plain, _ = O.denoise_step(x0, xt, 0.8, 0.6, W, sh)
+    assert rel(got, plain) > 1e-6  # the conditioning reaches the output
+
+
+def test_sample_conditioning_acts_only_through_modulation_and_text():
+    """With every modulation projection zero, the guidance scale and the
+    pooled vector cannot reach the output; with a zero text projection, the
+    text-encoder output cannot either (the text stream is its bias)."""
+    sh = SH_SAMPLE
+    W = _tiny_step_model(sh)
+    x0, txt, y = _sample_inputs(sh)
+    sig = O.sigma_schedule(2, 0.8)
+    Z = dict(W)
+    Z["final_mod_w"], Z["final_mod_b"] = np.zeros_like(W["final_mod_w"]), np.zeros_like(W["final_mod_b"])
+    Z["double"] = [{st: {k: (np.zeros_like(v) if k.startswith("mod") else v) for k, v in blk[st].items()}
+                    for st in ("txt", "img")} for blk in W["double"]]
+    Z["single"] = [{k: (np.zeros_like(v) if k.startswith("mod") else v) for k, v in blk.items()} for blk in W["single"]]
+    a = O.sample(x0, txt, y, 3.5, sig, Z, sh)
+    b = O.sample(x0, txt, 2.0 * y + 1.0, 1.0, sig, Z, sh)
+    assert np.array_equal(a, b)
+    T = dict(W)
+    T["txt_in_w"] = np.zeros_like(W["txt_in_w"])
+    assert np.array_equal(O.sample(x0, txt, y, 3.5, sig, T, sh), O.sample(x0, -txt, y, 3.5, sig, T, sh))
+    assert not np.array_equal(O.sample(x0, txt, y, 3.5, sig, W, sh), O.sample(x0, txt, y, 1.0, sig, W, sh))
+
+
 # ------------------------------------------------------------------ int8 quantiser
 def test_quantize_w8_invariants():
     w = S.normal_bf16("q.w", (64, 96), 0.02)
@@ -513,3 +608,26 @@ def test_planted_mistakes_are_caught(monkeypatch):
     for name, fn, t in cases:
         _planted(monkeypatch, name, fn, t)
         monkeypatch.setattr(O, name, orig[name])
+
+
+def test_planted_mistakes_in_the_sampling_loop_are_caught(monkeypatch):
+    orig_sinus, orig_denoise = O.timestep_sinusoid, O.denoise_step
+
+    def guidance_no_1000(g, w, sh):  # guidance fed to the sinusoid without the x1000 of the timestep
+        s = orig_sinus(np.full(sh.B, g), sh.t_dim)
+        return O.linear(O.silu(O.linear(s, w["g_w1"], w["g_b1"])), w["g_w2"], w["g_b2"])
+
+    def denoise_reversed(x, xt, s0, s1, W, sh, vec_add=None):  # Euler step with the wrong sign
+        return orig_denoise(x, xt, s1, s0, W, sh, vec_add)
+
+    def denoise_drop_vec_add(x, xt, s0, s1, W, sh, vec_add=None):
+        return orig_denoise(x, xt, s0, s1, W, sh, None)
+
+    orig_g = O.guidance_embed
+    _planted(monkeypatch, "guidance_embed", guidance_no_1000, test_conditioning_embeddings_vs_torch)
+    monkeypatch.setattr(O, "guidance_embed", orig_g)
+    _planted(monkeypatch, "denoise_step", denoise_reversed, test_sample_constant_velocity_closed_form)
+    monkeypatch.setattr(O, "denoise_step", orig_denoise)
+    _planted(monkeypatch, "denoise_step", denoise_drop_vec_add,
+             test_sample_conditioning_acts_only_through_modulation_and_text)
+    monkeypatch.setattr(O, "denoise_step", orig_denoise)
