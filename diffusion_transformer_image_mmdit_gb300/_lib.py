@@ -43,6 +43,13 @@ class StepW(Structure):
                 ("n_single", c_int)]
 
 
+class CondW(Structure):
+    _fields_ = [("txt_in", Linear), ("guid1", Linear), ("guid2", Linear), ("vec1", Linear), ("vec2", Linear),
+                ("C_txt", c_int), ("C_pool", c_int)]
+
+
+MMDIT_SAMPLE_GRAPH = 1
+
 # name -> (restype, argtypes)
 SIGNATURES = {
     "mmdit_status_string": (ctypes.c_char_p, [c_int]),
@@ -67,6 +74,9 @@ SIGNATURES = {
                                        c_void_p, c_void_p, c_size_t, c_void_p]),
     "mmdit_step_fwd": (c_int, [POINTER(Shape), POINTER(StepW), c_void_p, c_void_p, c_double, c_double, c_void_p,
                                c_void_p, c_size_t, c_void_p]),
+    "mmdit_sample_workspace_size": (c_int, [POINTER(Shape), c_int, c_int, c_int, c_int, POINTER(c_size_t)]),
+    "mmdit_sample": (c_int, [POINTER(Shape), POINTER(StepW), POINTER(CondW), c_void_p, c_void_p, c_void_p, c_double,
+                             POINTER(c_double), c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "euler_step": (c_int, [c_void_p, c_void_p, c_int, c_double, c_double, c_int64, c_void_p]),
     "mmdit_quantize_w8": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "mmdit_linear_fwd": (c_int, [POINTER(Linear), c_int, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p,

@@ -15,7 +15,7 @@ import torch
 from . import _lib
 from ._lib import (MMDIT_BF16, MMDIT_EPI_BF16, MMDIT_EPI_BF16_GELU, MMDIT_EPI_F32, MMDIT_EPI_RESID, MMDIT_F32,
                    MMDIT_I8W, MMDIT_OP_ATTENTION, MMDIT_OP_DOUBLE, MMDIT_OP_SINGLE, DoubleW, Linear, Shape, SingleW,
-                   StepW, call)
+                   StepW, CondW, MMDIT_SAMPLE_GRAPH, call)
 
 
 # ------------------------------------------------------------------ marshalling helpers
@@ -156,6 +156,37 @@ class StepWeights:
                            [d.quantized(stream) for d in self.doubles], [b.quantized(stream) for b in self.singles])
 
 
+@dataclass
+class CondWeights:
+    """Conditioning layers of the sampling loop (mmdit_cond_w_t): the text
+    projection C_txt -> D and the two-layer SiLU MLPs of the guidance scale
+    (t_dim -> D -> D) and of the pooled text vector (C_pool -> D -> D)."""
+    txt_in: LinearDev
+    guid1: LinearDev
+    guid2: LinearDev
+    vec1: LinearDev
+    vec2: LinearDev
+
+    @property
+    def C_txt(self) -> int:
+        return self.txt_in.w.shape[1]
+
+    @property
+    def C_pool(self) -> int:
+        return self.vec1.w.shape[1]
+
+    def struct(self) -> CondW:
+        c = CondW()
+        c.txt_in, c.guid1, c.guid2 = self.txt_in.struct(), self.guid1.struct(), self.guid2.struct()
+        c.vec1, c.vec2 = self.vec1.struct(), self.vec2.struct()
+        c.C_txt, c.C_pool = self.C_txt, self.C_pool
+        return c
+
+    def quantized(self, stream=None) -> "CondWeights":
+        q = lambda l: quantize_linear(l, stream)
+        return CondWeights(q(self.txt_in), q(self.guid1), q(self.guid2), q(self.vec1), q(self.vec2))
+
+
 # ------------------------------------------------------------------ entry points
 def workspace_size(shape: Shape, op: int) -> int:
     n = ctypes.c_size_t(0)
@@ -259,6 +290,25 @@ def mmdit_step_fwd(shape: Shape, w: StepWeights, x_lat, x_txt_in, sigma: float, 
     st = step_struct if step_struct is not None else w.struct()
     call("mmdit_step_fwd", ctypes.byref(shape), ctypes.byref(st), ptr(x_lat), ptr(x_txt_in), float(sigma),
          float(sigma_next), ptr(v_out), ptr(ws), ws.numel(), stream_handle(stream))
+
+
+def sample_workspace_size(shape: Shape, n_double: int, n_single: int, C_txt: int, n_steps: int) -> int:
+    n = ctypes.c_size_t(0)
+    call("mmdit_sample_workspace_size", ctypes.byref(shape), n_double, n_single, C_txt, n_steps, ctypes.byref(n))
+    return n.value
+
+
+def mmdit_sample(shape: Shape, w: StepWeights, cond: CondWeights, x_lat, txt, pooled, guidance: float, sigmas,
+                 ws: torch.Tensor, graph: bool = True, stream=None, step_struct: Optional[StepW] = None):
+    """The sampling loop over the host schedule sigmas (n_steps + 1 values),
+    x_lat updated in place; graph=True replays steps 1.. from one captured
+    CUDA graph (the call then waits for them)."""
+    st = step_struct if step_struct is not None else w.struct()
+    cs = cond.struct()
+    sig = (ctypes.c_double * len(sigmas))(*[float(v) for v in sigmas])
+    call("mmdit_sample", ctypes.byref(shape), ctypes.byref(st), ctypes.byref(cs), ptr(x_lat), ptr(txt), ptr(pooled),
+         float(guidance), sig, len(sigmas) - 1, MMDIT_SAMPLE_GRAPH if graph else 0, ptr(ws), ws.numel(),
+         stream_handle(stream))
 
 
 def euler_step(x: torch.Tensor, v: torch.Tensor, sigma: float, sigma_next: float, stream=None):

@@ -500,6 +500,115 @@ static bool single_w_ok(const mmdit_single_w_t* w, bool i8) {
   return w->q_norm && w->k_norm && al16(w->q_norm) && al16(w->k_norm);
 }
 
+static int step_w_check(const mmdit_shape_t& shape, const mmdit_step_w_t& w) {
+  if (w.n_double < 0 || w.n_single < 0 || (w.n_double && !w.doubles) || (w.n_single && !w.singles))
+    return MMDIT_ERR_ARG;
+  const bool i8 = shape.w_dtype == MMDIT_I8W;
+  if (!lin_ok(w.time1, i8) || !lin_ok(w.time2, i8) || !lin_ok(w.img_in, i8) || !lin_ok(w.final_mod, i8) ||
+      !lin_ok(w.final, i8))
+    return MMDIT_ERR_ARG;
+  for (int i = 0; i < w.n_double; ++i)
+    if (!double_w_ok(&w.doubles[i], i8)) return MMDIT_ERR_ARG;
+  for (int i = 0; i < w.n_single; ++i)
+    if (!single_w_ok(&w.singles[i], i8)) return MMDIT_ERR_ARG;
+  return MMDIT_OK;
+}
+
+// ----------------------------------------------------------------- step
+// One denoising step on the laid-out step workspace sw.  vec_add (or null)
+// is added to the timestep embedding.  With sig_tab / sig_idx set, sigma and
+// sigma_next are read on the device as sig_tab[k], sig_tab[k + 1] with
+// k = *sig_idx (the host values are ignored), so one captured step replays
+// for every step of a schedule.
+static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step_w_t& w, float* x_lat,
+                     const float* x_txt_in, double sigma, double sigma_next, float* v_out, const float* vec_add,
+                     const double* sig_tab, const int* sig_idx, bool build_rope, const StepWS& sw, cudaStream_t st) {
+  const bool i8 = shape.w_dtype == MMDIT_I8W;
+  const int D = d.D, C = shape.C_lat;
+  if (build_rope)
+    MMDIT_CUDA(launch_rope_build(d.Lt, shape.grid_w, d.L, shape.rope_axes, shape.rope_theta, nullptr, sw.cs,
+                                 sw.sn, st));
+  // timestep embedding: vec = time2 SiLU(time1 sinusoid(1000 sigma))
+  MMDIT_CUDA(launch_sinusoid(1000.0 * sigma, d.B, shape.t_dim, sw.temb, st, sig_tab, sig_idx, 1000.0));
+  float* th = sw.temb + (size_t)d.B * shape.t_dim;
+  MMDIT_CUDA(launch_gemv(w.time1.w, w.time1.scale != nullptr, w.time1.scale, w.time1.b, sw.temb, d.B, D,
+                         shape.t_dim, 0, th, st));
+  MMDIT_CUDA(launch_gemv(w.time2.w, w.time2.scale != nullptr, w.time2.scale, w.time2.b, th, d.B, D, D, 1,
+                         sw.vec, st));
+  if (vec_add) MMDIT_CUDA(launch_add(sw.vec, vec_add, (long long)d.B * D, st));
+  // modulation vectors of every block and of the final layer (they depend on vec only): one batched launch
+  std::vector<GemvJob> jobs;
+  float* mp = sw.mods;
+  for (int i = 0; i < w.n_double; ++i)
+    for (int s = 0; s < 2; ++s) {
+      const mmdit_linear_t& l = w.doubles[i].mod[s];
+      jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 6 * D});
+      mp += (size_t)d.B * 6 * D;
+    }
+  for (int i = 0; i < w.n_single; ++i) {
+    const mmdit_linear_t& l = w.singles[i].mod;
+    jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 3 * D});
+    mp += (size_t)d.B * 3 * D;
+  }
+  float* mod_final = mp;
+  jobs.push_back(GemvJob{w.final_mod.w, w.final_mod.scale, w.final_mod.b, mod_final, 2 * D});
+  MMDIT_CUDA(launch_gemv_batched(jobs.data(), (int)jobs.size(), i8, sw.vec, d.B, D, 1, st));
+  // residual stream x = [text; image] per sample: text copied in, image from img_in
+  if (d.Lt > 0)
+    MMDIT_CUDA(cudaMemcpy2DAsync(sw.x, (size_t)d.L * D * 4, x_txt_in, (size_t)d.Lt * D * 4, (size_t)d.Lt * D * 4, d.B,
+                                 cudaMemcpyDeviceToDevice, st));
+  MMDIT_CUDA(launch_cast_bf16(x_lat, sw.xlat, (long long)d.B * d.Li * C, st));
+  {
+    GemmParams p = gemm_params(GM_STORE_F32);
+    p.out = sw.x;
+    p.out_ld = D;
+    p.out_seg_rows = d.L;
+    p.out_row_off = d.Lt;
+    Carve bc{sw.block, 0};
+    uint16_t* wdeq = i8 ? bc.take<uint16_t>((size_t)D * C) : nullptr;
+    MMDIT_TRY(run_gemm(sw.xlat, C, d.Li, d.Li, d.B, C, w.img_in, D, p, wdeq, st));
+  }
+  // blocks
+  mp = sw.mods;
+  {
+    Carve bc{sw.block, 0};
+    DoubleWS dw;
+    layout_double(d, i8, false, bc, dw);
+    for (int i = 0; i < w.n_double; ++i) {
+      MMDIT_TRY(double_block_impl(shape, d, w.doubles[i], nullptr, mp, sw.x, d.L, sw.x + (size_t)d.Lt * D, d.L,
+                                  sw.cs, sw.sn, dw, st));
+      mp += (size_t)2 * d.B * 6 * D;
+    }
+  }
+  {
+    Carve bc{sw.block, 0};
+    SingleWS ssw;
+    layout_single(d, i8, false, bc, ssw);
+    for (int i = 0; i < w.n_single; ++i) {
+      MMDIT_TRY(single_block_impl(shape, d, w.singles[i], nullptr, mp, sw.x, sw.cs, sw.sn, ssw, st));
+      mp += (size_t)d.B * 3 * D;
+    }
+  }
+  // final layer on the image tokens and the Euler update
+  {
+    Carve bc{sw.block, 0};
+    uint16_t* y = bc.take<uint16_t>((size_t)d.B * d.Li * D);
+    uint16_t* wdeq = i8 ? bc.take<uint16_t>((size_t)D * C) : nullptr;
+    MMDIT_CUDA(launch_ln_modulate(sw.x + (size_t)d.Lt * D, d.L, d.Li, d.B, D, mod_final, mod_final + D, 2 * D,
+                                  shape.eps_ln, y, st));
+    GemmParams p = gemm_params(GM_STORE_F32);
+    float* v = v_out ? v_out : sw.v;
+    p.out = v;
+    p.out_ld = C;
+    p.out_seg_rows = d.Li;
+    MMDIT_TRY(run_gemm(y, D, d.Li, d.Li, d.B, D, w.final, C, p, wdeq, st));
+    MMDIT_CUDA(launch_euler(x_lat, v, false, (float)(sigma_next - sigma), (long long)d.B * d.Li * C, st, sig_tab,
+                            sig_idx));
+  }
+  return MMDIT_OK;
+}
+
+
 }  // namespace mmdit
 
 using namespace mmdit;
@@ -538,7 +647,8 @@ long long mmdit_launch_count(void) { return g_launches.load(); }
 const char* mmdit_kernel_name(int kernel_id) {
   static const char* names[KID_COUNT] = {"gemm_bf16_tc", "attn_fwd",   "ln_modulate", "gemv",      "sinusoid",
                                          "rope_build",   "rope_apply", "euler",       "quantize_w8", "dequant_i8",
-                                         "cast_bf16",    "attn_prep",  "wait_selftest"};
+                                         "cast_bf16",    "attn_prep",  "wait_selftest", "add_f32",
+                                         "step_counter"};
   return (kernel_id >= 0 && kernel_id < KID_COUNT) ? names[kernel_id] : "unknown";
 }
 
@@ -723,104 +833,133 @@ int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x
   Dims d;
   MMDIT_TRY(check_shape(shape, &d));
   if (!w || !x_lat || (d.Lt > 0 && !x_txt_in) || !ws) return MMDIT_ERR_ARG;
-  if (w->n_double < 0 || w->n_single < 0 || (w->n_double && !w->doubles) || (w->n_single && !w->singles))
-    return MMDIT_ERR_ARG;
-  const bool i8 = shape->w_dtype == MMDIT_I8W;
-  if (!lin_ok(w->time1, i8) || !lin_ok(w->time2, i8) || !lin_ok(w->img_in, i8) || !lin_ok(w->final_mod, i8) ||
-      !lin_ok(w->final, i8))
-    return MMDIT_ERR_ARG;
-  for (int i = 0; i < w->n_double; ++i)
-    if (!double_w_ok(&w->doubles[i], i8)) return MMDIT_ERR_ARG;
-  for (int i = 0; i < w->n_single; ++i)
-    if (!single_w_ok(&w->singles[i], i8)) return MMDIT_ERR_ARG;
+  MMDIT_TRY(step_w_check(*shape, *w));
   if (!al16(x_lat) || (x_txt_in && !al16(x_txt_in)) || !al16(ws) || (v_out && !al16(v_out))) return MMDIT_ERR_ALIGN;
   size_t need = 0;
   MMDIT_TRY(mmdit_step_workspace_size(shape, w->n_double, w->n_single, &need));
   if (ws_bytes < need) return MMDIT_ERR_WORKSPACE;
   MMDIT_TRY(check_device());
-  cudaStream_t st = S(stream);
-  const int D = d.D, C = shape->C_lat;
   Carve c{static_cast<uint8_t*>(ws), 0};
   StepWS sw;
   layout_step(d, *shape, w->n_double, w->n_single, c, sw);
+  return step_impl(*shape, d, *w, x_lat, x_txt_in, sigma, sigma_next, v_out, nullptr, nullptr, nullptr, true, sw,
+                   S(stream));
+}
+
+// Workspace of the sampling loop: the step's, then the conditioning.
+struct SampleWS {
+  float *x_txt, *vec_cond, *ctemb, *phid, *ptmp;
+  double* sig;
+  int* ctr;
+  uint16_t* wdeq;
+};
+static void layout_sample(const Dims& d, const mmdit_shape_t& s, int C_txt, int n_steps, Carve& c, SampleWS& w) {
+  const bool i8 = s.w_dtype == MMDIT_I8W;
+  w.x_txt = c.take<float>((size_t)d.B * d.Lt * d.D);
+  w.vec_cond = c.take<float>((size_t)d.B * d.D);
+  w.ctemb = c.take<float>((size_t)d.B * (s.t_dim + d.D));
+  w.phid = c.take<float>((size_t)d.B * d.D);
+  w.ptmp = c.take<float>((size_t)d.B * d.D);
+  w.sig = c.take<double>((size_t)n_steps + 1);
+  w.ctr = c.take<int>(4);
+  w.wdeq = i8 ? c.take<uint16_t>((size_t)d.D * C_txt) : nullptr;
+}
+
+int mmdit_sample_workspace_size(const mmdit_shape_t* shape, int n_double, int n_single, int C_txt, int n_steps,
+                                size_t* bytes) {
+  if (!bytes || n_steps < 1 || C_txt <= 0) return MMDIT_ERR_ARG;
+  size_t step = 0;
+  MMDIT_TRY(mmdit_step_workspace_size(shape, n_double, n_single, &step));
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  Carve c{nullptr, step};
+  SampleWS w;
+  layout_sample(d, *shape, C_txt, n_steps, c, w);
+  *bytes = c.off + 256;
+  return MMDIT_OK;
+}
+
+int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdit_cond_w_t* cond, float* x_lat,
+                 const void* txt, const float* pooled, double guidance, const double* sigmas, int n_steps, int flags,
+                 void* ws, size_t ws_bytes, void* stream) {
+  Dims d;
+  MMDIT_TRY(check_shape(shape, &d));
+  if (!w || !cond || !x_lat || (d.Lt > 0 && !txt) || !pooled || !sigmas || !ws || n_steps < 1) return MMDIT_ERR_ARG;
+  if (flags & ~MMDIT_SAMPLE_GRAPH) return MMDIT_ERR_ARG;
+  MMDIT_TRY(step_w_check(*shape, *w));
+  const bool i8 = shape->w_dtype == MMDIT_I8W;
+  if (!lin_ok(cond->txt_in, i8) || !lin_ok(cond->guid1, i8) || !lin_ok(cond->guid2, i8) || !lin_ok(cond->vec1, i8) ||
+      !lin_ok(cond->vec2, i8))
+    return MMDIT_ERR_ARG;
+  const int D = d.D, C_txt = cond->C_txt, C_pool = cond->C_pool;
+  if (C_txt <= 0 || C_txt % 64 || C_pool <= 0 || C_pool % 16) return MMDIT_ERR_SHAPE;
+  if ((size_t)d.B * (C_pool > D ? C_pool : D) * 4 > 200 * 1024) return MMDIT_ERR_SHAPE;  // GEMV input in shared memory
+  if (!al16(x_lat) || (txt && !al16(txt)) || !al16(pooled) || !al16(ws)) return MMDIT_ERR_ALIGN;
+  size_t need = 0;
+  MMDIT_TRY(mmdit_sample_workspace_size(shape, w->n_double, w->n_single, C_txt, n_steps, &need));
+  if (ws_bytes < need) return MMDIT_ERR_WORKSPACE;
+  MMDIT_TRY(check_device());
+  cudaStream_t st = S(stream);
+  Carve c{static_cast<uint8_t*>(ws), 0};
+  StepWS sw;
+  layout_step(d, *shape, w->n_double, w->n_single, c, sw);
+  SampleWS sa;
+  layout_sample(d, *shape, C_txt, n_steps, c, sa);
+
+  // step-independent work: RoPE tables, the text stream, the conditioning vector
   MMDIT_CUDA(launch_rope_build(d.Lt, shape->grid_w, d.L, shape->rope_axes, shape->rope_theta, nullptr, sw.cs, sw.sn,
                                st));
-  // timestep embedding: vec = time2 SiLU(time1 sinusoid(1000 sigma))
-  MMDIT_CUDA(launch_sinusoid(1000.0 * sigma, d.B, shape->t_dim, sw.temb, st));
-  float* th = sw.temb + (size_t)d.B * shape->t_dim;
-  MMDIT_CUDA(launch_gemv(w->time1.w, w->time1.scale != nullptr, w->time1.scale, w->time1.b, sw.temb, d.B, D,
-                         shape->t_dim, 0, th, st));
-  MMDIT_CUDA(launch_gemv(w->time2.w, w->time2.scale != nullptr, w->time2.scale, w->time2.b, th, d.B, D, D, 1,
-                         sw.vec, st));
-  // modulation vectors of every block and of the final layer (they depend on vec only): one batched launch
-  std::vector<GemvJob> jobs;
-  float* mp = sw.mods;
-  for (int i = 0; i < w->n_double; ++i)
-    for (int s = 0; s < 2; ++s) {
-      const mmdit_linear_t& l = w->doubles[i].mod[s];
-      jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 6 * D});
-      mp += (size_t)d.B * 6 * D;
-    }
-  for (int i = 0; i < w->n_single; ++i) {
-    const mmdit_linear_t& l = w->singles[i].mod;
-    jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 3 * D});
-    mp += (size_t)d.B * 3 * D;
-  }
-  float* mod_final = mp;
-  jobs.push_back(GemvJob{w->final_mod.w, w->final_mod.scale, w->final_mod.b, mod_final, 2 * D});
-  MMDIT_CUDA(launch_gemv_batched(jobs.data(), (int)jobs.size(), i8, sw.vec, d.B, D, 1, st));
-  // residual stream x = [text; image] per sample: text copied in, image from img_in
-  if (d.Lt > 0)
-    MMDIT_CUDA(cudaMemcpy2DAsync(sw.x, (size_t)d.L * D * 4, x_txt_in, (size_t)d.Lt * D * 4, (size_t)d.Lt * D * 4, d.B,
-                                 cudaMemcpyDeviceToDevice, st));
-  MMDIT_CUDA(launch_cast_bf16(x_lat, sw.xlat, (long long)d.B * d.Li * C, st));
-  {
+  if (d.Lt > 0) {
     GemmParams p = gemm_params(GM_STORE_F32);
-    p.out = sw.x;
+    p.out = sa.x_txt;
     p.out_ld = D;
-    p.out_seg_rows = d.L;
-    p.out_row_off = d.Lt;
-    Carve bc{sw.block, 0};
-    uint16_t* wdeq = i8 ? bc.take<uint16_t>((size_t)D * C) : nullptr;
-    MMDIT_TRY(run_gemm(sw.xlat, C, d.Li, d.Li, d.B, C, w->img_in, D, p, wdeq, st));
+    p.out_seg_rows = d.Lt;
+    MMDIT_TRY(run_gemm(txt, C_txt, d.Lt, d.Lt, d.B, C_txt, cond->txt_in, D, p, sa.wdeq, st));
   }
-  // blocks
-  mp = sw.mods;
-  {
-    Carve bc{sw.block, 0};
-    DoubleWS dw;
-    layout_double(d, i8, false, bc, dw);
-    for (int i = 0; i < w->n_double; ++i) {
-      MMDIT_TRY(double_block_impl(*shape, d, w->doubles[i], nullptr, mp, sw.x, d.L, sw.x + (size_t)d.Lt * D, d.L,
-                                  sw.cs, sw.sn, dw, st));
-      mp += (size_t)2 * d.B * 6 * D;
-    }
+  float* gh = sa.ctemb + (size_t)d.B * shape->t_dim;
+  MMDIT_CUDA(launch_sinusoid(1000.0 * guidance, d.B, shape->t_dim, sa.ctemb, st));
+  MMDIT_CUDA(launch_gemv(cond->guid1.w, i8, cond->guid1.scale, cond->guid1.b, sa.ctemb, d.B, D, shape->t_dim, 0, gh,
+                         st));
+  MMDIT_CUDA(launch_gemv(cond->guid2.w, i8, cond->guid2.scale, cond->guid2.b, gh, d.B, D, D, 1, sa.vec_cond, st));
+  MMDIT_CUDA(launch_gemv(cond->vec1.w, i8, cond->vec1.scale, cond->vec1.b, pooled, d.B, D, C_pool, 0, sa.phid, st));
+  MMDIT_CUDA(launch_gemv(cond->vec2.w, i8, cond->vec2.scale, cond->vec2.b, sa.phid, d.B, D, D, 1, sa.ptmp, st));
+  MMDIT_CUDA(launch_add(sa.vec_cond, sa.ptmp, (long long)d.B * D, st));
+
+  // step 0 eagerly (this also performs every one-time kernel set-up before a capture)
+  MMDIT_TRY(step_impl(*shape, d, *w, x_lat, sa.x_txt, sigmas[0], sigmas[1], nullptr, sa.vec_cond, nullptr, nullptr,
+                      false, sw, st));
+  const bool graph = (flags & MMDIT_SAMPLE_GRAPH) && n_steps > 1 && !g_trace.on;
+  if (!graph) {
+    for (int i = 1; i < n_steps; ++i)
+      MMDIT_TRY(step_impl(*shape, d, *w, x_lat, sa.x_txt, sigmas[i], sigmas[i + 1], nullptr, sa.vec_cond, nullptr,
+                          nullptr, false, sw, st));
+    return MMDIT_OK;
   }
-  {
-    Carve bc{sw.block, 0};
-    SingleWS ssw;
-    layout_single(d, i8, false, bc, ssw);
-    for (int i = 0; i < w->n_single; ++i) {
-      MMDIT_TRY(single_block_impl(*shape, d, w->singles[i], nullptr, mp, sw.x, sw.cs, sw.sn, ssw, st));
-      mp += (size_t)d.B * 3 * D;
-    }
+  // Steps 1 .. n - 1: one captured step reading sigma_k, sigma_{k+1} at the
+  // device counter k, which the captured step advances at its end.
+  MMDIT_CUDA(cudaMemcpyAsync(sa.sig, sigmas, sizeof(double) * ((size_t)n_steps + 1), cudaMemcpyHostToDevice, st));
+  MMDIT_CUDA(launch_counter(sa.ctr, 1, false, st));
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return MMDIT_ERR_CUDA;
+  cudaGraph_t graph_def = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int rc = MMDIT_OK;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    rc = MMDIT_ERR_CUDA;
+  } else {
+    rc = step_impl(*shape, d, *w, x_lat, sa.x_txt, 0.0, 0.0, nullptr, sa.vec_cond, sa.sig, sa.ctr, false, sw, cs);
+    if (rc == MMDIT_OK) rc = cuda_status(launch_counter(sa.ctr, 1, true, cs));
+    const cudaError_t e = cudaStreamEndCapture(cs, &graph_def);  // always closes the capture
+    if (rc == MMDIT_OK && e != cudaSuccess) rc = MMDIT_ERR_CUDA;
   }
-  // final layer on the image tokens and the Euler update
-  {
-    Carve bc{sw.block, 0};
-    uint16_t* y = bc.take<uint16_t>((size_t)d.B * d.Li * D);
-    uint16_t* wdeq = i8 ? bc.take<uint16_t>((size_t)D * C) : nullptr;
-    MMDIT_CUDA(launch_ln_modulate(sw.x + (size_t)d.Lt * D, d.L, d.Li, d.B, D, mod_final, mod_final + D, 2 * D,
-                                  shape->eps_ln, y, st));
-    GemmParams p = gemm_params(GM_STORE_F32);
-    float* v = v_out ? v_out : sw.v;
-    p.out = v;
-    p.out_ld = C;
-    p.out_seg_rows = d.Li;
-    MMDIT_TRY(run_gemm(y, D, d.Li, d.Li, d.B, D, w->final, C, p, wdeq, st));
-    MMDIT_CUDA(launch_euler(x_lat, v, false, (float)(sigma_next - sigma), (long long)d.B * d.Li * C, st));
-  }
-  return MMDIT_OK;
+  if (rc == MMDIT_OK && cudaGraphInstantiate(&exec, graph_def, 0) != cudaSuccess) rc = MMDIT_ERR_CUDA;
+  for (int i = 1; rc == MMDIT_OK && i < n_steps; ++i)
+    if (cudaGraphLaunch(exec, st) != cudaSuccess) rc = MMDIT_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess && rc == MMDIT_OK) rc = MMDIT_ERR_CUDA;  // replays done
+  if (exec) cudaGraphExecDestroy(exec);
+  if (graph_def) cudaGraphDestroy(graph_def);
+  cudaStreamDestroy(cs);
+  return rc;
 }
 
 int mmdit_selftest_wait_timeout(unsigned limit_us, void* stream) {

@@ -199,16 +199,29 @@ __global__ void __launch_bounds__(256) gemv_batched_kernel(const __grid_constant
 }
 
 // ------------------------------------------------------------------ timestep sinusoid
-__global__ void sinusoid_kernel(double t, int B, int dim, float* __restrict__ out) {
+// t_tab != null: t = t_scale * t_tab[*t_idx] (the step's sigma read on the
+// device, so that a captured step replays for every step of a schedule).
+__global__ void sinusoid_kernel(double t, const double* __restrict__ t_tab, const int* __restrict__ t_idx,
+                                double t_scale, int B, int dim, float* __restrict__ out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const int half = dim / 2;
   if (i >= B * dim) return;
+  if (t_tab) t = t_scale * t_tab[*t_idx];
   const int j = i % dim;
   const int jj = j < half ? j : j - half;
   const double f = exp(-log(10000.0) * (double)jj / (double)half);
   const double a = t * f;
   out[i] = (float)(j < half ? cos(a) : sin(a));
 }
+
+// y[i] += x[i]
+__global__ void add_f32_kernel(float* __restrict__ y, const float* __restrict__ x, long long n) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] += x[i];
+}
+
+// The device step counter of a replayed step: set once, advanced at the end of each step.
+__global__ void counter_kernel(int* c, int value, int add) { *c = add ? *c + value : value; }
 
 // ------------------------------------------------------------------ RoPE
 // ids [L,3] and cos/sin [L, d/2]: angle = pos_axis * theta^(-2i/d_axis), fp64.
@@ -268,7 +281,17 @@ __global__ void rope_apply_kernel(uint16_t* __restrict__ x, long long rows, int 
 }
 
 // ------------------------------------------------------------------ Euler
-__global__ void euler_f32_kernel(float* __restrict__ x, const float* __restrict__ v, float dt, long long n) {
+// sig_tab != null: dt = sig_tab[k + 1] - sig_tab[k], k = *sig_idx, rounded once
+// to fp32 (the same rounding as the host-side dt).
+__device__ __forceinline__ float euler_dt(float dt, const double* sig_tab, const int* sig_idx) {
+  if (!sig_tab) return dt;
+  const int k = *sig_idx;
+  return (float)(sig_tab[k + 1] - sig_tab[k]);
+}
+
+__global__ void euler_f32_kernel(float* __restrict__ x, const float* __restrict__ v, float dt,
+                                 const double* __restrict__ sig_tab, const int* __restrict__ sig_idx, long long n) {
+  dt = euler_dt(dt, sig_tab, sig_idx);
   const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i + 3 < n) {
     float4 a = *reinterpret_cast<float4*>(x + i);
@@ -280,7 +303,9 @@ __global__ void euler_f32_kernel(float* __restrict__ x, const float* __restrict_
   }
 }
 
-__global__ void euler_bf16_kernel(float* __restrict__ x, const uint16_t* __restrict__ v, float dt, long long n) {
+__global__ void euler_bf16_kernel(float* __restrict__ x, const uint16_t* __restrict__ v, float dt,
+                                  const double* __restrict__ sig_tab, const int* __restrict__ sig_idx, long long n) {
+  dt = euler_dt(dt, sig_tab, sig_idx);
   const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i + 3 < n) {
     float4 a = *reinterpret_cast<float4*>(x + i);
@@ -504,10 +529,11 @@ cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const 
   return cudaSuccess;
 }
 
-cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st) {
+cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st, const double* t_tab,
+                            const int* t_idx, double t_scale) {
   const int n = B * dim;
   launch_begin(KID_SINUSOID, st);
-  sinusoid_kernel<<<(n + 255) / 256, 256, 0, st>>>(t, B, dim, out);
+  sinusoid_kernel<<<(n + 255) / 256, 256, 0, st>>>(t, t_tab, t_idx, t_scale, B, dim, out);
   launch_end(st);
   return cudaGetLastError();
 }
@@ -531,14 +557,29 @@ cudaError_t launch_rope_apply(uint16_t* x, long long rows, int L, int H, int d, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long long n, cudaStream_t st) {
+cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long long n, cudaStream_t st,
+                         const double* sig_tab, const int* sig_idx) {
   const long long threads = (n + 3) / 4;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
   launch_begin(KID_EULER, st);
   if (v_bf16)
-    euler_bf16_kernel<<<blocks, 256, 0, st>>>(x, reinterpret_cast<const uint16_t*>(v), dt, n);
+    euler_bf16_kernel<<<blocks, 256, 0, st>>>(x, reinterpret_cast<const uint16_t*>(v), dt, sig_tab, sig_idx, n);
   else
-    euler_f32_kernel<<<blocks, 256, 0, st>>>(x, reinterpret_cast<const float*>(v), dt, n);
+    euler_f32_kernel<<<blocks, 256, 0, st>>>(x, reinterpret_cast<const float*>(v), dt, sig_tab, sig_idx, n);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add(float* y, const float* x, long long n, cudaStream_t st) {
+  launch_begin(KID_ADD, st);
+  add_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, x, n);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_counter(int* c, int value, bool add, cudaStream_t st) {
+  launch_begin(KID_COUNTER, st);
+  counter_kernel<<<1, 1, 0, st>>>(c, value, add ? 1 : 0);
   launch_end(st);
   return cudaGetLastError();
 }

@@ -23,12 +23,20 @@ struct GemvJob {
 };
 cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const float* x, int B, int K, int act,
                                 cudaStream_t st);
-cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st);
+// t_tab != null: t = t_scale * t_tab[*t_idx], read on the device.
+cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st, const double* t_tab = nullptr,
+                            const int* t_idx = nullptr, double t_scale = 1.0);
 cudaError_t launch_rope_build(int L_txt, int grid_w, int L, const int axes[3], double theta, int32_t* ids, float* cs,
                               float* sn, cudaStream_t st);
 cudaError_t launch_rope_apply(uint16_t* x, long long rows, int L, int H, int d, int row_stride, const float* cs,
                               const float* sn, cudaStream_t st);
-cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long long n, cudaStream_t st);
+// sig_tab != null: dt = sig_tab[k + 1] - sig_tab[k], k = *sig_idx, read on the device.
+cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long long n, cudaStream_t st,
+                         const double* sig_tab = nullptr, const int* sig_idx = nullptr);
+// y += x (n floats).
+cudaError_t launch_add(float* y, const float* x, long long n, cudaStream_t st);
+// *c = value (add = false) or *c += value (add = true), one thread.
+cudaError_t launch_counter(int* c, int value, bool add, cudaStream_t st);
 cudaError_t launch_quantize(const void* w, bool w_bf16, int N, int K, int8_t* q, float* scale, cudaStream_t st);
 cudaError_t launch_dequant_i8(const int8_t* q, uint16_t* out, long long n, cudaStream_t st);
 cudaError_t launch_cast_bf16(const float* x, uint16_t* y, long long n, cudaStream_t st);

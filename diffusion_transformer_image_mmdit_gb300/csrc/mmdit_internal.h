@@ -102,6 +102,8 @@ enum KernelId : int {
   KID_CAST,
   KID_ATTN_PREP,
   KID_SELFTEST,
+  KID_ADD,
+  KID_COUNTER,
   KID_COUNT
 };
 // Bracket every kernel launch: counts launches and, while a trace is on,

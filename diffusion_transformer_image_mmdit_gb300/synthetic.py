@@ -171,6 +171,18 @@ def embed_params(D: int, C_lat: int, t_dim: int = 256, seed: int = 0) -> dict:
     return w
 
 
+def cond_params(D: int, t_dim: int, C_txt: int, C_pool: int, seed: int = 0) -> dict:
+    """Conditioning layers of the sampling loop: text projection, guidance and
+    pooled-text MLPs."""
+    w = {}
+    w["txt_in_w"], w["txt_in_b"] = linear_params("cond.txt_in", D, C_txt, seed)
+    w["g_w1"], w["g_b1"] = linear_params("cond.guid1", D, t_dim, seed)
+    w["g_w2"], w["g_b2"] = linear_params("cond.guid2", D, D, seed)
+    w["y_w1"], w["y_b1"] = linear_params("cond.vec1", D, C_pool, seed)
+    w["y_w2"], w["y_b2"] = linear_params("cond.vec2", D, D, seed)
+    return w
+
+
 def activations(B: int, L_txt: int, L_img: int, D: int, C_lat: int = 0, seed: int = 0) -> dict:
     a = {"vec": normal_f32("vec", (B, D), seed=seed),
          "x_txt": normal_f32("x_txt", (B, L_txt, D), seed=seed),

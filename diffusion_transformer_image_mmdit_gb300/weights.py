@@ -8,7 +8,7 @@ from typing import Optional
 import numpy as np
 import torch
 
-from .api import DoubleWeights, LinearDev, SingleWeights, StepWeights
+from .api import CondWeights, DoubleWeights, LinearDev, SingleWeights, StepWeights
 
 
 def _bf16(a: np.ndarray, device) -> torch.Tensor:
@@ -45,6 +45,12 @@ def step_from_host(p: dict, device="cuda") -> StepWeights:
                        linear_from_host(p["final_w"], p["final_b"], device),
                        [double_from_host(d, device) for d in p["double"]],
                        [single_from_host(s, device) for s in p["single"]])
+
+
+def cond_from_host(p: dict, device="cuda") -> CondWeights:
+    L = lambda w, b: linear_from_host(p[w], p[b], device)
+    return CondWeights(L("txt_in_w", "txt_in_b"), L("g_w1", "g_b1"), L("g_w2", "g_b2"), L("y_w1", "y_b1"),
+                       L("y_w2", "y_b2"))
 
 
 # ------------------------------------------------------------------ drawn on the GPU
@@ -84,3 +90,7 @@ class DeviceDraw:
         return StepWeights(self.linear(D, t_dim), self.linear(D, D), self.linear(D, C_lat), self.linear(2 * D, D),
                            self.linear(C_lat, D), [self.double(D, d, Dm) for _ in range(n_double)],
                            [self.single(D, d, Dm) for _ in range(n_single)])
+
+    def cond(self, D: int, t_dim: int, C_txt: int, C_pool: int) -> CondWeights:
+        return CondWeights(self.linear(D, C_txt), self.linear(D, t_dim), self.linear(D, D), self.linear(D, C_pool),
+                           self.linear(D, D))

@@ -249,6 +249,48 @@ int mmdit_single_block_fwd(const mmdit_shape_t* shape, const mmdit_single_w_t* w
 int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_txt_in,
                    double sigma, double sigma_next, float* v_out, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------ sampling loop */
+/* Conditioning around the denoiser.  The SGLang blog ("Architecture") has a
+ * text encoder produce the conditioning embeddings that the DiT denoises
+ * against over 20-50 steps; the flux-amd-rocm benchmark notes sample
+ * FLUX.1-dev for 28 steps at guidance 3.5.  Neither defines the layers;
+ * readings taken: txt_in is one linear projection C_txt -> D of the
+ * text-encoder output; the guidance scale g goes through the timestep's
+ * sinusoid of 1000 g and a two-layer SiLU MLP (guid1: t_dim -> D,
+ * guid2: D -> D); the pooled text vector y through vec1: C_pool -> D, SiLU,
+ * vec2: D -> D.  Both MLP outputs are added to the timestep embedding of
+ * every step.  Weights follow shape->w_dtype like the step's.
+ * C_txt a multiple of 64, C_pool a multiple of 16. */
+typedef struct {
+  mmdit_linear_t txt_in, guid1, guid2, vec1, vec2;
+  int C_txt, C_pool;
+} mmdit_cond_w_t;
+
+/* Replay the step through one captured CUDA graph (see mmdit_sample). */
+#define MMDIT_SAMPLE_GRAPH 1
+
+/* Workspace bytes of mmdit_sample for the given block counts, text width
+ * and number of steps. */
+int mmdit_sample_workspace_size(const mmdit_shape_t* shape, int n_double, int n_single, int C_txt, int n_steps,
+                                size_t* bytes);
+
+/* The sampling loop over sigmas[0 .. n_steps] (host array, fp64).
+ * x_txt = txt_in(txt) and vec_cond = guid2 SiLU(guid1 sinusoid(1000
+ * guidance)) + vec2 SiLU(vec1 pooled) are formed once; then for i = 0 ..
+ * n_steps - 1 the step of mmdit_step_fwd runs with sigma_i, sigma_{i+1}
+ * and vec_cond added to its timestep embedding, updating x_lat in place.
+ * x_lat: device fp32 [B, L_img, C_lat]; txt: device bf16 [B, L_txt, C_txt]
+ * (ignored when L_txt = 0); pooled: device fp32 [B, C_pool].
+ * flags & MMDIT_SAMPLE_GRAPH: step 0 runs eagerly, steps 1 .. n_steps - 1
+ * replay one captured graph of a step that reads its sigmas from the
+ * workspace on the device (bit-identical results); the call then returns
+ * only after the replays complete, and falls back to eager launches while
+ * a kernel trace is being recorded.  Without the flag the call only
+ * enqueues work on `stream`. */
+int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdit_cond_w_t* cond, float* x_lat,
+                 const void* txt, const float* pooled, double guidance, const double* sigmas, int n_steps, int flags,
+                 void* ws, size_t ws_bytes, void* stream);
+
 /* Flow-matching Euler update (Luminal blog, "The AMD MI300X pipeline": the
  * sampler integrates the latent in fp32): x[i] += (sigma_next - sigma) v[i].
  * x: device fp32 [n]; v: device [n], v_dtype MMDIT_F32 or MMDIT_BF16.

@@ -93,6 +93,38 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
                                    256, ctypes.c_void_p(16), 1 << 30, None) == -2
 
 
+def test_sample_arguments_rejected_before_launch(lib):
+    from diffusion_transformer_image_mmdit_gb300 import _lib
+    s = _shape()
+    s.C_lat, s.t_dim = 64, 256
+    n_big = ctypes.c_size_t(0)
+    n_small = ctypes.c_size_t(0)
+    assert lib.mmdit_sample_workspace_size(ctypes.byref(s), 1, 1, 128, 28, ctypes.byref(n_big)) == 0
+    assert lib.mmdit_sample_workspace_size(ctypes.byref(s), 1, 1, 128, 1, ctypes.byref(n_small)) == 0
+    step = ctypes.c_size_t(0)
+    assert lib.mmdit_step_workspace_size(ctypes.byref(s), 1, 1, ctypes.byref(step)) == 0
+    assert n_big.value >= n_small.value > step.value
+    assert lib.mmdit_sample_workspace_size(ctypes.byref(s), 1, 1, 128, 0, ctypes.byref(n_small)) == -1
+    w = _lib.StepW()
+    sig = (ctypes.c_double * 3)(1.0, 0.5, 0.0)
+    p16 = ctypes.c_void_p(256)
+    # no conditioning weights
+    assert lib.mmdit_sample(ctypes.byref(s), ctypes.byref(w), None, p16, p16, p16, 3.5, sig, 2, 0, p16, 1 << 30,
+                            None) == -1
+    lin = _lib.Linear(ctypes.c_void_p(512), None, None)
+    w.time1 = w.time2 = w.img_in = w.final_mod = w.final = lin
+    c = _lib.CondW(lin, lin, lin, lin, lin, 96, 64)  # C_txt not a multiple of 64
+    assert lib.mmdit_sample(ctypes.byref(s), ctypes.byref(w), ctypes.byref(c), p16, p16, p16, 3.5, sig, 2, 0, p16,
+                            1 << 30, None) == -2
+    c.C_txt = 128
+    assert lib.mmdit_sample(ctypes.byref(s), ctypes.byref(w), ctypes.byref(c), p16, p16, p16, 3.5, sig, 2, 4, p16,
+                            1 << 30, None) == -1  # unknown flag
+    assert lib.mmdit_sample(ctypes.byref(s), ctypes.byref(w), ctypes.byref(c), ctypes.c_void_p(260), p16, p16, 3.5,
+                            sig, 2, 0, p16, 1 << 30, None) == -3  # misaligned latent
+    assert lib.mmdit_sample(ctypes.byref(s), ctypes.byref(w), ctypes.byref(c), p16, p16, p16, 3.5, sig, 2, 0, p16,
+                            16, None) == -4  # workspace too small
+
+
 def test_product_path_has_no_cpu_fallback():
     """The package never imports the oracle; the binding refuses to run without the library."""
     pkg = os.path.join(ROOT, "diffusion_transformer_image_mmdit_gb300")

@@ -9,7 +9,7 @@ import torch
 
 from diffusion_transformer_image_mmdit_gb300 import api, synthetic as S, weights as Wt
 from oracle import mmdit_oracle as O
-from tests.gpu_common import (CONFIGS, FULL, MAX_ABS, REL_L2_INT8_SCHEME, api_shape, assert_close, check_status, f32,
+from tests.gpu_common import (CONFIGS, FULL, MAX_ABS, REL_L2_INT8_SCHEME, api_shape, assert_close, bf16, check_status, f32,
                               gpu_tables, host, need_gpu, oracle_shape, rel_l2, tables)
 
 pytestmark = pytest.mark.gpu
@@ -168,6 +168,54 @@ def test_step_small(i8):
     tol = REL_L2_INT8_SCHEME if i8 else 1e-2
     assert rel_l2(host(v), ref_v) <= tol, rel_l2(host(v), ref_v)
     assert_close(host(xl), ref_x, rel=tol, what="step x_lat")
+
+
+# ------------------------------------------------------------------ sampling loop
+def _sample_case(n_steps, i8=False):
+    cfg = dict(CONFIGS["d128"])
+    cfg["B"] = 2
+    sh = oracle_shape(cfg)
+    sh.C_lat, sh.t_dim = 64, 256
+    C_txt, C_pool = 128, 64
+    W = S.embed_params(cfg["D"], sh.C_lat, sh.t_dim, seed=4)
+    W.update(S.cond_params(cfg["D"], sh.t_dim, C_txt, C_pool, seed=4))
+    W["double"] = [S.double_block_params("smp.d0", cfg["D"], cfg["d_head"], cfg["D_mlp"])]
+    W["single"] = [S.single_block_params("smp.s0", cfg["D"], cfg["d_head"], cfg["D_mlp"])]
+    x_lat = S.normal_f32("smp.lat", (cfg["B"], sh.L_img, sh.C_lat))
+    txt = S.normal_bf16("smp.txt", (cfg["B"], cfg["L_txt"], C_txt))
+    pooled = S.normal_f32("smp.y", (cfg["B"], C_pool))
+    sig = O.sigma_schedule(n_steps, O.shift_mu(sh.L_img))
+    shape = api_shape(cfg, C_lat=sh.C_lat, t_dim=sh.t_dim, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_BF16)
+    w, cond = Wt.step_from_host(W), Wt.cond_from_host(W)
+    if i8:
+        w, cond = w.quantized(), cond.quantized()
+    ws = api.alloc_workspace(api.sample_workspace_size(shape, 1, 1, C_txt, n_steps))
+    return cfg, sh, W, x_lat, txt, pooled, sig, shape, w, cond, ws
+
+
+def _run_sample(case, graph):
+    cfg, sh, W, x_lat, txt, pooled, sig, shape, w, cond, ws = case
+    xl = f32(x_lat)
+    api.mmdit_sample(shape, w, cond, xl, bf16(txt), f32(pooled), 3.5, sig, ws, graph=graph)
+    check_status()
+    return host(xl)
+
+
+@pytest.mark.parametrize("graph,i8", [(False, False), (True, False), (True, True)])
+def test_sample_loop_small(graph, i8):
+    case = _sample_case(3, i8)
+    cfg, sh, W, x_lat, txt, pooled, sig = case[:7]
+    got = _run_sample(case, graph)
+    ref = O.sample(x_lat, txt, pooled, 3.5, sig, W, sh)
+    # the update x_N - x_0 = sum_i (sigma_{i+1} - sigma_i) v_i carries the model's error
+    tol = REL_L2_INT8_SCHEME if i8 else 1e-2
+    assert rel_l2(got - x_lat, ref - x_lat) <= tol, rel_l2(got - x_lat, ref - x_lat)
+    assert_close(got, ref, rel=tol, what="sampled latent")
+
+
+def test_sample_graph_replay_is_bit_identical_to_launches():
+    case = _sample_case(4)
+    assert np.array_equal(_run_sample(case, False), _run_sample(case, True))
 
 
 # ------------------------------------------------------------------ Flux-sized blocks, sampled rows
