@@ -36,6 +36,9 @@ CONFIGS = {
     "c3pair": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=1, n_single=1, int8=False, n_steps=50, **FLUX),
     # one double block at 512^2 (512 + 1024 tokens)
     "c2": dict(B=1, L_txt=512, grid_h=32, grid_w=32, n_double=1, n_single=0, int8=False, n_steps=50, **FLUX),
+    # the whole sampling loop at 1024^2: 28 steps, guidance 3.5, text encoder width 4096, pooled width 768
+    "sample1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=False, n_steps=28,
+                       C_txt=4096, C_pool=768, guidance=3.5, **FLUX),
 }
 WORKLOAD_NAME = {
     "c4": "full denoising step, 19 double + 38 single blocks, D=3072, 24x128 heads, MLP 12288, 512 text + 83x83 "
@@ -46,6 +49,9 @@ WORKLOAD_NAME = {
     "c3pair": "one double + one single block (with embedding, img_in, final layer, Euler) at 512 text + 64x64 image "
               "tokens, batch 1, bf16",
     "c2": "one double block (with embedding, img_in, final layer, Euler) at 512 text + 32x32 image tokens, batch 1",
+    "sample1024": "sampling loop, 28 Euler steps of the 57-block bf16 model at 512 text + 64x64 image tokens "
+                  "(1024^2), batch 1, guidance 3.5, text projection 4096 -> 3072, pooled vector 768; steps 1.. "
+                  "replayed from one captured CUDA graph",
 }
 
 
@@ -337,6 +343,70 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int):
     return res
 
 
+def run_sample(args, c: dict):
+    """One 'step' of this workload is a whole sampling loop (n_steps Euler
+    steps through mmdit_sample, graph replay on)."""
+    import torch
+    from diffusion_transformer_image_mmdit_gb300 import api, build, schedule
+    from diffusion_transformer_image_mmdit_gb300.weights import DeviceDraw
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build.build()
+    api._lib.load()
+    shape = api.make_shape(B=c["B"], L_txt=c["L_txt"], grid_h=c["grid_h"], grid_w=c["grid_w"], D=c["D"], H=c["H"],
+                           d_head=c["d_head"], D_mlp=c["D_mlp"], rope_axes=c["rope_axes"], C_lat=c["C_lat"],
+                           t_dim=c["t_dim"])
+    draw = DeviceDraw(seed=1000, device=dev)
+    w = draw.step(c["D"], c["d_head"], c["D_mlp"], c["C_lat"], c["t_dim"], c["n_double"], c["n_single"])
+    cond = draw.cond(c["D"], c["t_dim"], c["C_txt"], c["C_pool"])
+    wstruct = w.struct()
+    Li = c["grid_h"] * c["grid_w"]
+    x0 = draw.normal((c["B"], Li, c["C_lat"]))
+    txt = draw.normal((c["B"], c["L_txt"], c["C_txt"]), dtype=torch.bfloat16)
+    pooled = draw.normal((c["B"], c["C_pool"]))
+    sig = schedule.sigmas(c["n_steps"], schedule.mu_for_tokens(Li))
+    ws = api.alloc_workspace(api.sample_workspace_size(shape, c["n_double"], c["n_single"], c["C_txt"],
+                                                       c["n_steps"]), device=dev)
+    stream = torch.cuda.current_stream()
+    x = torch.empty_like(x0)
+
+    def loop():
+        x.copy_(x0)
+        api.mmdit_sample(shape, w, cond, x, txt, pooled, c["guidance"], sig, ws, graph=True, stream=stream,
+                         step_struct=wstruct)
+
+    for _ in range(args.warmup):
+        loop()
+    torch.cuda.synchronize()
+    if api.sync_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            loop()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if api.sync_status() != 0:
+        raise RuntimeError("device status after timed region")
+    ms = e0.elapsed_time(e1) / args.steps
+    fl = step_flops(c)
+    cond_flops = 2 * c["B"] * (c["L_txt"] * c["C_txt"] * c["D"] + c["t_dim"] * c["D"] + c["C_pool"] * c["D"]
+                               + 2 * c["D"] * c["D"])
+    loop_flops = c["n_steps"] * fl["total"] + cond_flops
+    out = {"metric": METRIC, "value": round(loop_flops / ms / 1e9, 2), "unit": "TFLOP/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+           "ms_per_denoise_step": round(ms / c["n_steps"], 3), "s_per_image": round(ms / 1e3 / c["B"], 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (random-init weights, N(0,1) latents, text and pooled inputs)",
+           "config": {"workload": WORKLOAD_NAME[args.config], "global_batch": c["B"], "seq_len": fl["L"],
+                      "n_steps": c["n_steps"], "guidance": c["guidance"],
+                      "l2": f"inputs larger than L2: {step_weight_bytes(c) / 1e9:.2f} GB of weights read per step"},
+           "clocks": clk.summary()}
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -349,6 +419,13 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     c = CONFIGS[args.config]
+    if args.config == "sample1024":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the oracle on one "
+                              "denoising step; a sampling loop is only measured for this implementation"}))
+            return
+        run_sample(args, c)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
