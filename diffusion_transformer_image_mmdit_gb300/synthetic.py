@@ -135,7 +135,9 @@ def norm_gain(prefix: str, d: int, seed: int = 0):
     return normal_f32(prefix, (d,), W_STD, mean=1.0, seed=seed)
 
 
-def double_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int = 0) -> dict:
+def double_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int = 0, mlp: str = "gelu") -> dict:
+    """mlp = "swiglu": the first MLP projection has 2 D_mlp output rows [gate; up]."""
+    n_in = 2 * D_mlp if mlp == "swiglu" else D_mlp
     out = {}
     for s in ("txt", "img"):
         p = f"{prefix}.{s}"
@@ -143,7 +145,7 @@ def double_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int 
         w["mod_w"], w["mod_b"] = linear_params(p + ".mod", 6 * D, D, seed)
         w["qkv_w"], w["qkv_b"] = linear_params(p + ".qkv", 3 * D, D, seed)
         w["proj_w"], w["proj_b"] = linear_params(p + ".proj", D, D, seed)
-        w["mlp_in_w"], w["mlp_in_b"] = linear_params(p + ".mlp_in", D_mlp, D, seed)
+        w["mlp_in_w"], w["mlp_in_b"] = linear_params(p + ".mlp_in", n_in, D, seed)
         w["mlp_out_w"], w["mlp_out_b"] = linear_params(p + ".mlp_out", D, D_mlp, seed)
         w["q_norm"] = norm_gain(p + ".q_norm", d_head, seed)
         w["k_norm"] = norm_gain(p + ".k_norm", d_head, seed)
@@ -151,10 +153,11 @@ def double_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int 
     return out
 
 
-def single_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int = 0) -> dict:
+def single_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int = 0, mlp: str = "gelu") -> dict:
+    """mlp = "swiglu": lin1 has 3 D + 2 D_mlp output rows [q; k; v; gate; up]."""
     w = {}
     w["mod_w"], w["mod_b"] = linear_params(prefix + ".mod", 3 * D, D, seed)
-    w["lin1_w"], w["lin1_b"] = linear_params(prefix + ".lin1", 3 * D + D_mlp, D, seed)
+    w["lin1_w"], w["lin1_b"] = linear_params(prefix + ".lin1", 3 * D + (2 if mlp == "swiglu" else 1) * D_mlp, D, seed)
     w["lin2_w"], w["lin2_b"] = linear_params(prefix + ".lin2", D, D + D_mlp, seed)
     w["q_norm"] = norm_gain(prefix + ".q_norm", d_head, seed)
     w["k_norm"] = norm_gain(prefix + ".k_norm", d_head, seed)

@@ -51,6 +51,7 @@ class Shape:
     t_dim: int = 256
     n_double: int = 1
     n_single: int = 0
+    mlp: str = "gelu"  # "gelu": GELU-tanh MLP; "swiglu": SiLU(gate) * up over [gate; up] projections
 
     @property
     def L_img(self) -> int:
@@ -87,6 +88,22 @@ def layer_norm(x, eps):
     mu = x.mean(axis=-1, keepdims=True)
     var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
     return (x - mu) / np.sqrt(var + eps)
+
+
+def swiglu(h):
+    """SwiGLU over the last axis of h = [gate | up] (two halves): SiLU(gate) * up.
+    The Luminal blog (section "What the compiler found on its own") lists the
+    SwiGLU activation among the fused elementwise kernels of a Flux.2 Klein
+    step; the [gate; up] order of the projection's output rows is the reading
+    taken."""
+    n = h.shape[-1] // 2
+    return silu(h[..., :n]) * h[..., n:]
+
+
+def mlp_act(h, sh):
+    """The MLP activation of the model: GELU-tanh, or SwiGLU (which halves the
+    width)."""
+    return swiglu(h) if sh.mlp == "swiglu" else gelu_tanh(h)
 
 
 def modulate(y, shift, scale):
@@ -193,7 +210,8 @@ def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows
     adaLN-Zero modulation from vec, LN+modulate, QKV linear, per-head RMSNorm
     of q and k; then RoPE on the concatenated [text; image] sequence and one
     joint softmax attention; per stream: output projection with gated
-    residual, LN+modulate, GELU-tanh MLP with gated residual.
+    residual, LN+modulate, MLP (GELU-tanh, or SwiGLU when sh.mlp is
+    "swiglu") with gated residual.
 
     rows_txt / rows_img (optional index arrays) restrict the outputs to those
     query rows; keys and values always cover the whole sequence.
@@ -228,7 +246,7 @@ def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows
         o = R(attention(q[:, off + idx], k, v, rnd).reshape(x.shape[0], len(idx), sh.D))
         xr = x[:, idx] + g1 * linear(o, w["proj_w"], w["proj_b"])
         y2 = R(modulate(layer_norm(xr, sh.eps_ln), sh2, sc2))
-        hid = R(gelu_tanh(linear(y2, w["mlp_in_w"], w["mlp_in_b"])))
+        hid = R(mlp_act(linear(y2, w["mlp_in_w"], w["mlp_in_b"]), sh))
         xr = xr + g2 * linear(hid, w["mlp_out_w"], w["mlp_out_b"])
         outs.append(xr)
     return outs[0], outs[1]
@@ -236,9 +254,10 @@ def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows
 
 def single_block(x, vec, w, sh: Shape, cos, sin, rows=None, rnd=None):
     """Single-stream block on x = [text; image] [B, L, D]: LN+modulate, one
-    linear D -> 3D + D_mlp, RMSNorm of q and k, RoPE, joint attention in
-    parallel with GELU-tanh on the MLP columns, one linear over the
-    concatenation [attention output | GELU(mlp)], gated residual.
+    linear D -> 3D + D_mlp (3D + 2 D_mlp with SwiGLU), RMSNorm of q and k,
+    RoPE, joint attention in parallel with the MLP activation on the MLP
+    columns, one linear over the concatenation [attention output | act(mlp)],
+    gated residual.
     rnd: optional precision model, as in double_block."""
     R = _ident if rnd is None else rnd
     D, H = sh.D, sh.H
@@ -250,7 +269,7 @@ def single_block(x, vec, w, sh: Shape, cos, sin, rows=None, rnd=None):
     v = R(_heads(h[..., 2 * D:3 * D], H))
     idx = np.arange(x.shape[1]) if rows is None else np.asarray(rows)
     o = R(attention(q[:, idx], k, v, rnd).reshape(x.shape[0], len(idx), D))
-    cat = np.concatenate([o, R(gelu_tanh(h[:, idx, 3 * D:]))], axis=-1)
+    cat = np.concatenate([o, R(mlp_act(h[:, idx, 3 * D:], sh))], axis=-1)
     return x[:, idx] + gate * linear(cat, w["lin2_w"], w["lin2_b"])
 
 

@@ -215,6 +215,13 @@ def _torch_rope(x, sh):
     return torch.view_as_real(z * torch.polar(torch.ones_like(ang), ang)[:, None, :]).reshape(B, L, H, d)
 
 
+def _torch_act(t, sh):
+    if sh.mlp == "swiglu":
+        gate, up = t.chunk(2, dim=-1)
+        return F.silu(gate) * up
+    return F.gelu(t, approximate="tanh")
+
+
 def _torch_double(x_txt, x_img, vec, wt, sh):
     T = torch.from_numpy
     D, H, d = sh.D, sh.H, sh.d_head
@@ -238,7 +245,7 @@ def _torch_double(x_txt, x_img, vec, wt, sh):
         x, w, m, *_ = st[s]
         x = x + m[2] * F.linear(o[:, sl], w["proj_w"], w["proj_b"])
         y = F.layer_norm(x, (D,), eps=sh.eps_ln) * (1 + m[4]) + m[3]
-        x = x + m[5] * F.linear(F.gelu(F.linear(y, w["mlp_in_w"], w["mlp_in_b"]), approximate="tanh"), w["mlp_out_w"], w["mlp_out_b"])
+        x = x + m[5] * F.linear(_torch_act(F.linear(y, w["mlp_in_w"], w["mlp_in_b"]), sh), w["mlp_out_w"], w["mlp_out_b"])
         outs.append(x.numpy())
     return outs
 
@@ -251,13 +258,13 @@ def _torch_single(x, vec, wt, sh):
     m = F.linear(F.silu(T(vec)), w["mod_w"], w["mod_b"]).unsqueeze(1).chunk(3, dim=-1)
     y = F.layer_norm(x, (D,), eps=sh.eps_ln) * (1 + m[1]) + m[0]
     h = F.linear(y, w["lin1_w"], w["lin1_b"])
-    q, k, v, mlp = h.split([D, D, D, sh.D_mlp], dim=-1)
+    q, k, v, mlp = h.split([D, D, D, h.shape[-1] - 3 * D], dim=-1)
     B, L, _ = q.shape
     q = _torch_rope(F.rms_norm(q.reshape(B, L, H, d), (d,), weight=w["q_norm"], eps=sh.eps_rms), sh)
     k = _torch_rope(F.rms_norm(k.reshape(B, L, H, d), (d,), weight=w["k_norm"], eps=sh.eps_rms), sh)
     o = F.scaled_dot_product_attention(q.transpose(1, 2), k.transpose(1, 2), v.reshape(B, L, H, d).transpose(1, 2))
     o = o.transpose(1, 2).reshape(B, L, D)
-    return (x + m[2] * F.linear(torch.cat([o, F.gelu(mlp, approximate="tanh")], -1), w["lin2_w"], w["lin2_b"])).numpy()
+    return (x + m[2] * F.linear(torch.cat([o, _torch_act(mlp, sh)], -1), w["lin2_w"], w["lin2_b"])).numpy()
 
 
 def _double_inputs(sh, scale_w=1.0):
@@ -305,6 +312,41 @@ def test_single_block_vs_torch_restatement():
     assert rel(got, _torch_single(x, vec, w, sh)) < 1e-12
     part = O.single_block(x, vec, w, sh, c, s, rows=[0, 7, 16])
     assert rel(part, got[:, [0, 7, 16]]) < 1e-14
+
+
+def test_swiglu_vs_torch():
+    h = rnd("sw.h", (3, 5, 40), 3.0)
+    got = O.swiglu(h)
+    t = torch.from_numpy(h)
+    assert got.shape == (3, 5, 20)
+    assert rel(got, (F.silu(t[..., :20]) * t[..., 20:]).numpy()) < 1e-15
+    assert rel(O.mlp_act(h, O.Shape(1, 1, 1, 1, 4, 1, 4, 4, mlp="swiglu")), got) == 0.0
+
+
+@pytest.mark.parametrize("which", ["double", "single"])
+def test_swiglu_blocks_vs_torch_restatement(which):
+    import dataclasses
+    sh = dataclasses.replace(TINY, mlp="swiglu")
+    c, s = _tables(sh)
+    if which == "double":
+        wt = S.double_block_params("pin.swd", sh.D, sh.d_head, sh.D_mlp, mlp="swiglu")
+        for st in wt.values():
+            for k in st:
+                if k.endswith("_w"):
+                    st[k] = st[k] * 25.0
+        a = S.activations(sh.B, sh.L_txt, sh.L_img, sh.D)
+        got = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s)
+        ref = _torch_double(a["x_txt"], a["x_img"], a["vec"], wt, sh)
+        assert rel(got[0], ref[0]) < 1e-12 and rel(got[1], ref[1]) < 1e-12
+        assert rel(got[1], a["x_img"]) > 0.1
+    else:
+        w = S.single_block_params("pin.sws", sh.D, sh.d_head, sh.D_mlp, mlp="swiglu")
+        for k in w:
+            if k.endswith("_w"):
+                w[k] = w[k] * 25.0
+        x = S.normal_f32("pin.swx", (sh.B, sh.L, sh.D))
+        vec = S.normal_f32("pin.swv", (sh.B, sh.D))
+        assert rel(O.single_block(x, vec, w, sh, c, s), _torch_single(x, vec, w, sh)) < 1e-12
 
 
 def _zero_gates(mod_w, mod_b, n_chunks, gate_chunks):
@@ -623,6 +665,16 @@ def test_planted_mistakes_in_the_sampling_loop_are_caught(monkeypatch):
     def denoise_drop_vec_add(x, xt, s0, s1, W, sh, vec_add=None):
         return orig_denoise(x, xt, s0, s1, W, sh, None)
 
+    orig_sw = O.swiglu
+
+    def swiglu_swapped(h):
+        n = h.shape[-1] // 2
+        return O.silu(h[..., n:]) * h[..., :n]
+
+    _planted(monkeypatch, "swiglu", swiglu_swapped, test_swiglu_vs_torch)
+    monkeypatch.setattr(O, "swiglu", orig_sw)
+    _planted(monkeypatch, "swiglu", swiglu_swapped, lambda: test_swiglu_blocks_vs_torch_restatement("double"))
+    monkeypatch.setattr(O, "swiglu", orig_sw)
     orig_g = O.guidance_embed
     _planted(monkeypatch, "guidance_embed", guidance_no_1000, test_conditioning_embeddings_vs_torch)
     monkeypatch.setattr(O, "guidance_embed", orig_g)
