@@ -21,7 +21,13 @@ ERRORS = {-1: "ARG", -2: "SHAPE", -3: "ALIGN", -4: "WORKSPACE", -5: "CUDA", -6: 
 class Shape(Structure):
     _fields_ = [("B", c_int), ("L_txt", c_int), ("grid_h", c_int), ("grid_w", c_int), ("D", c_int), ("H", c_int),
                 ("d_head", c_int), ("D_mlp", c_int), ("rope_axes", c_int * 3), ("rope_theta", c_double),
-                ("eps_ln", c_float), ("eps_rms", c_float), ("w_dtype", c_int), ("C_lat", c_int), ("t_dim", c_int)]
+                ("eps_ln", c_float), ("eps_rms", c_float), ("w_dtype", c_int), ("C_lat", c_int), ("t_dim", c_int),
+                ("mlp_act", c_int)]
+
+
+MMDIT_EPI_SWIGLU = 4
+MMDIT_MLP_GELU = 0
+MMDIT_MLP_SWIGLU = 1
 
 
 class Linear(Structure):

@@ -15,7 +15,7 @@ import torch
 from . import _lib
 from ._lib import (MMDIT_BF16, MMDIT_EPI_BF16, MMDIT_EPI_BF16_GELU, MMDIT_EPI_F32, MMDIT_EPI_RESID, MMDIT_F32,
                    MMDIT_I8W, MMDIT_OP_ATTENTION, MMDIT_OP_DOUBLE, MMDIT_OP_SINGLE, DoubleW, Linear, Shape, SingleW,
-                   StepW, CondW, MMDIT_SAMPLE_GRAPH, call)
+                   StepW, CondW, MMDIT_SAMPLE_GRAPH, MMDIT_EPI_SWIGLU, MMDIT_MLP_GELU, MMDIT_MLP_SWIGLU, call)
 
 
 # ------------------------------------------------------------------ marshalling helpers
@@ -37,13 +37,14 @@ def stream_handle(stream: Optional[torch.cuda.Stream] = None):
 
 
 def make_shape(B, L_txt, grid_h, grid_w, D, H, d_head, D_mlp, rope_axes=(16, 56, 56), rope_theta=10000.0,
-               eps_ln=1e-6, eps_rms=1e-6, w_dtype=MMDIT_BF16, C_lat=128, t_dim=256) -> Shape:
+               eps_ln=1e-6, eps_rms=1e-6, w_dtype=MMDIT_BF16, C_lat=128, t_dim=256, mlp_act=0) -> Shape:
     s = Shape()
     s.B, s.L_txt, s.grid_h, s.grid_w = B, L_txt, grid_h, grid_w
     s.D, s.H, s.d_head, s.D_mlp = D, H, d_head, D_mlp
     s.rope_axes[0], s.rope_axes[1], s.rope_axes[2] = rope_axes
     s.rope_theta, s.eps_ln, s.eps_rms = rope_theta, eps_ln, eps_rms
     s.w_dtype, s.C_lat, s.t_dim = w_dtype, C_lat, t_dim
+    s.mlp_act = mlp_act
     return s
 
 

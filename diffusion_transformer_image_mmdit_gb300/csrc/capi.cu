@@ -150,6 +150,7 @@ struct Carve {
 
 struct Dims {
   int B, Lt, Li, L, Lpad, D, H, d, Dm;
+  bool swiglu;  // SwiGLU MLP: the first MLP projection has 2 Dm rows [gate; up]
 };
 
 static int check_shape(const mmdit_shape_t* s, Dims* out) {
@@ -162,12 +163,15 @@ static int check_shape(const mmdit_shape_t* s, Dims* out) {
   const int a0 = s->rope_axes[0], a1 = s->rope_axes[1], a2 = s->rope_axes[2];
   if (a0 < 0 || a1 < 0 || a2 < 0 || (a0 | a1 | a2) & 1 || a0 + a1 + a2 != s->d_head) return MMDIT_ERR_SHAPE;
   if (s->w_dtype != MMDIT_BF16 && s->w_dtype != MMDIT_I8W) return MMDIT_ERR_ARG;
+  if (s->mlp_act != MMDIT_MLP_GELU && s->mlp_act != MMDIT_MLP_SWIGLU) return MMDIT_ERR_ARG;
+  if (s->mlp_act == MMDIT_MLP_SWIGLU && s->D_mlp % 128) return MMDIT_ERR_SHAPE;
   const long long L = (long long)s->L_txt + (long long)s->grid_h * s->grid_w;
   if (L > (1 << 24)) return MMDIT_ERR_SHAPE;
   if (out) {
     out->B = s->B, out->Lt = s->L_txt, out->Li = s->grid_h * s->grid_w, out->L = (int)L;
     out->Lpad = (int)((L + 7) / 8 * 8);
     out->D = s->D, out->H = s->H, out->d = s->d_head, out->Dm = s->D_mlp;
+    out->swiglu = s->mlp_act == MMDIT_MLP_SWIGLU;
   }
   return MMDIT_OK;
 }
@@ -200,6 +204,7 @@ static int prepare_gemm(const void* A, long long a_ld, long long a_seg_rows, int
                         const mmdit_linear_t& lin, int N, GemmParams p, uint16_t* wdeq, cudaStream_t st,
                         GemmProblem& out) {
   if (K % kBK || N % 32 || M_seg < 1 || n_seg < 1) return MMDIT_ERR_SHAPE;
+  if (p.mode == GM_SWIGLU && N % kBN) return MMDIT_ERR_SHAPE;  // whole 128-row gate / up halves
   if (!al16(A) || (a_ld * 2) % 16) return MMDIT_ERR_ALIGN;
   const void* W = lin.w;
   p.wscale = nullptr;
@@ -222,7 +227,9 @@ static int prepare_gemm(const void* A, long long a_ld, long long a_seg_rows, int
   p.N = N;
   p.K = K;
   p.tiles_m = (M_seg + kBM - 1) / kBM;
-  p.tiles_n = (N + kBN - 1) / kBN;
+  // SwiGLU: N = 2 x output width; an N tile pairs 128 gate rows with the 128 matching up rows
+  p.swiglu_up = p.mode == GM_SWIGLU ? N / 2 : 0;
+  p.tiles_n = p.mode == GM_SWIGLU ? (N / 2) / (kBN / 2) : (N + kBN - 1) / kBN;
   // Work units are pairs of vertically adjacent M tiles (one per CTA of a
   // cluster) at one N tile.
   const int pairs_m = (p.tiles_m * n_seg + 1) / 2;
@@ -311,7 +318,8 @@ static void layout_double(const Dims& d, bool i8, bool need_mod, Carve& c, Doubl
   w.vT = c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
   w.O = c.take<uint16_t>((size_t)d.B * d.L * d.D);
   w.h = c.take<uint16_t>((size_t)d.B * d.L * d.Dm);
-  const size_t wmax = (size_t)(3 * d.D > d.Dm ? 3 * d.D : d.Dm) * d.D;
+  const size_t wmlp = (size_t)(d.swiglu ? 2 : 1) * d.Dm;
+  const size_t wmax = ((size_t)3 * d.D > wmlp ? (size_t)3 * d.D : wmlp) * d.D;
   w.wdeq[0] = i8 ? c.take<uint16_t>(wmax) : nullptr;
   w.wdeq[1] = i8 ? c.take<uint16_t>(wmax) : nullptr;
 }
@@ -326,7 +334,7 @@ static void layout_single(const Dims& d, bool i8, bool need_mod, Carve& c, Singl
   w.qk = c.take<uint16_t>((size_t)d.B * d.L * 2 * d.D);
   w.vT = c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
   w.cat = c.take<uint16_t>((size_t)d.B * d.L * (d.D + d.Dm));
-  w.wdeq = i8 ? c.take<uint16_t>((size_t)(3 * d.D + d.Dm) * d.D) : nullptr;
+  w.wdeq = i8 ? c.take<uint16_t>(((size_t)3 * d.D + (size_t)(d.swiglu ? 2 : 1) * d.Dm) * d.D) : nullptr;
 }
 
 struct StepWS {
@@ -421,12 +429,13 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, modp(i) + 3 * D, modp(i) + 4 * D, 6 * D, s.eps_ln,
                                   yp(i), st));
   for (int i = first; i < 2; ++i) {
-    GemmParams p = gemm_params(GM_STORE_BF16);
+    GemmParams p = gemm_params(d.swiglu ? GM_SWIGLU : GM_STORE_BF16);
     p.gelu_from = 0;
     p.out = hp(i);
     p.out_ld = d.Dm;
     p.out_seg_rows = Ls[i];
-    MMDIT_TRY(prepare_gemm(yp(i), D, Ls[i], Ls[i], d.B, D, w.mlp_in[i], d.Dm, p, ws.wdeq[i], st, pr[i]));
+    MMDIT_TRY(prepare_gemm(yp(i), D, Ls[i], Ls[i], d.B, D, w.mlp_in[i], d.swiglu ? 2 * d.Dm : d.Dm, p, ws.wdeq[i], st,
+                           pr[i]));
   }
   MMDIT_TRY(grouped(pr));
   // x += gate2 * (h W2^T + b2)
@@ -471,7 +480,27 @@ static int single_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
   p.aux = ws.cat;
   p.aux_ld = cat_ld;
   p.aux_col_off = D;
-  MMDIT_TRY(run_gemm(ws.y, D, d.L, d.L, d.B, D, w.lin1, 3 * D + d.Dm, p, ws.wdeq, st));
+  if (!d.swiglu) {
+    MMDIT_TRY(run_gemm(ws.y, D, d.L, d.L, d.B, D, w.lin1, 3 * D + d.Dm, p, ws.wdeq, st));
+  } else {
+    // lin1 rows [q; k; v] (QKV epilogue) and [gate; up] (SwiGLU into the columns
+    // [D, D + Dm) of cat) as the two problems of one launch
+    const bool i8 = w.lin1.scale != nullptr;
+    const size_t wb = i8 ? 1 : 2;
+    mmdit_linear_t mlp = w.lin1;
+    mlp.w = static_cast<const uint8_t*>(w.lin1.w) + (size_t)3 * D * D * wb;
+    if (w.lin1.b) mlp.b = static_cast<const float*>(w.lin1.b) + 3 * D;
+    if (w.lin1.scale) mlp.scale = w.lin1.scale + 3 * D;
+    GemmProblem pr[2];
+    MMDIT_TRY(prepare_gemm(ws.y, D, d.L, d.L, d.B, D, w.lin1, 3 * D, p, ws.wdeq, st, pr[0]));
+    GemmParams ps = gemm_params(GM_SWIGLU);
+    ps.out = ws.cat + D;
+    ps.out_ld = cat_ld;
+    ps.out_seg_rows = d.L;
+    MMDIT_TRY(prepare_gemm(ws.y, D, d.L, d.L, d.B, D, mlp, 2 * d.Dm, ps, ws.wdeq ? ws.wdeq + (size_t)3 * D * D : nullptr,
+                           st, pr[1]));
+    MMDIT_TRY(launch_problems(&pr[0], &pr[1], st));
+  }
   MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.cat, cat_ld, st));
   GemmParams p2 = gemm_params(GM_RESID);
   p2.resid = x;
@@ -1012,6 +1041,12 @@ int mmdit_linear_fwd(const mmdit_linear_t* lin, int M, int N, int K, const void*
       p = gemm_params(GM_STORE_F32);
       p.out = y;
       p.out_ld = N;
+      p.out_seg_rows = M;
+      break;
+    case MMDIT_EPI_SWIGLU:
+      p = gemm_params(GM_SWIGLU);
+      p.out = y;
+      p.out_ld = N / 2;
       p.out_seg_rows = M;
       break;
     case MMDIT_EPI_RESID:

@@ -350,6 +350,13 @@ __device__ __forceinline__ float gelu_tanh_f(float x) {
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
+// SiLU through one exp2 and a fast divide (for GEMM epilogues whose outputs
+// are stored as bf16): x / (1 + 2^(-x log2 e)); the -inf / +inf limits of
+// the denominator give -0 / x.
+__device__ __forceinline__ float silu_fast(float x) {
+  return __fdividef(x, 1.0f + ex2_approx(-1.4426950408889634f * x));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

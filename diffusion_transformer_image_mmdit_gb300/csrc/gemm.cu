@@ -260,6 +260,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     return;
   }
 
+  if (p.mode == GM_SWIGLU) {
+    // accumulator columns [0, 128): gate rows g0 + c; [128, 256): up rows p.swiglu_up + g0 + c
+    const int g0 = c.tn * (kBN / 2);
+    uint16_t* row0 = reinterpret_cast<uint16_t*>(p.out) + orow0 * p.out_ld + g0;
+#pragma unroll 1
+    for (int j = 0; j < kBN / 64; ++j) {
+      float g[32], u[32];
+      acc_chunk(tbase + j * 32, p, g0 + j * 32, g);
+      acc_chunk(tbase + kBN / 2 + j * 32, p, p.swiglu_up + g0 + j * 32, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) g[i] = silu_fast(g[i]) * u[i];
+      warp_store_bf16x32(stg, lane, g, row0 + j * 32, p.out_ld, nrows);
+    }
+    return;
+  }
+
 #pragma unroll 1
   for (int j = 0; j < kBN / 32; ++j) {
     const int n = n0 + j * 32;
@@ -352,6 +368,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         const GemmParams& p = g.p[q];
         const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0), rank);
         const int m0 = c.tm * kBM, n0 = c.tn * kBN;
+        // W rows of this CTA's half of the 256-row tile: rows n0 + 128 rank, or
+        // for SwiGLU the matching 128 gate rows (rank 0) and up rows (rank 1)
+        const int brow = p.mode == GM_SWIGLU ? c.tn * (kBN / 2) + rank * p.swiglu_up : n0 + rank * (kBN / 2);
         const int nk = p.K / kBK;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, status, ST_TIMEOUT_PRODUCER)) goto done;
@@ -359,7 +378,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
           mbar_expect_tx(full0 + 8 * stage, kStageA + kStageB);
           tma_load_3d(smem_u32(sA + stage * kStageA), &g.tmA[q], full0 + 8 * stage, kb * kBK, m0, c.seg);
           tma_load_3d_mc(smem_u32(sB + stage * kStageB + rank * (kStageB / 2)), &g.tmB[q], full0 + 8 * stage,
-                         kb * kBK, n0 + rank * (kBN / 2), 0, kPair);
+                         kb * kBK, brow, 0, kPair);
           ++n_fill;
           if (++stage == kStages) stage = 0, phase ^= 1;
         }

@@ -20,6 +20,7 @@ enum GemmMode : int {
   GM_STORE_F32 = 1,   // out fp32
   GM_RESID = 2,       // resid fp32 += gate * value
   GM_QKV = 3,         // q,k: RMSNorm + RoPE -> qk; v -> transposed vT; rest: GELU -> aux
+  GM_SWIGLU = 4,      // W rows [gate; up]: out bf16 = SiLU(gate) * up, N / 2 wide
 };
 
 // Rows are grouped in `n_seg` segments (samples) of M_seg rows each; the A
@@ -30,6 +31,7 @@ struct GemmParams {
   int tiles_m, tiles_n, num_tiles, group_m;
   int mode;
   int gelu_from;
+  int swiglu_up;  // GM_SWIGLU: row offset of the up half of W (= the output width)
   const float* bias;    // [N] or null
   const float* wscale;  // [N] or null (int8 weights)
   void* out;            // bf16 or fp32 output

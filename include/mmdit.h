@@ -79,7 +79,17 @@ typedef struct {
   int w_dtype;      /* MMDIT_BF16 or MMDIT_I8W for all linear weights */
   int C_lat;        /* latent channels per image token (step only) */
   int t_dim;        /* timestep sinusoid width (step only) */
+  int mlp_act;      /* MMDIT_MLP_GELU or MMDIT_MLP_SWIGLU (see below) */
 } mmdit_shape_t;
+
+/* MLP activation.  GELU-tanh: mlp_in (double) and the MLP rows of lin1
+ * (single) have D_mlp output rows.  SwiGLU (the Flux.2 Klein blocks; the
+ * Luminal blog, section "What the compiler found on its own", lists the
+ * SwiGLU activation among the fused kernels of a Klein step): they have
+ * 2 D_mlp rows [gate; up] and the activation is SiLU(gate) * up, D_mlp
+ * wide (D_mlp a multiple of 128). */
+#define MMDIT_MLP_GELU 0
+#define MMDIT_MLP_SWIGLU 1
 
 /* One linear layer.  w: device [N, K] (bf16, or int8 when scale != NULL);
  * b: device fp32 [N] or NULL; scale: device fp32 [N] for int8 weights. */
@@ -313,6 +323,8 @@ int mmdit_quantize_w8(const void* w, int w_dtype, int N, int K, int8_t* q, float
  *   MMDIT_EPI_BF16:        y device bf16 [M, N]
  *   MMDIT_EPI_BF16_GELU:   y device bf16 [M, N], GELU-tanh applied
  *   MMDIT_EPI_F32:         y device fp32 [M, N]
+ *   MMDIT_EPI_SWIGLU:      W rows [gate; up] (N a multiple of 256): y device bf16
+ *                          [M, N/2] = SiLU(x Wg^T + bg) * (x Wu^T + bu)
  *   MMDIT_EPI_RESID:       y device fp32 [M, N] += gate[n] * (x W^T + b),
  *                          gate device fp32 [N] (NULL = 1)
  * Int8 weights when lin->scale != NULL (y = (x q^T) * scale + b); they are
@@ -322,6 +334,7 @@ int mmdit_quantize_w8(const void* w, int w_dtype, int N, int K, int8_t* q, float
 #define MMDIT_EPI_BF16_GELU 1
 #define MMDIT_EPI_F32 2
 #define MMDIT_EPI_RESID 3
+#define MMDIT_EPI_SWIGLU 4
 int mmdit_linear_fwd(const mmdit_linear_t* lin, int M, int N, int K, const void* x, void* y, int epilogue,
                      const float* gate, void* ws, size_t ws_bytes, void* stream);
 

@@ -170,6 +170,79 @@ def test_step_small(i8):
     assert_close(host(xl), ref_x, rel=tol, what="step x_lat")
 
 
+# ------------------------------------------------------------------ SwiGLU blocks (Flux.2 Klein)
+KLEIN = dict(D=4096, H=32, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56), mlp_act=api.MMDIT_MLP_SWIGLU)
+
+
+def swiglu_shape(cfg):
+    sh = oracle_shape(cfg)
+    sh.mlp = "swiglu"
+    return sh
+
+
+@pytest.mark.parametrize("name", ["c1", "d128"])
+def test_swiglu_double_block(name):
+    cfg = dict(CONFIGS[name], mlp_act=api.MMDIT_MLP_SWIGLU)
+    sh = swiglu_shape(cfg)
+    p = S.double_block_params(f"swd.{name}", cfg["D"], cfg["d_head"], cfg["D_mlp"], mlp="swiglu")
+    a = S.activations(cfg["B"], cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, _ = run_double(cfg, p, a)
+    c, s = tables(cfg)
+    rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s)
+    assert_close(gt, rt, what="swiglu double x_txt")
+    assert_close(gi, ri, what="swiglu double x_img")
+
+
+@pytest.mark.parametrize("name,i8", [("c1", False), ("d128", False), ("d128", True)])
+def test_swiglu_single_block(name, i8):
+    cfg = dict(CONFIGS[name], mlp_act=api.MMDIT_MLP_SWIGLU)
+    sh = swiglu_shape(cfg)
+    p = S.single_block_params(f"sws.{name}", cfg["D"], cfg["d_head"], cfg["D_mlp"], mlp="swiglu")
+    x = S.normal_f32("sws.x", (cfg["B"], sh.L, cfg["D"]))
+    vec = S.normal_f32("sws.vec", (cfg["B"], cfg["D"]))
+    g, wq = run_single(cfg, p, x, vec, i8=i8)
+    c, s = tables(cfg)
+    if i8:
+        pd = dict(p)
+        for name_ in ("mod", "lin1", "lin2"):
+            lin = getattr(wq, name_)
+            pd[name_ + "_w"] = O.dequantize_w8(lin.w.cpu().numpy(), lin.scale.cpu().numpy())
+        assert_close(g, O.single_block(x, vec, pd, sh, c, s), what="int8 swiglu single vs dequantised")
+    else:
+        assert_close(g, O.single_block(x, vec, p, sh, c, s), what="swiglu single")
+
+
+def test_klein_double_block_sampled():
+    """Flux.2 Klein block shapes (D 4096, 32 heads, SwiGLU MLP 3D) at 512 text + 32x32 image tokens."""
+    cfg = dict(B=1, L_txt=512, grid_h=32, grid_w=32, **KLEIN)
+    sh = swiglu_shape(cfg)
+    p = S.double_block_params("klein.d", cfg["D"], cfg["d_head"], cfg["D_mlp"], mlp="swiglu")
+    a = S.activations(1, cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, _ = run_double(cfg, p, a)
+    rt_rows = _sample_rows(cfg["L_txt"], 4, 7)
+    ri_rows = _sample_rows(sh.L_img, 6, 8)
+    c, s = tables(cfg)
+    rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows)
+    et, ei = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows,
+                            rnd=S.round_bf16)
+    assert_close(gt[:, rt_rows], rt, max_abs=flux_max_abs(et, rt), what="klein double x_txt rows")
+    assert_close(gi[:, ri_rows], ri, max_abs=flux_max_abs(ei, ri), what="klein double x_img rows")
+
+
+def test_klein_single_block_sampled():
+    cfg = dict(B=1, L_txt=512, grid_h=32, grid_w=32, **KLEIN)
+    sh = swiglu_shape(cfg)
+    p = S.single_block_params("klein.s", cfg["D"], cfg["d_head"], cfg["D_mlp"], mlp="swiglu")
+    x = S.normal_f32("klein.x", (1, sh.L, cfg["D"]))
+    vec = S.normal_f32("klein.vec", (1, cfg["D"]))
+    g, _ = run_single(cfg, p, x, vec)
+    rows = _sample_rows(sh.L, 8, 9)
+    c, s = tables(cfg)
+    ref = O.single_block(x, vec, p, sh, c, s, rows=rows)
+    emu = O.single_block(x, vec, p, sh, c, s, rows=rows, rnd=S.round_bf16)
+    assert_close(g[:, rows], ref, max_abs=flux_max_abs(emu, ref), what="klein single rows")
+
+
 # ------------------------------------------------------------------ sampling loop
 def _sample_case(n_steps, i8=False):
     cfg = dict(CONFIGS["d128"])

@@ -162,6 +162,24 @@ def test_linear_int8(M, N, K):
     assert rel_l2(host(y), O.linear(x, w, b)) <= 3e-2
 
 
+@pytest.mark.parametrize("M,F,K,i8", [(300, 256, 256, False), (1, 128, 64, False), (260, 384, 192, True)])
+def test_linear_swiglu(M, F, K, i8):
+    """W rows [gate; up] (2F of them); y = SiLU(x Wg^T + bg) * (x Wu^T + bu), F wide."""
+    w, b = S.linear_params(f"sw{M}.{F}.{K}", 2 * F, K)
+    w = S.round_bf16(w * 10)
+    x = S.normal_bf16("sw.x", (M, K))
+    lin = LinearDev(bf16(w), f32(b))
+    ws = None
+    if i8:
+        lin = api.quantize_linear(lin)
+        ws = api.alloc_workspace(2 * F * K * 2)
+        w = O.dequantize_w8(lin.w.cpu().numpy(), lin.scale.cpu().numpy())
+    y = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
+    api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_SWIGLU, ws=ws)
+    ref = O.swiglu(O.linear(x, w, b))
+    assert_close(host(y), ref, max_abs=2.0 ** -8 * max(1.0, np.abs(ref).max()) + 1e-3, what="gemm swiglu")
+
+
 def test_gemm_large_tiles_and_ragged():
     """Several waves of persistent tiles, M tail of 9 rows, K = 3072."""
     M, N, K = 128 * 20 + 9, 1024, 3072
