@@ -36,6 +36,15 @@ CONFIGS = {
     "c3pair": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=1, n_single=1, int8=False, n_steps=50, **FLUX),
     # one double block at 512^2 (512 + 1024 tokens)
     "c2": dict(B=1, L_txt=512, grid_h=32, grid_w=32, n_double=1, n_single=0, int8=False, n_steps=50, **FLUX),
+    # Flux.2 Klein 9B block shapes (D 4096, 32 heads, SwiGLU MLP 12288, 8 double + 24 single) at 1024^2
+    "klein1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=8, n_single=24, int8=False, n_steps=4,
+                      swiglu=True, D=4096, H=32, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56), C_lat=128,
+                      t_dim=256),
+    # the same at the token count of the 1200x800 image-to-image workload: 512 text + 75x50 target + 75x50 reference
+    # latent tokens, the reference tokens laid out as a second 75x50 grid
+    "klein_i2i": dict(B=1, L_txt=512, grid_h=100, grid_w=75, n_double=8, n_single=24, int8=False, n_steps=4,
+                      swiglu=True, D=4096, H=32, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56), C_lat=128,
+                      t_dim=256),
     # the whole sampling loop at 1024^2: 28 steps, guidance 3.5, text encoder width 4096, pooled width 768
     "sample1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=False, n_steps=28,
                        C_txt=4096, C_pool=768, guidance=3.5, **FLUX),
@@ -49,6 +58,11 @@ WORKLOAD_NAME = {
     "c3pair": "one double + one single block (with embedding, img_in, final layer, Euler) at 512 text + 64x64 image "
               "tokens, batch 1, bf16",
     "c2": "one double block (with embedding, img_in, final layer, Euler) at 512 text + 32x32 image tokens, batch 1",
+    "klein1024": "Flux.2 Klein-shaped denoising step: 8 double + 24 single blocks, D=4096, 32x128 heads, SwiGLU "
+                 "MLP 12288, 512 text + 64x64 image tokens (1024^2), batch 1, bf16, step 0 of a 4-step schedule",
+    "klein_i2i": "Flux.2 Klein-shaped denoising step at the token count of 1200x800 image-to-image: 512 text + "
+                 "75x50 target + 75x50 reference latent tokens (8012), the reference tokens as a second grid "
+                 "(their RoPE time index is not modelled), batch 1, bf16",
     "sample1024": "sampling loop, 28 Euler steps of the 57-block bf16 model at 512 text + 64x64 image tokens "
                   "(1024^2), batch 1, guidance 3.5, text projection 4096 -> 3072, pooled vector 768; steps 1.. "
                   "replayed from one captured CUDA graph",
@@ -60,21 +74,23 @@ def step_flops(c: dict) -> dict:
     B, D, Dm, C, T = c["B"], c["D"], c["D_mlp"], c["C_lat"], c["t_dim"]
     Lt, Li = c["L_txt"], c["grid_h"] * c["grid_w"]
     L = Lt + Li
-    lin_double = 2 * L * (3 * D * D + D * D + 2 * D * Dm)
-    lin_single = 2 * L * (D * (3 * D + Dm) + (D + Dm) * D)
+    m_in = 2 * Dm if c.get("swiglu") else Dm  # rows of the first MLP projection ([gate; up] for SwiGLU)
+    lin_double = 2 * L * (3 * D * D + D * D + D * m_in + Dm * D)
+    lin_single = 2 * L * (D * (3 * D + m_in) + (D + Dm) * D)
     attn = 4 * L * L * D
     blocks = c["n_double"] * (lin_double + attn) + c["n_single"] * (lin_single + attn)
     small = 2 * (T * D + D * D) + c["n_double"] * 2 * 2 * D * 6 * D + c["n_single"] * 2 * D * 3 * D + 2 * D * 2 * D
     io = 2 * Li * C * D * 2
     gemm = B * (c["n_double"] * lin_double + c["n_single"] * lin_single + io)
     return {"total": B * (blocks + io) + B * small, "gemm": gemm, "attention": B * (c["n_double"] + c["n_single"]) * attn,
-            "block_flops": 24 * L * D * D + 4 * L * L * D, "L": L}
+            "block_flops": lin_double + attn, "L": L}
 
 
 def step_weight_bytes(c: dict) -> float:
     D, Dm, C, T = c["D"], c["D_mlp"], c["C_lat"], c["t_dim"]
-    per_double = 2 * (6 * D * D + 3 * D * D + D * D + 2 * D * Dm)
-    per_single = 3 * D * D + D * (3 * D + Dm) + (D + Dm) * D
+    m_in = 2 * Dm if c.get("swiglu") else Dm
+    per_double = 2 * (6 * D * D + 3 * D * D + D * D + D * m_in + Dm * D)
+    per_single = 3 * D * D + D * (3 * D + m_in) + (D + Dm) * D
     n = c["n_double"] * per_double + c["n_single"] * per_single + T * D + D * D + 2 * C * D + 2 * D * D
     return n * (1 if c["int8"] else 2)
 
@@ -246,9 +262,10 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int):
     shape = api.make_shape(B=c["B"], L_txt=c["L_txt"], grid_h=c["grid_h"], grid_w=c["grid_w"], D=c["D"], H=c["H"],
                            d_head=c["d_head"], D_mlp=c["D_mlp"], rope_axes=c["rope_axes"],
                            w_dtype=api.MMDIT_I8W if c["int8"] else api.MMDIT_BF16, C_lat=c["C_lat"],
-                           t_dim=c["t_dim"])
+                           t_dim=c["t_dim"], mlp_act=api.MMDIT_MLP_SWIGLU if c.get("swiglu") else api.MMDIT_MLP_GELU)
     draw = DeviceDraw(seed=1000 + rank, device=dev)
-    w = draw.step(c["D"], c["d_head"], c["D_mlp"], c["C_lat"], c["t_dim"], c["n_double"], c["n_single"])
+    w = draw.step(c["D"], c["d_head"], c["D_mlp"], c["C_lat"], c["t_dim"], c["n_double"], c["n_single"],
+                  swiglu=bool(c.get("swiglu")))
     if c["int8"]:
         wq = w.quantized()
         del w
@@ -356,9 +373,10 @@ def run_sample(args, c: dict):
     api._lib.load()
     shape = api.make_shape(B=c["B"], L_txt=c["L_txt"], grid_h=c["grid_h"], grid_w=c["grid_w"], D=c["D"], H=c["H"],
                            d_head=c["d_head"], D_mlp=c["D_mlp"], rope_axes=c["rope_axes"], C_lat=c["C_lat"],
-                           t_dim=c["t_dim"])
+                           t_dim=c["t_dim"], mlp_act=api.MMDIT_MLP_SWIGLU if c.get("swiglu") else api.MMDIT_MLP_GELU)
     draw = DeviceDraw(seed=1000, device=dev)
-    w = draw.step(c["D"], c["d_head"], c["D_mlp"], c["C_lat"], c["t_dim"], c["n_double"], c["n_single"])
+    w = draw.step(c["D"], c["d_head"], c["D_mlp"], c["C_lat"], c["t_dim"], c["n_double"], c["n_single"],
+                  swiglu=bool(c.get("swiglu")))
     cond = draw.cond(c["D"], c["t_dim"], c["C_txt"], c["C_pool"])
     wstruct = w.struct()
     Li = c["grid_h"] * c["grid_w"]

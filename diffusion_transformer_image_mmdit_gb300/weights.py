@@ -77,19 +77,20 @@ class DeviceDraw:
     def gain(self, d: int) -> torch.Tensor:
         return self.normal((d,), 0.02, 1.0)
 
-    def double(self, D: int, d: int, Dm: int) -> DoubleWeights:
+    def double(self, D: int, d: int, Dm: int, swiglu: bool = False) -> DoubleWeights:
         mk = lambda n_out, n_in: [self.linear(n_out, n_in) for _ in range(2)]
-        return DoubleWeights(mk(6 * D, D), mk(3 * D, D), mk(D, D), mk(Dm, D), mk(D, Dm),
+        return DoubleWeights(mk(6 * D, D), mk(3 * D, D), mk(D, D), mk((2 if swiglu else 1) * Dm, D), mk(D, Dm),
                              [self.gain(d), self.gain(d)], [self.gain(d), self.gain(d)])
 
-    def single(self, D: int, d: int, Dm: int) -> SingleWeights:
-        return SingleWeights(self.linear(3 * D, D), self.linear(3 * D + Dm, D), self.linear(D, D + Dm), self.gain(d),
-                             self.gain(d))
+    def single(self, D: int, d: int, Dm: int, swiglu: bool = False) -> SingleWeights:
+        return SingleWeights(self.linear(3 * D, D), self.linear(3 * D + (2 if swiglu else 1) * Dm, D),
+                             self.linear(D, D + Dm), self.gain(d), self.gain(d))
 
-    def step(self, D: int, d: int, Dm: int, C_lat: int, t_dim: int, n_double: int, n_single: int) -> StepWeights:
+    def step(self, D: int, d: int, Dm: int, C_lat: int, t_dim: int, n_double: int, n_single: int,
+             swiglu: bool = False) -> StepWeights:
         return StepWeights(self.linear(D, t_dim), self.linear(D, D), self.linear(D, C_lat), self.linear(2 * D, D),
-                           self.linear(C_lat, D), [self.double(D, d, Dm) for _ in range(n_double)],
-                           [self.single(D, d, Dm) for _ in range(n_single)])
+                           self.linear(C_lat, D), [self.double(D, d, Dm, swiglu) for _ in range(n_double)],
+                           [self.single(D, d, Dm, swiglu) for _ in range(n_single)])
 
     def cond(self, D: int, t_dim: int, C_txt: int, C_pool: int) -> CondWeights:
         return CondWeights(self.linear(D, C_txt), self.linear(D, t_dim), self.linear(D, D), self.linear(D, C_pool),
