@@ -87,6 +87,9 @@ SIGNATURES = {
     "mmdit_quantize_w8": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "mmdit_linear_fwd": (c_int, [POINTER(Linear), c_int, c_int, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
                                  c_size_t, c_void_p]),
+    "mmdit_quantize_f8": (c_int, [c_void_p, c_int, c_longlong, c_int, c_longlong, c_void_p, c_void_p, c_void_p]),
+    "mmdit_linear_f8_fwd": (c_int, [POINTER(Linear), c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int,
+                                    c_void_p, c_void_p]),
     "mmdit_ln_modulate": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int64, c_float, c_void_p,
                                   c_void_p]),
     "mmdit_gemv": (c_int, [POINTER(Linear), c_int, c_int, c_int, c_void_p, c_int, c_void_p, c_void_p]),

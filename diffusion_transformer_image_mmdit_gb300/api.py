@@ -331,6 +331,31 @@ def mmdit_linear_fwd(lin: LinearDev, x: torch.Tensor, y: torch.Tensor, epilogue:
          0 if ws is None else ws.numel(), stream_handle(stream))
 
 
+def quantize_f8(x: torch.Tensor, stream=None):
+    """Rows of a 2-D bf16 / fp32 tensor to e4m3 (uint8 codes) and fp32 row scales
+    (s = max|row| / 448)."""
+    rows, K = x.shape
+    q = torch.empty((rows, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    xd = {torch.float32: MMDIT_F32, torch.bfloat16: MMDIT_BF16}[x.dtype]
+    call("mmdit_quantize_f8", ptr(x, strided_ok=True), xd, rows, K, x.stride(0), ptr(q), ptr(s), stream_handle(stream))
+    return q, s
+
+
+def quantize_linear_f8(lin: LinearDev, stream=None) -> LinearDev:
+    """e4m3 per-channel copy of a bf16 linear (weights e4m3 codes, fp32 scales)."""
+    q, s = quantize_f8(lin.w, stream)
+    return LinearDev(q, lin.b, s)
+
+
+def mmdit_linear_f8_fwd(lin: LinearDev, x8: torch.Tensor, x_scale: torch.Tensor, y: torch.Tensor, epilogue: int,
+                        gate=None, stream=None):
+    M, K = x8.shape
+    st = lin.struct()
+    call("mmdit_linear_f8_fwd", ctypes.byref(st), M, lin.N, K, ptr(x8), ptr(x_scale), ptr(y), epilogue, ptr(gate),
+         stream_handle(stream))
+
+
 def mmdit_ln_modulate(x: torch.Tensor, shift: torch.Tensor, scale: torch.Tensor, mod_stride: int, eps: float,
                       y: torch.Tensor, stream=None):
     B, rows, D = x.shape

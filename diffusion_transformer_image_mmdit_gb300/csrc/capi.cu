@@ -196,32 +196,44 @@ static bool lin_ok(const mmdit_linear_t& l, bool want_i8) {
 struct GemmProblem {
   CUtensorMap ta, tb;
   GemmParams p;
+  bool f8;
 };
 
 // A row r of segment s at A + (s * a_seg_rows + r) * a_ld (bf16 elements).
 // Int8 weights are first widened into wdeq (exact), their scale goes to the epilogue.
+// FP8 problems: p.ascale set by the caller (the per-row scales of the e4m3
+// A); W is e4m3 with its per-channel scale in lin.scale; a K block is 128
+// elements (128 bytes), otherwise 64 bf16.
 static int prepare_gemm(const void* A, long long a_ld, long long a_seg_rows, int M_seg, int n_seg, int K,
                         const mmdit_linear_t& lin, int N, GemmParams p, uint16_t* wdeq, cudaStream_t st,
                         GemmProblem& out) {
-  if (K % kBK || N % 32 || M_seg < 1 || n_seg < 1) return MMDIT_ERR_SHAPE;
+  const bool f8 = p.ascale != nullptr;
+  const int kb = f8 ? 128 : kBK, eb = f8 ? 1 : 2;  // K elements per stage, bytes per element
+  if (K % kb || N % 32 || M_seg < 1 || n_seg < 1) return MMDIT_ERR_SHAPE;
   if (p.mode == GM_SWIGLU && N % kBN) return MMDIT_ERR_SHAPE;  // whole 128-row gate / up halves
-  if (!al16(A) || (a_ld * 2) % 16) return MMDIT_ERR_ALIGN;
+  if (!al16(A) || (a_ld * eb) % 16) return MMDIT_ERR_ALIGN;
   const void* W = lin.w;
   p.wscale = nullptr;
-  if (lin.scale) {
+  if (f8) {
+    if (!lin.scale) return MMDIT_ERR_ARG;
+    p.wscale = lin.scale;
+    p.ascale_seg_rows = a_seg_rows;
+  } else if (lin.scale) {
     if (!wdeq) return MMDIT_ERR_WORKSPACE;
     MMDIT_CUDA(launch_dequant_i8(static_cast<const int8_t*>(lin.w), wdeq, (long long)N * K, st));
     W = wdeq;
     p.wscale = lin.scale;
   }
   p.bias = lin.b;
-  if (!make_tmap_3d(&out.ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M_seg, (uint64_t)n_seg,
-                    (uint64_t)a_ld * 2, (uint64_t)a_seg_rows * a_ld * 2, kBK, kBM, true))
+  const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_tmap_3d(&out.ta, A, dt, eb, (uint64_t)K, (uint64_t)M_seg, (uint64_t)n_seg, (uint64_t)a_ld * eb,
+                    (uint64_t)a_seg_rows * a_ld * eb, kb, kBM, true))
     return MMDIT_ERR_ALIGN;
   // W is loaded in 128-row halves of the 256-row tile, one by each CTA of a cluster pair.
-  if (!make_tmap_3d(&out.tb, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, 1, (uint64_t)K * 2,
-                    (uint64_t)N * K * 2, kBK, kBN / 2, true))
+  if (!make_tmap_3d(&out.tb, W, dt, eb, (uint64_t)K, (uint64_t)N, 1, (uint64_t)K * eb, (uint64_t)N * K * eb, kb,
+                    kBN / 2, true))
     return MMDIT_ERR_ALIGN;
+  out.f8 = f8;
   p.M_seg = M_seg;
   p.n_seg = n_seg;
   p.N = N;
@@ -237,7 +249,7 @@ static int prepare_gemm(const void* A, long long a_ld, long long a_seg_rows, int
   // Raster: when the whole A operand fits comfortably in L2, sweep all M
   // tiles for each N tile (A stays resident, W streams once); otherwise
   // groups of 8 pairs (16 M tiles) bound the A footprint of a wave.
-  const double a_bytes = (double)n_seg * M_seg * K * 2.0;
+  const double a_bytes = (double)n_seg * M_seg * K * eb;
   p.group_m = a_bytes <= 48.0 * 1024 * 1024 ? pairs_m : 8;
   p.status = device_status_ptr();
   out.p = p;
@@ -252,6 +264,8 @@ static int launch_problems(const GemmProblem* a, const GemmProblem* b, cudaStrea
   g.tmB[0] = a->tb;
   g.p[0] = a->p;
   g.n_prob = 1;
+  g.f8 = a->f8 ? 1 : 0;
+  if (b && b->f8 != a->f8) return MMDIT_ERR_ARG;
   g.tiles0 = a->p.num_tiles;
   g.total_tiles = g.tiles0;
   if (b) {
@@ -677,7 +691,7 @@ const char* mmdit_kernel_name(int kernel_id) {
   static const char* names[KID_COUNT] = {"gemm_bf16_tc", "attn_fwd",   "ln_modulate", "gemv",      "sinusoid",
                                          "rope_build",   "rope_apply", "euler",       "quantize_w8", "dequant_i8",
                                          "cast_bf16",    "attn_prep",  "wait_selftest", "add_f32",
-                                         "step_counter"};
+                                         "step_counter", "quantize_f8"};
   return (kernel_id >= 0 && kernel_id < KID_COUNT) ? names[kernel_id] : "unknown";
 }
 
@@ -1014,6 +1028,67 @@ int mmdit_quantize_w8(const void* w, int w_dtype, int N, int K, int8_t* q, float
   return cuda_status(launch_quantize(w, w_dtype == MMDIT_BF16, N, K, q, scale, S(stream)));
 }
 
+int mmdit_quantize_f8(const void* x, int x_dtype, long long rows, int K, long long ld, uint8_t* q, float* s,
+                      void* stream) {
+  if (!x || !q || !s || rows < 0 || K < 2 || K % 2 || ld < K) return MMDIT_ERR_ARG;
+  if (x_dtype != MMDIT_BF16 && x_dtype != MMDIT_F32) return MMDIT_ERR_ARG;
+  if (rows > (1ll << 31) - 1) return MMDIT_ERR_SHAPE;
+  if (rows == 0) return MMDIT_OK;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_quantize_f8(x, x_dtype == MMDIT_BF16, rows, K, ld, q, K, s, S(stream)));
+}
+
+// The GEMM epilogue parameters of the test hooks' epilogue codes (y has N
+// columns; N / 2 for SwiGLU).
+static int linear_epilogue(int epilogue, int M, int N, void* y, const float* gate, GemmParams& p) {
+  switch (epilogue) {
+    case MMDIT_EPI_BF16:
+    case MMDIT_EPI_BF16_GELU:
+      p = gemm_params(GM_STORE_BF16);
+      if (epilogue == MMDIT_EPI_BF16_GELU) p.gelu_from = 0;
+      p.out = y;
+      p.out_ld = N;
+      p.out_seg_rows = M;
+      return MMDIT_OK;
+    case MMDIT_EPI_F32:
+      p = gemm_params(GM_STORE_F32);
+      p.out = y;
+      p.out_ld = N;
+      p.out_seg_rows = M;
+      return MMDIT_OK;
+    case MMDIT_EPI_SWIGLU:
+      p = gemm_params(GM_SWIGLU);
+      p.out = y;
+      p.out_ld = N / 2;
+      p.out_seg_rows = M;
+      return MMDIT_OK;
+    case MMDIT_EPI_RESID:
+      p = gemm_params(GM_RESID);
+      p.resid = static_cast<float*>(y);
+      p.resid_ld = N;
+      p.resid_seg_rows = M;
+      p.gate = gate;
+      p.gate_seg_stride = 0;
+      return MMDIT_OK;
+    default:
+      return MMDIT_ERR_ARG;
+  }
+}
+
+int mmdit_linear_f8_fwd(const mmdit_linear_t* lin, int M, int N, int K, const uint8_t* x, const float* x_scale,
+                        void* y, int epilogue, const float* gate, void* stream) {
+  if (!lin || !lin->w || !lin->scale || !x || !x_scale || !y) return MMDIT_ERR_ARG;
+  if (M < 1 || N < 32 || N % 32 || K < 128 || K % 128) return MMDIT_ERR_SHAPE;
+  if (!al16(x) || !al16(y) || !al16(lin->w) || !al16(lin->scale) || (lin->b && !al16(lin->b)) ||
+      (gate && !al16(gate)))
+    return MMDIT_ERR_ALIGN;
+  GemmParams p;
+  MMDIT_TRY(linear_epilogue(epilogue, M, N, y, gate, p));
+  MMDIT_TRY(check_device());
+  p.ascale = x_scale;
+  return run_gemm(x, K, M, M, 1, K, *lin, N, p, nullptr, S(stream));
+}
+
 int mmdit_linear_fwd(const mmdit_linear_t* lin, int M, int N, int K, const void* x, void* y, int epilogue,
                      const float* gate, void* ws, size_t ws_bytes, void* stream) {
   if (!lin || !x || !y) return MMDIT_ERR_ARG;
@@ -1026,40 +1101,9 @@ int mmdit_linear_fwd(const mmdit_linear_t* lin, int M, int N, int K, const void*
     if (!al16(ws)) return MMDIT_ERR_ALIGN;
     wdeq = static_cast<uint16_t*>(ws);
   }
-  MMDIT_TRY(check_device());
   GemmParams p;
-  switch (epilogue) {
-    case MMDIT_EPI_BF16:
-    case MMDIT_EPI_BF16_GELU:
-      p = gemm_params(GM_STORE_BF16);
-      if (epilogue == MMDIT_EPI_BF16_GELU) p.gelu_from = 0;
-      p.out = y;
-      p.out_ld = N;
-      p.out_seg_rows = M;
-      break;
-    case MMDIT_EPI_F32:
-      p = gemm_params(GM_STORE_F32);
-      p.out = y;
-      p.out_ld = N;
-      p.out_seg_rows = M;
-      break;
-    case MMDIT_EPI_SWIGLU:
-      p = gemm_params(GM_SWIGLU);
-      p.out = y;
-      p.out_ld = N / 2;
-      p.out_seg_rows = M;
-      break;
-    case MMDIT_EPI_RESID:
-      p = gemm_params(GM_RESID);
-      p.resid = static_cast<float*>(y);
-      p.resid_ld = N;
-      p.resid_seg_rows = M;
-      p.gate = gate;
-      p.gate_seg_stride = 0;
-      break;
-    default:
-      return MMDIT_ERR_ARG;
-  }
+  MMDIT_TRY(linear_epilogue(epilogue, M, N, y, gate, p));
+  MMDIT_TRY(check_device());
   return run_gemm(x, K, M, M, 1, K, *lin, N, p, wdeq, S(stream));
 }
 

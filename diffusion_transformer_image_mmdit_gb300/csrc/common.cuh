@@ -166,6 +166,17 @@ __device__ __forceinline__ void umma_bf16_if(uint32_t issue, uint32_t d_tmem, ui
       : "memory");
 }
 
+// FP8 (kind::f8f6f4) MMA: A and B e4m3 in shared memory, K = 32 per
+// instruction (32 bytes along K, like the 16-bit K = 16 step).
+__device__ __forceinline__ void umma_f8_if(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16_ta_if(uint32_t issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -243,6 +254,13 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with A and B e4m3 (format 0 in
+// bits 7-9 and 10-12), fp32 accumulator, both K-major, N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 #define MMDIT_TMEM_LD32(taddr, r)                                                                                   \

@@ -357,6 +357,42 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T* __restrict__ w, 
   }
 }
 
+// Two fp32 values to packed e4m3 (lo in the low byte), round to nearest
+// even, saturating at +-448.
+__device__ __forceinline__ uint16_t f8x2_e4m3(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// One CTA per row of x (row stride ld): s = max|x| / 448 (fp32, 1 for a zero
+// row), q = e4m3(x / s) with the quotient rounded once in fp32.  K even.
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_f8_kernel(const T* __restrict__ x, long long ld, int K,
+                                                          uint8_t* __restrict__ q, long long qld,
+                                                          float* __restrict__ scale) {
+  __shared__ float red[8];
+  const T* row = x + (long long)blockIdx.x * ld;
+  uint8_t* qrow = q + (long long)blockIdx.x * qld;
+  float m = 0.f;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) m = fmaxf(m, fabsf(load_w<T>(row, k)));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_max(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float amax = red[0];
+  const float s = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
+  if (threadIdx.x == 0) scale[blockIdx.x] = s;
+  for (int k = 2 * threadIdx.x; k < K; k += 2 * blockDim.x)
+    *reinterpret_cast<uint16_t*>(qrow + k) =
+        f8x2_e4m3(__fdiv_rn(load_w<T>(row, k), s), __fdiv_rn(load_w<T>(row, k + 1), s));
+}
+
 // int8 -> bf16 (exact: |q| <= 127 has at most 7 significant bits); 16 per thread.
 __global__ void dequant_i8_kernel(const int8_t* __restrict__ q, uint16_t* __restrict__ out, long long n16) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -590,6 +626,19 @@ cudaError_t launch_quantize(const void* w, bool w_bf16, int N, int K, int8_t* q,
     quantize_kernel<uint16_t><<<N, 256, 0, st>>>(reinterpret_cast<const uint16_t*>(w), K, q, scale);
   else
     quantize_kernel<float><<<N, 256, 0, st>>>(reinterpret_cast<const float*>(w), K, q, scale);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_f8(const void* x, bool x_bf16, long long rows, int K, long long ld, uint8_t* q,
+                               long long qld, float* scale, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  launch_begin(KID_QUANTIZE_F8, st);
+  if (x_bf16)
+    quantize_f8_kernel<uint16_t><<<(unsigned)rows, 256, 0, st>>>(reinterpret_cast<const uint16_t*>(x), ld, K, q, qld,
+                                                                  scale);
+  else
+    quantize_f8_kernel<float><<<(unsigned)rows, 256, 0, st>>>(reinterpret_cast<const float*>(x), ld, K, q, qld, scale);
   launch_end(st);
   return cudaGetLastError();
 }

@@ -39,6 +39,10 @@ cudaError_t launch_add(float* y, const float* x, long long n, cudaStream_t st);
 cudaError_t launch_counter(int* c, int value, bool add, cudaStream_t st);
 cudaError_t launch_quantize(const void* w, bool w_bf16, int N, int K, int8_t* q, float* scale, cudaStream_t st);
 cudaError_t launch_dequant_i8(const int8_t* q, uint16_t* out, long long n, cudaStream_t st);
+// FP8 (e4m3) rows: x [rows, K] (row stride ld, bf16 or fp32) -> q [rows, K]
+// (row stride qld) and scale [rows], s = max|row| / 448.
+cudaError_t launch_quantize_f8(const void* x, bool x_bf16, long long rows, int K, long long ld, uint8_t* q,
+                               long long qld, float* scale, cudaStream_t st);
 cudaError_t launch_cast_bf16(const float* x, uint16_t* y, long long n, cudaStream_t st);
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned* status, cudaStream_t st);
 cudaError_t launch_attn_prep(const uint16_t* qkv, long long qkv_ld, int B, int L, int L_txt, int H, int d,

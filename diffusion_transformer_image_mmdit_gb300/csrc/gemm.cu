@@ -73,14 +73,14 @@ __device__ __forceinline__ void load_vec32(const float* __restrict__ src, float*
   }
 }
 
-// Reads 32 accumulator columns of this thread's row and applies the int8
-// scale and the bias.
-__device__ __forceinline__ void acc_chunk(uint32_t taddr, const GemmParams& p, int n, float* v) {
+// Reads 32 accumulator columns of this thread's row and applies the fp8
+// row scale rs, the int8 / fp8 channel scale and the bias.
+__device__ __forceinline__ void acc_chunk(uint32_t taddr, const GemmParams& p, int n, float* v, float rs = 1.0f) {
   uint32_t raw[32];
   MMDIT_TMEM_LD32(taddr, raw);
   tmem_wait_ld();
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]) * rs;
   if (p.wscale) {
     float s[32];
     load_vec32(p.wscale + n, s);
@@ -166,14 +166,14 @@ __device__ __forceinline__ void warp_load_f32x32(uint8_t* stg, int lane, float* 
 template <int HD>
 __device__ __forceinline__ void epi_qk_head(uint32_t taddr, const GemmParams& p, int n, const float* __restrict__ g,
                                             int tok, uint8_t* stg, int lane, uint16_t* row0, long long ld,
-                                            int nrows) {
+                                            int nrows, float rs) {
   float v[HD];
 #pragma unroll
-  for (int c = 0; c < HD / 32; ++c) acc_chunk(taddr + c * 32, p, n + c * 32, v + c * 32);
+  for (int c = 0; c < HD / 32; ++c) acc_chunk(taddr + c * 32, p, n + c * 32, v + c * 32, rs);
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < HD; ++i) ss = fmaf(v[i], v[i], ss);
-  const float rs = rsqrtf(ss * (1.0f / HD) + p.eps);
+  const float rinv = rsqrtf(ss * (1.0f / HD) + p.eps);
   const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cos + (long long)tok * (HD / 2));
   const float4* sn4 = reinterpret_cast<const float4*>(p.rope_sin + (long long)tok * (HD / 2));
   const float4* g4 = reinterpret_cast<const float4*>(g);
@@ -188,8 +188,8 @@ __device__ __forceinline__ void epi_qk_head(uint32_t taddr, const GemmParams& p,
     const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float x0 = v[8 * q + 2 * j] * rs * gg[2 * j];
-      const float x1 = v[8 * q + 2 * j + 1] * rs * gg[2 * j + 1];
+      const float x0 = v[8 * q + 2 * j] * rinv * gg[2 * j];
+      const float x1 = v[8 * q + 2 * j + 1] * rinv * gg[2 * j + 1];
       v[8 * q + 2 * j] = x0 * cc[j] - x1 * sc[j];
       v[8 * q + 2 * j + 1] = x0 * sc[j] + x1 * cc[j];
     }
@@ -209,6 +209,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   const int nrows = min(32, p.M_seg - wm0);                // rows of this warp inside the problem (may be <= 0)
   const long long orow0 = (long long)c.seg * p.out_seg_rows + p.out_row_off + wm0;
   const int n0 = c.tn * kBN;
+  // fp8 GEMM: this row's activation scale (rows past the problem use 1; they are not stored)
+  const float rs = p.ascale && m < p.M_seg ? __ldg(p.ascale + (long long)c.seg * p.ascale_seg_rows + m) : 1.0f;
 
   if (p.mode == GM_QKV) {
     const int D = p.qkv_D;
@@ -220,11 +222,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       if (p.d_head == 128) {
 #pragma unroll 1
         for (int h = 0; h < kBN / 128; ++h)
-          epi_qk_head<128>(tbase + h * 128, p, n0 + h * 128, g, tok, stg, lane, row0 + h * 128, p.qk_ld, nrows);
+          epi_qk_head<128>(tbase + h * 128, p, n0 + h * 128, g, tok, stg, lane, row0 + h * 128, p.qk_ld, nrows, rs);
       } else {
 #pragma unroll 1
         for (int h = 0; h < kBN / 64; ++h)
-          epi_qk_head<64>(tbase + h * 64, p, n0 + h * 64, g, tok, stg, lane, row0 + h * 64, p.qk_ld, nrows);
+          epi_qk_head<64>(tbase + h * 64, p, n0 + h * 64, g, tok, stg, lane, row0 + h * 64, p.qk_ld, nrows, rs);
       }
     } else if (n0 < 3 * D) {
       // v^T: for each channel, the 32 lanes write 32 consecutive tokens (64 bytes)
@@ -234,7 +236,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       for (int j = 0; j < kBN / 32; ++j) {
         const int n = n0 + j * 32;
         float v[32];
-        acc_chunk(tbase + j * 32, p, n, v);
+        acc_chunk(tbase + j * 32, p, n, v, rs);
         if (lane < nrows) {
           const long long col = n - 2 * D;
 #pragma unroll
@@ -251,7 +253,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
         const int n = n0 + j * 32;
         if (n >= p.N) break;
         float v[32];
-        acc_chunk(tbase + j * 32, p, n, v);
+        acc_chunk(tbase + j * 32, p, n, v, rs);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_f(v[i]);
         warp_store_bf16x32(stg, lane, v, row0 + n, p.aux_ld, nrows);
@@ -267,8 +269,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 #pragma unroll 1
     for (int j = 0; j < kBN / 64; ++j) {
       float g[32], u[32];
-      acc_chunk(tbase + j * 32, p, g0 + j * 32, g);
-      acc_chunk(tbase + kBN / 2 + j * 32, p, p.swiglu_up + g0 + j * 32, u);
+      acc_chunk(tbase + j * 32, p, g0 + j * 32, g, rs);
+      acc_chunk(tbase + kBN / 2 + j * 32, p, p.swiglu_up + g0 + j * 32, u, rs);
 #pragma unroll
       for (int i = 0; i < 32; ++i) g[i] = silu_fast(g[i]) * u[i];
       warp_store_bf16x32(stg, lane, g, row0 + j * 32, p.out_ld, nrows);
@@ -281,7 +283,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     const int n = n0 + j * 32;
     if (n >= p.N) break;
     float v[32];
-    acc_chunk(tbase + j * 32, p, n, v);
+    acc_chunk(tbase + j * 32, p, n, v, rs);
     if (p.mode == GM_STORE_BF16) {
       if (n >= p.gelu_from) {
 #pragma unroll
@@ -308,7 +310,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   }
 }
 
+// F8: A and W are e4m3 (one byte per element, 128 elements per 128-byte
+// K block, kind::f8f6f4 MMAs of K = 32); otherwise bf16 (64 per K block,
+// kind::f16 MMAs of K = 16).  Either way a stage holds 16 KB of A and 32 KB
+// of W and takes four MMAs.
+template <bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmGroup g) {
+  constexpr int kKB = F8 ? 128 : kBK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -371,14 +379,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         // W rows of this CTA's half of the 256-row tile: rows n0 + 128 rank, or
         // for SwiGLU the matching 128 gate rows (rank 0) and up rows (rank 1)
         const int brow = p.mode == GM_SWIGLU ? c.tn * (kBN / 2) + rank * p.swiglu_up : n0 + rank * (kBN / 2);
-        const int nk = p.K / kBK;
+        const int nk = p.K / kKB;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, status, ST_TIMEOUT_PRODUCER)) goto done;
           // 16 KB of A from this CTA, 2 x 16 KB of W (one half from each CTA)
           mbar_expect_tx(full0 + 8 * stage, kStageA + kStageB);
-          tma_load_3d(smem_u32(sA + stage * kStageA), &g.tmA[q], full0 + 8 * stage, kb * kBK, m0, c.seg);
+          tma_load_3d(smem_u32(sA + stage * kStageA), &g.tmA[q], full0 + 8 * stage, kb * kKB, m0, c.seg);
           tma_load_3d_mc(smem_u32(sB + stage * kStageB + rank * (kStageB / 2)), &g.tmB[q], full0 + 8 * stage,
-                         kb * kBK, brow, 0, kPair);
+                         kb * kKB, brow, 0, kPair);
           ++n_fill;
           if (++stage == kStages) stage = 0, phase ^= 1;
         }
@@ -390,14 +398,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     // per MMA only a compile-time offset (in 16-byte units of the
     // start-address field) is added.
     const uint32_t leader = elect_one_sync();
-    const uint32_t idesc = idesc_bf16(kBM, kBN);
+    const uint32_t idesc = F8 ? idesc_e4m3(kBM, kBN) : idesc_bf16(kBM, kBN);
     const uint64_t dA0 = sdesc_k128(smem_u32(sA)), dB0 = sdesc_k128(smem_u32(sB));
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster; t < g.total_tiles; t += n_clusters) {
-      const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kBK;
+      const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kKB;
       if (!mbar_wait_warp(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
       tc_fence_after();
       const uint32_t d = tmem + acc * kBN;
@@ -407,7 +415,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         const uint64_t da = dA0 + (uint64_t)(stage * (kStageA >> 4));
         const uint64_t db = dB0 + (uint64_t)(stage * (kStageB >> 4));
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k) umma_bf16_if(leader, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+        for (int k = 0; k < 4; ++k) {  // 32 bytes of K per MMA
+          if (F8)
+            umma_f8_if(leader, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          else
+            umma_bf16_if(leader, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+        }
         umma_commit_mc_if(leader, empty0 + 8 * stage, kPair);  // frees the stage in both CTAs
         if (++stage == kStages) stage = 0, phase ^= 1;
       }
@@ -472,12 +485,14 @@ cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s) {
   if (dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
     cudaError_t e =
-        cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+        cudaFuncSetAttribute(gemm_bf16_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
     // Clusters of two that fit on the device at once (one CTA per SM).
     cfg.gridDim = dim3(2 * (num_sms() / 2));
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel<false>, &cfg);
     if (e != cudaSuccess) return e;
     if (n < 1) return cudaErrorInvalidConfiguration;
     max_clusters[dev] = n;
@@ -486,7 +501,8 @@ cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s) {
   const int clusters = g.total_tiles < max_clusters[dev] ? g.total_tiles : max_clusters[dev];
   cfg.gridDim = dim3(2 * clusters);
   launch_begin(KID_GEMM, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel, g);
+  cudaError_t e = g.f8 ? cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<true>, g)
+                       : cudaLaunchKernelEx(&cfg, gemm_bf16_tc_kernel<false>, g);
   launch_end(s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

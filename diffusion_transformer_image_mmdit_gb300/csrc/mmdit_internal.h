@@ -33,7 +33,9 @@ struct GemmParams {
   int gelu_from;
   int swiglu_up;  // GM_SWIGLU: row offset of the up half of W (= the output width)
   const float* bias;    // [N] or null
-  const float* wscale;  // [N] or null (int8 weights)
+  const float* wscale;  // [N] or null (int8 or fp8 weights)
+  const float* ascale;  // fp8 GEMM: scale of A row seg * ascale_seg_rows + m
+  long long ascale_seg_rows;
   void* out;            // bf16 or fp32 output
   long long out_ld;
   long long out_seg_rows;
@@ -72,6 +74,7 @@ struct GemmGroup {
   int n_prob;
   int tiles0;
   int total_tiles;
+  int f8;  // both problems fp8 (e4m3 A and W, kind::f8f6f4) instead of bf16
 };
 
 // ----------------------------------------------------------------- attention
@@ -106,6 +109,7 @@ enum KernelId : int {
   KID_SELFTEST,
   KID_ADD,
   KID_COUNTER,
+  KID_QUANTIZE_F8,
   KID_COUNT
 };
 // Bracket every kernel launch: counts launches and, while a trace is on,

@@ -330,6 +330,24 @@ int mmdit_quantize_w8(const void* w, int w_dtype, int N, int K, int8_t* q, float
  * Int8 weights when lin->scale != NULL (y = (x q^T) * scale + b); they are
  * widened to bf16 (exactly) in `ws`, which then needs N*K*2 bytes.
  * K a multiple of 64, N a multiple of 32. */
+/* FP8 (e4m3) row quantiser.  The SGLang blog ("Architecture") names FP8
+ * quantisation for serving without fixing a scheme; reading taken: each row
+ * (an output channel of a weight, or an activation row) gets s = max|row| /
+ * 448 (fp32; 1 for a zero row) and q = e4m3(x / s), the quotient rounded
+ * once in fp32, then to the nearest e4m3 (ties to even, saturating at 448).
+ * x: device [rows, K] with row stride ld elements, x_dtype MMDIT_BF16 or
+ * MMDIT_F32; q: device e4m3 bytes [rows, K] (row stride K); s: device fp32
+ * [rows].  K even. */
+int mmdit_quantize_f8(const void* x, int x_dtype, long long rows, int K, long long ld, uint8_t* q, float* s,
+                      void* stream);
+
+/* y = (x (.) sx) (W (.) sw)^T + b on e4m3 operands (tcgen05 kind::f8f6f4,
+ * fp32 accumulation): x device e4m3 [M, K] with row scales x_scale [M], W
+ * (lin->w) e4m3 [N, K] with channel scales lin->scale [N] (required).
+ * Epilogues and y as for mmdit_linear_fwd.  K a multiple of 128. */
+int mmdit_linear_f8_fwd(const mmdit_linear_t* lin, int M, int N, int K, const uint8_t* x, const float* x_scale,
+                        void* y, int epilogue, const float* gate, void* stream);
+
 #define MMDIT_EPI_BF16 0
 #define MMDIT_EPI_BF16_GELU 1
 #define MMDIT_EPI_F32 2

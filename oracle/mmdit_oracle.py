@@ -400,3 +400,43 @@ def quantize_w8(w):
 
 def dequantize_w8(q, s):
     return q.astype(np.float64) * s.astype(np.float64)[:, None]
+
+
+# --------------------------------------------------------------------------
+# FP8 (e4m3) rows: the SGLang blog ("Architecture") names FP8 quantisation
+# for serving; the scheme is not given.  Reading taken: each row (a weight's
+# output channel, or an activation row) is scaled by s = max|row| / 448
+# (float32; 1 for an all-zero row) and rounded to the nearest e4m3 value,
+# ties to even, saturating at +-448; the product of two such rows is
+# (q_x s_x) . (q_w s_w).
+E4M3_MAX = 448.0
+
+
+def round_e4m3(x):
+    """Nearest e4m3 value (1 sign, 4 exponent bits with bias 7, 3 mantissa
+    bits, no infinities; smallest normal 2^-6, subnormal step 2^-9), ties to
+    even, magnitudes beyond 448 saturated to 448."""
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    quantum = np.exp2(e - 3.0)
+    r = np.rint(a / quantum) * quantum
+    r = np.minimum(r, E4M3_MAX)
+    return np.where(a > 0, np.copysign(r, x), 0.0 * x)
+
+
+def quantize_f8_rows(x):
+    """Per row of x [..., K]: s = max|row| / 448 in float32 (1 for a zero
+    row); q = round_e4m3(x / s) with the quotient in float32.  Returns
+    (q float64 holding e4m3 values, s float32 [...])."""
+    x32 = np.asarray(x, np.float32)
+    amax = np.abs(x32).max(axis=-1)
+    s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+    q = round_e4m3((x32 / s[..., None]).astype(np.float32))
+    return q, s
+
+
+def dequantize_f8_rows(q, s):
+    return np.asarray(q, np.float64) * np.asarray(s, np.float64)[..., None]

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from diffusion_transformer_image_mmdit_gb300 import api, synthetic as S
+from diffusion_transformer_image_mmdit_gb300 import _lib, api, synthetic as S
 from diffusion_transformer_image_mmdit_gb300.api import LinearDev
 from oracle import mmdit_oracle as O
 from tests.gpu_common import (CONFIGS, FULL, api_shape, assert_close, bf16, check_status, f32, gpu_tables, host,
@@ -178,6 +178,71 @@ def test_linear_swiglu(M, F, K, i8):
     api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_SWIGLU, ws=ws)
     ref = O.swiglu(O.linear(x, w, b))
     assert_close(host(y), ref, max_abs=2.0 ** -8 * max(1.0, np.abs(ref).max()) + 1e-3, what="gemm swiglu")
+
+
+# ------------------------------------------------------------------ FP8 (e4m3)
+def decode_e4m3(codes) -> np.ndarray:
+    """e4m3 byte codes to values, from the bit layout (no NaN codes expected)."""
+    c = np.asarray(codes, np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 15, c & 7
+    assert not ((e == 15) & (m == 7)).any()
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    return sign * mag
+
+
+def test_quantize_f8_bit_exact():
+    x = S.normal_bf16("q8.x", (37, 384), 3.0)
+    x[5] = 0.0
+    x[7] *= 1e-3  # small rows reach the subnormal range after scaling
+    x = S.round_bf16(x)  # what the kernel reads
+    q, s = api.quantize_f8(bf16(x))
+    rq, rs = O.quantize_f8_rows(x)
+    assert np.array_equal(host(s).astype(np.float32), rs)
+    assert np.array_equal(decode_e4m3(q.cpu().numpy()), rq)
+    w = S.normal_f32("q8.w", (40, 256), 0.02)
+    qw, sw = api.quantize_f8(f32(w))
+    rqw, rsw = O.quantize_f8_rows(w)
+    assert np.array_equal(host(sw).astype(np.float32), rsw)
+    assert np.array_equal(decode_e4m3(qw.cpu().numpy()), rqw)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 512, 256), (1, 256, 128), (270, 384, 384)])
+@pytest.mark.parametrize("epi", ["f32", "bf16", "gelu", "swiglu", "resid"])
+def test_linear_f8(M, N, K, epi):
+    w, b = S.linear_params(f"l8.{M}.{N}.{K}", N, K)
+    x = S.normal_bf16("l8.x", (M, K))
+    lin8 = api.quantize_linear_f8(LinearDev(bf16(w), f32(b)))
+    x8, xs = api.quantize_f8(bf16(x))
+    xd = decode_e4m3(x8.cpu().numpy()) * host(xs)[:, None]
+    wd = decode_e4m3(lin8.w.cpu().numpy()) * host(lin8.scale)[:, None]
+    ref = O.linear(xd, wd, b)
+    if epi == "f32":
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        api.mmdit_linear_f8_fwd(lin8, x8, xs, y, api.MMDIT_EPI_F32)
+        assert_close(host(y), ref, rel=1e-4, max_abs=1e-4, what="fp8 gemm f32")
+        # the scheme against the exact product of the unquantised operands: the
+        # e4m3 step (2^-3 relative) leaves at most 2^-4 per operand, ~5% rms per dot product
+        assert rel_l2(host(y), O.linear(x, w, b)) <= 1e-1
+    elif epi == "resid":
+        r0 = S.normal_f32("l8.r", (M, N))
+        gate = S.normal_f32("l8.g", (N,))
+        y = f32(r0)
+        api.mmdit_linear_f8_fwd(lin8, x8, xs, y, api.MMDIT_EPI_RESID, gate=f32(gate))
+        assert_close(host(y), r0 + gate * ref, rel=1e-4, max_abs=1e-4, what="fp8 gemm resid")
+    else:
+        n_out = N // 2 if epi == "swiglu" else N
+        y = torch.empty((M, n_out), dtype=torch.bfloat16, device="cuda")
+        code = {"bf16": api.MMDIT_EPI_BF16, "gelu": api.MMDIT_EPI_BF16_GELU, "swiglu": api.MMDIT_EPI_SWIGLU}[epi]
+        if epi == "swiglu" and N % 256:
+            # gate and up must come in whole 128-row halves of a 256-row tile
+            with pytest.raises(_lib.MMDiTError) as e:
+                api.mmdit_linear_f8_fwd(lin8, x8, xs, y, code)
+            assert e.value.status == -2
+            return
+        api.mmdit_linear_f8_fwd(lin8, x8, xs, y, code)
+        r = {"bf16": ref, "gelu": O.gelu_tanh(ref), "swiglu": O.swiglu(ref)}[epi]
+        assert_close(host(y), r, max_abs=2.0 ** -8 * max(1.0, np.abs(r).max()) + 1e-4, what=f"fp8 gemm {epi}")
 
 
 def test_gemm_large_tiles_and_ragged():

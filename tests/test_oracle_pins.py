@@ -485,6 +485,52 @@ def test_time_embed_and_final_layer_vs_torch():
     assert rel(O.final_layer(x, vec, W, sh), F.linear(y, T["final_w"], T["final_b"]).numpy()) < 1e-14
 
 
+# ------------------------------------------------------------------ FP8 (e4m3)
+def _e4m3_table():
+    """All finite e4m3 codes decoded from the bit layout: sign, 4 exponent bits
+    (bias 7; 0 = subnormal), 3 mantissa bits; exponent 15 with mantissa 7 is
+    NaN.  Returns (values, mantissa LSB) of the non-negative codes."""
+    vals, lsb = [], []
+    for code in range(128):
+        e, m = (code >> 3) & 15, code & 7
+        if e == 15 and m == 7:
+            continue
+        v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+        vals.append(v)
+        lsb.append(m & 1)
+    return np.array(vals), np.array(lsb)
+
+
+def test_round_e4m3_brute_force():
+    vals, lsb = _e4m3_table()
+    assert vals.max() == 448.0 and vals[vals > 0].min() == 2.0 ** -9 and len(vals) == 127
+    xs = np.concatenate([rnd("f8.x", (4000,), 1.0), rnd("f8.y", (2000,), 60.0), rnd("f8.z", (1000,), 0.01),
+                         (vals[1:] + vals[:-1]) / 2, -(vals[1:] + vals[:-1]) / 2, [500.0, -1e4, 0.0]])
+    got = O.round_e4m3(xs)
+    for x, g in zip(xs, got):
+        a = min(abs(x), 448.0)
+        d = np.abs(vals - a)
+        cand = np.flatnonzero(d == d.min())
+        pick = cand[0] if len(cand) == 1 else cand[lsb[cand] == 0][0]  # ties to the even mantissa
+        assert g == math.copysign(vals[pick], x) or (x == 0 and g == 0), (x, g, vals[pick])
+
+
+def test_quantize_f8_rows_invariants():
+    x = rnd("f8.rows", (6, 100), 3.0)
+    x[2] = 0.0
+    q, s = O.quantize_f8_rows(x)
+    assert np.abs(q).max() <= 448.0
+    vals, _ = _e4m3_table()
+    assert np.isin(np.abs(q), vals).all()
+    for r in (0, 1, 3, 4, 5):
+        assert np.abs(q[r]).max() == 448.0
+    assert s[2] == 1.0 and not q[2].any()
+    # every element within half a local e4m3 step (relative 2^-4 of the normal range) of x / s
+    xs = x / s[:, None].astype(np.float64)
+    step = np.exp2(np.maximum(np.floor(np.log2(np.maximum(np.abs(xs), 1e-30))), -6.0) - 3.0)
+    assert (np.abs(q - xs) <= step / 2 * (1 + 1e-6) + 1e-12).all()
+
+
 # ------------------------------------------------------------------ conditioning and the sampling loop
 def _cond_params(sh, C_txt, C_pool):
     W = S.embed_params(sh.D, sh.C_lat, sh.t_dim, seed=5)
@@ -665,6 +711,17 @@ def test_planted_mistakes_in_the_sampling_loop_are_caught(monkeypatch):
     def denoise_drop_vec_add(x, xt, s0, s1, W, sh, vec_add=None):
         return orig_denoise(x, xt, s0, s1, W, sh, None)
 
+    orig_r8 = O.round_e4m3
+
+    def round_e4m3_half_up(x):  # ties away from zero instead of to even
+        x = np.asarray(x, np.float64)
+        a = np.abs(x)
+        e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6.0)
+        qn = np.exp2(e - 3.0)
+        return np.copysign(np.minimum(np.floor(a / qn + 0.5) * qn, 448.0), x)
+
+    _planted(monkeypatch, "round_e4m3", round_e4m3_half_up, test_round_e4m3_brute_force)
+    monkeypatch.setattr(O, "round_e4m3", orig_r8)
     orig_sw = O.swiglu
 
     def swiglu_swapped(h):
