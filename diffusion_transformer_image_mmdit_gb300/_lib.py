@@ -12,7 +12,7 @@ from ctypes import POINTER, Structure, c_double, c_float, c_int, c_int64, c_long
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmmdit.so")
 
 MMDIT_OK = 0
-MMDIT_BF16, MMDIT_F32, MMDIT_I8W = 0, 1, 2
+MMDIT_BF16, MMDIT_F32, MMDIT_I8W, MMDIT_F8W = 0, 1, 2, 3
 MMDIT_OP_DOUBLE, MMDIT_OP_SINGLE, MMDIT_OP_ATTENTION = 1, 2, 3
 MMDIT_EPI_BF16, MMDIT_EPI_BF16_GELU, MMDIT_EPI_F32, MMDIT_EPI_RESID = 0, 1, 2, 3
 ERRORS = {-1: "ARG", -2: "SHAPE", -3: "ALIGN", -4: "WORKSPACE", -5: "CUDA", -6: "TIMEOUT", -7: "UNSUPPORTED"}

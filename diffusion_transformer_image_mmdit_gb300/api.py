@@ -14,7 +14,7 @@ import torch
 
 from . import _lib
 from ._lib import (MMDIT_BF16, MMDIT_EPI_BF16, MMDIT_EPI_BF16_GELU, MMDIT_EPI_F32, MMDIT_EPI_RESID, MMDIT_F32,
-                   MMDIT_I8W, MMDIT_OP_ATTENTION, MMDIT_OP_DOUBLE, MMDIT_OP_SINGLE, DoubleW, Linear, Shape, SingleW,
+                   MMDIT_I8W, MMDIT_F8W, MMDIT_OP_ATTENTION, MMDIT_OP_DOUBLE, MMDIT_OP_SINGLE, DoubleW, Linear, Shape, SingleW,
                    StepW, CondW, MMDIT_SAMPLE_GRAPH, MMDIT_EPI_SWIGLU, MMDIT_MLP_GELU, MMDIT_MLP_SWIGLU, call)
 
 
@@ -107,6 +107,12 @@ class DoubleWeights:
         return DoubleWeights(q(self.mod), q(self.qkv), q(self.proj), q(self.mlp_in), q(self.mlp_out), self.q_norm,
                              self.k_norm)
 
+    def quantized_f8(self, stream=None) -> "DoubleWeights":
+        """MMDIT_F8W copy: the four GEMM linears in e4m3, modulation kept bf16."""
+        q = lambda ls: [quantize_linear_f8(l, stream) for l in ls]
+        return DoubleWeights(self.mod, q(self.qkv), q(self.proj), q(self.mlp_in), q(self.mlp_out), self.q_norm,
+                             self.k_norm)
+
 
 @dataclass
 class SingleWeights:
@@ -125,6 +131,11 @@ class SingleWeights:
     def quantized(self, stream=None) -> "SingleWeights":
         q = lambda l: quantize_linear(l, stream)
         return SingleWeights(q(self.mod), q(self.lin1), q(self.lin2), self.q_norm, self.k_norm)
+
+    def quantized_f8(self, stream=None) -> "SingleWeights":
+        """MMDIT_F8W copy: lin1 and lin2 in e4m3, modulation kept bf16."""
+        q = lambda l: quantize_linear_f8(l, stream)
+        return SingleWeights(self.mod, q(self.lin1), q(self.lin2), self.q_norm, self.k_norm)
 
 
 @dataclass
@@ -155,6 +166,11 @@ class StepWeights:
         q = lambda l: quantize_linear(l, stream)
         return StepWeights(q(self.time1), q(self.time2), q(self.img_in), q(self.final_mod), q(self.final),
                            [d.quantized(stream) for d in self.doubles], [b.quantized(stream) for b in self.singles])
+
+    def quantized_f8(self, stream=None) -> "StepWeights":
+        """MMDIT_F8W copy: the block GEMM linears in e4m3; every other linear bf16."""
+        return StepWeights(self.time1, self.time2, self.img_in, self.final_mod, self.final,
+                           [d.quantized_f8(stream) for d in self.doubles], [b.quantized_f8(stream) for b in self.singles])
 
 
 @dataclass

@@ -151,6 +151,7 @@ struct Carve {
 struct Dims {
   int B, Lt, Li, L, Lpad, D, H, d, Dm;
   bool swiglu;  // SwiGLU MLP: the first MLP projection has 2 Dm rows [gate; up]
+  bool f8;      // FP8 block GEMMs (MMDIT_F8W)
 };
 
 static int check_shape(const mmdit_shape_t* s, Dims* out) {
@@ -162,7 +163,7 @@ static int check_shape(const mmdit_shape_t* s, Dims* out) {
   if (s->D_mlp <= 0 || s->D_mlp % 64) return MMDIT_ERR_SHAPE;
   const int a0 = s->rope_axes[0], a1 = s->rope_axes[1], a2 = s->rope_axes[2];
   if (a0 < 0 || a1 < 0 || a2 < 0 || (a0 | a1 | a2) & 1 || a0 + a1 + a2 != s->d_head) return MMDIT_ERR_SHAPE;
-  if (s->w_dtype != MMDIT_BF16 && s->w_dtype != MMDIT_I8W) return MMDIT_ERR_ARG;
+  if (s->w_dtype != MMDIT_BF16 && s->w_dtype != MMDIT_I8W && s->w_dtype != MMDIT_F8W) return MMDIT_ERR_ARG;
   if (s->mlp_act != MMDIT_MLP_GELU && s->mlp_act != MMDIT_MLP_SWIGLU) return MMDIT_ERR_ARG;
   if (s->mlp_act == MMDIT_MLP_SWIGLU && s->D_mlp % 128) return MMDIT_ERR_SHAPE;
   const long long L = (long long)s->L_txt + (long long)s->grid_h * s->grid_w;
@@ -172,6 +173,8 @@ static int check_shape(const mmdit_shape_t* s, Dims* out) {
     out->Lpad = (int)((L + 7) / 8 * 8);
     out->D = s->D, out->H = s->H, out->d = s->d_head, out->Dm = s->D_mlp;
     out->swiglu = s->mlp_act == MMDIT_MLP_SWIGLU;
+    out->f8 = s->w_dtype == MMDIT_F8W;
+    if (out->f8 && (s->D % 128 || s->D_mlp % 128)) return MMDIT_ERR_SHAPE;  // whole e4m3 K blocks
   }
   return MMDIT_OK;
 }
@@ -321,6 +324,8 @@ static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, 
 struct DoubleWS {
   float* mod;
   uint16_t *y, *qk, *vT, *O, *h, *wdeq[2];
+  uint8_t* a8;  // FP8: e4m3 copy of the current GEMM input (all rows), and its row scales
+  float* as;
 };
 // y and h hold both streams at once (text rows first), so that each linear
 // of the two streams runs as one grouped launch; int8 weights need one
@@ -336,11 +341,15 @@ static void layout_double(const Dims& d, bool i8, bool need_mod, Carve& c, Doubl
   const size_t wmax = ((size_t)3 * d.D > wmlp ? (size_t)3 * d.D : wmlp) * d.D;
   w.wdeq[0] = i8 ? c.take<uint16_t>(wmax) : nullptr;
   w.wdeq[1] = i8 ? c.take<uint16_t>(wmax) : nullptr;
+  w.a8 = d.f8 ? c.take<uint8_t>((size_t)d.B * d.L * (d.D > d.Dm ? d.D : d.Dm)) : nullptr;
+  w.as = d.f8 ? c.take<float>((size_t)d.B * d.L) : nullptr;
 }
 
 struct SingleWS {
   float* mod;
   uint16_t *y, *qk, *vT, *cat, *wdeq;
+  uint8_t* a8;
+  float* as;
 };
 static void layout_single(const Dims& d, bool i8, bool need_mod, Carve& c, SingleWS& w) {
   w.mod = need_mod ? c.take<float>((size_t)d.B * 3 * d.D) : nullptr;
@@ -349,6 +358,8 @@ static void layout_single(const Dims& d, bool i8, bool need_mod, Carve& c, Singl
   w.vT = c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
   w.cat = c.take<uint16_t>((size_t)d.B * d.L * (d.D + d.Dm));
   w.wdeq = i8 ? c.take<uint16_t>(((size_t)3 * d.D + (size_t)(d.swiglu ? 2 : 1) * d.Dm) * d.D) : nullptr;
+  w.a8 = d.f8 ? c.take<uint8_t>((size_t)d.B * d.L * (d.D + d.Dm)) : nullptr;
+  w.as = d.f8 ? c.take<float>((size_t)d.B * d.L) : nullptr;
 }
 
 struct StepWS {
@@ -404,10 +415,22 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
   auto grouped = [&](const GemmProblem* pr) -> int {
     return launch_problems(&pr[first], first == 0 ? &pr[1] : nullptr, st);
   };
+  // FP8: a linear reads the e4m3 copy of its bf16 input, made by one row
+  // quantisation pass over all B L rows (K wide) into ws.a8 / ws.as; stream
+  // i's A operand and row scales start at the same row offset.
+  auto quant = [&](const uint16_t* src, int K) -> int {
+    return cuda_status(launch_quantize_f8(src, true, (long long)d.B * d.L, K, K, ws.a8, K, ws.as, st));
+  };
+  auto a_op = [&](const uint16_t* src, long long row0, int K, GemmParams& p) -> const void* {
+    if (!d.f8) return src + row0 * K;
+    p.ascale = ws.as + row0;
+    return ws.a8 + row0 * K;
+  };
   GemmProblem pr[2];
   // LN + modulate, then the fused QKV / RMSNorm / RoPE GEMM
   for (int i = first; i < 2; ++i)
     MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, modp(i), modp(i) + D, 6 * D, s.eps_ln, yp(i), st));
+  if (d.f8) MMDIT_TRY(quant(ws.y, D));
   for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(GM_QKV);
     p.out_seg_rows = d.L;
@@ -423,10 +446,12 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     p.qk_ld = 2 * D;
     p.vT = ws.vT;
     p.vT_ld = d.Lpad;
-    MMDIT_TRY(prepare_gemm(yp(i), D, Ls[i], Ls[i], d.B, D, w.qkv[i], 3 * D, p, ws.wdeq[i], st, pr[i]));
+    const void* A = a_op(ws.y, (long long)off[i] * d.B, D, p);
+    MMDIT_TRY(prepare_gemm(A, D, Ls[i], Ls[i], d.B, D, w.qkv[i], 3 * D, p, ws.wdeq[i], st, pr[i]));
   }
   MMDIT_TRY(grouped(pr));
   MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.O, D, st));
+  if (d.f8) MMDIT_TRY(quant(ws.O, D));
   // x += gate1 * (o Wp^T + bp)
   for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(GM_RESID);
@@ -435,23 +460,27 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     p.resid_seg_rows = xseg[i];
     p.gate = modp(i) + 2 * D;
     p.gate_seg_stride = 6 * D;
-    MMDIT_TRY(prepare_gemm(ws.O + (size_t)off[i] * D, D, d.L, Ls[i], d.B, D, w.proj[i], D, p, ws.wdeq[i], st, pr[i]));
+    const void* A = a_op(ws.O, off[i], D, p);
+    MMDIT_TRY(prepare_gemm(A, D, d.L, Ls[i], d.B, D, w.proj[i], D, p, ws.wdeq[i], st, pr[i]));
   }
   MMDIT_TRY(grouped(pr));
   // y2 = LN(x)(1 + scale2) + shift2; h = GELU(y2 W1^T + b1)
   for (int i = first; i < 2; ++i)
     MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, modp(i) + 3 * D, modp(i) + 4 * D, 6 * D, s.eps_ln,
                                   yp(i), st));
+  if (d.f8) MMDIT_TRY(quant(ws.y, D));
   for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(d.swiglu ? GM_SWIGLU : GM_STORE_BF16);
     p.gelu_from = 0;
     p.out = hp(i);
     p.out_ld = d.Dm;
     p.out_seg_rows = Ls[i];
-    MMDIT_TRY(prepare_gemm(yp(i), D, Ls[i], Ls[i], d.B, D, w.mlp_in[i], d.swiglu ? 2 * d.Dm : d.Dm, p, ws.wdeq[i], st,
+    const void* A = a_op(ws.y, (long long)off[i] * d.B, D, p);
+    MMDIT_TRY(prepare_gemm(A, D, Ls[i], Ls[i], d.B, D, w.mlp_in[i], d.swiglu ? 2 * d.Dm : d.Dm, p, ws.wdeq[i], st,
                            pr[i]));
   }
   MMDIT_TRY(grouped(pr));
+  if (d.f8) MMDIT_TRY(quant(ws.h, d.Dm));
   // x += gate2 * (h W2^T + b2)
   for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(GM_RESID);
@@ -460,7 +489,8 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     p.resid_seg_rows = xseg[i];
     p.gate = modp(i) + 5 * D;
     p.gate_seg_stride = 6 * D;
-    MMDIT_TRY(prepare_gemm(hp(i), d.Dm, Ls[i], Ls[i], d.B, d.Dm, w.mlp_out[i], D, p, ws.wdeq[i], st, pr[i]));
+    const void* A = a_op(ws.h, (long long)off[i] * d.B, d.Dm, p);
+    MMDIT_TRY(prepare_gemm(A, d.Dm, Ls[i], Ls[i], d.B, d.Dm, w.mlp_out[i], D, p, ws.wdeq[i], st, pr[i]));
   }
   MMDIT_TRY(grouped(pr));
   return MMDIT_OK;
@@ -477,7 +507,12 @@ static int single_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
   }
   MMDIT_CUDA(launch_ln_modulate(x, d.L, d.L, d.B, D, mod, mod + D, 3 * D, s.eps_ln, ws.y, st));
   const long long cat_ld = D + d.Dm;
+  const long long rows = (long long)d.B * d.L;
+  // FP8: lin1 reads the e4m3 rows of y, lin2 those of [O | act(mlp)]
+  if (d.f8) MMDIT_CUDA(launch_quantize_f8(ws.y, true, rows, D, D, ws.a8, D, ws.as, st));
+  const void* A1 = d.f8 ? static_cast<const void*>(ws.a8) : static_cast<const void*>(ws.y);
   GemmParams p = gemm_params(GM_QKV);
+  p.ascale = d.f8 ? ws.as : nullptr;
   p.out_seg_rows = d.L;
   p.out_row_off = 0;
   p.qkv_D = D;
@@ -495,7 +530,7 @@ static int single_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
   p.aux_ld = cat_ld;
   p.aux_col_off = D;
   if (!d.swiglu) {
-    MMDIT_TRY(run_gemm(ws.y, D, d.L, d.L, d.B, D, w.lin1, 3 * D + d.Dm, p, ws.wdeq, st));
+    MMDIT_TRY(run_gemm(A1, D, d.L, d.L, d.B, D, w.lin1, 3 * D + d.Dm, p, ws.wdeq, st));
   } else {
     // lin1 rows [q; k; v] (QKV epilogue) and [gate; up] (SwiGLU into the columns
     // [D, D + Dm) of cat) as the two problems of one launch
@@ -506,40 +541,51 @@ static int single_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     if (w.lin1.b) mlp.b = static_cast<const float*>(w.lin1.b) + 3 * D;
     if (w.lin1.scale) mlp.scale = w.lin1.scale + 3 * D;
     GemmProblem pr[2];
-    MMDIT_TRY(prepare_gemm(ws.y, D, d.L, d.L, d.B, D, w.lin1, 3 * D, p, ws.wdeq, st, pr[0]));
+    MMDIT_TRY(prepare_gemm(A1, D, d.L, d.L, d.B, D, w.lin1, 3 * D, p, ws.wdeq, st, pr[0]));
     GemmParams ps = gemm_params(GM_SWIGLU);
+    ps.ascale = p.ascale;
     ps.out = ws.cat + D;
     ps.out_ld = cat_ld;
     ps.out_seg_rows = d.L;
-    MMDIT_TRY(prepare_gemm(ws.y, D, d.L, d.L, d.B, D, mlp, 2 * d.Dm, ps, ws.wdeq ? ws.wdeq + (size_t)3 * D * D : nullptr,
+    MMDIT_TRY(prepare_gemm(A1, D, d.L, d.L, d.B, D, mlp, 2 * d.Dm, ps, ws.wdeq ? ws.wdeq + (size_t)3 * D * D : nullptr,
                            st, pr[1]));
     MMDIT_TRY(launch_problems(&pr[0], &pr[1], st));
   }
   MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.cat, cat_ld, st));
+  if (d.f8) MMDIT_CUDA(launch_quantize_f8(ws.cat, true, rows, (int)cat_ld, cat_ld, ws.a8, cat_ld, ws.as, st));
   GemmParams p2 = gemm_params(GM_RESID);
+  p2.ascale = d.f8 ? ws.as : nullptr;
   p2.resid = x;
   p2.resid_ld = D;
   p2.resid_seg_rows = d.L;
   p2.gate = mod + 2 * D;
   p2.gate_seg_stride = 3 * D;
-  MMDIT_TRY(run_gemm(ws.cat, cat_ld, d.L, d.L, d.B, (int)cat_ld, w.lin2, D, p2, ws.wdeq, st));
+  MMDIT_TRY(run_gemm(d.f8 ? static_cast<const void*>(ws.a8) : static_cast<const void*>(ws.cat), cat_ld, d.L, d.L, d.B,
+                     (int)cat_ld, w.lin2, D, p2, ws.wdeq, st));
   return MMDIT_OK;
 }
 
-static bool double_w_ok(const mmdit_double_w_t* w, bool i8) {
+// Which linears carry a per-channel scale: every linear for int8 weights;
+// only the block GEMM linears for FP8 (modulation stays bf16).
+static bool scaled_gemv(int w_dtype) { return w_dtype == MMDIT_I8W; }
+static bool scaled_gemm(int w_dtype) { return w_dtype == MMDIT_I8W || w_dtype == MMDIT_F8W; }
+
+static bool double_w_ok(const mmdit_double_w_t* w, int w_dtype) {
   if (!w) return false;
+  const bool qv = scaled_gemv(w_dtype), qg = scaled_gemm(w_dtype);
   for (int i = 0; i < 2; ++i) {
-    if (!lin_ok(w->mod[i], i8) || !lin_ok(w->qkv[i], i8) || !lin_ok(w->proj[i], i8) || !lin_ok(w->mlp_in[i], i8) ||
-        !lin_ok(w->mlp_out[i], i8))
+    if (!lin_ok(w->mod[i], qv) || !lin_ok(w->qkv[i], qg) || !lin_ok(w->proj[i], qg) || !lin_ok(w->mlp_in[i], qg) ||
+        !lin_ok(w->mlp_out[i], qg))
       return false;
     if (!w->q_norm[i] || !w->k_norm[i] || !al16(w->q_norm[i]) || !al16(w->k_norm[i])) return false;
   }
   return true;
 }
 
-static bool single_w_ok(const mmdit_single_w_t* w, bool i8) {
+static bool single_w_ok(const mmdit_single_w_t* w, int w_dtype) {
   if (!w) return false;
-  if (!lin_ok(w->mod, i8) || !lin_ok(w->lin1, i8) || !lin_ok(w->lin2, i8)) return false;
+  const bool qv = scaled_gemv(w_dtype), qg = scaled_gemm(w_dtype);
+  if (!lin_ok(w->mod, qv) || !lin_ok(w->lin1, qg) || !lin_ok(w->lin2, qg)) return false;
   return w->q_norm && w->k_norm && al16(w->q_norm) && al16(w->k_norm);
 }
 
@@ -551,9 +597,9 @@ static int step_w_check(const mmdit_shape_t& shape, const mmdit_step_w_t& w) {
       !lin_ok(w.final, i8))
     return MMDIT_ERR_ARG;
   for (int i = 0; i < w.n_double; ++i)
-    if (!double_w_ok(&w.doubles[i], i8)) return MMDIT_ERR_ARG;
+    if (!double_w_ok(&w.doubles[i], shape.w_dtype)) return MMDIT_ERR_ARG;
   for (int i = 0; i < w.n_single; ++i)
-    if (!single_w_ok(&w.singles[i], i8)) return MMDIT_ERR_ARG;
+    if (!single_w_ok(&w.singles[i], shape.w_dtype)) return MMDIT_ERR_ARG;
   return MMDIT_OK;
 }
 
@@ -829,7 +875,7 @@ int mmdit_double_block_fwd(const mmdit_shape_t* shape, const mmdit_double_w_t* w
   Dims d;
   MMDIT_TRY(check_shape(shape, &d));
   const bool i8 = shape->w_dtype == MMDIT_I8W;
-  if (!double_w_ok(w, i8)) return MMDIT_ERR_ARG;
+  if (!double_w_ok(w, shape->w_dtype)) return MMDIT_ERR_ARG;
   if ((vec == nullptr) == (mod_precomputed == nullptr)) return MMDIT_ERR_ARG;
   if (!x_img || (d.Lt > 0 && !x_txt) || !cos_ || !sin_ || !ws) return MMDIT_ERR_ARG;
   if ((x_txt && !al16(x_txt)) || !al16(x_img) || !al16(cos_) || !al16(sin_) || !al16(ws) ||
@@ -853,7 +899,7 @@ int mmdit_single_block_fwd(const mmdit_shape_t* shape, const mmdit_single_w_t* w
   Dims d;
   MMDIT_TRY(check_shape(shape, &d));
   const bool i8 = shape->w_dtype == MMDIT_I8W;
-  if (!single_w_ok(w, i8)) return MMDIT_ERR_ARG;
+  if (!single_w_ok(w, shape->w_dtype)) return MMDIT_ERR_ARG;
   if ((vec == nullptr) == (mod_precomputed == nullptr)) return MMDIT_ERR_ARG;
   if (!x || !cos_ || !sin_ || !ws) return MMDIT_ERR_ARG;
   if (!al16(x) || !al16(cos_) || !al16(sin_) || !al16(ws) || (vec && !al16(vec)) ||

@@ -393,6 +393,53 @@ __global__ void __launch_bounds__(256) quantize_f8_kernel(const T* __restrict__ 
         f8x2_e4m3(__fdiv_rn(load_w<T>(row, k), s), __fdiv_rn(load_w<T>(row, k + 1), s));
 }
 
+// The same for bf16 rows read once: each thread holds CPT 16-byte chunks (8
+// values) of the row in registers, so the row is read from memory once and
+// written once as e4m3.  K a multiple of 8, K <= 2048 CPT; row starts 16-byte
+// aligned.
+template <int CPT>
+__global__ void __launch_bounds__(256) quantize_f8_bf16_kernel(const uint16_t* __restrict__ x, long long ld, int K,
+                                                               uint8_t* __restrict__ q, long long qld,
+                                                               float* __restrict__ scale) {
+  __shared__ float red[8];
+  const int nch = K / 8;
+  const uint4* row = reinterpret_cast<const uint4*>(x + (long long)blockIdx.x * ld);
+  uint2* qrow = reinterpret_cast<uint2*>(q + (long long)blockIdx.x * qld);
+  uint4 v[CPT];
+  float m = 0.f;
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const int i = threadIdx.x + c * 256;
+    v[c] = i < nch ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < 8 ? red[threadIdx.x] : 0.f;
+    t = warp_max(t);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float amax = red[0];
+  const float s = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
+  if (threadIdx.x == 0) scale[blockIdx.x] = s;
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const int i = threadIdx.x + c * 256;
+    if (i < nch) {
+      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+      uint16_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = f8x2_e4m3(__fdiv_rn(bf16_lo(w[j]), s), __fdiv_rn(bf16_hi(w[j]), s));
+      qrow[i] = make_uint2((uint32_t)o[0] | ((uint32_t)o[1] << 16), (uint32_t)o[2] | ((uint32_t)o[3] << 16));
+    }
+  }
+}
+
 // int8 -> bf16 (exact: |q| <= 127 has at most 7 significant bits); 16 per thread.
 __global__ void dequant_i8_kernel(const int8_t* __restrict__ q, uint16_t* __restrict__ out, long long n16) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -634,7 +681,20 @@ cudaError_t launch_quantize_f8(const void* x, bool x_bf16, long long rows, int K
                                long long qld, float* scale, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   launch_begin(KID_QUANTIZE_F8, st);
-  if (x_bf16)
+  const bool vec = x_bf16 && K % 8 == 0 && K <= 2048 * 8 && ld % 8 == 0 && qld % 8 == 0 &&
+                   (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(q) & 7) == 0;
+  if (vec) {
+    const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
+    const int cpt = (K / 8 + 255) / 256;
+    if (cpt <= 1)
+      quantize_f8_bf16_kernel<1><<<(unsigned)rows, 256, 0, st>>>(xb, ld, K, q, qld, scale);
+    else if (cpt <= 2)
+      quantize_f8_bf16_kernel<2><<<(unsigned)rows, 256, 0, st>>>(xb, ld, K, q, qld, scale);
+    else if (cpt <= 4)
+      quantize_f8_bf16_kernel<4><<<(unsigned)rows, 256, 0, st>>>(xb, ld, K, q, qld, scale);
+    else
+      quantize_f8_bf16_kernel<8><<<(unsigned)rows, 256, 0, st>>>(xb, ld, K, q, qld, scale);
+  } else if (x_bf16)
     quantize_f8_kernel<uint16_t><<<(unsigned)rows, 256, 0, st>>>(reinterpret_cast<const uint16_t*>(x), ld, K, q, qld,
                                                                   scale);
   else

@@ -61,6 +61,11 @@ extern "C" {
 #define MMDIT_BF16 0
 #define MMDIT_F32 1
 #define MMDIT_I8W 2 /* int8 weight with fp32 per-output-channel scale */
+/* e4m3 weights with fp32 per-output-channel scales for the block GEMMs (qkv,
+ * proj, mlp_in, mlp_out, lin1, lin2: mmdit_quantize_f8 codes), their
+ * activations quantised to e4m3 per row on the fly, tcgen05 kind::f8f6f4
+ * MMAs; modulation and step-level linears stay bf16 (scale NULL). */
+#define MMDIT_F8W 3
 
 /* ---------------------------------------------------------------- shapes */
 typedef struct {
@@ -76,7 +81,7 @@ typedef struct {
   double rope_theta;
   float eps_ln;     /* LayerNorm epsilon */
   float eps_rms;    /* q/k RMSNorm epsilon */
-  int w_dtype;      /* MMDIT_BF16 or MMDIT_I8W for all linear weights */
+  int w_dtype;      /* MMDIT_BF16, MMDIT_I8W (all linears) or MMDIT_F8W (block GEMM linears) */
   int C_lat;        /* latent channels per image token (step only) */
   int t_dim;        /* timestep sinusoid width (step only) */
   int mlp_act;      /* MMDIT_MLP_GELU or MMDIT_MLP_SWIGLU (see below) */

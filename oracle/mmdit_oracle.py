@@ -204,7 +204,7 @@ def _ident(x):
     return x
 
 
-def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows_img=None, rnd=None):
+def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows_img=None, rnd=None, qin=None):
     """Double-stream block.  x_txt [B, L_txt, D], x_img [B, L_img, D], vec
     [B, D]; wt['txt'] / wt['img'] hold each stream's weights.  Per stream:
     adaLN-Zero modulation from vec, LN+modulate, QKV linear, per-head RMSNorm
@@ -219,8 +219,13 @@ def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows
     rnd (optional) is a precision model, not part of the definition: when
     given, it is applied where a bf16 implementation stores a matmul operand
     (LN+modulate outputs, q/k after RoPE, v, softmax weights, attention
-    output, MLP hidden).  Left as None the block is the plain definition."""
+    output, MLP hidden).  Left as None the block is the plain definition.
+
+    qin (optional) is a quantisation model of the inputs of the four GEMM
+    linears (QKV, projection, both MLP projections), e.g. e4m3 rows; None
+    leaves them exact."""
     R = _ident if rnd is None else rnd
+    Q = _ident if qin is None else qin
     H = sh.H
     streams = (("txt", x_txt, rows_txt, 0), ("img", x_img, rows_img, sh.L_txt))
     qs, ks, vs, mods = [], [], [], {}
@@ -229,7 +234,7 @@ def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows
         sh1, sc1, g1, sh2, sc2, g2 = modulation(vec, w["mod_w"], w["mod_b"], 6)
         mods[name] = (sh1, sc1, g1, sh2, sc2, g2)
         y = R(modulate(layer_norm(x, sh.eps_ln), sh1, sc1))
-        qkv = linear(y, w["qkv_w"], w["qkv_b"])
+        qkv = linear(Q(y), w["qkv_w"], w["qkv_b"])
         D = sh.D
         q = rms_norm(_heads(qkv[..., :D], H), w["q_norm"], sh.eps_rms)
         k = rms_norm(_heads(qkv[..., D:2 * D], H), w["k_norm"], sh.eps_rms)
@@ -244,33 +249,34 @@ def double_block(x_txt, x_img, vec, wt, sh: Shape, cos, sin, rows_txt=None, rows
         sh1, sc1, g1, sh2, sc2, g2 = mods[name]
         idx = np.arange(x.shape[1]) if rows is None else np.asarray(rows)
         o = R(attention(q[:, off + idx], k, v, rnd).reshape(x.shape[0], len(idx), sh.D))
-        xr = x[:, idx] + g1 * linear(o, w["proj_w"], w["proj_b"])
+        xr = x[:, idx] + g1 * linear(Q(o), w["proj_w"], w["proj_b"])
         y2 = R(modulate(layer_norm(xr, sh.eps_ln), sh2, sc2))
-        hid = R(mlp_act(linear(y2, w["mlp_in_w"], w["mlp_in_b"]), sh))
-        xr = xr + g2 * linear(hid, w["mlp_out_w"], w["mlp_out_b"])
+        hid = R(mlp_act(linear(Q(y2), w["mlp_in_w"], w["mlp_in_b"]), sh))
+        xr = xr + g2 * linear(Q(hid), w["mlp_out_w"], w["mlp_out_b"])
         outs.append(xr)
     return outs[0], outs[1]
 
 
-def single_block(x, vec, w, sh: Shape, cos, sin, rows=None, rnd=None):
+def single_block(x, vec, w, sh: Shape, cos, sin, rows=None, rnd=None, qin=None):
     """Single-stream block on x = [text; image] [B, L, D]: LN+modulate, one
     linear D -> 3D + D_mlp (3D + 2 D_mlp with SwiGLU), RMSNorm of q and k,
     RoPE, joint attention in parallel with the MLP activation on the MLP
     columns, one linear over the concatenation [attention output | act(mlp)],
     gated residual.
     rnd: optional precision model, as in double_block."""
+    Q = _ident if qin is None else qin  # quantisation model of the lin1 and lin2 inputs, as in double_block
     R = _ident if rnd is None else rnd
     D, H = sh.D, sh.H
     shift, scale, gate = modulation(vec, w["mod_w"], w["mod_b"], 3)
     y = R(modulate(layer_norm(x, sh.eps_ln), shift, scale))
-    h = linear(y, w["lin1_w"], w["lin1_b"])
+    h = linear(Q(y), w["lin1_w"], w["lin1_b"])
     q = R(rope_apply(rms_norm(_heads(h[..., :D], H), w["q_norm"], sh.eps_rms), cos, sin))
     k = R(rope_apply(rms_norm(_heads(h[..., D:2 * D], H), w["k_norm"], sh.eps_rms), cos, sin))
     v = R(_heads(h[..., 2 * D:3 * D], H))
     idx = np.arange(x.shape[1]) if rows is None else np.asarray(rows)
     o = R(attention(q[:, idx], k, v, rnd).reshape(x.shape[0], len(idx), D))
     cat = np.concatenate([o, R(mlp_act(h[:, idx, 3 * D:], sh))], axis=-1)
-    return x[:, idx] + gate * linear(cat, w["lin2_w"], w["lin2_b"])
+    return x[:, idx] + gate * linear(Q(cat), w["lin2_w"], w["lin2_b"])
 
 
 # --------------------------------------------------------------------------

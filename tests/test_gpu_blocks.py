@@ -9,6 +9,7 @@ import torch
 
 from diffusion_transformer_image_mmdit_gb300 import api, synthetic as S, weights as Wt
 from oracle import mmdit_oracle as O
+from tests.test_gpu_kernels import decode_e4m3
 from tests.gpu_common import (CONFIGS, FULL, MAX_ABS, REL_L2_INT8_SCHEME, api_shape, assert_close, bf16, check_status, f32,
                               gpu_tables, host, need_gpu, oracle_shape, rel_l2, tables)
 
@@ -31,11 +32,13 @@ def _zero_gates(mod_w, mod_b, n_chunks, gates):
     return mod_w, mod_b
 
 
-def run_double(cfg, params, acts, i8=False):
-    shape = api_shape(cfg, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_BF16)
+def run_double(cfg, params, acts, i8=False, f8=False):
+    shape = api_shape(cfg, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_F8W if f8 else api.MMDIT_BF16)
     w = Wt.double_from_host(params)
     if i8:
         w = w.quantized()
+    if f8:
+        w = w.quantized_f8()
     _, cs, sn = gpu_tables(shape)
     xt, xi = f32(acts["x_txt"]), f32(acts["x_img"])
     ws = api.alloc_workspace(api.workspace_size(shape, api.MMDIT_OP_DOUBLE))
@@ -43,11 +46,13 @@ def run_double(cfg, params, acts, i8=False):
     return host(xt), host(xi), w
 
 
-def run_single(cfg, params, x, vec, i8=False):
-    shape = api_shape(cfg, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_BF16)
+def run_single(cfg, params, x, vec, i8=False, f8=False):
+    shape = api_shape(cfg, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_F8W if f8 else api.MMDIT_BF16)
     w = Wt.single_from_host(params)
     if i8:
         w = w.quantized()
+    if f8:
+        w = w.quantized_f8()
     _, cs, sn = gpu_tables(shape)
     xg = f32(x)
     ws = api.alloc_workspace(api.workspace_size(shape, api.MMDIT_OP_SINGLE))
@@ -241,6 +246,61 @@ def test_klein_single_block_sampled():
     ref = O.single_block(x, vec, p, sh, c, s, rows=rows)
     emu = O.single_block(x, vec, p, sh, c, s, rows=rows, rnd=S.round_bf16)
     assert_close(g[:, rows], ref, max_abs=flux_max_abs(emu, ref), what="klein single rows")
+
+
+# ------------------------------------------------------------------ FP8 (e4m3) blocks
+def _f8_rows(x):
+    """The kernels' activation path: a bf16 store, then e4m3 rows."""
+    return O.dequantize_f8_rows(*O.quantize_f8_rows(S.round_bf16(x)))
+
+
+def _f8_weight(lin):
+    return decode_e4m3(lin.w.cpu().numpy()) * host(lin.scale)[:, None]
+
+
+# the e4m3 step (2^-3 relative) leaves at most 2^-4 per operand: about 5% rms on each GEMM output, and
+# the residual update of a block passes through two GEMMs in sequence
+REL_L2_F8_SCHEME = 1e-1
+
+
+@pytest.mark.parametrize("name,mlp", [("c1", "gelu"), ("d128", "gelu"), ("d128", "swiglu")])
+def test_f8_double_block(name, mlp):
+    cfg = dict(CONFIGS[name], mlp_act=api.MMDIT_MLP_SWIGLU if mlp == "swiglu" else api.MMDIT_MLP_GELU)
+    sh = oracle_shape(cfg)
+    sh.mlp = mlp
+    p = S.double_block_params(f"f8d.{name}", cfg["D"], cfg["d_head"], cfg["D_mlp"], mlp=mlp)
+    a = S.activations(cfg["B"], cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, w8 = run_double(cfg, p, a, f8=True)
+    pd = {}
+    for i, st in enumerate(("txt", "img")):
+        pd[st] = dict(p[st])
+        for n in ("qkv", "proj", "mlp_in", "mlp_out"):
+            pd[st][n + "_w"] = _f8_weight(getattr(w8, n)[i])
+    c, s = tables(cfg)
+    rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], pd, sh, c, s, qin=_f8_rows)
+    assert_close(gt, rt, what="fp8 double x_txt vs the e4m3 operands")
+    assert_close(gi, ri, what="fp8 double x_img vs the e4m3 operands")
+    bt, bi = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s)
+    assert rel_l2(gi - a["x_img"], bi - a["x_img"]) <= REL_L2_F8_SCHEME
+    assert rel_l2(gt - a["x_txt"], bt - a["x_txt"]) <= REL_L2_F8_SCHEME
+
+
+@pytest.mark.parametrize("name,mlp", [("d128", "gelu"), ("d128", "swiglu")])
+def test_f8_single_block(name, mlp):
+    cfg = dict(CONFIGS[name], mlp_act=api.MMDIT_MLP_SWIGLU if mlp == "swiglu" else api.MMDIT_MLP_GELU)
+    sh = oracle_shape(cfg)
+    sh.mlp = mlp
+    p = S.single_block_params(f"f8s.{name}", cfg["D"], cfg["d_head"], cfg["D_mlp"], mlp=mlp)
+    x = S.normal_f32("f8s.x", (cfg["B"], sh.L, cfg["D"]))
+    vec = S.normal_f32("f8s.vec", (cfg["B"], cfg["D"]))
+    g, w8 = run_single(cfg, p, x, vec, f8=True)
+    pd = dict(p)
+    for n in ("lin1", "lin2"):
+        pd[n + "_w"] = _f8_weight(getattr(w8, n))
+    c, s = tables(cfg)
+    assert_close(g, O.single_block(x, vec, pd, sh, c, s, qin=_f8_rows), what="fp8 single vs the e4m3 operands")
+    ref = O.single_block(x, vec, p, sh, c, s)
+    assert rel_l2(g - x, ref - x) <= REL_L2_F8_SCHEME
 
 
 # ------------------------------------------------------------------ sampling loop

@@ -349,6 +349,30 @@ def test_swiglu_blocks_vs_torch_restatement(which):
         assert rel(O.single_block(x, vec, w, sh, c, s), _torch_single(x, vec, w, sh)) < 1e-12
 
 
+def test_quantisation_hook_reaches_exactly_the_gemm_inputs():
+    """qin sees the inputs of the four GEMM linears per stream (double) and of
+    lin1 and lin2 (single), with their widths, and nothing else; identity
+    leaves the block unchanged."""
+    sh = TINY
+    wt, a = _double_inputs(sh)
+    c, s = _tables(sh)
+    seen = []
+
+    def spy(x):
+        seen.append(x.shape[-1])
+        return x
+    plain = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s)
+    got = O.double_block(a["x_txt"], a["x_img"], a["vec"], wt, sh, c, s, qin=spy)
+    assert sorted(seen) == sorted([sh.D, sh.D, sh.D, sh.D_mlp] * 2)
+    assert rel(got[1], plain[1]) == 0.0
+    seen.clear()
+    w = S.single_block_params("pin.q8s", sh.D, sh.d_head, sh.D_mlp)
+    x = S.normal_f32("pin.q8x", (sh.B, sh.L, sh.D))
+    vec = S.normal_f32("pin.q8v", (sh.B, sh.D))
+    O.single_block(x, vec, w, sh, c, s, qin=spy)
+    assert sorted(seen) == [sh.D, sh.D + sh.D_mlp]
+
+
 def _zero_gates(mod_w, mod_b, n_chunks, gate_chunks):
     D = mod_w.shape[0] // n_chunks
     mod_w, mod_b = mod_w.copy(), mod_b.copy()
