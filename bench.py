@@ -45,6 +45,13 @@ CONFIGS = {
     "klein_i2i": dict(B=1, L_txt=512, grid_h=100, grid_w=75, n_double=8, n_single=24, int8=False, n_steps=4,
                       swiglu=True, D=4096, H=32, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56), C_lat=128,
                       t_dim=256),
+    # the 1328^2 step with e4m3 block linears (per-channel weight scales, per-row activation scales)
+    "c4_f8": dict(B=1, L_txt=512, grid_h=83, grid_w=83, n_double=19, n_single=38, int8=False, f8=True, n_steps=50,
+                  **FLUX),
+    # the Klein-shaped 1024^2 step with e4m3 block linears
+    "klein1024_f8": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=8, n_single=24, int8=False, f8=True,
+                         n_steps=4, swiglu=True, D=4096, H=32, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56),
+                         C_lat=128, t_dim=256),
     # the whole sampling loop at 1024^2: 28 steps, guidance 3.5, text encoder width 4096, pooled width 768
     "sample1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=False, n_steps=28,
                        C_txt=4096, C_pool=768, guidance=3.5, **FLUX),
@@ -63,6 +70,12 @@ WORKLOAD_NAME = {
     "klein_i2i": "Flux.2 Klein-shaped denoising step at the token count of 1200x800 image-to-image: 512 text + "
                  "75x50 target + 75x50 reference latent tokens (8012), the reference tokens as a second grid "
                  "(their RoPE time index is not modelled), batch 1, bf16",
+    "c4_f8": "full denoising step at 1328^2 (19 double + 38 single blocks, 512 text + 83x83 image tokens, batch 1) "
+             "with the block linears in e4m3 (per-channel weight scales, per-row activation scales, fp32 "
+             "accumulation); modulation, embedders and the final layer in bf16",
+    "klein1024_f8": "Flux.2 Klein-shaped denoising step at 1024^2 (8 double + 24 single blocks, D=4096, SwiGLU MLP "
+                    "12288, 512 text + 64x64 image tokens) with the block linears in e4m3; modulation, embedders "
+                    "and the final layer in bf16",
     "sample1024": "sampling loop, 28 Euler steps of the 57-block bf16 model at 512 text + 64x64 image tokens "
                   "(1024^2), batch 1, guidance 3.5, text projection 4096 -> 3072, pooled vector 768; steps 1.. "
                   "replayed from one captured CUDA graph",
@@ -82,17 +95,25 @@ def step_flops(c: dict) -> dict:
     small = 2 * (T * D + D * D) + c["n_double"] * 2 * 2 * D * 6 * D + c["n_single"] * 2 * D * 3 * D + 2 * D * 2 * D
     io = 2 * Li * C * D * 2
     gemm = B * (c["n_double"] * lin_double + c["n_single"] * lin_single + io)
-    return {"total": B * (blocks + io) + B * small, "gemm": gemm, "attention": B * (c["n_double"] + c["n_single"]) * attn,
-            "block_flops": lin_double + attn, "L": L}
+    # with e4m3 block linears only the embedder and final-layer GEMMs stay bf16
+    gemm_f8 = B * (c["n_double"] * lin_double + c["n_single"] * lin_single) if c.get("f8") else 0
+    return {"total": B * (blocks + io) + B * small, "gemm": gemm, "gemm_f8": gemm_f8,
+            "attention": B * (c["n_double"] + c["n_single"]) * attn, "block_flops": lin_double + attn, "L": L}
 
 
 def step_weight_bytes(c: dict) -> float:
     D, Dm, C, T = c["D"], c["D_mlp"], c["C_lat"], c["t_dim"]
     m_in = 2 * Dm if c.get("swiglu") else Dm
-    per_double = 2 * (6 * D * D + 3 * D * D + D * D + D * m_in + Dm * D)
-    per_single = 3 * D * D + D * (3 * D + m_in) + (D + Dm) * D
-    n = c["n_double"] * per_double + c["n_single"] * per_single + T * D + D * D + 2 * C * D + 2 * D * D
-    return n * (1 if c["int8"] else 2)
+    lin_double = 2 * (3 * D * D + D * D + D * m_in + Dm * D)
+    lin_single = D * (3 * D + m_in) + (D + Dm) * D
+    mod = c["n_double"] * 2 * 6 * D * D + c["n_single"] * 3 * D * D
+    lin = c["n_double"] * lin_double + c["n_single"] * lin_single
+    rest = T * D + D * D + 2 * C * D + 2 * D * D
+    if c["int8"]:
+        return float(mod + lin + rest)
+    if c.get("f8"):
+        return float(lin + 2 * (mod + rest))
+    return float(2 * (mod + lin + rest))
 
 
 def peaks() -> dict:
@@ -261,13 +282,14 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int):
     fl = step_flops(c)
     shape = api.make_shape(B=c["B"], L_txt=c["L_txt"], grid_h=c["grid_h"], grid_w=c["grid_w"], D=c["D"], H=c["H"],
                            d_head=c["d_head"], D_mlp=c["D_mlp"], rope_axes=c["rope_axes"],
-                           w_dtype=api.MMDIT_I8W if c["int8"] else api.MMDIT_BF16, C_lat=c["C_lat"],
+                           w_dtype=(api.MMDIT_I8W if c["int8"] else api.MMDIT_F8W if c.get("f8") else
+                                    api.MMDIT_BF16), C_lat=c["C_lat"],
                            t_dim=c["t_dim"], mlp_act=api.MMDIT_MLP_SWIGLU if c.get("swiglu") else api.MMDIT_MLP_GELU)
     draw = DeviceDraw(seed=1000 + rank, device=dev)
     w = draw.step(c["D"], c["d_head"], c["D_mlp"], c["C_lat"], c["t_dim"], c["n_double"], c["n_single"],
                   swiglu=bool(c.get("swiglu")))
-    if c["int8"]:
-        wq = w.quantized()
+    if c["int8"] or c.get("f8"):
+        wq = w.quantized() if c["int8"] else w.quantized_f8()
         del w
         w = wq
     torch.cuda.synchronize()
@@ -487,10 +509,19 @@ def main():
     value = whole_job_tflops(fl["total"], world, r["ms_step"])
     e2e_value = whole_job_tflops(fl["total"], world, r["e2e_ms"])
     gemm_peak = pk["bf16_tflops_sustained"]
+    peak_note = f"{pk['source']} bf16 sustained (kernel timed inside the step)"
+    if fl["gemm_f8"]:
+        # e4m3 tensor rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s dense); the launches mix e4m3 block linears with
+        # bf16 embedder / final-layer GEMMs, so the bound is the time-weighted mix of the two peaks
+        f8_peak = 2.0 * pk["bf16_tflops_sustained"]
+        gemm_peak = fl["gemm"] / (fl["gemm_f8"] / f8_peak + (fl["gemm"] - fl["gemm_f8"]) / pk["bf16_tflops_sustained"])
+        peak_note = (f"{pk['source']} bf16 sustained x 2 for the e4m3 share ({fl['gemm_f8'] / fl['gemm']:.4f} of the "
+                     f"GEMM FLOPs), bf16 sustained for the rest; kernel timed inside the step")
+    attn_peak = pk["bf16_tflops_sustained"]
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8w-bf16" if c["int8"] else "bf16",
+        "vs_baseline": None, "dtype": "int8w-bf16" if c["int8"] else "e4m3-bf16" if c.get("f8") else "bf16",
         "data": "synthetic: seeded GPU draws, weights N(0,0.02), latents and text tokens N(0,1); random init",
         "config": cfg_json,
         "clocks": r["clocks"],
@@ -498,16 +529,16 @@ def main():
                 "d2h_bytes_per_step": r["d2h"], "ms_per_step": round(r["e2e_ms"], 3)},
         "gpu_launches": int(round(r["launches_per_step"] * args.steps)),
         "roofline": {"kernel": "gemm_bf16_tc", "bound": "tensor",
-                     "achieved": round(r["gemm_tflops"], 1) if r["gemm_tflops"] else None, "peak": gemm_peak,
+                     "achieved": round(r["gemm_tflops"], 1) if r["gemm_tflops"] else None, "peak": round(gemm_peak, 1),
                      "unit": "TFLOP/s",
                      "frac": round(r["gemm_tflops"] / gemm_peak, 3) if r["gemm_tflops"] else None,
                      "traffic": gemm_traffic_per_launch(args.config),
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-                     "peak_source": f"{pk['source']} bf16 sustained (kernel timed inside the step)",
+                     "peak_source": peak_note,
                      "launches_per_step": r["gemm_launches"],
                      "flops_per_launch": round(fl["gemm"] / max(1, r["gemm_launches"]))},
         "attention": {"achieved": round(r["attn_tflops"], 1) if r["attn_tflops"] else None, "unit": "TFLOP/s",
-                      "frac": round(r["attn_tflops"] / gemm_peak, 3) if r["attn_tflops"] else None,
+                      "frac": round(r["attn_tflops"] / attn_peak, 3) if r["attn_tflops"] else None,
                       "launches_per_step": r["attn_launches"]},
         "per_kernel": r["per_kernel"],
         "block_tflop": round(fl["block_flops"] / 1e12, 4),

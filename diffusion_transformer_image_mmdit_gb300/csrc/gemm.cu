@@ -5,7 +5,7 @@
 // bf16 contractions with fp32 accumulation (Luminal blog, section "The AMD
 // MI300X pipeline": all bf16 GEMMs accumulate in fp32, with bias epilogues).
 //
-// Structure (one CTA per SM, 192 threads, clusters of two CTAs):
+// Structure (one CTA per SM, 320 threads, clusters of two CTAs):
 //   The two CTAs of a cluster compute the vertically adjacent 128x256 output
 //   tiles (m, n) and (m + 1, n), which share their 256x64 W tile for every K
 //   block: each CTA loads one 128-row half of it and multicasts it into both
@@ -18,22 +18,26 @@
 //               multicast commits).
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
 //               and issues tcgen05.mma (M=128, N=256, K=16) from one thread.
-//   warps 2-5   epilogue: tcgen05.ld of the finished accumulator (one TMEM
-//               lane = one output row per thread), fused bias / per-channel
-//               int8 scale / GELU-tanh / gated fp32 residual / q-k RMSNorm +
-//               RoPE / transposed V store, overlapping the next tile's MMAs.
+//   warps 2-9   epilogue: tcgen05.ld of the finished accumulator (one TMEM
+//               lane = one output row per thread; two warps per lane
+//               quadrant, one per 128-column half), fused bias / per-channel
+//               scale / GELU-tanh / SwiGLU / gated fp32 residual / q-k
+//               RMSNorm + RoPE / transposed V store, overlapping the next
+//               tile's MMAs.
 #include "common.cuh"
 
 namespace mmdit {
 
 namespace {
 
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, one per 128-column half
+constexpr int kGemmThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t kStageA = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kStageB = kBN * kBK * 2;  // 32 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiStageBytes = 4096;  // staging area of one epilogue warp
-constexpr size_t kGemmSmem = 1024 + kStages * (kStageA + kStageB) + 256 + 4 * kEpiStageBytes;
+constexpr size_t kGemmSmem = 1024 + kStages * (kStageA + kStageB) + 256 + kEpiWarps * kEpiStageBytes;
+static_assert(kGemmSmem <= 232448, "GEMM shared memory above the 227 KB a CTA can have");
 
 struct TileCoord {
   int seg, tm, tn;
@@ -162,53 +166,66 @@ __device__ __forceinline__ void warp_load_f32x32(uint8_t* stg, int lane, float* 
 }
 
 // q/k head of HD columns: bias, RMSNorm with gain g, adjacent-pair RoPE at
-// table row `tok`, bf16 store of the whole head row (HD / 32 staged chunks).
+// table row `tok`, bf16 store of the whole head row.  Two passes over the
+// accumulator (TMEM reads are cheap): the first sums squares, the second
+// normalises, rotates and stores 32 columns at a time, so a thread never
+// holds more than one 32-column chunk.
 template <int HD>
 __device__ __forceinline__ void epi_qk_head(uint32_t taddr, const GemmParams& p, int n, const float* __restrict__ g,
                                             int tok, uint8_t* stg, int lane, uint16_t* row0, long long ld,
                                             int nrows, float rs) {
-  float v[HD];
-#pragma unroll
-  for (int c = 0; c < HD / 32; ++c) acc_chunk(taddr + c * 32, p, n + c * 32, v + c * 32, rs);
   float ss = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < HD / 32; ++c) {
+    float v[32];
+    acc_chunk(taddr + c * 32, p, n + c * 32, v, rs);
 #pragma unroll
-  for (int i = 0; i < HD; ++i) ss = fmaf(v[i], v[i], ss);
-  const float rinv = rsqrtf(ss * (1.0f / HD) + p.eps);
-  const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cos + (long long)tok * (HD / 2));
-  const float4* sn4 = reinterpret_cast<const float4*>(p.rope_sin + (long long)tok * (HD / 2));
-  const float4* g4 = reinterpret_cast<const float4*>(g);
-#pragma unroll
-  for (int q = 0; q < HD / 8; ++q) {  // 8 channels = 4 pairs per iteration
-    const float4 c = __ldg(cs4 + q);
-    const float4 s = __ldg(sn4 + q);
-    const float4 ga = __ldg(g4 + 2 * q);
-    const float4 gb = __ldg(g4 + 2 * q + 1);
-    const float cc[4] = {c.x, c.y, c.z, c.w};
-    const float sc[4] = {s.x, s.y, s.z, s.w};
-    const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float x0 = v[8 * q + 2 * j] * rinv * gg[2 * j];
-      const float x1 = v[8 * q + 2 * j + 1] * rinv * gg[2 * j + 1];
-      v[8 * q + 2 * j] = x0 * cc[j] - x1 * sc[j];
-      v[8 * q + 2 * j + 1] = x0 * sc[j] + x1 * cc[j];
-    }
+    for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
   }
+  const float rinv = rsqrtf(ss * (1.0f / HD) + p.eps);
+#pragma unroll 1
+  for (int c = 0; c < HD / 32; ++c) {
+    float v[32];
+    acc_chunk(taddr + c * 32, p, n + c * 32, v, rs);
+    // pairs 16c .. 16c + 15 of the head: table columns of this token
+    const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cos + (long long)tok * (HD / 2) + 16 * c);
+    const float4* sn4 = reinterpret_cast<const float4*>(p.rope_sin + (long long)tok * (HD / 2) + 16 * c);
+    const float4* g4 = reinterpret_cast<const float4*>(g + 32 * c);
 #pragma unroll
-  for (int c = 0; c < HD / 32; ++c) warp_store_bf16x32(stg, lane, v + 32 * c, row0 + 32 * c, ld, nrows);
+    for (int q = 0; q < 4; ++q) {  // 8 channels = 4 pairs per iteration
+      const float4 cq = __ldg(cs4 + q);
+      const float4 sq = __ldg(sn4 + q);
+      const float4 ga = __ldg(g4 + 2 * q);
+      const float4 gb = __ldg(g4 + 2 * q + 1);
+      const float cc[4] = {cq.x, cq.y, cq.z, cq.w};
+      const float sc[4] = {sq.x, sq.y, sq.z, sq.w};
+      const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float x0 = v[8 * q + 2 * j] * rinv * gg[2 * j];
+        const float x1 = v[8 * q + 2 * j + 1] * rinv * gg[2 * j + 1];
+        v[8 * q + 2 * j] = x0 * cc[j] - x1 * sc[j];
+        v[8 * q + 2 * j + 1] = x0 * sc[j] + x1 * cc[j];
+      }
+    }
+    warp_store_bf16x32(stg, lane, v, row0 + 32 * c, ld, nrows);
+  }
 }
 
-// One 128 x 256 accumulator tile; thread r of the four epilogue warps owns
-// tile row r (TMEM lane r).  All 32 lanes of each warp take part in every
-// staged store; rows past M_seg are computed but not written.
+// One epilogue warp's share of a finished 128 x 256 accumulator: the 32 rows
+// of its TMEM lane quadrant (thread = row r of the tile) and the 128 columns
+// of column half `half`.  `tbase` addresses the quadrant's lanes at column 0
+// of the accumulator.
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& c, uint32_t tbase, int r,
-                                              uint8_t* stg) {
+                                              int half, uint8_t* stg) {
+  constexpr int kHalf = kBN / 2;
   const int lane = r & 31;
   const int m = c.tm * kBM + r;
   const int wm0 = m - lane;                                // the warp's first row
   const int nrows = min(32, p.M_seg - wm0);                // rows of this warp inside the problem (may be <= 0)
   const long long orow0 = (long long)c.seg * p.out_seg_rows + p.out_row_off + wm0;
-  const int n0 = c.tn * kBN;
+  const int n0 = c.tn * kBN + half * kHalf;                // first output column of this half
+  const uint32_t tb = tbase + half * kHalf;
   // fp8 GEMM: this row's activation scale (rows past the problem use 1; they are not stored)
   const float rs = p.ascale && m < p.M_seg ? __ldg(p.ascale + (long long)c.seg * p.ascale_seg_rows + m) : 1.0f;
 
@@ -220,23 +237,21 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       const int tok = m < p.M_seg ? p.out_row_off + m : 0;
       uint16_t* row0 = p.qk + orow0 * p.qk_ld + n0;
       if (p.d_head == 128) {
-#pragma unroll 1
-        for (int h = 0; h < kBN / 128; ++h)
-          epi_qk_head<128>(tbase + h * 128, p, n0 + h * 128, g, tok, stg, lane, row0 + h * 128, p.qk_ld, nrows, rs);
+        epi_qk_head<128>(tb, p, n0, g, tok, stg, lane, row0, p.qk_ld, nrows, rs);
       } else {
 #pragma unroll 1
-        for (int h = 0; h < kBN / 64; ++h)
-          epi_qk_head<64>(tbase + h * 64, p, n0 + h * 64, g, tok, stg, lane, row0 + h * 64, p.qk_ld, nrows, rs);
+        for (int h = 0; h < kHalf / 64; ++h)
+          epi_qk_head<64>(tb + h * 64, p, n0 + h * 64, g, tok, stg, lane, row0 + h * 64, p.qk_ld, nrows, rs);
       }
     } else if (n0 < 3 * D) {
       // v^T: for each channel, the 32 lanes write 32 consecutive tokens (64 bytes)
       const int tok = p.out_row_off + m;
       uint16_t* vt = p.vT + (long long)c.seg * D * p.vT_ld + tok;
 #pragma unroll 1
-      for (int j = 0; j < kBN / 32; ++j) {
+      for (int j = 0; j < kHalf / 32; ++j) {
         const int n = n0 + j * 32;
         float v[32];
-        acc_chunk(tbase + j * 32, p, n, v, rs);
+        acc_chunk(tb + j * 32, p, n, v, rs);
         if (lane < nrows) {
           const long long col = n - 2 * D;
 #pragma unroll
@@ -249,11 +264,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     } else {
       uint16_t* row0 = p.aux + orow0 * p.aux_ld + p.aux_col_off - 3 * D;
 #pragma unroll 1
-      for (int j = 0; j < kBN / 32; ++j) {
+      for (int j = 0; j < kHalf / 32; ++j) {
         const int n = n0 + j * 32;
         if (n >= p.N) break;
         float v[32];
-        acc_chunk(tbase + j * 32, p, n, v, rs);
+        acc_chunk(tb + j * 32, p, n, v, rs);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh_f(v[i]);
         warp_store_bf16x32(stg, lane, v, row0 + n, p.aux_ld, nrows);
@@ -263,27 +278,29 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   }
 
   if (p.mode == GM_SWIGLU) {
-    // accumulator columns [0, 128): gate rows g0 + c; [128, 256): up rows p.swiglu_up + g0 + c
-    const int g0 = c.tn * (kBN / 2);
+    // accumulator columns [0, 128): gate rows g0 + c; [128, 256): up rows p.swiglu_up + g0 + c.
+    // Half h takes gate / up column pairs 64 h .. 64 h + 63.
+    const int g0 = c.tn * kHalf;
     uint16_t* row0 = reinterpret_cast<uint16_t*>(p.out) + orow0 * p.out_ld + g0;
 #pragma unroll 1
-    for (int j = 0; j < kBN / 64; ++j) {
-      float g[32], u[32];
-      acc_chunk(tbase + j * 32, p, g0 + j * 32, g, rs);
-      acc_chunk(tbase + kBN / 2 + j * 32, p, p.swiglu_up + g0 + j * 32, u, rs);
+    for (int jj = 0; jj < kHalf / 64; ++jj) {
+      const int j = half * (kHalf / 64) + jj;
+      float gt[32], u[32];
+      acc_chunk(tbase + j * 32, p, g0 + j * 32, gt, rs);
+      acc_chunk(tbase + kHalf + j * 32, p, p.swiglu_up + g0 + j * 32, u, rs);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) g[i] = silu_fast(g[i]) * u[i];
-      warp_store_bf16x32(stg, lane, g, row0 + j * 32, p.out_ld, nrows);
+      for (int i = 0; i < 32; ++i) gt[i] = silu_fast(gt[i]) * u[i];
+      warp_store_bf16x32(stg, lane, gt, row0 + j * 32, p.out_ld, nrows);
     }
     return;
   }
 
 #pragma unroll 1
-  for (int j = 0; j < kBN / 32; ++j) {
+  for (int j = 0; j < kHalf / 32; ++j) {
     const int n = n0 + j * 32;
     if (n >= p.N) break;
     float v[32];
-    acc_chunk(tbase + j * 32, p, n, v, rs);
+    acc_chunk(tb + j * 32, p, n, v, rs);
     if (p.mode == GM_STORE_BF16) {
       if (n >= p.gelu_from) {
 #pragma unroll
@@ -308,6 +325,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       warp_store_f32x32(stg, lane, x, x0, p.resid_ld, nrows);
     }
   }
+}
+
+// GM_RESID reads this thread's row of the fp32 residual tile in its
+// epilogue.  Issued before the wait for the accumulator, the prefetch runs
+// while the tile's MMAs do, so the epilogue's loads hit L2 instead of
+// waiting on DRAM one 32-column chunk at a time.
+__device__ __forceinline__ void prefetch_resid_row(const GemmParams& p, const TileCoord& c, int r, int half) {
+  const int m = c.tm * kBM + r;
+  const int n0 = c.tn * kBN + half * (kBN / 2);
+  if (m >= p.M_seg || n0 >= p.N) return;
+  const uint32_t bytes = (uint32_t)(min(kBN / 2, p.N - n0) * 4) & ~15u;
+  const float* row = p.resid + ((long long)c.seg * p.resid_seg_rows + m) * p.resid_ld + n0;
+  if (bytes && (reinterpret_cast<uintptr_t>(row) & 15) == 0) prefetch_l2_bulk(row, bytes);
 }
 
 // F8: A and W are e4m3 (one byte per element, 128 elements per 128-byte
@@ -343,7 +373,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, kEpiWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -428,18 +458,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
       if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
   } else {
+    // warps 2..9: TMEM lane quadrant warp % 4 (a warp may only read its own
+    // quadrant's lanes), column half 0 for warps 2-5 and 1 for warps 6-9
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
-    uint8_t* stg = reinterpret_cast<uint8_t*>(bars) + 256 + quad * kEpiStageBytes;
+    uint8_t* stg = reinterpret_cast<uint8_t*>(bars) + 256 + (warp - 2) * kEpiStageBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster; t < g.total_tiles; t += n_clusters) {
       const int q = t < g.tiles0 ? 0 : 1;
       const GemmParams& p = g.p[q];
       const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0), rank);
+      if (p.mode == GM_RESID && c.valid) prefetch_resid_row(p, c, r, half);
       if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, status, ST_TIMEOUT_EPILOGUE)) break;
       tc_fence_after();
-      if (c.valid) epilogue_tile(p, c, tmem + ((uint32_t)(quad * 32) << 16) + acc * kBN, r, stg);
+      if (c.valid) epilogue_tile(p, c, tmem + ((uint32_t)(quad * 32) << 16) + acc * kBN, r, half, stg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
