@@ -43,9 +43,8 @@ constexpr float kRescaleThreshold = 16.0f;
 //               only after PV(j), which precedes it in the MMA issue order.
 //   warps 10-11 idle (they complete the third warpgroup, which gives its
 //               registers to the softmax warpgroups).
-// Softmax per KV tile: one TMEM load of the S row, tree max/sum, exp2 on the MUFU for 3 of
-//               every 4 column pairs and a cubic on the FMA pipe for the
-//               4th, lazy O rescale in TMEM, final O / l and bf16 store.
+// Softmax per KV tile: one TMEM load of the S row, tree max/sum, exp2 on the
+//               MUFU, lazy O rescale in TMEM, final O / l and bf16 store.
 constexpr int kAttn2Threads = 384;
 // Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512);
 // warpgroup 2 drops to 72 and the two softmax warpgroups rise to 216:
@@ -184,9 +183,11 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
           m_run = m_new;
         }
       }
-      // exponentials on column pairs (f32x2 arithmetic), row sum in 4 packed
-      // partial sums, bf16 P over the first 64 columns of S.  1 of every 4
-      // pairs uses the FMA-pipe polynomial, the rest the MUFU ex2.
+      // exponentials on column pairs (f32x2 arithmetic for the argument and the
+      // sums), row sum in 4 packed partial sums, bf16 P over the first 64
+      // columns of S.  Every exponential is a MUFU ex2: at 32 results per
+      // cycle per SM it takes fewer issue slots than a polynomial on the FMA
+      // pipe, and the softmax is issue-bound.
       const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_run, -m_run);
       uint64_t ls2[4];
 #pragma unroll
@@ -196,11 +197,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       for (int c = 0; c < kAttnBN / 2; ++c) {
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sl2x2, negm2), x0, x1);
-        uint64_t p2;
-        if ((c & 3) == 3)
-          p2 = ex2_poly2(x0, x1);
-        else
-          p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
+        const uint64_t p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
         ls2[c & 3] = f2_add(ls2[c & 3], p2);
         float p0, p1;
         f2_unpack(p2, p0, p1);

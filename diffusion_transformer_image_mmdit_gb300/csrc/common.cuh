@@ -300,25 +300,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, for x <= 126 (inputs below -125 are clamped; the
-// result there is below 2^-124, negligible next to the 2^0 terms it is summed
-// with).  Cody-Waite style split x = n + f, n = round(x) obtained by adding
-// 1.5 * 2^23 (the integer lands in the low mantissa bits), |f| <= 1/2; 2^f
-// from a cubic whose coefficients were fitted here by least squares on the
-// relative error at 2000 Chebyshev nodes of [-1/2, 1/2] (max relative error
-// 7.7e-5, far below the 2^-9 of the bf16 weights it feeds); n is added to the
-// exponent field.
-__device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -125.0f);
-  const float r = x + 12582912.0f;
-  const float n = r - 12582912.0f;
-  const float f = x - n;
-  const float p = fmaf(fmaf(fmaf(0.05508868396282196f, f, 0.24260404706001282f), f, 0.6932762265205383f), f,
-                       0.9999289512634277f);
-  return __int_as_float(__float_as_int(p) + ((__float_as_int(r) - 0x4B400000) << 23));
-}
-
-// ---- packed fp32 pairs (one 64-bit register, two lanes of f32x2 arithmetic)
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
@@ -342,25 +323,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// ex2_poly on a pair, the float steps as f32x2 arithmetic.
-__device__ __forceinline__ uint64_t ex2_poly2(float x0, float x1) {
-  const uint64_t x = f2_pack(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
-  const uint64_t r = f2_add(x, f2_pack(12582912.0f, 12582912.0f));
-  const uint64_t n = f2_add(r, f2_pack(-12582912.0f, -12582912.0f));
-  float n0, n1;
-  f2_unpack(n, n0, n1);
-  const uint64_t f = f2_add(x, f2_pack(-n0, -n1));
-  uint64_t q = f2_fma(f2_pack(0.05508868396282196f, 0.05508868396282196f), f,
-                      f2_pack(0.24260404706001282f, 0.24260404706001282f));
-  q = f2_fma(q, f, f2_pack(0.6932762265205383f, 0.6932762265205383f));
-  q = f2_fma(q, f, f2_pack(0.9999289512634277f, 0.9999289512634277f));
-  float p0, p1, r0, r1;
-  f2_unpack(q, p0, p1);
-  f2_unpack(r, r0, r1);
-  return f2_pack(__int_as_float(__float_as_int(p0) + ((__float_as_int(r0) - 0x4B400000) << 23)),
-                 __int_as_float(__float_as_int(p1) + ((__float_as_int(r1) - 0x4B400000) << 23)));
-}
-
 // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3),
 // evaluated through the identity 0.5 (1 + tanh(u)) = 1 / (1 + exp(-2u)):
 // one exp2 and one fast divide.  For u -> -inf the denominator overflows to
