@@ -92,6 +92,8 @@ SIGNATURES = {
                                     c_void_p, c_void_p]),
     "mmdit_ln_modulate": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int64, c_float, c_void_p,
                                   c_void_p]),
+    "mmdit_ln_modulate_f8": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int64, c_float, c_void_p,
+                                     c_void_p, c_void_p, c_void_p]),
     "mmdit_gemv": (c_int, [POINTER(Linear), c_int, c_int, c_int, c_void_p, c_int, c_void_p, c_void_p]),
     "mmdit_time_embed": (c_int, [POINTER(Shape), POINTER(Linear), POINTER(Linear), c_double, c_void_p, c_void_p,
                                  c_void_p]),

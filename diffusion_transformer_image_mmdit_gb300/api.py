@@ -379,6 +379,17 @@ def mmdit_ln_modulate(x: torch.Tensor, shift: torch.Tensor, scale: torch.Tensor,
          stream_handle(stream))
 
 
+def mmdit_ln_modulate_f8(x: torch.Tensor, shift: torch.Tensor, scale: torch.Tensor, mod_stride: int, eps: float,
+                         y: Optional[torch.Tensor] = None, stream=None):
+    """LN + modulate with the e4m3 rows of its bf16 result: (codes uint8 [B, rows, D], scales fp32 [B, rows])."""
+    B, rows, D = x.shape
+    q = torch.empty((B, rows, D), dtype=torch.uint8, device=x.device)
+    s = torch.empty((B, rows), dtype=torch.float32, device=x.device)
+    call("mmdit_ln_modulate_f8", ptr(x), B, rows, D, ptr(shift, True), ptr(scale, True), mod_stride, eps, ptr(y),
+         ptr(q), ptr(s), stream_handle(stream))
+    return q, s
+
+
 def mmdit_gemv(lin: LinearDev, x: torch.Tensor, act: int, y: torch.Tensor, stream=None):
     B, K = x.shape
     st = lin.struct()

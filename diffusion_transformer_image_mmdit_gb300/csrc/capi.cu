@@ -426,11 +426,17 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     p.ascale = ws.as + row0;
     return ws.a8 + row0 * K;
   };
+  // LN + modulate of stream i; with FP8 it writes the e4m3 rows and their scales straight into ws.a8 / ws.as
+  // (at the stream's row offset) instead of bf16 rows
+  auto ln_mod = [&](int i, const float* shift, const float* scale) -> int {
+    const long long r0 = (long long)off[i] * d.B;
+    return cuda_status(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, shift, scale, 6 * D, s.eps_ln,
+                                          d.f8 ? nullptr : yp(i), st, d.f8 ? ws.a8 + r0 * D : nullptr,
+                                          d.f8 ? ws.as + r0 : nullptr));
+  };
   GemmProblem pr[2];
   // LN + modulate, then the fused QKV / RMSNorm / RoPE GEMM
-  for (int i = first; i < 2; ++i)
-    MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, modp(i), modp(i) + D, 6 * D, s.eps_ln, yp(i), st));
-  if (d.f8) MMDIT_TRY(quant(ws.y, D));
+  for (int i = first; i < 2; ++i) MMDIT_TRY(ln_mod(i, modp(i), modp(i) + D));
   for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(GM_QKV);
     p.out_seg_rows = d.L;
@@ -465,10 +471,7 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
   }
   MMDIT_TRY(grouped(pr));
   // y2 = LN(x)(1 + scale2) + shift2; h = GELU(y2 W1^T + b1)
-  for (int i = first; i < 2; ++i)
-    MMDIT_CUDA(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, modp(i) + 3 * D, modp(i) + 4 * D, 6 * D, s.eps_ln,
-                                  yp(i), st));
-  if (d.f8) MMDIT_TRY(quant(ws.y, D));
+  for (int i = first; i < 2; ++i) MMDIT_TRY(ln_mod(i, modp(i) + 3 * D, modp(i) + 4 * D));
   for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(d.swiglu ? GM_SWIGLU : GM_STORE_BF16);
     p.gelu_from = 0;
@@ -505,11 +508,11 @@ static int single_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     MMDIT_CUDA(launch_gemv(w.mod.w, w.mod.scale != nullptr, w.mod.scale, w.mod.b, vec, d.B, 3 * D, D, 1, ws.mod, st));
     mod = ws.mod;
   }
-  MMDIT_CUDA(launch_ln_modulate(x, d.L, d.L, d.B, D, mod, mod + D, 3 * D, s.eps_ln, ws.y, st));
+  // FP8: lin1 reads the e4m3 rows of y (written by LN + modulate itself), lin2 those of [O | act(mlp)]
+  MMDIT_CUDA(launch_ln_modulate(x, d.L, d.L, d.B, D, mod, mod + D, 3 * D, s.eps_ln, d.f8 ? nullptr : ws.y, st,
+                                d.f8 ? ws.a8 : nullptr, d.f8 ? ws.as : nullptr));
   const long long cat_ld = D + d.Dm;
   const long long rows = (long long)d.B * d.L;
-  // FP8: lin1 reads the e4m3 rows of y, lin2 those of [O | act(mlp)]
-  if (d.f8) MMDIT_CUDA(launch_quantize_f8(ws.y, true, rows, D, D, ws.a8, D, ws.as, st));
   const void* A1 = d.f8 ? static_cast<const void*>(ws.a8) : static_cast<const void*>(ws.y);
   GemmParams p = gemm_params(GM_QKV);
   p.ascale = d.f8 ? ws.as : nullptr;
@@ -1161,6 +1164,17 @@ int mmdit_ln_modulate(const float* x, int B, int rows, int D, const float* shift
   MMDIT_TRY(check_device());
   return cuda_status(
       launch_ln_modulate(x, rows, rows, B, D, shift, scale, mod_stride, eps, static_cast<uint16_t*>(y), S(stream)));
+}
+
+int mmdit_ln_modulate_f8(const float* x, int B, int rows, int D, const float* shift, const float* scale,
+                         int64_t mod_stride, float eps, void* y, uint8_t* q, float* s, void* stream) {
+  if (!x || !shift || !scale || !q || !s) return MMDIT_ERR_ARG;
+  if (B < 1 || rows < 1 || D < 256 || D % 256 || D > 4096) return MMDIT_ERR_SHAPE;
+  if (!al16(x) || !al16(shift) || !al16(scale) || (y && !al16(y)) || !al16(q) || !al16(s) || (mod_stride % 4))
+    return MMDIT_ERR_ALIGN;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_ln_modulate(x, rows, rows, B, D, shift, scale, mod_stride, eps, static_cast<uint16_t*>(y),
+                                        S(stream), q, s));
 }
 
 int mmdit_gemv(const mmdit_linear_t* lin, int B, int N, int K, const float* x, int act, float* y, void* stream) {

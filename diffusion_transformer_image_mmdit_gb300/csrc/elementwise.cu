@@ -2,6 +2,8 @@
 // modulation / timestep GEMVs, RoPE tables and rotation, the Euler update,
 // the int8 quantiser and dequantiser, and the attention input prep.
 // Vectorised 16-byte global accesses, one warp per row where a row reduces.
+#include <mutex>
+
 #include "common.cuh"
 #include "elementwise.h"
 
@@ -20,117 +22,194 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// ------------------------------------------------------------------ LN + modulate
-// y = (x - mean) / sqrt(var + eps) * (1 + scale) + shift over one row of D
-// floats per CTA of D/8 threads (8 consecutive floats each); statistics in
-// fp32, two passes over registers.
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  v = warp_sum(v);
-  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[w] = v;
-  __syncthreads();
-  float t = 0.f;
-  for (int i = 0; i < nw; ++i) t += red[i];
-  return t;
+// Two fp32 values to e4m3 (round to nearest even, saturating at +-448); lo in
+// the low byte.
+__device__ __forceinline__ uint16_t f8x2_e4m3(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
-__global__ void __launch_bounds__(512) ln_mod_kernel(const float* __restrict__ x, long long x_seg_rows, int rows,
-                                                     int D, const float* __restrict__ shift,
+// ------------------------------------------------------------------ LN + modulate
+// y = (x - mean) / sqrt(var + eps) * (1 + scale) + shift over one row of D
+// floats per warp: lane l holds the float4 chunks l, l + 32, ... (NV = D/128
+// of them), so both statistics reduce with shuffles alone (no block
+// barrier), and the row stays in registers between the two passes.  fp32
+// statistics, the variance from the centred values.
+//
+// F8: the row is also quantised to e4m3 the way the standalone row quantiser
+// does it from the stored bf16 values: s = max|bf16(y)| / 448 (1 for a zero
+// row), q = e4m3(bf16(y) / s), written to q (row stride D) and qs; the bf16
+// row is stored only when y is given.
+template <int NV, bool F8>
+__global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x, long long x_seg_rows, int rows,
+                                                     int n_rows, const float* __restrict__ shift,
                                                      const float* __restrict__ scale, long long mod_stride, float eps,
-                                                     uint16_t* __restrict__ y) {
-  __shared__ float red[32];
-  const int row = blockIdx.x;
+                                                     uint16_t* __restrict__ y, uint8_t* __restrict__ q,
+                                                     float* __restrict__ qs) {
+  constexpr int D = NV * 128;
+  const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
   const int seg = row / rows, i = row - seg * rows;
-  const int t = threadIdx.x;
-  const float4* xr = reinterpret_cast<const float4*>(x + ((long long)seg * x_seg_rows + i) * D) + 2 * t;
-  const float4 a = __ldg(xr), b = __ldg(xr + 1);
-  const float inv_d = 1.0f / (float)D;
-  const float mean = block_sum((a.x + a.y) + (a.z + a.w) + (b.x + b.y) + (b.z + b.w), red) * inv_d;
-  float v[8] = {a.x - mean, a.y - mean, a.z - mean, a.w - mean, b.x - mean, b.y - mean, b.z - mean, b.w - mean};
-  float q = 0.f;
+  const float4* xr = reinterpret_cast<const float4*>(x + ((long long)seg * x_seg_rows + i) * D) + lane;
+  float4 v[NV];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) q = fmaf(v[j], v[j], q);
-  const float rstd = rsqrtf(block_sum(q, red) * inv_d + eps);
-  const float4* sc4 = reinterpret_cast<const float4*>(scale + (long long)seg * mod_stride) + 2 * t;
-  const float4* sh4 = reinterpret_cast<const float4*>(shift + (long long)seg * mod_stride) + 2 * t;
-  const float4 s0 = __ldg(sc4), s1 = __ldg(sc4 + 1), h0 = __ldg(sh4), h1 = __ldg(sh4 + 1);
-  const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  const float sh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-  uint32_t o[4];
+  for (int c = 0; c < NV; ++c) v[c] = __ldg(xr + 32 * c);
+  constexpr float inv_d = 1.0f / (float)D;
+  float s = 0.f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    o[j] = pack_bf16x2(v[2 * j] * rstd * (1.f + sc[2 * j]) + sh[2 * j],
-                       v[2 * j + 1] * rstd * (1.f + sc[2 * j + 1]) + sh[2 * j + 1]);
-  reinterpret_cast<uint4*>(y + (long long)row * D)[t] = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int c = 0; c < NV; ++c) s += (v[c].x + v[c].y) + (v[c].z + v[c].w);
+  const float mean = warp_sum(s) * inv_d;
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < NV; ++c) {
+    v[c].x -= mean, v[c].y -= mean, v[c].z -= mean, v[c].w -= mean;
+    ss = fmaf(v[c].x, v[c].x, fmaf(v[c].y, v[c].y, fmaf(v[c].z, v[c].z, fmaf(v[c].w, v[c].w, ss))));
+  }
+  const float rstd = rsqrtf(warp_sum(ss) * inv_d + eps);
+  const float4* sc4 = reinterpret_cast<const float4*>(scale + (long long)seg * mod_stride) + lane;
+  const float4* sh4 = reinterpret_cast<const float4*>(shift + (long long)seg * mod_stride) + lane;
+  uint2* yr = y ? reinterpret_cast<uint2*>(y + (long long)row * D) + lane : nullptr;
+  float amax = 0.f;
+#pragma unroll
+  for (int c = 0; c < NV; ++c) {
+    const float4 sc = __ldg(sc4 + 32 * c), sh = __ldg(sh4 + 32 * c);
+    const uint2 o = make_uint2(pack_bf16x2(v[c].x * rstd * (1.f + sc.x) + sh.x, v[c].y * rstd * (1.f + sc.y) + sh.y),
+                               pack_bf16x2(v[c].z * rstd * (1.f + sc.z) + sh.z, v[c].w * rstd * (1.f + sc.w) + sh.w));
+    if (!F8 || yr) yr[32 * c] = o;
+    if (F8) {
+      // keep the bf16-rounded values for the quantisation
+      v[c] = make_float4(bf16_lo(o.x), bf16_hi(o.x), bf16_lo(o.y), bf16_hi(o.y));
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[c].x), fabsf(v[c].y)), fmaxf(fabsf(v[c].z), fabsf(v[c].w))));
+    }
+  }
+  if (F8) {
+    amax = warp_max(amax);
+    const float s = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (lane == 0) qs[row] = s;
+    uint32_t* qr = reinterpret_cast<uint32_t*>(q + (long long)row * D) + lane;
+#pragma unroll
+    for (int c = 0; c < NV; ++c)
+      qr[32 * c] = (uint32_t)f8x2_e4m3(__fdiv_rn(v[c].x, s), __fdiv_rn(v[c].y, s)) |
+                   ((uint32_t)f8x2_e4m3(__fdiv_rn(v[c].z, s), __fdiv_rn(v[c].w, s)) << 16);
+  }
 }
 
 // ------------------------------------------------------------------ GEMV
 // y[b, n] = sum_k W[n, k] act(x[b, k]) (* scale[n]) + bias[n] for B <= 8 rows
-// of x: one warp per output row, 16-byte weight loads along K, x staged in
-// shared memory after the activation.
+// of x (K a multiple of 16): one warp per output row, 16-byte weight loads
+// along K, x staged in shared memory after the activation once per CTA.  The grid is a few CTAs
+// per SM striding over the rows, so the staging is paid once per CTA rather
+// than once per 32 rows.
 constexpr int kGemvRowsPerWarp = 4;
 constexpr int kGemvWarps = 8;
+constexpr int kGemvVecBatch = 12;  // a whole 3072-wide bf16 row per lane in flight
+constexpr int kGemvCtasPerSm = 4;
+
+// Shared-memory slot of x[k] in a staged row.  Lane l reads the weights of
+// 16-byte vectors v = l, l + 32, ... (EPV = 8 bf16 or 16 int8 values) and, for
+// each, the EPV / 4 float4s of x at the same positions.  Stored plainly, the
+// float4s of 8 consecutive lanes would sit 32 or 64 bytes apart (2- or 4-way
+// bank conflicts); float4 j of vector v is therefore kept at slot
+// j ^ sw(v) of the vector, sw(v) = (v >> 2) & 1 (bf16) or (v >> 1) & 3 (int8),
+// which spreads any 8 consecutive lanes over 8 distinct bank groups.
+template <bool I8>
+__device__ __forceinline__ int gemv_slot(int k) {
+  constexpr int EPV = I8 ? 16 : 8;
+  const int v = k / EPV, j = (k % EPV) >> 2;
+  const int sw = I8 ? ((v >> 1) & 3) : ((v >> 2) & 1);
+  return v * EPV + 4 * (j ^ sw) + (k & 3);
+}
+
+// One output row (K a multiple of EPV): up to kGemvVecBatch 16-byte weight
+// loads per lane in flight before use.
+template <bool I8>
+__device__ __forceinline__ void gemv_row(const uint8_t* __restrict__ wrow, const float* xs, int B, int K, int lane,
+                                         float* acc) {
+  constexpr int EPV = I8 ? 16 : 8;
+  const int nvec = K / EPV;
+  const uint4* wr = reinterpret_cast<const uint4*>(wrow);
+#pragma unroll 1
+  for (int v0 = lane; v0 < nvec; v0 += 32 * kGemvVecBatch) {
+    uint4 wv[kGemvVecBatch];
+#pragma unroll
+    for (int u = 0; u < kGemvVecBatch; ++u)
+      if (v0 + 32 * u < nvec) wv[u] = __ldg(wr + v0 + 32 * u);
+#pragma unroll
+    for (int u = 0; u < kGemvVecBatch; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= nvec) break;
+      float w[EPV];
+      const uint32_t q[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+      if (I8) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = (float)(int8_t)((q[e >> 2] >> (8 * (e & 3))) & 0xFF);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[2 * e] = bf16_lo(q[e]), w[2 * e + 1] = bf16_hi(q[e]);
+      }
+      const int sw = I8 ? ((v >> 1) & 3) : ((v >> 2) & 1);
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (b < B) {
+          const float4* xv = reinterpret_cast<const float4*>(xs + b * K + v * EPV);
+          float t = acc[b];
+#pragma unroll
+          for (int j = 0; j < EPV / 4; ++j) {
+            const float4 xj = xv[j ^ sw];
+            t = fmaf(w[4 * j + 3], xj.w, fmaf(w[4 * j + 2], xj.z, fmaf(w[4 * j + 1], xj.y, fmaf(w[4 * j], xj.x, t))));
+          }
+          acc[b] = t;
+        }
+      }
+    }
+  }
+}
+
+template <bool I8>
+__device__ __forceinline__ void gemv_stage_x(const float* __restrict__ x, int B, int K, int act, float* xs) {
+  for (int i = threadIdx.x; i < B * K; i += blockDim.x) {
+    const float t = x[i];
+    const int b = i / K, k = i - b * K;
+    xs[b * K + gemv_slot<I8>(k)] = act ? silu_f(t) : t;
+  }
+  __syncthreads();
+}
+
 
 template <bool I8>
 __global__ void __launch_bounds__(256) gemv_kernel(const void* __restrict__ W, const float* __restrict__ wscale,
                                                    const float* __restrict__ bias, const float* __restrict__ x, int B,
                                                    int N, int K, int act, float* __restrict__ y) {
   extern __shared__ float xs[];
-  for (int i = threadIdx.x; i < B * K; i += blockDim.x) {
-    const float t = x[i];
-    xs[i] = act ? silu_f(t) : t;
-  }
-  __syncthreads();
+  gemv_stage_x<I8>(x, B, K, act, xs);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp;
-  constexpr int EPV = I8 ? 16 : 8;  // elements per 16-byte vector
-  const int nvec = K / EPV;
+  const int stride = gridDim.x * kGemvWarps * kGemvRowsPerWarp;
 #pragma unroll 1
-  for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
-    const int n = row0 + rr;
-    if (n >= N) break;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const uint4* wr = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(W) + (long long)n * K * (I8 ? 1 : 2));
-#pragma unroll 4
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 wv = __ldg(wr + v);
-      float w[EPV];
-      if (I8) {
-        const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int j = 0; j < 16; ++j) w[j] = (float)(int8_t)((u[j >> 2] >> (8 * (j & 3))) & 0xFF);
-      } else {
-        const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[2 * j] = bf16_lo(u[j]), w[2 * j + 1] = bf16_hi(u[j]);
-      }
-      const int k0 = v * EPV;
+  for (int row0 = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp; row0 < N; row0 += stride) {
+#pragma unroll 1
+    for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
+      const int n = row0 + rr;
+      if (n >= N) break;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      gemv_row<I8>(reinterpret_cast<const uint8_t*>(W) + (long long)n * K * (I8 ? 1 : 2), xs, B, K, lane, acc);
+      const float sc = wscale ? wscale[n] : 1.0f;
+      const float bi = bias ? bias[n] : 0.0f;
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
         if (b < B) {
-          const float* xb = xs + b * K + k0;
-          float a = acc[b];
-#pragma unroll
-          for (int j = 0; j < EPV; ++j) a = fmaf(w[j], xb[j], a);
-          acc[b] = a;
+          const float t = warp_sum(acc[b]);
+          if (lane == 0) y[(long long)b * N + n] = t * sc + bi;
         }
-      }
-    }
-    const float sc = wscale ? wscale[n] : 1.0f;
-    const float bi = bias ? bias[n] : 0.0f;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      if (b < B) {
-        const float t = warp_sum(acc[b]);
-        if (lane == 0) y[(long long)b * N + n] = t * sc + bi;
       }
     }
   }
 }
 
 // Batched form: the jobs' output rows are numbered consecutively; each warp
-// finds the job of its row in the kernel-parameter table.
+// finds the job of its row in the kernel-parameter table (its rows only
+// increase, so the search resumes where it stopped).
 constexpr int kMaxGemvJobs = 96;
 struct GemvBatch {
   GemvJob job[kMaxGemvJobs];
@@ -142,61 +221,35 @@ template <bool I8>
 __global__ void __launch_bounds__(256) gemv_batched_kernel(const __grid_constant__ GemvBatch jb,
                                                            const float* __restrict__ x, int B, int K, int act) {
   extern __shared__ float xs[];
-  for (int i = threadIdx.x; i < B * K; i += blockDim.x) {
-    const float t = x[i];
-    xs[i] = act ? silu_f(t) : t;
-  }
-  __syncthreads();
+  gemv_stage_x<I8>(x, B, K, act, xs);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row_base = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp;
-  constexpr int EPV = I8 ? 16 : 8;
-  const int nvec = K / EPV;
+  const int total = jb.row0[jb.n_jobs];
+  const int stride = gridDim.x * kGemvWarps * kGemvRowsPerWarp;
   int j = 0;
 #pragma unroll 1
-  for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
-    const int R = row_base + rr;
-    if (R >= jb.row0[jb.n_jobs]) break;
-    while (R >= jb.row0[j + 1]) ++j;
-    const GemvJob& job = jb.job[j];
-    const int n = R - jb.row0[j];
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const uint4* wr =
-        reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(job.W) + (long long)n * K * (I8 ? 1 : 2));
-#pragma unroll 4
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 wv = __ldg(wr + v);
-      float w[EPV];
-      const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
-      if (I8) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = (float)(int8_t)((u[e >> 2] >> (8 * (e & 3))) & 0xFF);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) w[2 * e] = bf16_lo(u[e]), w[2 * e + 1] = bf16_hi(u[e]);
-      }
-      const int k0 = v * EPV;
+  for (int row_base = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp; row_base < total; row_base += stride) {
+#pragma unroll 1
+    for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
+      const int R = row_base + rr;
+      if (R >= total) break;
+      while (R >= jb.row0[j + 1]) ++j;
+      const GemvJob& job = jb.job[j];
+      const int n = R - jb.row0[j];
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      gemv_row<I8>(reinterpret_cast<const uint8_t*>(job.W) + (long long)n * K * (I8 ? 1 : 2), xs, B, K, lane, acc);
+      const float sc = job.scale ? job.scale[n] : 1.0f;
+      const float bi = job.bias ? job.bias[n] : 0.0f;
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
         if (b < B) {
-          const float* xb = xs + b * K + k0;
-          float a = acc[b];
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) a = fmaf(w[e], xb[e], a);
-          acc[b] = a;
+          const float t = warp_sum(acc[b]);
+          if (lane == 0) job.out[(long long)b * job.N + n] = t * sc + bi;
         }
-      }
-    }
-    const float sc = job.scale ? job.scale[n] : 1.0f;
-    const float bi = job.bias ? job.bias[n] : 0.0f;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      if (b < B) {
-        const float t = warp_sum(acc[b]);
-        if (lane == 0) job.out[(long long)b * job.N + n] = t * sc + bi;
       }
     }
   }
 }
+
 
 // ------------------------------------------------------------------ timestep sinusoid
 // t_tab != null: t = t_scale * t_tab[*t_idx] (the step's sigma read on the
@@ -359,11 +412,6 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T* __restrict__ w, 
 
 // Two fp32 values to packed e4m3 (lo in the low byte), round to nearest
 // even, saturating at +-448.
-__device__ __forceinline__ uint16_t f8x2_e4m3(float lo, float hi) {
-  uint16_t d;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
-  return d;
-}
 
 // One CTA per row of x (row stride ld): s = max|x| / 448 (fp32, 1 for a zero
 // row), q = e4m3(x / s) with the quotient rounded once in fp32.  K even.
@@ -545,12 +593,57 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned* status, 
 }
 
 cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
-                               const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st) {
-  if (D % 256 || D > 4096) return cudaErrorInvalidValue;
+                               const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st,
+                               uint8_t* q, float* qs) {
+  if (D % 256 || D > 4096 || rows < 1 || n_seg < 1) return cudaErrorInvalidValue;
+  if ((q == nullptr) != (qs == nullptr) || (!q && !y)) return cudaErrorInvalidValue;
+  const int n_rows = rows * n_seg;
+  const int blocks = (n_rows + 3) / 4;  // four rows (warps) per CTA
   launch_begin(KID_LN_MODULATE, st);
-  ln_mod_kernel<<<rows * n_seg, D / 8, 0, st>>>(x, x_seg_rows, rows, D, shift, scale, mod_stride, eps, y);
+  switch (D / 128) {
+#define MMDIT_LN_CASE(nv)                                                                                 \
+  case nv:                                                                                                \
+    if (q)                                                                                                \
+      ln_mod_kernel<nv, true><<<blocks, 128, 0, st>>>(x, x_seg_rows, rows, n_rows, shift, scale, mod_stride, eps, \
+                                                       y, q, qs);                                        \
+    else                                                                                                  \
+      ln_mod_kernel<nv, false><<<blocks, 128, 0, st>>>(x, x_seg_rows, rows, n_rows, shift, scale, mod_stride,   \
+                                                        eps, y, nullptr, nullptr);                       \
+    break;
+    MMDIT_LN_CASE(2) MMDIT_LN_CASE(4) MMDIT_LN_CASE(6) MMDIT_LN_CASE(8) MMDIT_LN_CASE(10) MMDIT_LN_CASE(12)
+    MMDIT_LN_CASE(14) MMDIT_LN_CASE(16) MMDIT_LN_CASE(18) MMDIT_LN_CASE(20) MMDIT_LN_CASE(22) MMDIT_LN_CASE(24)
+    MMDIT_LN_CASE(26) MMDIT_LN_CASE(28) MMDIT_LN_CASE(30) MMDIT_LN_CASE(32)
+#undef MMDIT_LN_CASE
+    default:
+      break;
+  }
   launch_end(st);
   return cudaGetLastError();
+}
+
+// CTAs of a GEMV kernel that are resident at once (the grid-stride loop
+// wants no second wave).  Cached per (kernel, shared memory), so launches
+// inside a stream capture make no query.
+static int gemv_resident_ctas(const void* kern, size_t smem) {
+  static std::mutex mu;
+  static struct {
+    const void* k;
+    size_t smem;
+    int n;
+  } cache[16];
+  static int n_cache = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].k == kern && cache[i].smem == smem) return cache[i].n;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess || per_sm < 1) {
+    (void)cudaGetLastError();
+    per_sm = 1;
+  }
+  if (per_sm > kGemvCtasPerSm) per_sm = kGemvCtasPerSm;
+  const int n = per_sm * num_sms();
+  if (n_cache < 16) cache[n_cache++] = {kern, smem, n};
+  return n;
 }
 
 cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
@@ -565,7 +658,10 @@ cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float
     attr_done[dev] = true;
   }
   const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
-  const int blocks = (N + rows_per_cta - 1) / rows_per_cta;
+  int blocks = (N + rows_per_cta - 1) / rows_per_cta;
+  const int resident =
+      gemv_resident_ctas(i8 ? (const void*)gemv_kernel<true> : (const void*)gemv_kernel<false>, smem);
+  if (blocks > resident) blocks = resident;
   launch_begin(KID_GEMV, st);
   if (i8)
     gemv_kernel<true><<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
@@ -599,7 +695,10 @@ cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const 
       jb.row0[i + 1] = jb.row0[jb.n_jobs];
     }
     const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
-    const int blocks = (jb.row0[jb.n_jobs] + rows_per_cta - 1) / rows_per_cta;
+    int blocks = (jb.row0[jb.n_jobs] + rows_per_cta - 1) / rows_per_cta;
+    const int resident = gemv_resident_ctas(
+        i8 ? (const void*)gemv_batched_kernel<true> : (const void*)gemv_batched_kernel<false>, smem);
+    if (blocks > resident) blocks = resident;
     launch_begin(KID_GEMV, st);
     if (i8)
       gemv_batched_kernel<true><<<blocks, 256, smem, st>>>(jb, x, B, K, act);

@@ -7,8 +7,11 @@
 namespace mmdit {
 
 // y[seg][i] = LN(x[seg*x_seg_rows + i]) (1 + scale[seg]) + shift[seg]; D % 256 == 0, D <= 4096.
+// With q and qs: also the e4m3 rows of the bf16 result (row scale max|y| / 448 into qs[row], codes into
+// q[row * D ..]); y may then be null (bf16 rows not stored).
 cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
-                               const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st);
+                               const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st,
+                               uint8_t* q = nullptr, float* qs = nullptr);
 cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
                         int K, int act, float* y, cudaStream_t st);
 // Many GEMVs sharing one input vector set x [B, K] (after the activation):

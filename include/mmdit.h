@@ -367,6 +367,16 @@ int mmdit_linear_fwd(const mmdit_linear_t* lin, int M, int N, int K, const void*
 int mmdit_ln_modulate(const float* x, int B, int rows, int D, const float* shift, const float* scale,
                       int64_t mod_stride, float eps, void* y, void* stream);
 
+/* mmdit_ln_modulate followed by the e4m3 row quantisation of its bf16 result
+ * (the activation path of MMDIT_F8W), in one pass: q device e4m3 bytes
+ * [B, rows, D], s device fp32 [B, rows] with s = max|bf16 row| / 448 (1 for
+ * a zero row) and q = e4m3(bf16 value / s), the decisions of
+ * mmdit_quantize_f8 on the bf16 rows; y (device bf16 [B, rows, D]) may be
+ * NULL, else the bf16 rows are stored too.  Same shape and alignment rules
+ * as mmdit_ln_modulate; errors as there. */
+int mmdit_ln_modulate_f8(const float* x, int B, int rows, int D, const float* shift, const float* scale,
+                         int64_t mod_stride, float eps, void* y, uint8_t* q, float* s, void* stream);
+
 /* y[b, n] = W act(x[b, :]) + bias, x device fp32 [B, K] (B <= 8),
  * act 0 = identity, 1 = SiLU; y device fp32 [B, N]. */
 int mmdit_gemv(const mmdit_linear_t* lin, int B, int N, int K, const float* x, int act, float* y, void* stream);

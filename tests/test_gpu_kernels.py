@@ -100,6 +100,32 @@ def test_ln_modulate(D):
     assert_close(host(y), ref, what="ln_modulate")
 
 
+@pytest.mark.parametrize("D", [256, 3072])
+def test_ln_modulate_f8_fused(D):
+    """LN + modulate with its e4m3 rows written in the same pass (the activation
+    path of the e4m3 blocks): the bf16 rows equal mmdit_ln_modulate's, and the
+    codes and scales equal the oracle's row quantiser on those bf16 rows, bit
+    for bit, with or without the bf16 rows stored."""
+    B, rows = 2, 37
+    x = S.normal_f32("lnq.x", (B, rows, D)) * 2 + 0.5
+    mod = S.normal_f32("lnq.m", (B, 3 * D)) * 0.3
+    x[1, 5] = 0.25  # a constant row: LN output 0, the row is the shift alone
+    xt, mt = f32(x), f32(mod)
+    sh, sc = mt[:, :D], mt[:, D:2 * D]
+    y = torch.empty((B, rows, D), dtype=torch.bfloat16, device="cuda")
+    api.mmdit_ln_modulate(xt, sh, sc, 3 * D, 1e-6, y)
+    y1 = torch.empty_like(y)
+    q1, s1 = api.mmdit_ln_modulate_f8(xt, sh, sc, 3 * D, 1e-6, y1)
+    q0, s0 = api.mmdit_ln_modulate_f8(xt, sh, sc, 3 * D, 1e-6)
+    check_status()
+    assert torch.equal(y1, y)
+    yb = host(y).reshape(B * rows, D)
+    rq, rs = O.quantize_f8_rows(yb)
+    for q, s in ((q1, s1), (q0, s0)):
+        assert np.array_equal(host(s).reshape(-1).astype(np.float32), rs)
+        assert np.array_equal(decode_e4m3(q.reshape(B * rows, D).cpu().numpy()), rq)
+
+
 @pytest.mark.parametrize("i8", [False, True])
 @pytest.mark.parametrize("act", [0, 1])
 def test_gemv(i8, act):
