@@ -93,6 +93,20 @@ def test_null_and_misaligned_arguments_rejected_before_launch(lib):
                                    256, ctypes.c_void_p(16), 1 << 30, None) == -2
 
 
+def test_ln_modulate_f8_arguments_rejected_before_launch(lib):
+    p16 = ctypes.c_void_p(256)
+    # codes or scales missing
+    assert lib.mmdit_ln_modulate_f8(p16, 1, 4, 256, p16, p16, 768, ctypes.c_float(1e-6), None, None, p16, None) == -1
+    assert lib.mmdit_ln_modulate_f8(p16, 1, 4, 256, p16, p16, 768, ctypes.c_float(1e-6), None, p16, None, None) == -1
+    # D not a multiple of 256, or above 4096
+    assert lib.mmdit_ln_modulate_f8(p16, 1, 4, 384, p16, p16, 768, ctypes.c_float(1e-6), None, p16, p16, None) == -2
+    assert lib.mmdit_ln_modulate_f8(p16, 1, 4, 4352, p16, p16, 768, ctypes.c_float(1e-6), None, p16, p16, None) == -2
+    # misaligned codes, or a modulation stride that breaks the 16-byte rows
+    assert lib.mmdit_ln_modulate_f8(p16, 1, 4, 256, p16, p16, 768, ctypes.c_float(1e-6), None, ctypes.c_void_p(264),
+                                    p16, None) == -3
+    assert lib.mmdit_ln_modulate_f8(p16, 1, 4, 256, p16, p16, 770, ctypes.c_float(1e-6), None, p16, p16, None) == -3
+
+
 def test_sample_arguments_rejected_before_launch(lib):
     from diffusion_transformer_image_mmdit_gb300 import _lib
     s = _shape()

@@ -25,3 +25,17 @@ def test_bench_flop_accounting():
     assert abs(57 * per_block / 1e12 - 133.9) < 0.05
     c5 = bench.step_flops(bench.CONFIGS["c5"])
     assert abs(c5["total"] / 1e12 - 297.4) / 297.4 < 3e-3
+
+
+def test_bench_e4m3_accounting():
+    """The e4m3 configs count the same FLOPs as their bf16 twins; all block-linear FLOPs (not the embedder and
+    final-layer GEMMs) are e4m3; the weights read per step shrink by the block linears' half."""
+    import bench
+    for f8, bf in (("c4_f8", "c4"), ("klein1024_f8", "klein1024")):
+        a, b = bench.step_flops(bench.CONFIGS[f8]), bench.step_flops(bench.CONFIGS[bf])
+        assert a["total"] == b["total"] and a["gemm"] == b["gemm"] and b["gemm_f8"] == 0
+        c = bench.CONFIGS[f8]
+        io = 2 * c["grid_h"] * c["grid_w"] * c["C_lat"] * c["D"] * 2 * c["B"]
+        assert a["gemm"] - a["gemm_f8"] == io
+        wa, wb = bench.step_weight_bytes(bench.CONFIGS[f8]), bench.step_weight_bytes(bench.CONFIGS[bf])
+        assert 0.5 * wb < wa < 0.7 * wb
