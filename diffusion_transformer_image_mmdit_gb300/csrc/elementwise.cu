@@ -123,8 +123,9 @@ __device__ __forceinline__ int gemv_slot(int k) {
 }
 
 // One output row (K a multiple of EPV): up to kGemvVecBatch 16-byte weight
-// loads per lane in flight before use.
-template <bool I8>
+// loads per lane in flight before use; B <= BM rows of x (BM a compile-time
+// bound, so B = 1 keeps one accumulator and few registers).
+template <bool I8, int BM>
 __device__ __forceinline__ void gemv_row(const uint8_t* __restrict__ wrow, const float* xs, int B, int K, int lane,
                                          float* acc) {
   constexpr int EPV = I8 ? 16 : 8;
@@ -151,7 +152,7 @@ __device__ __forceinline__ void gemv_row(const uint8_t* __restrict__ wrow, const
       }
       const int sw = I8 ? ((v >> 1) & 3) : ((v >> 2) & 1);
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
+      for (int b = 0; b < BM; ++b) {
         if (b < B) {
           const float4* xv = reinterpret_cast<const float4*>(xs + b * K + v * EPV);
           float t = acc[b];
@@ -178,7 +179,7 @@ __device__ __forceinline__ void gemv_stage_x(const float* __restrict__ x, int B,
 }
 
 
-template <bool I8>
+template <bool I8, int BM>
 __global__ void __launch_bounds__(256) gemv_kernel(const void* __restrict__ W, const float* __restrict__ wscale,
                                                    const float* __restrict__ bias, const float* __restrict__ x, int B,
                                                    int N, int K, int act, float* __restrict__ y) {
@@ -192,12 +193,14 @@ __global__ void __launch_bounds__(256) gemv_kernel(const void* __restrict__ W, c
     for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
       const int n = row0 + rr;
       if (n >= N) break;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      gemv_row<I8>(reinterpret_cast<const uint8_t*>(W) + (long long)n * K * (I8 ? 1 : 2), xs, B, K, lane, acc);
+      float acc[BM];
+#pragma unroll
+      for (int b = 0; b < BM; ++b) acc[b] = 0.f;
+      gemv_row<I8, BM>(reinterpret_cast<const uint8_t*>(W) + (long long)n * K * (I8 ? 1 : 2), xs, B, K, lane, acc);
       const float sc = wscale ? wscale[n] : 1.0f;
       const float bi = bias ? bias[n] : 0.0f;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
+      for (int b = 0; b < BM; ++b) {
         if (b < B) {
           const float t = warp_sum(acc[b]);
           if (lane == 0) y[(long long)b * N + n] = t * sc + bi;
@@ -217,7 +220,7 @@ struct GemvBatch {
   int n_jobs;
 };
 
-template <bool I8>
+template <bool I8, int BM>
 __global__ void __launch_bounds__(256) gemv_batched_kernel(const __grid_constant__ GemvBatch jb,
                                                            const float* __restrict__ x, int B, int K, int act) {
   extern __shared__ float xs[];
@@ -235,12 +238,14 @@ __global__ void __launch_bounds__(256) gemv_batched_kernel(const __grid_constant
       while (R >= jb.row0[j + 1]) ++j;
       const GemvJob& job = jb.job[j];
       const int n = R - jb.row0[j];
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      gemv_row<I8>(reinterpret_cast<const uint8_t*>(job.W) + (long long)n * K * (I8 ? 1 : 2), xs, B, K, lane, acc);
+      float acc[BM];
+#pragma unroll
+      for (int b = 0; b < BM; ++b) acc[b] = 0.f;
+      gemv_row<I8, BM>(reinterpret_cast<const uint8_t*>(job.W) + (long long)n * K * (I8 ? 1 : 2), xs, B, K, lane, acc);
       const float sc = job.scale ? job.scale[n] : 1.0f;
       const float bi = job.bias ? job.bias[n] : 0.0f;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
+      for (int b = 0; b < BM; ++b) {
         if (b < B) {
           const float t = warp_sum(acc[b]);
           if (lane == 0) job.out[(long long)b * job.N + n] = t * sc + bi;
@@ -646,42 +651,65 @@ static int gemv_resident_ctas(const void* kern, size_t smem) {
   return n;
 }
 
-cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
-                        int K, int act, float* y, cudaStream_t st) {
-  const size_t smem = (size_t)B * K * sizeof(float);
-  static bool attr_done[64] = {};
+// The kernel instance for B rows of x: the smallest batch bound >= B.
+using GemvFn = void (*)(const void*, const float*, const float*, const float*, int, int, int, int, float*);
+using GemvBatchedFn = void (*)(const GemvBatch, const float*, int, int, int);
+template <bool I8>
+static GemvFn gemv_fn(int B) {
+  return B <= 1 ? gemv_kernel<I8, 1> : B <= 2 ? gemv_kernel<I8, 2> : B <= 4 ? gemv_kernel<I8, 4> : gemv_kernel<I8, 8>;
+}
+template <bool I8>
+static GemvBatchedFn gemv_batched_fn(int B) {
+  return B <= 1 ? gemv_batched_kernel<I8, 1>
+                : B <= 2 ? gemv_batched_kernel<I8, 2> : B <= 4 ? gemv_batched_kernel<I8, 4> : gemv_batched_kernel<I8, 8>;
+}
+
+// Lets every GEMV instance use up to 200 KB of dynamic shared memory (x of up
+// to 8 rows); once per device.
+static cudaError_t gemv_attributes() {
+  static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaFuncSetAttribute(gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    cudaFuncSetAttribute(gemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_done[dev] = true;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  const void* fns[16];
+  int n = 0;
+  for (int B : {1, 2, 4, 8}) {
+    fns[n++] = (const void*)gemv_fn<false>(B);
+    fns[n++] = (const void*)gemv_fn<true>(B);
+    fns[n++] = (const void*)gemv_batched_fn<false>(B);
+    fns[n++] = (const void*)gemv_batched_fn<true>(B);
   }
+  for (int i = 0; i < n; ++i) {
+    const cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+  }
+  done[dev] = true;
+  return cudaSuccess;
+}
+
+cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
+                        int K, int act, float* y, cudaStream_t st) {
+  const cudaError_t ea = gemv_attributes();
+  if (ea != cudaSuccess) return ea;
+  const size_t smem = (size_t)B * K * sizeof(float);
+  const GemvFn fn = i8 ? gemv_fn<true>(B) : gemv_fn<false>(B);
   const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
   int blocks = (N + rows_per_cta - 1) / rows_per_cta;
-  const int resident =
-      gemv_resident_ctas(i8 ? (const void*)gemv_kernel<true> : (const void*)gemv_kernel<false>, smem);
+  const int resident = gemv_resident_ctas((const void*)fn, smem);
   if (blocks > resident) blocks = resident;
   launch_begin(KID_GEMV, st);
-  if (i8)
-    gemv_kernel<true><<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
-  else
-    gemv_kernel<false><<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
+  fn<<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
   launch_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const float* x, int B, int K, int act,
                                 cudaStream_t st) {
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaFuncSetAttribute(gemv_batched_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    cudaFuncSetAttribute(gemv_batched_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_done[dev] = true;
-  }
+  const cudaError_t ea = gemv_attributes();
+  if (ea != cudaSuccess) return ea;
   const size_t smem = (size_t)B * K * sizeof(float);
+  const GemvBatchedFn fn = i8 ? gemv_batched_fn<true>(B) : gemv_batched_fn<false>(B);
   for (int first = 0; first < n_jobs; first += kMaxGemvJobs) {
     GemvBatch jb;
     jb.n_jobs = n_jobs - first < kMaxGemvJobs ? n_jobs - first : kMaxGemvJobs;
@@ -696,14 +724,10 @@ cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const 
     }
     const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
     int blocks = (jb.row0[jb.n_jobs] + rows_per_cta - 1) / rows_per_cta;
-    const int resident = gemv_resident_ctas(
-        i8 ? (const void*)gemv_batched_kernel<true> : (const void*)gemv_batched_kernel<false>, smem);
+    const int resident = gemv_resident_ctas((const void*)fn, smem);
     if (blocks > resident) blocks = resident;
     launch_begin(KID_GEMV, st);
-    if (i8)
-      gemv_batched_kernel<true><<<blocks, 256, smem, st>>>(jb, x, B, K, act);
-    else
-      gemv_batched_kernel<false><<<blocks, 256, smem, st>>>(jb, x, B, K, act);
+    fn<<<blocks, 256, smem, st>>>(jb, x, B, K, act);
     launch_end(st);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
