@@ -600,7 +600,8 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned* status, 
 cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
                                const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st,
                                uint8_t* q, float* qs) {
-  if (D % 256 || D > 4096 || rows < 1 || n_seg < 1) return cudaErrorInvalidValue;
+  // D / 128 is then one of the even cases 2 .. 32 below
+  if (D % 256 || D < 256 || D > 4096 || rows < 1 || n_seg < 1) return cudaErrorInvalidValue;
   if ((q == nullptr) != (qs == nullptr) || (!q && !y)) return cudaErrorInvalidValue;
   const int n_rows = rows * n_seg;
   const int blocks = (n_rows + 3) / 4;  // four rows (warps) per CTA
@@ -634,12 +635,14 @@ static int gemv_resident_ctas(const void* kern, size_t smem) {
   static struct {
     const void* k;
     size_t smem;
-    int n;
-  } cache[16];
+    int dev, n;
+  } cache[32];
   static int n_cache = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_cache; ++i)
-    if (cache[i].k == kern && cache[i].smem == smem) return cache[i].n;
+    if (cache[i].k == kern && cache[i].smem == smem && cache[i].dev == dev) return cache[i].n;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess || per_sm < 1) {
     (void)cudaGetLastError();
@@ -647,7 +650,7 @@ static int gemv_resident_ctas(const void* kern, size_t smem) {
   }
   if (per_sm > kGemvCtasPerSm) per_sm = kGemvCtasPerSm;
   const int n = per_sm * num_sms();
-  if (n_cache < 16) cache[n_cache++] = {kern, smem, n};
+  if (n_cache < 32) cache[n_cache++] = {kern, smem, dev, n};
   return n;
 }
 
