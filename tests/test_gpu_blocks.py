@@ -175,6 +175,33 @@ def test_step_small(i8):
     assert_close(host(xl), ref_x, rel=tol, what="step x_lat")
 
 
+def test_step_small_f8():
+    """A whole step (2 double + 2 single blocks, batch 2) with the block linears in e4m3, against the
+    bf16-weight oracle: the velocity within the e4m3 scheme bar (the blocks themselves are pinned against
+    the oracle's e4m3 model in the block tests), the Euler-updated latent within 1e-2."""
+    cfg = dict(CONFIGS["d128"])
+    cfg["B"] = 2
+    sh = oracle_shape(cfg)
+    sh.C_lat, sh.t_dim = 64, 256
+    W = S.embed_params(cfg["D"], sh.C_lat, sh.t_dim, seed=5)
+    W["double"] = [S.double_block_params(f"st8.d{i}", cfg["D"], cfg["d_head"], cfg["D_mlp"]) for i in range(2)]
+    W["single"] = [S.single_block_params(f"st8.s{i}", cfg["D"], cfg["d_head"], cfg["D_mlp"]) for i in range(2)]
+    x_lat = S.normal_f32("st8.lat", (cfg["B"], sh.L_img, sh.C_lat))
+    x_txt = S.normal_f32("st8.txt", (cfg["B"], cfg["L_txt"], cfg["D"]))
+    sig = O.sigma_schedule(50, O.shift_mu(sh.L_img))
+    shape = api_shape(cfg, C_lat=sh.C_lat, t_dim=sh.t_dim, w_dtype=api.MMDIT_F8W)
+    w = Wt.step_from_host(W).quantized_f8()
+    ws = api.alloc_workspace(api.step_workspace_size(shape, 2, 2))
+    xl = f32(x_lat)
+    v = torch.empty_like(xl)
+    api.mmdit_step_fwd(shape, w, xl, f32(x_txt), sig[0], sig[1], v, ws)
+    check_status()
+    ref_x, ref_v = O.denoise_step(x_lat, x_txt, sig[0], sig[1], W, sh)
+    assert np.all(np.isfinite(host(v)))
+    assert rel_l2(host(v), ref_v) <= REL_L2_F8_SCHEME, rel_l2(host(v), ref_v)
+    assert_close(host(xl), ref_x, rel=1e-2, max_abs=np.inf, what="e4m3 step x_lat")
+
+
 # ------------------------------------------------------------------ SwiGLU blocks (Flux.2 Klein)
 KLEIN = dict(D=4096, H=32, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56), mlp_act=api.MMDIT_MLP_SWIGLU)
 
