@@ -326,11 +326,14 @@ def euler_step(x, v, sigma, sigma_next):
     return x + (sigma_next - sigma) * v
 
 
-def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape, vec_add=None):
+def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape, vec_add=None, rnd=None, qin=None):
     """One full step: timestep embedding, img_in, the double blocks, the
     single blocks on [text; image], the final layer on the image tokens, the
     Euler update.  vec_add ([B, D] or None) is added to the timestep
     embedding (the step-independent conditioning of the sampling loop).
+    rnd and qin are handed to every block unchanged (precision and
+    activation-quantisation models, see double_block); None leaves the
+    plain definition.
     Returns (x_lat_next, v)."""
     ids = rope_ids(sh.L_txt, sh.grid_h, sh.grid_w)
     cos, sin = rope_tables(ids, sh.rope_axes, sh.rope_theta)
@@ -340,10 +343,10 @@ def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape, vec_add=None):
     h_img = img_in(x_lat, W)
     h_txt = x_txt
     for blk in W["double"]:
-        h_txt, h_img = double_block(h_txt, h_img, vec, blk, sh, cos, sin)
+        h_txt, h_img = double_block(h_txt, h_img, vec, blk, sh, cos, sin, rnd=rnd, qin=qin)
     x = np.concatenate([h_txt, h_img], axis=1)
     for blk in W["single"]:
-        x = single_block(x, vec, blk, sh, cos, sin)
+        x = single_block(x, vec, blk, sh, cos, sin, rnd=rnd, qin=qin)
     v = final_layer(x[:, sh.L_txt:], vec, W, sh)
     return euler_step(x_lat, v, sigma, sigma_next), v
 

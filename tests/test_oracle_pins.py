@@ -373,6 +373,30 @@ def test_quantisation_hook_reaches_exactly_the_gemm_inputs():
     assert sorted(seen) == [sh.D, sh.D + sh.D_mlp]
 
 
+def test_step_hooks_reach_every_block_linear():
+    """denoise_step hands qin to every block: per double block the four GEMM inputs of each stream, per
+    single block lin1's and lin2's; identity hooks leave the step bit-identical."""
+    sh = O.Shape(B=1, L_txt=8, grid_h=4, grid_w=4, D=64, H=2, d_head=32, D_mlp=128, rope_axes=(8, 12, 12),
+                 C_lat=16, t_dim=32)
+    W = S.embed_params(sh.D, sh.C_lat, sh.t_dim, seed=9)
+    W["double"] = [S.double_block_params(f"pin.sh.d{i}", sh.D, sh.d_head, sh.D_mlp) for i in range(2)]
+    W["single"] = [S.single_block_params(f"pin.sh.s{i}", sh.D, sh.d_head, sh.D_mlp) for i in range(3)]
+    x_lat = S.normal_f32("pin.sh.lat", (sh.B, sh.L_img, sh.C_lat))
+    x_txt = S.normal_f32("pin.sh.txt", (sh.B, sh.L_txt, sh.D))
+    seen = []
+
+    def spy(x):
+        seen.append(x.shape[-1])
+        return x
+    plain = O.denoise_step(x_lat, x_txt, 1.0, 0.9, W, sh)
+    got = O.denoise_step(x_lat, x_txt, 1.0, 0.9, W, sh, qin=spy)
+    assert sorted(seen) == sorted([sh.D, sh.D, sh.D, sh.D_mlp] * 2 * 2 + [sh.D, sh.D + sh.D_mlp] * 3)
+    assert np.array_equal(got[0], plain[0]) and np.array_equal(got[1], plain[1])
+    # an identity precision model only changes the fp64 evaluation order inside the attention
+    ident = O.denoise_step(x_lat, x_txt, 1.0, 0.9, W, sh, rnd=lambda t: t)
+    assert rel(ident[1], plain[1]) < 1e-12
+
+
 def _zero_gates(mod_w, mod_b, n_chunks, gate_chunks):
     D = mod_w.shape[0] // n_chunks
     mod_w, mod_b = mod_w.copy(), mod_b.copy()
