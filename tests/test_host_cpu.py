@@ -39,3 +39,21 @@ def test_bench_e4m3_accounting():
         assert a["gemm"] - a["gemm_f8"] == io
         wa, wb = bench.step_weight_bytes(bench.CONFIGS[f8]), bench.step_weight_bytes(bench.CONFIGS[bf])
         assert 0.5 * wb < wa < 0.7 * wb
+
+
+def test_clock_sampler_summary():
+    """The bench's clock record from nvidia-smi CSV rows: median SM clock under load, the maximum clock,
+    and every throttle reason seen active at any sample (the rules that reject or annotate a run)."""
+    import bench
+    cs = bench.ClockSampler(0)
+    assert cs.summary()["reasons"] == ["unsampled"]
+    line = "0, {sm}, 2070, {pw}, 0x{act}, {hw}, Not Active, Not Active, {cap}"
+    cs.rows = [[x.strip() for x in line.format(sm=sm, pw=pw, act=a, hw=hw, cap=cap).split(",")]
+               for sm, pw, a, hw, cap in ((1965, 1100.5, "4", "Not Active", "Active"),
+                                          (1980, 1371.0, "4", "Not Active", "Active"),
+                                          (1890, 900.25, "0", "Not Active", "Not Active"))]
+    s = cs.summary()
+    assert s["sm_mhz"] == 1965 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1371.0
+    cs.rows.append([x.strip() for x in line.format(sm=1200, pw=800, act="8", hw="Active", cap="Not Active").split(",")])
+    assert bench.ClockSampler.summary(cs)["reasons"] == ["hw_slowdown", "sw_power_cap"]
