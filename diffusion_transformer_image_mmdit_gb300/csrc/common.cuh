@@ -201,18 +201,6 @@ __device__ __forceinline__ void umma_commit_if(uint32_t issue, uint32_t bar) {
       : "memory");
 }
 
-// Multicast commit: arrives on the mbarrier at the same shared-memory offset
-// in every CTA of the cluster named by `mask`, once this thread's prior MMAs
-// complete.
-__device__ __forceinline__ void umma_commit_mc_if(uint32_t issue, uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
-      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
-          bar),
-      "h"(mask), "r"(issue)
-      : "memory");
-}
-
 // ----------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -226,15 +214,97 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// TMA tile load written to the same shared-memory offset in every CTA of
-// `mask`; each destination CTA's mbarrier at offset `bar` receives the bytes
-// it got.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* map, uint32_t bar, int x, int y, int z,
-                                               uint16_t mask) {
+// Shared::cluster address of the shared variable at CTA-local address `a`
+// in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster, given by its
+// shared::cluster address, with the default CTA-scope release: it orders
+// this thread's earlier accesses as a local arrive would, without the
+// cluster-wide fence a cluster-scope release costs.  Used to hand a drained
+// tensor-memory accumulator back to the MMA-issuing CTA: the tcgen05.ld that
+// read it has completed (tcgen05.wait::ld) and is ordered before the arrive
+// by tcgen05.fence::before_thread_sync.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// Arrival with an expected byte count on an mbarrier of any CTA of the
+// cluster, relaxed: it orders none of this thread's memory accesses.  Meant
+// for a barrier that guards the bytes of TMA copies, whose completion the
+// transaction count tracks by itself; a release at cluster scope here costs
+// a cluster-wide fence per arrival.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster),
+               "r"(bytes)
+               : "memory");
+}
+
+// Stores a 32-bit value into the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr_cluster, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr_cluster), "r"(v) : "memory");
+}
+
+// ------------------------------------------------------------ CTA pairs
+// A CTA pair (the two CTAs of a cluster of two) runs one tcgen05.mma of
+// M = 256: each CTA holds 128 rows of A and one half of the N rows of B in
+// its own shared memory, at the same offsets, and receives its 128 rows of
+// the accumulator in its own tensor memory.  Only CTA 0 of the pair issues
+// the MMAs.  Every tcgen05 instruction of such a kernel uses cta_group::2.
+
+// TMA tile load into this CTA's shared memory whose completion is counted
+// on an mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* map, uint32_t bar_cluster, int x, int y,
+                                                 int z) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-      "[%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(mask)
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Allocation by one warp of each CTA of the pair, collectively: the same
+// columns in both CTAs' tensor memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Pair MMA, kind::f16 (bf16 A and B) or kind::f8f6f4 (e4m3 A and B),
+// predicated on `issue` (the elected lane of the issuing warp).
+__device__ __forceinline__ void umma_bf16_pair_if(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+__device__ __forceinline__ void umma_f8_pair_if(uint32_t issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
+// Arrive on an mbarrier of either CTA of the pair (shared::cluster address)
+// once every pair MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit_pair_if(uint32_t issue, uint32_t bar_cluster) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar_cluster),
+      "r"(issue)
       : "memory");
 }
 

@@ -5,25 +5,33 @@
 // bf16 contractions with fp32 accumulation (Luminal blog, section "The AMD
 // MI300X pipeline": all bf16 GEMMs accumulate in fp32, with bias epilogues).
 //
-// Structure (one CTA per SM, 320 threads, clusters of two CTAs):
-//   The two CTAs of a cluster compute the vertically adjacent 128x256 output
-//   tiles (m, n) and (m + 1, n), which share their 256x64 W tile for every K
-//   block: each CTA loads one 128-row half of it and multicasts it into both
-//   CTAs' shared memory, so the pair reads W from L2 once (32 KB per CTA and
-//   K block instead of 48 KB).
-//   warp 0      TMA producer: its A tile 128x64 and its W half 128x64
-//               (multicast) per K block into a 4-stage ring (128-byte
-//               swizzle).  A stage is refilled only when the MMAs of both
-//               CTAs have released it (the empty barrier counts two
-//               multicast commits).
+// Structure (one CTA per SM, 320 threads, clusters of two CTAs = one CTA
+// pair):
+//   The pair computes the vertically adjacent 128x256 output tiles (m, n)
+//   and (m + 1, n) with one stream of tcgen05.mma.cta_group::2 (M = 256,
+//   N = 256): each CTA loads its own 128 rows of A and one 128-row half of
+//   the 256-row W tile into its own shared memory (plain TMA tile loads),
+//   and the MMA reads both CTAs' halves, so W crosses L2 -> SM once per pair
+//   and the pair issues half the MMAs two independent CTAs would.
+//   warp 0      TMA producer (both CTAs): its A tile 128x64 and its W half
+//               128x64 per K block into a 6-stage ring (128-byte swizzle,
+//               32 KB per stage).  Both CTAs' loads complete on CTA 0's
+//               full barrier (two arrivals with their byte counts).  CTA 0's
+//               MMAs release a stage on CTA 0's empty barrier; CTA 0's
+//               producer passes each release on to CTA 1's empty barrier.
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//               and issues tcgen05.mma (M=128, N=256, K=16) from one thread.
-//   warps 2-9   epilogue: tcgen05.ld of the finished accumulator (one TMEM
-//               lane = one output row per thread; two warps per lane
-//               quadrant, one per 128-column half), fused bias / per-channel
-//               scale / GELU-tanh / SwiGLU / gated fp32 residual / q-k
-//               RMSNorm + RoPE / transposed V store, overlapping the next
-//               tile's MMAs.
+//               in both CTAs (one collective pair allocation); in CTA 0 it
+//               issues the pair MMAs (M=256, N=256, K=16) from one elected
+//               lane; the accumulator-ready commit goes to both CTAs.
+//   warps 2-9   epilogue (both CTAs): tcgen05.ld of the finished
+//               accumulator of this CTA's 128 rows (one TMEM lane = one
+//               output row per thread; two warps per lane quadrant, one per
+//               128-column half), fused bias / per-channel scale / GELU-tanh
+//               / SwiGLU / gated fp32 residual / q-k RMSNorm + RoPE /
+//               transposed V store, overlapping the next tile's MMAs; the
+//               drained accumulator is handed back on CTA 0's barrier.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace mmdit {
@@ -32,11 +40,12 @@ namespace {
 
 constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, one per 128-column half
 constexpr int kGemmThreads = 32 * (2 + kEpiWarps);
-constexpr uint32_t kStageA = kBM * kBK * 2;  // 16 KB
-constexpr uint32_t kStageB = kBN * kBK * 2;  // 32 KB
+constexpr int kRing = 6;                          // stages of the TMA ring
+constexpr uint32_t kStageA = kBM * kBK * 2;       // 16 KB: this CTA's 128 rows of A
+constexpr uint32_t kStageB = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128-row half of the W tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiStageBytes = 4096;  // staging area of one epilogue warp
-constexpr size_t kGemmSmem = 1024 + kStages * (kStageA + kStageB) + 256 + kEpiWarps * kEpiStageBytes;
+constexpr size_t kGemmSmem = 1024 + kRing * (kStageA + kStageB) + 256 + kEpiWarps * kEpiStageBytes;
 static_assert(kGemmSmem <= 232448, "GEMM shared memory above the 227 KB a CTA can have");
 
 struct TileCoord {
@@ -342,40 +351,44 @@ __device__ __forceinline__ void prefetch_resid_row(const GemmParams& p, const Ti
 
 // F8: A and W are e4m3 (one byte per element, 128 elements per 128-byte
 // K block, kind::f8f6f4 MMAs of K = 32); otherwise bf16 (64 per K block,
-// kind::f16 MMAs of K = 16).  Either way a stage holds 16 KB of A and 32 KB
-// of W and takes four MMAs.
+// kind::f16 MMAs of K = 16).  Either way a stage holds 16 KB of A and 16 KB
+// of W per CTA and takes four pair MMAs.
 template <bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmGroup g) {
   constexpr int kKB = F8 ? 128 : kBK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kStageA;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kStageB);
+  uint8_t* sB = smem + kRing * kStageA;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kRing * kStageB);
+  // full[kRing], tempty[2], mma_done: used in CTA 0 only; empty[kRing], tfull[2]: in both CTAs
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = smem_u32(bars + kStages);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
-  const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  const uint32_t empty0 = smem_u32(bars + kRing);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kRing);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kRing + 2);
+  const uint32_t mma_done = smem_u32(bars + 2 * kRing + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kRing + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* peer_fills = reinterpret_cast<volatile int*>(tmem_slot + 2);  // CTA 0: CTA 1's fill count
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = (int)cluster_ctarank();
   const int cluster = blockIdx.x >> 1;
   const int n_clusters = gridDim.x >> 1;
-  constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 2);  // one multicast commit from each CTA of the pair
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(full0 + 8 * s, 2);  // one arrive.expect_tx from each CTA's producer
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, kEpiWarps);
+      mbar_init(tempty0 + 8 * a, 2 * kEpiWarps);  // the epilogue warps of both CTAs
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
+    *peer_fills = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -384,12 +397,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
       tma_prefetch_desc(&g.tmB[q]);
     }
   }
+  uint32_t elected = 0;
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    elected = elect_one_sync();
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  // Both CTAs' barriers are initialised before either CTA's multicast loads
+  // Both CTAs' barriers are initialised before either CTA's loads, arrivals
   // or commits can reach them.
   cluster_sync();
   tc_fence_after();
@@ -399,6 +414,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint32_t full_c0 = mapa_shared(full0, 0);    // CTA 0's full barriers, as seen from this CTA
+      const uint32_t empty_c1 = mapa_shared(empty0, 1);  // CTA 1's empty barriers
       int stage = 0;
       uint32_t phase = 0;
       for (int t = cluster; t < g.total_tiles; t += n_clusters) {
@@ -412,50 +429,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         const int nk = p.K / kKB;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, status, ST_TIMEOUT_PRODUCER)) goto done;
-          // 16 KB of A from this CTA, 2 x 16 KB of W (one half from each CTA)
-          mbar_expect_tx(full0 + 8 * stage, kStageA + kStageB);
-          tma_load_3d(smem_u32(sA + stage * kStageA), &g.tmA[q], full0 + 8 * stage, kb * kKB, m0, c.seg);
-          tma_load_3d_mc(smem_u32(sB + stage * kStageB + rank * (kStageB / 2)), &g.tmB[q], full0 + 8 * stage,
-                         kb * kKB, brow, 0, kPair);
+          // CTA 0's MMAs commit to CTA 0's empty barrier only (one commit per
+          // stage keeps the MMA warp's issue free for MMAs); CTA 0's producer
+          // passes the release on to CTA 1 once it has seen it.
+          if (rank == 0 && n_fill >= kRing) mbar_arrive_cluster(empty_c1 + 8 * stage);
+          const uint32_t fb = full_c0 + 8 * stage;
+          if (rank == 0)
+            mbar_expect_tx(full0 + 8 * stage, kStageA + kStageB);
+          else
+            mbar_arrive_expect_tx_cluster(fb, kStageA + kStageB);
+          tma_load_3d_pair(smem_u32(sA + stage * kStageA), &g.tmA[q], fb, kb * kKB, m0, c.seg);
+          tma_load_3d_pair(smem_u32(sB + stage * kStageB), &g.tmB[q], fb, kb * kKB, brow, 0);
           ++n_fill;
-          if (++stage == kStages) stage = 0, phase ^= 1;
+          if (++stage == kRing) stage = 0, phase ^= 1;
         }
       }
     }
   } else if (warp == 1) {
-    // The whole warp runs the issue loop (warp-uniform operands); the
-    // elected lane issues the MMAs and commits.  Descriptors are built once;
-    // per MMA only a compile-time offset (in 16-byte units of the
-    // start-address field) is added.
-    const uint32_t leader = elect_one_sync();
-    const uint32_t idesc = F8 ? idesc_e4m3(kBM, kBN) : idesc_bf16(kBM, kBN);
-    const uint64_t dA0 = sdesc_k128(smem_u32(sA)), dB0 = sdesc_k128(smem_u32(sB));
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int t = cluster; t < g.total_tiles; t += n_clusters) {
-      const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kKB;
-      if (!mbar_wait_warp(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
-      tc_fence_after();
-      const uint32_t d = tmem + acc * kBN;
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait_warp(full0 + 8 * stage, phase, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
+    if (rank == 0) {
+      // The whole warp runs the issue loop (warp-uniform operands); the
+      // elected lane issues the pair MMAs and commits.  Descriptors are
+      // built once; per MMA only a compile-time offset (in 16-byte units of
+      // the start-address field) is added.  The same shared-memory offsets
+      // address the operands in both CTAs.
+      const uint32_t idesc = F8 ? idesc_e4m3(2 * kBM, kBN) : idesc_bf16(2 * kBM, kBN);
+      const uint64_t dA0 = sdesc_k128(smem_u32(sA)), dB0 = sdesc_k128(smem_u32(sB));
+      const uint32_t tfull_c1 = mapa_shared(tfull0, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = cluster; t < g.total_tiles; t += n_clusters) {
+        const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kKB;
+        if (!mbar_wait_warp(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
         tc_fence_after();
-        const uint64_t da = dA0 + (uint64_t)(stage * (kStageA >> 4));
-        const uint64_t db = dB0 + (uint64_t)(stage * (kStageB >> 4));
+        const uint32_t d = tmem + acc * kBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_warp(full0 + 8 * stage, phase, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
+          tc_fence_after();
+          const uint64_t da = dA0 + (uint64_t)(stage * (kStageA >> 4));
+          const uint64_t db = dB0 + (uint64_t)(stage * (kStageB >> 4));
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // 32 bytes of K per MMA
-          if (F8)
-            umma_f8_if(leader, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-          else
-            umma_bf16_if(leader, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          for (int k = 0; k < 4; ++k) {  // 32 bytes of K per MMA
+            if (F8)
+              umma_f8_pair_if(elected, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+            else
+              umma_bf16_pair_if(elected, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          }
+          umma_commit_pair_if(elected, empty0 + 8 * stage);  // frees the stage (CTA 1 via CTA 0's producer)
+          if (++stage == kRing) stage = 0, phase ^= 1;
         }
-        umma_commit_mc_if(leader, empty0 + 8 * stage, kPair);  // frees the stage in both CTAs
-        if (++stage == kStages) stage = 0, phase ^= 1;
+        umma_commit_pair_if(elected, tfull0 + 8 * acc);
+        umma_commit_pair_if(elected, tfull_c1 + 8 * acc);
+        if (++acc == 2) acc = 0, acc_phase ^= 1;
       }
-      umma_commit_if(leader, tfull0 + 8 * acc);
-      if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
   } else {
     // warps 2..9: TMEM lane quadrant warp % 4 (a warp may only read its own
@@ -464,6 +491,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
     uint8_t* stg = reinterpret_cast<uint8_t*>(bars) + 256 + (warp - 2) * kEpiStageBytes;
+    const uint32_t tempty_c0 = mapa_shared(tempty0, 0);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster; t < g.total_tiles; t += n_clusters) {
@@ -476,35 +504,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
       if (c.valid) epilogue_tile(p, c, tmem + ((uint32_t)(quad * 32) << 16) + acc * kBN, r, half, stg);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (lane == 0) mbar_arrive_cluster(tempty_c0 + 8 * acc);
       if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
   }
 done:
-  if (warp == 0 && lane == 0 && *abort_flag) {
-    // After a time-out: wait (bounded) until this CTA's own fills of the
-    // last ring round have landed before its shared memory goes away.
-    for (int i = max(0, n_fill - kStages); i < n_fill; ++i)
-      mbar_wait(full0 + 8 * (i % kStages), (uint32_t)(i / kStages) & 1, nullptr, nullptr, 0, 100000000ull);
+  __syncwarp();
+  // Every pair MMA of CTA 0 has completed (they read both CTAs' shared
+  // memory and write both CTAs' tensor memory) before either CTA moves on.
+  if (warp == 1 && rank == 0) {
+    umma_commit_pair_if(elected, mma_done);
+    mbar_wait_warp(mma_done, 0, nullptr, nullptr, 0);
+  }
+  // CTA 1 tells CTA 0 how many stages it filled.
+  if (warp == 0 && lane == 0 && rank == 1) st_shared_cluster_u32(mapa_shared(smem_u32((const void*)peer_fills), 0), n_fill);
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 0 && lane == 0 && rank == 0) {
+    // Every fill of either CTA completes on CTA 0's full barriers.  After a
+    // time-out the two producers may have stopped at different fills (at
+    // most one ring apart): CTA 0 supplies the arrivals of the CTA that did
+    // not fill a stage, then waits (bounded) until the last ring round of
+    // fills has landed, so no copy is still writing into either CTA's
+    // shared memory when the CTAs exit.  Without a time-out both counts
+    // are equal and every wait returns at once.
+    const int n_other = *peer_fills;
+    const int n_lo = min(n_fill, n_other), n_hi = max(n_fill, n_other);
+    for (int i = n_lo; i < n_hi; ++i) {
+      if (i >= kRing)
+        mbar_wait(full0 + 8 * ((i - kRing) % kRing), (uint32_t)((i - kRing) / kRing) & 1, nullptr, nullptr, 0,
+                  100000000ull);
+      mbar_arrive(full0 + 8 * (i % kRing));
+    }
+    for (int i = max(0, n_hi - kRing); i < n_hi; ++i)
+      mbar_wait(full0 + 8 * (i % kRing), (uint32_t)(i / kRing) & 1, nullptr, nullptr, 0, 100000000ull);
   }
   __syncwarp();
-  tc_fence_before();
-  // Neither CTA leaves while the other can still multicast into it or
-  // arrive on its barriers.
+  // Neither CTA leaves (or frees its tensor memory) before the other is done
+  // with its barriers and shared memory.
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s) {
-  static bool attr_done[64] = {};
-  static int max_clusters[64] = {};
+  // One-time set-up per device (shared-memory opt-in, resident cluster
+  // count), safe under concurrent first calls from several host threads.
+  static std::once_flag once[64];
+  static cudaError_t setup_err[64];
+  static int max_clusters[64];
   int dev = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -516,22 +571,23 @@ cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
+  std::call_once(once[dev], [&] {
     cudaError_t e =
         cudaFuncSetAttribute(gemm_bf16_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_bf16_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-    if (e != cudaSuccess) return e;
-    // Clusters of two that fit on the device at once (one CTA per SM).
-    cfg.gridDim = dim3(2 * (num_sms() / 2));
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel<false>, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
+    if (e == cudaSuccess) {
+      // Clusters of two that fit on the device at once (one CTA per SM).
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(2 * (num_sms() / 2));
+      e = cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tc_kernel<false>, &q);
+    }
+    if (e == cudaSuccess && n < 1) e = cudaErrorInvalidConfiguration;
     max_clusters[dev] = n;
-    attr_done[dev] = true;
-  }
+    setup_err[dev] = e;
+  });
+  if (setup_err[dev] != cudaSuccess) return setup_err[dev];
   const int clusters = g.total_tiles < max_clusters[dev] ? g.total_tiles : max_clusters[dev];
   cfg.gridDim = dim3(2 * clusters);
   launch_begin(KID_GEMM, s);
