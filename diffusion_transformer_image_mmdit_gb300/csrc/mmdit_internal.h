@@ -8,12 +8,11 @@
 namespace mmdit {
 
 // ----------------------------------------------------------------- GEMM
-// Tile shape of the tcgen05 GEMM: 128 x 256 output tile per CTA, K blocks of
-// 64 bf16 (one 128-byte swizzle row), a 4-stage TMA ring.
+// Tile shape of the tcgen05 GEMM: 128 x 256 output tile per CTA (a CTA pair
+// computes 256 x 256), K blocks of 64 bf16 (one 128-byte swizzle row).
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 
 enum GemmMode : int {
   GM_STORE_BF16 = 0,  // out bf16, GELU on columns >= gelu_from
@@ -128,5 +127,15 @@ cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s);
 cudaError_t launch_attention(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, int d_head,
                              cudaStream_t s);
 int num_sms();
+
+// Status (an MMDIT_* code) of the current device for the kernels: sm_103,
+// the tensor-map encoder of the driver found, the status word reachable.
+int device_check();
+
+// Joint attention over prepared operands: q and k rows in qk [B][L][2D]
+// (normalised and rotated), v transposed in vT [B][D][Lpad]; writes out
+// [B][L][out_ld] bf16.  Returns an MMDIT_* status.
+int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint16_t* qk, const uint16_t* vT,
+                           uint16_t* out, long long out_ld, cudaStream_t st);
 
 }  // namespace mmdit

@@ -674,6 +674,107 @@ def test_sample_conditioning_acts_only_through_modulation_and_text():
     assert not np.array_equal(O.sample(x0, txt, y, 3.5, sig, W, sh), O.sample(x0, txt, y, 1.0, sig, W, sh))
 
 
+# ------------------------------------------------------------------ whole step composition
+# One denoising step in the order the Luminal blog's per-step operation list
+# (section "What the compiler found on its own") and its model description
+# (section "Flux.2 Klein 9B") give: timestep embedding, latent patch
+# projection, the double-stream blocks on separate text and image streams,
+# the concatenation [text; image], the single-stream blocks, the final
+# LayerNorm + modulate + projection on the image tokens, and the Euler update
+# of the sampler (section "The AMD MI300X pipeline").  Restated below with
+# torch library routines (F.linear, F.layer_norm, scaled_dot_product_attention)
+# and compared with the oracle's denoise_step.
+SH_STEP = O.Shape(B=2, L_txt=5, grid_h=3, grid_w=4, D=64, H=2, d_head=32, D_mlp=96, rope_axes=(8, 12, 12),
+                  C_lat=64, t_dim=32, n_double=2, n_single=2)
+
+
+def _step_case(sh):
+    """Weights scaled up (x10) so that every layer visibly moves the result;
+    C_lat = D so that a step that skips the patch projection still runs."""
+    W = S.embed_params(sh.D, sh.C_lat, sh.t_dim, seed=9)
+    W["double"] = [S.double_block_params(f"stp.d{i}", sh.D, sh.d_head, sh.D_mlp, 9) for i in range(sh.n_double)]
+    W["single"] = [S.single_block_params(f"stp.s{i}", sh.D, sh.d_head, sh.D_mlp, 9) for i in range(sh.n_single)]
+    for d in [W] + W["single"] + [blk[st] for blk in W["double"] for st in ("txt", "img")]:
+        for k in list(d):
+            if k.endswith("_w"):
+                d[k] = d[k] * 10.0
+    x_lat = rnd("stp.lat", (sh.B, sh.L_img, sh.C_lat))
+    x_txt = rnd("stp.txt", (sh.B, sh.L_txt, sh.D))
+    vec_add = rnd("stp.add", (sh.B, sh.D))
+    return W, x_lat, x_txt, vec_add
+
+
+def _torch_step(x_lat, x_txt, sigma, sigma_next, W, sh, vec_add):
+    T = torch.from_numpy
+    w = {k: T(v) for k, v in W.items() if isinstance(v, np.ndarray)}
+    half = sh.t_dim // 2
+    f = torch.exp(-math.log(10000.0) * torch.arange(half) / half)
+    a = torch.full((sh.B, 1), 1000.0 * sigma) * f[None]
+    vec = F.linear(F.silu(F.linear(torch.cat([a.cos(), a.sin()], 1), w["t_w1"], w["t_b1"])), w["t_w2"], w["t_b2"])
+    vec = vec + T(vec_add)
+    h_txt = x_txt
+    h_img = F.linear(T(x_lat), w["img_in_w"], w["img_in_b"]).numpy()
+    for blk in W["double"]:
+        h_txt, h_img = _torch_double(h_txt, h_img, vec.numpy(), blk, sh)
+    x = torch.cat([T(h_txt), T(h_img)], 1)
+    for blk in W["single"]:
+        x = T(_torch_single(x.numpy(), vec.numpy(), blk, sh))
+    m = F.linear(F.silu(vec), w["final_mod_w"], w["final_mod_b"]).unsqueeze(1).chunk(2, -1)
+    y = F.layer_norm(x[:, sh.L_txt:], (sh.D,), eps=sh.eps_ln) * (1 + m[1]) + m[0]
+    v = F.linear(y, w["final_w"], w["final_b"])
+    return (T(x_lat) + (sigma_next - sigma) * v).numpy(), v.numpy()
+
+
+def test_denoise_step_vs_torch_restatement():
+    sh = SH_STEP
+    W, x_lat, x_txt, vec_add = _step_case(sh)
+    sig = O.sigma_schedule(50, O.shift_mu(sh.L_img))
+    got_x, got_v = O.denoise_step(x_lat, x_txt, sig[3], sig[4], W, sh, vec_add=vec_add)
+    ref_x, ref_v = _torch_step(x_lat, x_txt, sig[3], sig[4], W, sh, vec_add)
+    assert rel(got_v, ref_v) < 1e-12, rel(got_v, ref_v)
+    assert rel(got_x - x_lat, ref_x - x_lat) < 1e-12
+    assert rel(got_x, x_lat) > 1e-3  # the step moves the latent
+
+
+def _step_variant(x_lat, x_txt, sigma, sigma_next, W, sh, vec_add=None, rnd=None, qin=None, *, final_head=False,
+                  skip_img_in=False, img_first=False, drop_vec_add=False):
+    """The step composed from the oracle's public pieces, with switches that
+    each plant one composition mistake (all off: the oracle's own step)."""
+    cos, sin = O.rope_tables(O.rope_ids(sh.L_txt, sh.grid_h, sh.grid_w), sh.rope_axes, sh.rope_theta)
+    vec = O.time_embed(sigma, W, sh)
+    if vec_add is not None and not drop_vec_add:
+        vec = vec + vec_add
+    h_img = np.asarray(x_lat, np.float64) if skip_img_in else O.img_in(x_lat, W)
+    h_txt = x_txt
+    for blk in W["double"]:
+        h_txt, h_img = O.double_block(h_txt, h_img, vec, blk, sh, cos, sin)
+    x = np.concatenate([h_img, h_txt] if img_first else [h_txt, h_img], axis=1)
+    for blk in W["single"]:
+        x = O.single_block(x, vec, blk, sh, cos, sin)
+    img = x[:, :sh.L_img] if (img_first or final_head) else x[:, sh.L_txt:]
+    v = O.final_layer(img, vec, W, sh)
+    return O.euler_step(x_lat, v, sigma, sigma_next), v
+
+
+def test_step_variant_without_switches_is_the_oracle_step():
+    sh = SH_STEP
+    W, x_lat, x_txt, vec_add = _step_case(sh)
+    a = O.denoise_step(x_lat, x_txt, 0.7, 0.65, W, sh, vec_add=vec_add)
+    b = _step_variant(x_lat, x_txt, 0.7, 0.65, W, sh, vec_add)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("mistake", ["final_head", "skip_img_in", "img_first", "drop_vec_add"])
+def test_planted_step_composition_mistakes_are_caught(monkeypatch, mistake):
+    """Each plant: the final layer reading the first L_img rows (text
+    included) instead of the image slice; the patch projection skipped; the
+    sequence concatenated as [image; text]; the conditioning vector dropped."""
+    def planted(*args, **kw):
+        return _step_variant(*args, **kw, **{mistake: True})
+
+    _planted(monkeypatch, "denoise_step", planted, test_denoise_step_vs_torch_restatement)
+
+
 # ------------------------------------------------------------------ int8 quantiser
 def test_quantize_w8_invariants():
     w = S.normal_bf16("q.w", (64, 96), 0.02)
