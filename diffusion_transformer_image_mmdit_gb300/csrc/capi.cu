@@ -179,12 +179,13 @@ static int check_shape(const mmdit_shape_t* s, Dims* out) {
   return MMDIT_OK;
 }
 
-static int check_device() {
+int device_check() {
   if (!device_ok()) return MMDIT_ERR_UNSUPPORTED;
   if (!encode_fn()) return MMDIT_ERR_UNSUPPORTED;
   if (!device_status_ptr()) return MMDIT_ERR_CUDA;
   return MMDIT_OK;
 }
+static int check_device() { return device_check(); }
 
 static bool lin_ok(const mmdit_linear_t& l, bool want_i8) {
   if (!l.w || !al16(l.w)) return false;
@@ -297,27 +298,35 @@ static GemmParams gemm_params(int mode) {
 }
 
 // ----------------------------------------------------------------- attention
-static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, uint16_t* out, long long out_ld,
-                         cudaStream_t st) {
+int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint16_t* qk, const uint16_t* vT,
+                           uint16_t* out, long long out_ld, cudaStream_t st) {
   CUtensorMap tq, tv;
-  const uint64_t D2 = 2ull * d.D;
-  if (!make_tmap_3d(&tq, qk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D2, (uint64_t)d.L, (uint64_t)d.B, D2 * 2,
-                    D2 * 2 * d.L, 64, kAttnBM, true))
+  const int D = H * d_head;
+  const uint64_t D2 = 2ull * D;
+  if (!make_tmap_3d(&tq, qk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D2, (uint64_t)L, (uint64_t)B, D2 * 2, D2 * 2 * L,
+                    64, kAttnBM, true))
     return MMDIT_ERR_ALIGN;
-  if (!make_tmap_3d(&tv, vT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)d.L, (uint64_t)d.D, (uint64_t)d.B,
-                    (uint64_t)d.Lpad * 2, (uint64_t)d.Lpad * 2 * d.D, 64, (uint32_t)d.d, true))
+  // The key extent of V^T is L (not Lpad): keys at or beyond L read as zeros.
+  if (!make_tmap_3d(&tv, vT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)L, (uint64_t)D, (uint64_t)B,
+                    (uint64_t)Lpad * 2, (uint64_t)Lpad * 2 * D, 64, (uint32_t)d_head, true))
     return MMDIT_ERR_ALIGN;
   AttnParams p;
-  p.L = d.L;
-  p.H = d.H;
-  p.B = d.B;
-  p.n_q_tiles = (d.L + kAttnBM - 1) / kAttnBM;
-  p.n_kv_tiles = (d.L + kAttnBN - 1) / kAttnBN;
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.d));
+  std::memset(&p, 0, sizeof(p));
+  p.L = L;
+  p.H = H;
+  p.B = B;
+  p.n_q_tiles = (L + kAttnBM - 1) / kAttnBM;
+  p.n_kv_tiles = (L + kAttnBN - 1) / kAttnBN;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d_head));
   p.out = out;
   p.out_ld = out_ld;
   p.status = device_status_ptr();
-  return cuda_status(launch_attention(tq, tv, p, d.d, st));
+  return cuda_status(launch_attention(tq, tv, p, d_head, st));
+}
+
+static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, uint16_t* out, long long out_ld,
+                         cudaStream_t st) {
+  return run_attention_prepared(d.B, d.L, d.H, d.d, d.Lpad, qk, vT, out, out_ld, st);
 }
 
 // ----------------------------------------------------------------- workspace layouts
@@ -1052,6 +1061,20 @@ int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdi
   if (graph_def) cudaGraphDestroy(graph_def);
   cudaStreamDestroy(cs);
   return rc;
+}
+
+double mmdit_shift_mu(int n_image_tokens) {
+  return 0.5 + ((double)n_image_tokens - 256.0) * (1.15 - 0.5) / (4096.0 - 256.0);
+}
+
+int mmdit_sigma_schedule(int n_steps, double mu, double* sigmas) {
+  if (n_steps < 1 || !sigmas) return MMDIT_ERR_ARG;
+  const double s = std::exp(mu);
+  for (int i = 0; i <= n_steps; ++i) {
+    const double t = 1.0 - (double)i / n_steps;
+    sigmas[i] = s * t / (1.0 + (s - 1.0) * t);
+  }
+  return MMDIT_OK;
 }
 
 int mmdit_selftest_wait_timeout(unsigned limit_us, void* stream) {

@@ -1,26 +1,18 @@
-"""Host-side sigma schedule of the flow-matching sampler.
-
-The pages name an Euler sampler but print no schedule.  Reading taken (the
-common shifted-linear choice for Flux-style models): t_i = 1 - i/n for
-i = 0..n, sigma_i = s t_i / (1 + (s - 1) t_i) with s = exp(mu), and mu
-linear in the image-token count through (256, 0.5) and (4096, 1.15).
-The kernels only consume (sigma_i, sigma_{i+1}) pairs.
-"""
+"""The sampler's sigma schedule, computed by the library (mmdit_shift_mu,
+mmdit_sigma_schedule in include/mmdit.h); this module only marshals it."""
 from __future__ import annotations
 
-import math
+import ctypes
 from typing import List
+
+from . import _lib
 
 
 def mu_for_tokens(n_img_tokens: int) -> float:
-    slope = (1.15 - 0.5) / (4096.0 - 256.0)
-    return 0.5 + slope * (n_img_tokens - 256.0)
+    return float(_lib.load().mmdit_shift_mu(int(n_img_tokens)))
 
 
 def sigmas(n_steps: int, mu: float) -> List[float]:
-    s = math.exp(mu)
-    out = []
-    for i in range(n_steps + 1):
-        t = 1.0 - i / n_steps
-        out.append(s * t / (1.0 + (s - 1.0) * t))
-    return out
+    out = (ctypes.c_double * (n_steps + 1))()
+    _lib.call("mmdit_sigma_schedule", int(n_steps), float(mu), out)
+    return list(out)

@@ -264,6 +264,21 @@ int mmdit_single_block_fwd(const mmdit_shape_t* shape, const mmdit_single_w_t* w
 int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_txt_in,
                    double sigma, double sigma_next, float* v_out, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------ sigma schedule */
+/* The sampler's noise levels.  The Luminal blog (section "The AMD MI300X
+ * pipeline") integrates the latent with an Euler sampler, and the flux-amd-rocm
+ * benchmark notes run 28 steps; no page prints the schedule.  Reading taken
+ * (the shifted-linear schedule of Flux-style models): t_i = 1 - i / n_steps,
+ * sigma_i = s t_i / (1 + (s - 1) t_i) with s = exp(mu), i = 0 .. n_steps, so
+ * sigma_0 = 1, sigma_n = 0; mu is linear in the image-token count through
+ * (256, 0.5) and (4096, 1.15).  Host arithmetic in double precision; no
+ * device work, callable without a GPU.
+ * mmdit_shift_mu: mu for n_image_tokens (any value; no error case).
+ * mmdit_sigma_schedule: writes sigmas[0 .. n_steps] (host array of n_steps + 1
+ * doubles, caller-owned); MMDIT_ERR_ARG for n_steps < 1 or a NULL array. */
+double mmdit_shift_mu(int n_image_tokens);
+int mmdit_sigma_schedule(int n_steps, double mu, double* sigmas);
+
 /* ------------------------------------------------------------ sampling loop */
 /* Conditioning around the denoiser.  The SGLang blog ("Architecture") has a
  * text encoder produce the conditioning embeddings that the DiT denoises

@@ -1,18 +1,28 @@
 """Host logic of the product path checked against the oracle on CPU: the
-sigma schedule, and the benchmark's FLOP accounting against the per-block
-formula 24 L D^2 + 4 L^2 D."""
+library's sigma schedule (host code behind the C ABI, no GPU needed), and the
+benchmark's FLOP accounting against the per-block formula 24 L D^2 + 4 L^2 D."""
 import numpy as np
+import pytest
 
 from diffusion_transformer_image_mmdit_gb300 import schedule
 from oracle import mmdit_oracle as O
 
 
-def test_schedule_matches_oracle():
+@pytest.fixture(scope="module")
+def built():
+    from diffusion_transformer_image_mmdit_gb300 import build
+    build.build()
+
+
+def test_schedule_matches_oracle(built):
     for n, tokens in ((50, 6889), (28, 4096), (4, 1024)):
         got = np.array(schedule.sigmas(n, schedule.mu_for_tokens(tokens)))
         ref = O.sigma_schedule(n, O.shift_mu(tokens))
         assert np.abs(got - ref).max() < 1e-15
     assert schedule.sigmas(4, 0.0) == [1.0, 0.75, 0.5, 0.25, 0.0]
+    from diffusion_transformer_image_mmdit_gb300 import _lib
+    with pytest.raises(_lib.MMDiTError):
+        schedule.sigmas(0, 0.0)
 
 
 def test_bench_flop_accounting():
