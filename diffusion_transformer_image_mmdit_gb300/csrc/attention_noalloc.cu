@@ -23,9 +23,6 @@
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (with that device current) and caches it; make
 //    that first call before any stream capture.
-#include <cmath>
-#include <cstring>
-
 #include "elementwise.h"
 #include "mmdit.h"
 #include "mmdit_internal.h"
@@ -80,16 +77,14 @@ extern "C" int joint_attention_fwd_noalloc(const mmdit_shape_t* shape, const voi
   const float* gk1 = k_norm ? k_norm[1] : nullptr;
   if (gq0 && (!gq1 || !gk0 || !gk1)) return MMDIT_ERR_ARG;
 
+  // Same device checks as every other entry point (sm_103, the driver's
+  // tensor-map encoder, the status word) before anything is launched.
+  const int dc = device_check();
+  if (dc != MMDIT_OK) return dc;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MMDIT_ERR_CUDA;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return MMDIT_ERR_CUDA;
-  if (major != 10 || minor != 3) return MMDIT_ERR_UNSUPPORTED;
   unsigned char* base = static_cast<unsigned char*>(scratch_address(dev));
-  unsigned* status = device_status_ptr();
-  if (!base || !status) return MMDIT_ERR_CUDA;
+  if (!base) return MMDIT_ERR_CUDA;
 
   // Same carving as the workspace variant: qk [B][L][2D], then vT [B][D][Lpad], 256-byte aligned.
   const size_t qk_bytes = (size_t)B * L * 2 * D * 2;
@@ -99,25 +94,5 @@ extern "C" int joint_attention_fwd_noalloc(const mmdit_shape_t* shape, const voi
   if (launch_attn_prep(static_cast<const uint16_t*>(qkv), qkv_row_stride, B, L, Lt, H, d, gq0, gq1, gk0, gk1,
                        shape->eps_rms, cos_, sin_, qk, vT, Lpad, s) != cudaSuccess)
     return MMDIT_ERR_CUDA;
-
-  CUtensorMap tq, tv;
-  const uint64_t D2 = 2ull * D;
-  if (!make_tmap_3d(&tq, qk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D2, (uint64_t)L, (uint64_t)B, D2 * 2, D2 * 2 * L, 64,
-                    kAttnBM, true))
-    return MMDIT_ERR_ALIGN;
-  if (!make_tmap_3d(&tv, vT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)L, (uint64_t)D, (uint64_t)B,
-                    (uint64_t)Lpad * 2, (uint64_t)Lpad * 2 * D, 64, (uint32_t)d, true))
-    return MMDIT_ERR_ALIGN;
-  AttnParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.L = L;
-  p.H = H;
-  p.B = B;
-  p.n_q_tiles = (L + kAttnBM - 1) / kAttnBM;
-  p.n_kv_tiles = (L + kAttnBN - 1) / kAttnBN;
-  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  p.out = static_cast<uint16_t*>(out);
-  p.out_ld = out_row_stride;
-  p.status = status;
-  return launch_attention(tq, tv, p, d, s) == cudaSuccess ? MMDIT_OK : MMDIT_ERR_CUDA;
+  return run_attention_prepared(B, L, H, d, Lpad, qk, vT, static_cast<uint16_t*>(out), out_row_stride, s);
 }

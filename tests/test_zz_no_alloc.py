@@ -9,7 +9,9 @@ import pytest
 import torch
 
 from diffusion_transformer_image_mmdit_gb300 import _lib, api, synthetic as S
-from tests.gpu_common import CONFIGS, FULL, api_shape, assert_close, bf16, check_status, f32, gpu_tables, host, need_gpu
+from oracle import mmdit_oracle as O
+from tests.gpu_common import (CONFIGS, FULL, api_shape, assert_close, bf16, check_status, f32, gpu_tables, host, need_gpu,
+                              tables)
 
 pytestmark = pytest.mark.gpu
 
@@ -17,9 +19,22 @@ pytestmark = pytest.mark.gpu
 def _inputs(cfg, tag):
     shape = api_shape(cfg)
     B, L, H, d, D = cfg["B"], api.seq_len(shape), cfg["H"], cfg["d_head"], cfg["D"]
-    qkv = bf16(S.normal_bf16(f"na.{tag}", (B, L, 3 * D)))
-    g = [f32(S.norm_gain(f"na.{tag}.g{i}", d)) for i in range(4)]
-    return shape, qkv, [g[0], g[1]], [g[2], g[3]]
+    qkv_h = S.normal_bf16(f"na.{tag}", (B, L, 3 * D))
+    g_h = [S.norm_gain(f"na.{tag}.g{i}", d) for i in range(4)]
+    return shape, bf16(qkv_h), [f32(g_h[0]), f32(g_h[1])], [f32(g_h[2]), f32(g_h[3])], qkv_h, g_h
+
+
+def _oracle(cfg, qkv_h, g):
+    """The float64 oracle of the same attention: per-stream RMSNorm of q and
+    k (text gains for the first L_txt tokens), RoPE, softmax attention."""
+    B, H, d, D, Lt = cfg["B"], cfg["H"], cfg["d_head"], cfg["D"], cfg["L_txt"]
+    L = qkv_h.shape[1]
+    x = qkv_h.reshape(B, L, 3, H, d)
+    q, k, v = x[:, :, 0], x[:, :, 1], x[:, :, 2]
+    q = np.concatenate([O.rms_norm(q[:, :Lt], g[0], 1e-6), O.rms_norm(q[:, Lt:], g[1], 1e-6)], axis=1)
+    k = np.concatenate([O.rms_norm(k[:, :Lt], g[2], 1e-6), O.rms_norm(k[:, Lt:], g[3], 1e-6)], axis=1)
+    c, s = tables(cfg)
+    return O.attention(O.rope_apply(q, c, s), O.rope_apply(k, c, s), v).reshape(B, L, D)
 
 
 def _with_workspace(shape, qkv, qn, kn, cs, sn):
@@ -39,14 +54,18 @@ def _no_alloc(shape, qkv, qn, kn, cs, sn):
 
 @pytest.mark.parametrize("name", ["d128", "c1"])
 def test_no_alloc_matches_workspace_variant_on_consecutive_calls(name):
+    """Both variants run the same kernels on the same inputs, so their outputs
+    must be identical bit for bit; each is also checked against the oracle
+    at the bf16 bar."""
     need_gpu()
     cfg = CONFIGS[name]
     for call in range(2):  # the second call runs on scratch the first one left behind
-        shape, qkv, qn, kn = _inputs(cfg, f"{name}.{call}")
+        shape, qkv, qn, kn, qkv_h, g_h = _inputs(cfg, f"{name}.{call}")
         _, cs, sn = gpu_tables(shape)
         ref = host(_with_workspace(shape, qkv, qn, kn, cs, sn))
         got = host(_no_alloc(shape, qkv, qn, kn, cs, sn))
-        assert_close(got, ref, what=f"no-alloc attention, call {call + 1}")
+        assert np.array_equal(got, ref), f"no-alloc attention differs from the workspace variant, call {call + 1}"
+        assert_close(got, _oracle(cfg, qkv_h, g_h), what=f"no-alloc attention vs oracle, call {call + 1}")
     check_status()
 
 
