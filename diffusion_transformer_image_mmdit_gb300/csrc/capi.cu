@@ -435,17 +435,22 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     p.ascale = ws.as + row0;
     return ws.a8 + row0 * K;
   };
-  // LN + modulate of stream i; with FP8 it writes the e4m3 rows and their scales straight into ws.a8 / ws.as
-  // (at the stream's row offset) instead of bf16 rows
-  auto ln_mod = [&](int i, const float* shift, const float* scale) -> int {
-    const long long r0 = (long long)off[i] * d.B;
-    return cuda_status(launch_ln_modulate(xs[i], xseg[i], Ls[i], d.B, D, shift, scale, 6 * D, s.eps_ln,
-                                          d.f8 ? nullptr : yp(i), st, d.f8 ? ws.a8 + r0 * D : nullptr,
-                                          d.f8 ? ws.as + r0 : nullptr));
+  // LN + modulate of both streams in one launch at modulation chunk c (shift c, scale c + 1); with FP8 it
+  // writes the e4m3 rows and their scales straight into ws.a8 / ws.as (at each stream's row offset) instead
+  // of bf16 rows
+  auto ln_mod = [&](int c) -> int {
+    LnJob jobs[2];
+    int n = 0;
+    for (int i = first; i < 2; ++i) {
+      const long long r0 = (long long)off[i] * d.B;
+      jobs[n++] = LnJob{xs[i], xseg[i], Ls[i], d.B, modp(i) + (size_t)c * D, modp(i) + (size_t)(c + 1) * D, 6 * D,
+                        d.f8 ? nullptr : yp(i), d.f8 ? ws.a8 + r0 * D : nullptr, d.f8 ? ws.as + r0 : nullptr};
+    }
+    return cuda_status(launch_ln_modulate_jobs(jobs, n, D, s.eps_ln, st));
   };
   GemmProblem pr[2];
   // LN + modulate, then the fused QKV / RMSNorm / RoPE GEMM
-  for (int i = first; i < 2; ++i) MMDIT_TRY(ln_mod(i, modp(i), modp(i) + D));
+  MMDIT_TRY(ln_mod(0));
   for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(GM_QKV);
     p.out_seg_rows = d.L;
@@ -480,7 +485,7 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
   }
   MMDIT_TRY(grouped(pr));
   // y2 = LN(x)(1 + scale2) + shift2; h = GELU(y2 W1^T + b1)
-  for (int i = first; i < 2; ++i) MMDIT_TRY(ln_mod(i, modp(i) + 3 * D, modp(i) + 4 * D));
+  MMDIT_TRY(ln_mod(3));
   for (int i = first; i < 2; ++i) {
     GemmParams p = gemm_params(d.swiglu ? GM_SWIGLU : GM_STORE_BF16);
     p.gelu_from = 0;

@@ -37,22 +37,25 @@ __device__ __forceinline__ uint16_t f8x2_e4m3(float lo, float hi) {
 // barrier), and the row stays in registers between the two passes.  fp32
 // statistics, the variance from the centred values.
 //
+// One launch serves up to two jobs (the text and image streams of a double
+// block at one LN position): warp rows [0, n0) belong to job 0, the rest to
+// job 1, so no launch is as short as one stream's text rows.
+//
 // F8: the row is also quantised to e4m3 the way the standalone row quantiser
 // does it from the stored bf16 values: s = max|bf16(y)| / 448 (1 for a zero
 // row), q = e4m3(bf16(y) / s), written to q (row stride D) and qs; the bf16
 // row is stored only when y is given.
 template <int NV, bool F8>
-__global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x, long long x_seg_rows, int rows,
-                                                     int n_rows, const float* __restrict__ shift,
-                                                     const float* __restrict__ scale, long long mod_stride, float eps,
-                                                     uint16_t* __restrict__ y, uint8_t* __restrict__ q,
-                                                     float* __restrict__ qs) {
+__global__ void __launch_bounds__(128) ln_mod_kernel(const __grid_constant__ LnJobs J) {
   constexpr int D = NV * 128;
-  const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int grow = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= n_rows) return;
-  const int seg = row / rows, i = row - seg * rows;
-  const float4* xr = reinterpret_cast<const float4*>(x + ((long long)seg * x_seg_rows + i) * D) + lane;
+  if (grow >= J.n_total) return;
+  const int jb = grow < J.n0 ? 0 : 1;
+  const LnJob& jo = J.job[jb];
+  const int row = grow - (jb ? J.n0 : 0);  // row of this job (output row)
+  const int seg = row / jo.rows, i = row - seg * jo.rows;
+  const float4* xr = reinterpret_cast<const float4*>(jo.x + ((long long)seg * jo.x_seg_rows + i) * D) + lane;
   float4 v[NV];
 #pragma unroll
   for (int c = 0; c < NV; ++c) v[c] = __ldg(xr + 32 * c);
@@ -67,10 +70,10 @@ __global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x
     v[c].x -= mean, v[c].y -= mean, v[c].z -= mean, v[c].w -= mean;
     ss = fmaf(v[c].x, v[c].x, fmaf(v[c].y, v[c].y, fmaf(v[c].z, v[c].z, fmaf(v[c].w, v[c].w, ss))));
   }
-  const float rstd = rsqrtf(warp_sum(ss) * inv_d + eps);
-  const float4* sc4 = reinterpret_cast<const float4*>(scale + (long long)seg * mod_stride) + lane;
-  const float4* sh4 = reinterpret_cast<const float4*>(shift + (long long)seg * mod_stride) + lane;
-  uint2* yr = y ? reinterpret_cast<uint2*>(y + (long long)row * D) + lane : nullptr;
+  const float rstd = rsqrtf(warp_sum(ss) * inv_d + J.eps);
+  const float4* sc4 = reinterpret_cast<const float4*>(jo.scale + (long long)seg * jo.mod_stride) + lane;
+  const float4* sh4 = reinterpret_cast<const float4*>(jo.shift + (long long)seg * jo.mod_stride) + lane;
+  uint2* yr = jo.y ? reinterpret_cast<uint2*>(jo.y + (long long)row * D) + lane : nullptr;
   float amax = 0.f;
 #pragma unroll
   for (int c = 0; c < NV; ++c) {
@@ -86,13 +89,13 @@ __global__ void __launch_bounds__(128) ln_mod_kernel(const float* __restrict__ x
   }
   if (F8) {
     amax = warp_max(amax);
-    const float s = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
-    if (lane == 0) qs[row] = s;
-    uint32_t* qr = reinterpret_cast<uint32_t*>(q + (long long)row * D) + lane;
+    const float sq = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    if (lane == 0) jo.qs[row] = sq;
+    uint32_t* qr = reinterpret_cast<uint32_t*>(jo.q + (long long)row * D) + lane;
 #pragma unroll
     for (int c = 0; c < NV; ++c)
-      qr[32 * c] = (uint32_t)f8x2_e4m3(__fdiv_rn(v[c].x, s), __fdiv_rn(v[c].y, s)) |
-                   ((uint32_t)f8x2_e4m3(__fdiv_rn(v[c].z, s), __fdiv_rn(v[c].w, s)) << 16);
+      qr[32 * c] = (uint32_t)f8x2_e4m3(__fdiv_rn(v[c].x, sq), __fdiv_rn(v[c].y, sq)) |
+                   ((uint32_t)f8x2_e4m3(__fdiv_rn(v[c].z, sq), __fdiv_rn(v[c].w, sq)) << 16);
   }
 }
 
@@ -597,24 +600,34 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned* status, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
-                               const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st,
-                               uint8_t* q, float* qs) {
+cudaError_t launch_ln_modulate_jobs(const LnJob* jobs, int n_jobs, int D, float eps, cudaStream_t st) {
   // D / 128 is then one of the even cases 2 .. 32 below
-  if (D % 256 || D < 256 || D > 4096 || rows < 1 || n_seg < 1) return cudaErrorInvalidValue;
-  if ((q == nullptr) != (qs == nullptr) || (!q && !y)) return cudaErrorInvalidValue;
-  const int n_rows = rows * n_seg;
-  const int blocks = (n_rows + 3) / 4;  // four rows (warps) per CTA
+  if (D % 256 || D < 256 || D > 4096 || n_jobs < 1 || n_jobs > 2) return cudaErrorInvalidValue;
+  LnJobs J;
+  J.n0 = 0;
+  J.n_total = 0;
+  J.eps = eps;
+  bool f8 = false;
+  for (int k = 0; k < n_jobs; ++k) {
+    const LnJob& jo = jobs[k];
+    if (jo.rows < 1 || jo.n_seg < 1) return cudaErrorInvalidValue;
+    if ((jo.q == nullptr) != (jo.qs == nullptr) || (!jo.q && !jo.y)) return cudaErrorInvalidValue;
+    if (k > 0 && (jo.q != nullptr) != f8) return cudaErrorInvalidValue;  // one output kind per launch
+    f8 = jo.q != nullptr;
+    J.job[k] = jo;
+    J.n_total += jo.rows * jo.n_seg;
+    if (k == 0) J.n0 = J.n_total;
+  }
+  if (n_jobs == 1) J.job[1] = J.job[0];
+  const int blocks = (J.n_total + 3) / 4;  // four rows (warps) per CTA
   launch_begin(KID_LN_MODULATE, st);
   switch (D / 128) {
-#define MMDIT_LN_CASE(nv)                                                                                 \
-  case nv:                                                                                                \
-    if (q)                                                                                                \
-      ln_mod_kernel<nv, true><<<blocks, 128, 0, st>>>(x, x_seg_rows, rows, n_rows, shift, scale, mod_stride, eps, \
-                                                       y, q, qs);                                        \
-    else                                                                                                  \
-      ln_mod_kernel<nv, false><<<blocks, 128, 0, st>>>(x, x_seg_rows, rows, n_rows, shift, scale, mod_stride,   \
-                                                        eps, y, nullptr, nullptr);                       \
+#define MMDIT_LN_CASE(nv)                                        \
+  case nv:                                                       \
+    if (f8)                                                      \
+      ln_mod_kernel<nv, true><<<blocks, 128, 0, st>>>(J);        \
+    else                                                         \
+      ln_mod_kernel<nv, false><<<blocks, 128, 0, st>>>(J);       \
     break;
     MMDIT_LN_CASE(2) MMDIT_LN_CASE(4) MMDIT_LN_CASE(6) MMDIT_LN_CASE(8) MMDIT_LN_CASE(10) MMDIT_LN_CASE(12)
     MMDIT_LN_CASE(14) MMDIT_LN_CASE(16) MMDIT_LN_CASE(18) MMDIT_LN_CASE(20) MMDIT_LN_CASE(22) MMDIT_LN_CASE(24)
@@ -625,6 +638,13 @@ cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, i
   }
   launch_end(st);
   return cudaGetLastError();
+}
+
+cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
+                               const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st,
+                               uint8_t* q, float* qs) {
+  LnJob jo{x, x_seg_rows, rows, n_seg, shift, scale, mod_stride, y, q, qs};
+  return launch_ln_modulate_jobs(&jo, 1, D, eps, st);
 }
 
 // CTAs of a GEMV kernel that are resident at once (the grid-stride loop

@@ -9,6 +9,24 @@ namespace mmdit {
 // y[seg][i] = LN(x[seg*x_seg_rows + i]) (1 + scale[seg]) + shift[seg]; D % 256 == 0, D <= 4096.
 // With q and qs: also the e4m3 rows of the bf16 result (row scale max|y| / 448 into qs[row], codes into
 // q[row * D ..]); y may then be null (bf16 rows not stored).
+struct LnJob {
+  const float* x;
+  long long x_seg_rows;
+  int rows, n_seg;  // rows per segment (sample), segments
+  const float* shift;
+  const float* scale;  // modulation of segment s at shift / scale + s * mod_stride
+  long long mod_stride;
+  uint16_t* y;  // output row r (r = s * rows + i) at y + r * D
+  uint8_t* q;
+  float* qs;
+};
+struct LnJobs {
+  LnJob job[2];
+  int n0, n_total;  // rows of job 0; rows of both jobs
+  float eps;
+};
+// One launch over one or two jobs with the same D and output kind (bf16 or e4m3 rows).
+cudaError_t launch_ln_modulate_jobs(const LnJob* jobs, int n_jobs, int D, float eps, cudaStream_t st);
 cudaError_t launch_ln_modulate(const float* x, long long x_seg_rows, int rows, int n_seg, int D, const float* shift,
                                const float* scale, long long mod_stride, float eps, uint16_t* y, cudaStream_t st,
                                uint8_t* q = nullptr, float* qs = nullptr);
