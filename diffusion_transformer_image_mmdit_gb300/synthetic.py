@@ -126,39 +126,46 @@ def normal_f32(name: str, shape, std: float = 1.0, mean: float = 0.0, seed: int 
 W_STD = 0.02
 
 
-def linear_params(prefix: str, n_out: int, n_in: int, seed: int = 0):
-    return (normal_bf16(prefix + ".w", (n_out, n_in), W_STD, seed=seed),
-            normal_bf16(prefix + ".b", (n_out,), W_STD, seed=seed))
+def linear_params(prefix: str, n_out: int, n_in: int, seed: int = 0, f32: bool = False):
+    """f32: the same draws rounded to float32 instead of bf16 (a float32-weight
+    model; the kernels then take bf16 operands of these weights)."""
+    r = normal_f32 if f32 else normal_bf16
+    return (r(prefix + ".w", (n_out, n_in), W_STD, seed=seed), r(prefix + ".b", (n_out,), W_STD, seed=seed))
 
 
 def norm_gain(prefix: str, d: int, seed: int = 0):
     return normal_f32(prefix, (d,), W_STD, mean=1.0, seed=seed)
 
 
-def double_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int = 0, mlp: str = "gelu") -> dict:
-    """mlp = "swiglu": the first MLP projection has 2 D_mlp output rows [gate; up]."""
+def double_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int = 0, mlp: str = "gelu",
+                        f32: bool = False) -> dict:
+    """mlp = "swiglu": the first MLP projection has 2 D_mlp output rows [gate; up].
+    f32: float32 weights and biases (see linear_params)."""
     n_in = 2 * D_mlp if mlp == "swiglu" else D_mlp
     out = {}
     for s in ("txt", "img"):
         p = f"{prefix}.{s}"
         w = {}
-        w["mod_w"], w["mod_b"] = linear_params(p + ".mod", 6 * D, D, seed)
-        w["qkv_w"], w["qkv_b"] = linear_params(p + ".qkv", 3 * D, D, seed)
-        w["proj_w"], w["proj_b"] = linear_params(p + ".proj", D, D, seed)
-        w["mlp_in_w"], w["mlp_in_b"] = linear_params(p + ".mlp_in", n_in, D, seed)
-        w["mlp_out_w"], w["mlp_out_b"] = linear_params(p + ".mlp_out", D, D_mlp, seed)
+        w["mod_w"], w["mod_b"] = linear_params(p + ".mod", 6 * D, D, seed, f32)
+        w["qkv_w"], w["qkv_b"] = linear_params(p + ".qkv", 3 * D, D, seed, f32)
+        w["proj_w"], w["proj_b"] = linear_params(p + ".proj", D, D, seed, f32)
+        w["mlp_in_w"], w["mlp_in_b"] = linear_params(p + ".mlp_in", n_in, D, seed, f32)
+        w["mlp_out_w"], w["mlp_out_b"] = linear_params(p + ".mlp_out", D, D_mlp, seed, f32)
         w["q_norm"] = norm_gain(p + ".q_norm", d_head, seed)
         w["k_norm"] = norm_gain(p + ".k_norm", d_head, seed)
         out[s] = w
     return out
 
 
-def single_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int = 0, mlp: str = "gelu") -> dict:
-    """mlp = "swiglu": lin1 has 3 D + 2 D_mlp output rows [q; k; v; gate; up]."""
+def single_block_params(prefix: str, D: int, d_head: int, D_mlp: int, seed: int = 0, mlp: str = "gelu",
+                        f32: bool = False) -> dict:
+    """mlp = "swiglu": lin1 has 3 D + 2 D_mlp output rows [q; k; v; gate; up].
+    f32: float32 weights and biases (see linear_params)."""
     w = {}
-    w["mod_w"], w["mod_b"] = linear_params(prefix + ".mod", 3 * D, D, seed)
-    w["lin1_w"], w["lin1_b"] = linear_params(prefix + ".lin1", 3 * D + (2 if mlp == "swiglu" else 1) * D_mlp, D, seed)
-    w["lin2_w"], w["lin2_b"] = linear_params(prefix + ".lin2", D, D + D_mlp, seed)
+    w["mod_w"], w["mod_b"] = linear_params(prefix + ".mod", 3 * D, D, seed, f32)
+    w["lin1_w"], w["lin1_b"] = linear_params(prefix + ".lin1", 3 * D + (2 if mlp == "swiglu" else 1) * D_mlp, D,
+                                             seed, f32)
+    w["lin2_w"], w["lin2_b"] = linear_params(prefix + ".lin2", D, D + D_mlp, seed, f32)
     w["q_norm"] = norm_gain(prefix + ".q_norm", d_head, seed)
     w["k_norm"] = norm_gain(prefix + ".k_norm", d_head, seed)
     return w

@@ -3,6 +3,8 @@ metrics.  The oracle sees exactly the values the kernels read (bf16-rounded
 weights, fp32 activations)."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -70,9 +72,20 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
+def report(line: str) -> None:
+    """Prints a measured parity figure (shown by pytest for failures, or with
+    -rP) and appends it to the file named by MMDIT_PARITY_LOG when set."""
+    print(line)
+    path = os.environ.get("MMDIT_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(line + "\n")
+
+
 def assert_close(gpu, ref, rel=REL_L2, max_abs=MAX_ABS, what=""):
     r = rel_l2(gpu, ref)
     m = float(np.abs(np.asarray(gpu, np.float64) - np.asarray(ref, np.float64)).max()) if np.size(ref) else 0.0
+    report(f"PARITY {what}: rel_l2={r:.3e} (bar {rel:.3g}) max_abs={m:.3e} (bar {max_abs:.3g})")
     assert np.all(np.isfinite(gpu)), f"{what}: non-finite output"
     assert r <= rel and m <= max_abs, f"{what}: rel_l2={r:.3e} (<= {rel}) max_abs={m:.3e} (<= {max_abs})"
     return r, m

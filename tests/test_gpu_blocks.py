@@ -10,8 +10,8 @@ import torch
 from diffusion_transformer_image_mmdit_gb300 import api, synthetic as S, weights as Wt
 from oracle import mmdit_oracle as O
 from tests.test_gpu_kernels import decode_e4m3
-from tests.gpu_common import (CONFIGS, FULL, MAX_ABS, REL_L2_INT8_SCHEME, api_shape, assert_close, bf16, check_status, f32,
-                              gpu_tables, host, need_gpu, oracle_shape, rel_l2, tables)
+from tests.gpu_common import (CONFIGS, FULL, MAX_ABS, REL_L2, REL_L2_INT8_SCHEME, api_shape, assert_close, bf16, check_status, f32,
+                              gpu_tables, host, need_gpu, oracle_shape, rel_l2, report, tables)
 
 pytestmark = pytest.mark.gpu
 
@@ -96,6 +96,31 @@ def test_single_block(name):
     g, _ = run_single(cfg, p, x, vec)
     c, s = tables(cfg)
     assert_close(g, O.single_block(x, vec, p, sh, c, s), what=f"single {name}")
+
+
+def test_c1_fp32_weights():
+    """The tiny config as stated, with float32 weights and biases: the kernels
+    take bf16 operands of the float32 weights (fp32 biases), the oracle runs on
+    the float32 weights themselves.  Checked at the bf16 bar on the block
+    outputs and, stricter, on the residual update of each stream."""
+    cfg = CONFIGS["c1"]
+    sh = oracle_shape(cfg)
+    c, s = tables(cfg)
+    p = S.double_block_params("c1.f32", cfg["D"], cfg["d_head"], cfg["D_mlp"], f32=True)
+    a = S.activations(cfg["B"], cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, _ = run_double(cfg, p, a)
+    rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s)
+    assert_close(gt, rt, what="c1 fp32-weight double x_txt")
+    assert_close(gi, ri, what="c1 fp32-weight double x_img")
+    assert rel_l2(gt - a["x_txt"], rt - a["x_txt"]) <= REL_L2
+    assert rel_l2(gi - a["x_img"], ri - a["x_img"]) <= REL_L2
+    q = S.single_block_params("c1.f32s", cfg["D"], cfg["d_head"], cfg["D_mlp"], f32=True)
+    x = S.normal_f32("c1.f32.x", (cfg["B"], sh.L, cfg["D"]))
+    vec = S.normal_f32("c1.f32.vec", (cfg["B"], cfg["D"]))
+    g, _ = run_single(cfg, q, x, vec)
+    r = O.single_block(x, vec, q, sh, c, s)
+    assert_close(g, r, what="c1 fp32-weight single")
+    assert rel_l2(g - x, r - x) <= REL_L2
 
 
 def test_zero_gates_identity_bit_exact():
@@ -257,8 +282,8 @@ def test_klein_double_block_sampled():
     rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows)
     et, ei = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows,
                             rnd=S.round_bf16)
-    assert_close(gt[:, rt_rows], rt, max_abs=flux_max_abs(et, rt), what="klein double x_txt rows")
-    assert_close(gi[:, ri_rows], ri, max_abs=flux_max_abs(ei, ri), what="klein double x_img rows")
+    flux_check("klein double x_txt rows", gt[:, rt_rows], et, rt, stated=False)
+    flux_check("klein double x_img rows", gi[:, ri_rows], ei, ri, stated=False)
 
 
 def test_klein_single_block_sampled():
@@ -272,7 +297,7 @@ def test_klein_single_block_sampled():
     c, s = tables(cfg)
     ref = O.single_block(x, vec, p, sh, c, s, rows=rows)
     emu = O.single_block(x, vec, p, sh, c, s, rows=rows, rnd=S.round_bf16)
-    assert_close(g[:, rows], ref, max_abs=flux_max_abs(emu, ref), what="klein single rows")
+    flux_check("klein single rows", g[:, rows], emu, ref, stated=False)
 
 
 # ------------------------------------------------------------------ FP8 (e4m3) blocks
@@ -379,23 +404,32 @@ def test_sample_graph_replay_is_bit_identical_to_launches():
 
 
 # ------------------------------------------------------------------ Flux-sized blocks, sampled rows
-def flux_max_abs(emulated, ref):
-    """Max-abs bar for Flux-sized blocks: the stated 5e-2, or twice the max-abs
-    error of the same rows computed by the oracle with every matmul operand
-    rounded to bf16 where the kernels store one, whichever is larger.  At
-    D=3072 with a 12288-wide MLP that rounding alone reaches 3-4e-2."""
-    return max(MAX_ABS, 2.0 * float(np.abs(np.asarray(emulated) - np.asarray(ref)).max()))
+def flux_check(what, got, emulated, ref, stated=True):
+    """Parity of a Flux-sized block output (sampled rows) against the exact
+    oracle, next to the oracle's own bf16 emulation of the same rows (every
+    matmul operand rounded to bf16 where the kernels store one).
 
-
-def flux_rel(emulated, ref):
-    """rel-L2 bar for the e4m3 path at Flux size: the stated 1e-2, or twice
-    the rel-L2 of the same rows computed by the oracle with bf16 rounding
-    where the kernels store an operand, whichever is larger.  Rounding to
-    e4m3 is a step function: a bf16-sized change of an input (2^-9) crosses
-    an e4m3 midpoint about once in 2^-9 / 2^-3 = 1/64 elements and moves that
-    element by a whole e4m3 step, so two correct evaluations of the same
-    e4m3 block differ by about 2e-2 at D=3072 (the bf16 path: 2e-3)."""
-    return max(1e-2, 2.0 * rel_l2(emulated, ref))
+    stated: the spec bars as given, rel-L2 <= 1e-2 and max-abs <= 5e-2
+    (the BASELINE configs' blocks).  Otherwise (Flux.2 Klein widths, e4m3
+    linears, where the emulation alone passes 5e-2) the bars are 1.25 x the
+    emulation's rel-L2 and max-abs, at least the stated ones.
+    Always, two statistics that do not swing with a single element: the
+    kernel's rel-L2 within 1.1 x the emulation's, and the mean over rows of the
+    per-row max-abs within 1.25 x the emulation's.  The max over tens of
+    thousands of elements is noisy: two equally exact bf16 evaluations of the
+    same block (the kernel and the emulation) measure it 1.0-1.3 x apart, while
+    their rel-L2 agree within 2%."""
+    g, e, r = (np.asarray(t, np.float64).reshape(-1, np.shape(ref)[-1]) for t in (got, emulated, ref))
+    e_rel, e_max, e_row = rel_l2(e, r), float(np.abs(e - r).max()), float(np.abs(e - r).max(1).mean())
+    k_rel, k_row = rel_l2(g, r), float(np.abs(g - r).max(1).mean())
+    report(f"EMU {what}: kernel rel_l2={k_rel:.3e} max={np.abs(g - r).max():.3e} rowmax_mean={k_row:.3e} | "
+           f"emulation rel_l2={e_rel:.3e} max={e_max:.3e} rowmax_mean={e_row:.3e}")
+    if stated:
+        assert_close(got, ref, what=what)
+    else:
+        assert_close(got, ref, rel=max(REL_L2, 1.25 * e_rel), max_abs=max(MAX_ABS, 1.25 * e_max), what=what)
+    assert k_rel <= 1.1 * e_rel, f"{what}: rel_l2 {k_rel:.3e} above 1.1 x the emulation's {e_rel:.3e}"
+    assert k_row <= 1.25 * e_row, f"{what}: mean row max {k_row:.3e} above 1.25 x the emulation's {e_row:.3e}"
 
 
 def _sample_rows(n, k, seed):
@@ -417,8 +451,8 @@ def test_double_block_flux_sampled(name):
     rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows)
     et, ei = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows,
                             rnd=S.round_bf16)
-    assert_close(gt[:, rt_rows], rt, max_abs=flux_max_abs(et, rt), what=f"{name} double x_txt rows")
-    assert_close(gi[:, ri_rows], ri, max_abs=flux_max_abs(ei, ri), what=f"{name} double x_img rows")
+    flux_check(f"{name} double x_txt rows", gt[:, rt_rows], et, rt)
+    flux_check(f"{name} double x_img rows", gi[:, ri_rows], ei, ri)
 
 
 @pytest.mark.parametrize("name", ["c3", "c4"])
@@ -433,7 +467,7 @@ def test_single_block_flux_sampled(name):
     c, s = tables(cfg)
     ref = O.single_block(x, vec, p, sh, c, s, rows=rows)
     emu = O.single_block(x, vec, p, sh, c, s, rows=rows, rnd=S.round_bf16)
-    assert_close(g[:, rows], ref, max_abs=flux_max_abs(emu, ref), what=f"{name} single rows")
+    flux_check(f"{name} single rows", g[:, rows], emu, ref)
 
 
 def test_double_block_int8_flux_batch4_sampled():
@@ -457,8 +491,8 @@ def test_double_block_int8_flux_batch4_sampled():
                                 rows_img=ri_rows)
         et, ei = O.double_block(sub["x_txt"], sub["x_img"], sub["vec"], pd, sh_b1(sh), c, s, rows_txt=rt_rows,
                                 rows_img=ri_rows, rnd=S.round_bf16)
-        assert_close(gt[b:b + 1, rt_rows], rt, max_abs=flux_max_abs(et, rt), what=f"int8 b={b} x_txt rows")
-        assert_close(gi[b:b + 1, ri_rows], ri, max_abs=flux_max_abs(ei, ri), what=f"int8 b={b} x_img rows")
+        flux_check(f"int8 b={b} x_txt rows", gt[b:b + 1, rt_rows], et, rt)
+        flux_check(f"int8 b={b} x_img rows", gi[b:b + 1, ri_rows], ei, ri)
         bt, bi = O.double_block(sub["x_txt"], sub["x_img"], sub["vec"], p, sh_b1(sh), c, s, rows_txt=rt_rows,
                                 rows_img=ri_rows)
         x0 = sub["x_img"][:, ri_rows]
@@ -469,9 +503,9 @@ def test_f8_blocks_flux_1328_sampled():
     """e4m3 double and single blocks at the 1328^2 step's shape (512 text +
     83x83 image tokens, D=3072, MLP 12288), in the launch configuration the
     step uses: sampled rows against the oracle on the e4m3 weights with its
-    activation quantisation model; the bars are twice the distance of the
-    oracle's own bf16-rounded evaluation from its exact one (flux_rel,
-    flux_max_abs), at least the stated 1e-2 / 5e-2."""
+    activation quantisation model; the bars are 1.25 x the distance of the
+    oracle's own bf16-rounded evaluation from its exact one, at least the
+    stated 1e-2 / 5e-2 (flux_check)."""
     cfg = FULL["c4"]
     sh = oracle_shape(cfg)
     c, s = tables(cfg)
@@ -489,8 +523,8 @@ def test_f8_blocks_flux_1328_sampled():
     kw = dict(rows_txt=rt_rows, rows_img=ri_rows, qin=_f8_rows)
     rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], pd, sh, c, s, **kw)
     et, ei = O.double_block(a["x_txt"], a["x_img"], a["vec"], pd, sh, c, s, rnd=S.round_bf16, **kw)
-    assert_close(gt[:, rt_rows], rt, rel=flux_rel(et, rt), max_abs=flux_max_abs(et, rt), what="1328 fp8 double x_txt")
-    assert_close(gi[:, ri_rows], ri, rel=flux_rel(ei, ri), max_abs=flux_max_abs(ei, ri), what="1328 fp8 double x_img")
+    flux_check("1328 fp8 double x_txt", gt[:, rt_rows], et, rt, stated=False)
+    flux_check("1328 fp8 double x_img", gi[:, ri_rows], ei, ri, stated=False)
 
     ps = S.single_block_params("full.f8s", cfg["D"], cfg["d_head"], cfg["D_mlp"])
     x = S.normal_f32("full.f8s.x", (1, sh.L, cfg["D"]))
@@ -503,7 +537,7 @@ def test_f8_blocks_flux_1328_sampled():
     rows = _sample_rows(sh.L, 8, 9)
     ref = O.single_block(x, vec, pd, sh, c, s, rows=rows, qin=_f8_rows)
     emu = O.single_block(x, vec, pd, sh, c, s, rows=rows, qin=_f8_rows, rnd=S.round_bf16)
-    assert_close(g[:, rows], ref, rel=flux_rel(emu, ref), max_abs=flux_max_abs(emu, ref), what="1328 fp8 single rows")
+    flux_check("1328 fp8 single rows", g[:, rows], emu, ref, stated=False)
 
 
 def sh_b1(sh):
