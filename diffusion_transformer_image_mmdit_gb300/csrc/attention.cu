@@ -20,6 +20,8 @@
 // than 16 (a factor 2^16), which stays exact because the same reference is
 // used for the numerator and the row sum: P entries stay below 2^16 (bf16
 // keeps its relative precision there) and the fp32 sums far from overflow.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace mmdit {
@@ -79,7 +81,8 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
   const uint32_t p_full0 = smem_u32(bars + 9);    // [2] per tile
   const uint32_t pv_done0 = smem_u32(bars + 11);  // [2] per tile
   const uint32_t v_empty0 = smem_u32(bars + 13);  // [2] per stage: freed after both P V MMAs of the V tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  const uint32_t mma_done = smem_u32(bars + 15);  // after a time-out: every issued MMA has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -100,6 +103,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       mbar_init(p_full0 + 8 * i, 4);
       mbar_init(pv_done0 + 8 * i, 1);
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -248,10 +252,12 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         // Loads in the order the MMAs need them: K(j + 1) (for S(j + 1)) before
         // V(j) (for P V(j)).  K and V rings are freed independently, so a K
         // slot is refilled as soon as both S MMAs that read it complete.
+        int n_k = 0, n_v = 0;  // tiles whose loads were issued (for the drain after a time-out)
         auto load_k = [&](int j) -> bool {
           const int st = j & 1;
           if (!mbar_wait(k_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER))
             return false;
+          ++n_k;
           mbar_expect_tx(k_full0 + 8 * st, SM::K);
 #pragma unroll
           for (int hf = 0; hf < HD / 64; ++hf)
@@ -263,6 +269,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
           const int st = j & 1;
           if (!mbar_wait(v_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER))
             return false;
+          ++n_v;
           mbar_expect_tx(v_full0 + 8 * st, SM::V);
 #pragma unroll
           for (int kh = 0; kh < 2; ++kh)
@@ -272,6 +279,18 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         };
         bool okp = load_k(0);
         for (int j = 0; okp && j < nkv; ++j) okp = (j + 1 >= nkv || load_k(j + 1)) && load_v(j);
+        if (*abort_flag) {
+          // After a time-out anywhere in the CTA: wait (bounded) until every
+          // copy still in flight into this CTA's shared memory has landed (Q,
+          // and the last two K and V tiles, one per ring stage) before the CTA
+          // frees its resources and exits.
+          constexpr unsigned long long kDrainNs = 100000000ull;
+          mbar_wait(q_full, 0, nullptr, nullptr, 0, kDrainNs);
+          for (int j = max(0, n_k - 2); j < n_k; ++j)
+            mbar_wait(k_full0 + 8 * (j & 1), (j >> 1) & 1, nullptr, nullptr, 0, kDrainNs);
+          for (int j = max(0, n_v - 2); j < n_v; ++j)
+            mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, nullptr, nullptr, 0, kDrainNs);
+        }
       }
     } else if (warp == 9) {
       // The whole warp runs the issue loop (warp-uniform operands); the
@@ -325,6 +344,12 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         ok = issue_pv(0, j) && (j + 1 >= nkv || issue_s(0, j + 1)) && issue_pv(1, j) &&
              (j + 1 >= nkv || issue_s(1, j + 1));
       }
+      if (*abort_flag) {
+        // every MMA this warp issued (they read shared memory and write the
+        // tensor memory about to be freed) completes first
+        umma_commit_if(leader, mma_done);
+        mbar_wait_warp(mma_done, 0, nullptr, nullptr, 0);
+      }
     }
   }
   tc_fence_before();
@@ -337,15 +362,16 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
 
 template <int HD>
 cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, cudaStream_t s) {
-  static bool attr_done[64] = {};
+  // shared-memory opt-in once per device, safe under concurrent first calls
+  static std::once_flag once[64];
+  static cudaError_t setup_err[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Attn2Smem<HD>::total);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    setup_err[dev] = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)Attn2Smem<HD>::total);
+  });
+  if (setup_err[dev] != cudaSuccess) return setup_err[dev];
   dim3 grid((p.n_q_tiles + 1) / 2, p.H, p.B);
   launch_begin(KID_ATTENTION, s);
   attn_fwd_kernel<HD><<<grid, kAttn2Threads, Attn2Smem<HD>::total, s>>>(tmQK, tmV, p);
