@@ -40,9 +40,9 @@ CONFIGS = {
     "klein1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=8, n_single=24, int8=False, n_steps=4,
                       swiglu=True, D=4096, H=32, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56), C_lat=128,
                       t_dim=256),
-    # the same at the token count of the 1200x800 image-to-image workload: 512 text + 75x50 target + 75x50 reference
-    # latent tokens, the reference tokens laid out as a second 75x50 grid
-    "klein_i2i": dict(B=1, L_txt=512, grid_h=100, grid_w=75, n_double=8, n_single=24, int8=False, n_steps=4,
+    # the 1200x800 image-to-image workload: 512 text + 75x50 target + 75x50 reference latent tokens
+    "klein_i2i": dict(B=1, L_txt=512, grid_h=75, grid_w=50, ref_h=75, ref_w=50, n_double=8, n_single=24, int8=False,
+                      n_steps=4,
                       swiglu=True, D=4096, H=32, d_head=128, D_mlp=12288, rope_axes=(16, 56, 56), C_lat=128,
                       t_dim=256),
     # the 1328^2 step with e4m3 block linears (per-channel weight scales, per-row activation scales)
@@ -67,9 +67,8 @@ WORKLOAD_NAME = {
     "c2": "one double block (with embedding, img_in, final layer, Euler) at 512 text + 32x32 image tokens, batch 1",
     "klein1024": "Flux.2 Klein-shaped denoising step: 8 double + 24 single blocks, D=4096, 32x128 heads, SwiGLU "
                  "MLP 12288, 512 text + 64x64 image tokens (1024^2), batch 1, bf16, step 0 of a 4-step schedule",
-    "klein_i2i": "Flux.2 Klein-shaped denoising step at the token count of 1200x800 image-to-image: 512 text + "
-                 "75x50 target + 75x50 reference latent tokens (8012), the reference tokens as a second grid "
-                 "(their RoPE time index is not modelled), batch 1, bf16",
+    "klein_i2i": "Flux.2 Klein-shaped image-to-image denoising step at 1200x800: 512 text + 75x50 target + 75x50 "
+                 "reference latent tokens (8012; reference positions (1, h, w)), batch 1, bf16",
     "c4_f8": "full denoising step at 1328^2 (19 double + 38 single blocks, 512 text + 83x83 image tokens, batch 1) "
              "with the block linears in e4m3 (per-channel weight scales, per-row activation scales, fp32 "
              "accumulation); modulation, embedders and the final layer in bf16",
@@ -85,7 +84,8 @@ WORKLOAD_NAME = {
 def step_flops(c: dict) -> dict:
     """Algorithmic FLOPs of one step: 2*M*N*K per linear, 4*L^2*D per joint attention."""
     B, D, Dm, C, T = c["B"], c["D"], c["D_mlp"], c["C_lat"], c["t_dim"]
-    Lt, Li = c["L_txt"], c["grid_h"] * c["grid_w"]
+    Lg = c["grid_h"] * c["grid_w"]  # target image tokens
+    Lt, Li = c["L_txt"], Lg + c.get("ref_h", 0) * c.get("ref_w", 0)  # all image tokens (target + reference)
     L = Lt + Li
     m_in = 2 * Dm if c.get("swiglu") else Dm  # rows of the first MLP projection ([gate; up] for SwiGLU)
     lin_double = 2 * L * (3 * D * D + D * D + D * m_in + Dm * D)
@@ -93,7 +93,7 @@ def step_flops(c: dict) -> dict:
     attn = 4 * L * L * D
     blocks = c["n_double"] * (lin_double + attn) + c["n_single"] * (lin_single + attn)
     small = 2 * (T * D + D * D) + c["n_double"] * 2 * 2 * D * 6 * D + c["n_single"] * 2 * D * 3 * D + 2 * D * 2 * D
-    io = 2 * Li * C * D * 2
+    io = 2 * C * D * (Li + Lg)  # img_in over every image token, the final layer over the target tokens
     gemm = B * (c["n_double"] * lin_double + c["n_single"] * lin_single + io)
     # with e4m3 block linears only the embedder and final-layer GEMMs stay bf16
     gemm_f8 = B * (c["n_double"] * lin_double + c["n_single"] * lin_single) if c.get("f8") else 0
@@ -345,7 +345,8 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int, full: bool =
                            d_head=c["d_head"], D_mlp=c["D_mlp"], rope_axes=c["rope_axes"],
                            w_dtype=(api.MMDIT_I8W if c["int8"] else api.MMDIT_F8W if c.get("f8") else
                                     api.MMDIT_BF16), C_lat=c["C_lat"],
-                           t_dim=c["t_dim"], mlp_act=api.MMDIT_MLP_SWIGLU if c.get("swiglu") else api.MMDIT_MLP_GELU)
+                           t_dim=c["t_dim"], mlp_act=api.MMDIT_MLP_SWIGLU if c.get("swiglu") else api.MMDIT_MLP_GELU,
+                           ref_h=c.get("ref_h", 0), ref_w=c.get("ref_w", 0))
     draw = DeviceDraw(seed=1000 + rank, device=dev)
     w = draw.step(c["D"], c["d_head"], c["D_mlp"], c["C_lat"], c["t_dim"], c["n_double"], c["n_single"],
                   swiglu=bool(c.get("swiglu")))
@@ -357,6 +358,8 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int, full: bool =
     wstruct = w.struct()
     Li = c["grid_h"] * c["grid_w"]
     x_lat = draw.normal((c["B"], Li, c["C_lat"]))
+    Lr = c.get("ref_h", 0) * c.get("ref_w", 0)
+    x_ref = draw.normal((c["B"], Lr, c["C_lat"])) if Lr else None  # the reference latent, fixed over the steps
     x_txt = draw.normal((c["B"], c["L_txt"], c["D"]))
     v = torch.empty_like(x_lat)
     ws = api.alloc_workspace(api.step_workspace_size(shape, c["n_double"], c["n_single"]), device=dev)
@@ -365,7 +368,11 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int, full: bool =
 
     def step(i):
         j = i % c["n_steps"]
-        api.mmdit_step_fwd(shape, w, x_lat, x_txt, sig[j], sig[j + 1], v, ws, stream, step_struct=wstruct)
+        if x_ref is None:
+            api.mmdit_step_fwd(shape, w, x_lat, x_txt, sig[j], sig[j + 1], v, ws, stream, step_struct=wstruct)
+        else:
+            api.mmdit_step_i2i_fwd(shape, w, x_lat, x_ref, x_txt, sig[j], sig[j + 1], v, ws, stream,
+                                   step_struct=wstruct)
 
     for i in range(args.warmup):
         step(i)

@@ -22,7 +22,7 @@ class Shape(Structure):
     _fields_ = [("B", c_int), ("L_txt", c_int), ("grid_h", c_int), ("grid_w", c_int), ("D", c_int), ("H", c_int),
                 ("d_head", c_int), ("D_mlp", c_int), ("rope_axes", c_int * 3), ("rope_theta", c_double),
                 ("eps_ln", c_float), ("eps_rms", c_float), ("w_dtype", c_int), ("C_lat", c_int), ("t_dim", c_int),
-                ("mlp_act", c_int)]
+                ("mlp_act", c_int), ("ref_h", c_int), ("ref_w", c_int)]
 
 
 MMDIT_EPI_SWIGLU = 4
@@ -80,6 +80,8 @@ SIGNATURES = {
                                        c_void_p, c_void_p, c_size_t, c_void_p]),
     "mmdit_step_fwd": (c_int, [POINTER(Shape), POINTER(StepW), c_void_p, c_void_p, c_double, c_double, c_void_p,
                                c_void_p, c_size_t, c_void_p]),
+    "mmdit_step_i2i_fwd": (c_int, [POINTER(Shape), POINTER(StepW), c_void_p, c_void_p, c_void_p, c_double, c_double,
+                                   c_void_p, c_void_p, c_size_t, c_void_p]),
     "mmdit_sample_workspace_size": (c_int, [POINTER(Shape), c_int, c_int, c_int, c_int, POINTER(c_size_t)]),
     "mmdit_sample": (c_int, [POINTER(Shape), POINTER(StepW), POINTER(CondW), c_void_p, c_void_p, c_void_p, c_double,
                              POINTER(c_double), c_int, c_int, c_void_p, c_size_t, c_void_p]),

@@ -37,7 +37,8 @@ def stream_handle(stream: Optional[torch.cuda.Stream] = None):
 
 
 def make_shape(B, L_txt, grid_h, grid_w, D, H, d_head, D_mlp, rope_axes=(16, 56, 56), rope_theta=10000.0,
-               eps_ln=1e-6, eps_rms=1e-6, w_dtype=MMDIT_BF16, C_lat=128, t_dim=256, mlp_act=0) -> Shape:
+               eps_ln=1e-6, eps_rms=1e-6, w_dtype=MMDIT_BF16, C_lat=128, t_dim=256, mlp_act=0, ref_h=0,
+               ref_w=0) -> Shape:
     s = Shape()
     s.B, s.L_txt, s.grid_h, s.grid_w = B, L_txt, grid_h, grid_w
     s.D, s.H, s.d_head, s.D_mlp = D, H, d_head, D_mlp
@@ -45,11 +46,13 @@ def make_shape(B, L_txt, grid_h, grid_w, D, H, d_head, D_mlp, rope_axes=(16, 56,
     s.rope_theta, s.eps_ln, s.eps_rms = rope_theta, eps_ln, eps_rms
     s.w_dtype, s.C_lat, s.t_dim = w_dtype, C_lat, t_dim
     s.mlp_act = mlp_act
+    s.ref_h, s.ref_w = ref_h, ref_w
     return s
 
 
 def seq_len(s: Shape) -> int:
-    return s.L_txt + s.grid_h * s.grid_w
+    """Tokens per sample: text, target image, reference image."""
+    return s.L_txt + s.grid_h * s.grid_w + s.ref_h * s.ref_w
 
 
 # ------------------------------------------------------------------ weights on the device
@@ -307,6 +310,13 @@ def mmdit_step_fwd(shape: Shape, w: StepWeights, x_lat, x_txt_in, sigma: float, 
     st = step_struct if step_struct is not None else w.struct()
     call("mmdit_step_fwd", ctypes.byref(shape), ctypes.byref(st), ptr(x_lat), ptr(x_txt_in), float(sigma),
          float(sigma_next), ptr(v_out), ptr(ws), ws.numel(), stream_handle(stream))
+
+
+def mmdit_step_i2i_fwd(shape: Shape, w: StepWeights, x_lat, x_ref, x_txt_in, sigma: float, sigma_next: float, v_out,
+                       ws: torch.Tensor, stream=None, step_struct: Optional[StepW] = None):
+    st = step_struct if step_struct is not None else w.struct()
+    call("mmdit_step_i2i_fwd", ctypes.byref(shape), ctypes.byref(st), ptr(x_lat), ptr(x_ref), ptr(x_txt_in),
+         float(sigma), float(sigma_next), ptr(v_out), ptr(ws), ws.numel(), stream_handle(stream))
 
 
 def sample_workspace_size(shape: Shape, n_double: int, n_single: int, C_txt: int, n_steps: int) -> int:

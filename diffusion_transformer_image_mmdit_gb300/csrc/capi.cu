@@ -150,6 +150,7 @@ struct Carve {
 
 struct Dims {
   int B, Lt, Li, L, Lpad, D, H, d, Dm;
+  int Lg, Lr;  // image tokens per sample: Li = Lg target + Lr reference
   bool swiglu;  // SwiGLU MLP: the first MLP projection has 2 Dm rows [gate; up]
   bool f8;      // FP8 block GEMMs (MMDIT_F8W)
 };
@@ -157,6 +158,7 @@ struct Dims {
 static int check_shape(const mmdit_shape_t* s, Dims* out) {
   if (!s) return MMDIT_ERR_ARG;
   if (s->B < 1 || s->L_txt < 0 || s->grid_h < 1 || s->grid_w < 1) return MMDIT_ERR_SHAPE;
+  if (s->ref_h < 0 || s->ref_w < 0 || (s->ref_h == 0) != (s->ref_w == 0)) return MMDIT_ERR_SHAPE;
   if (s->D <= 0 || s->D % 256 || s->D > 4096) return MMDIT_ERR_SHAPE;
   if (s->d_head != 64 && s->d_head != 128) return MMDIT_ERR_SHAPE;
   if (s->H * s->d_head != s->D) return MMDIT_ERR_SHAPE;
@@ -166,10 +168,12 @@ static int check_shape(const mmdit_shape_t* s, Dims* out) {
   if (s->w_dtype != MMDIT_BF16 && s->w_dtype != MMDIT_I8W && s->w_dtype != MMDIT_F8W) return MMDIT_ERR_ARG;
   if (s->mlp_act != MMDIT_MLP_GELU && s->mlp_act != MMDIT_MLP_SWIGLU) return MMDIT_ERR_ARG;
   if (s->mlp_act == MMDIT_MLP_SWIGLU && s->D_mlp % 128) return MMDIT_ERR_SHAPE;
-  const long long L = (long long)s->L_txt + (long long)s->grid_h * s->grid_w;
+  const long long Lg = (long long)s->grid_h * s->grid_w, Lr = (long long)s->ref_h * s->ref_w;
+  const long long L = (long long)s->L_txt + Lg + Lr;
   if (L > (1 << 24)) return MMDIT_ERR_SHAPE;
   if (out) {
-    out->B = s->B, out->Lt = s->L_txt, out->Li = s->grid_h * s->grid_w, out->L = (int)L;
+    out->B = s->B, out->Lt = s->L_txt, out->Li = (int)(Lg + Lr), out->L = (int)L;
+    out->Lg = (int)Lg, out->Lr = (int)Lr;
     out->Lpad = (int)((L + 7) / 8 * 8);
     out->D = s->D, out->H = s->H, out->d = s->d_head, out->Dm = s->D_mlp;
     out->swiglu = s->mlp_act == MMDIT_MLP_SWIGLU;
@@ -386,8 +390,8 @@ static void layout_step(const Dims& d, const mmdit_shape_t& s, int n_double, int
   w.temb = c.take<float>((size_t)d.B * (s.t_dim + d.D));
   w.mods = c.take<float>(mods_floats(d, n_double, n_single));
   w.x = c.take<float>((size_t)d.B * d.L * d.D);
-  w.v = c.take<float>((size_t)d.B * d.Li * s.C_lat);
-  w.xlat = c.take<uint16_t>((size_t)d.B * d.Li * s.C_lat);
+  w.v = c.take<float>((size_t)d.B * d.Lg * s.C_lat);
+  w.xlat = c.take<uint16_t>((size_t)d.B * d.Li * s.C_lat);  // bf16 target latents, then reference latents
   w.cs = c.take<float>((size_t)d.L * (d.d / 2));
   w.sn = c.take<float>((size_t)d.L * (d.d / 2));
   Carve c1{nullptr, 0}, c2{nullptr, 0};
@@ -627,13 +631,14 @@ static int step_w_check(const mmdit_shape_t& shape, const mmdit_step_w_t& w) {
 // k = *sig_idx (the host values are ignored), so one captured step replays
 // for every step of a schedule.
 static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step_w_t& w, float* x_lat,
-                     const float* x_txt_in, double sigma, double sigma_next, float* v_out, const float* vec_add,
+                     const float* x_ref, const float* x_txt_in, double sigma, double sigma_next, float* v_out,
+                     const float* vec_add,
                      const double* sig_tab, const int* sig_idx, bool build_rope, const StepWS& sw, cudaStream_t st) {
   const bool i8 = shape.w_dtype == MMDIT_I8W;
   const int D = d.D, C = shape.C_lat;
   if (build_rope)
-    MMDIT_CUDA(launch_rope_build(d.Lt, shape.grid_w, d.L, shape.rope_axes, shape.rope_theta, nullptr, sw.cs,
-                                 sw.sn, st));
+    MMDIT_CUDA(launch_rope_build(d.Lt, shape.grid_w, d.Lg, shape.ref_w, d.L, shape.rope_axes, shape.rope_theta,
+                                 nullptr, sw.cs, sw.sn, st));
   // timestep embedding: vec = time2 SiLU(time1 sinusoid(1000 sigma))
   MMDIT_CUDA(launch_sinusoid(1000.0 * sigma, d.B, shape.t_dim, sw.temb, st, sig_tab, sig_idx, 1000.0));
   float* th = sw.temb + (size_t)d.B * shape.t_dim;
@@ -663,7 +668,11 @@ static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step
   if (d.Lt > 0)
     MMDIT_CUDA(cudaMemcpy2DAsync(sw.x, (size_t)d.L * D * 4, x_txt_in, (size_t)d.Lt * D * 4, (size_t)d.Lt * D * 4, d.B,
                                  cudaMemcpyDeviceToDevice, st));
-  MMDIT_CUDA(launch_cast_bf16(x_lat, sw.xlat, (long long)d.B * d.Li * C, st));
+  // img_in: the target latents into image rows [0, Lg) of each sample, the reference latents (if any) into
+  // rows [Lg, Li), as the two problems of one launch
+  uint16_t* xref16 = sw.xlat + (size_t)d.B * d.Lg * C;
+  MMDIT_CUDA(launch_cast_bf16(x_lat, sw.xlat, (long long)d.B * d.Lg * C, st));
+  if (d.Lr > 0) MMDIT_CUDA(launch_cast_bf16(x_ref, xref16, (long long)d.B * d.Lr * C, st));
   {
     GemmParams p = gemm_params(GM_STORE_F32);
     p.out = sw.x;
@@ -672,7 +681,17 @@ static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step
     p.out_row_off = d.Lt;
     Carve bc{sw.block, 0};
     uint16_t* wdeq = i8 ? bc.take<uint16_t>((size_t)D * C) : nullptr;
-    MMDIT_TRY(run_gemm(sw.xlat, C, d.Li, d.Li, d.B, C, w.img_in, D, p, wdeq, st));
+    GemmProblem pr[2];
+    MMDIT_TRY(prepare_gemm(sw.xlat, C, d.Lg, d.Lg, d.B, C, w.img_in, D, p, wdeq, st, pr[0]));
+    if (d.Lr > 0) {
+      p.out_row_off = d.Lt + d.Lg;
+      // int8 weights were widened into wdeq by the first problem's preparation: the second reads that copy,
+      // with the same per-channel scale in its epilogue
+      const mmdit_linear_t lin = wdeq ? mmdit_linear_t{wdeq, w.img_in.b, nullptr} : w.img_in;
+      MMDIT_TRY(prepare_gemm(xref16, C, d.Lr, d.Lr, d.B, C, lin, D, p, nullptr, st, pr[1]));
+      if (wdeq) pr[1].p.wscale = w.img_in.scale;
+    }
+    MMDIT_TRY(launch_problems(&pr[0], d.Lr > 0 ? &pr[1] : nullptr, st));
   }
   // blocks
   mp = sw.mods;
@@ -698,17 +717,17 @@ static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step
   // final layer on the image tokens and the Euler update
   {
     Carve bc{sw.block, 0};
-    uint16_t* y = bc.take<uint16_t>((size_t)d.B * d.Li * D);
+    uint16_t* y = bc.take<uint16_t>((size_t)d.B * d.Lg * D);
     uint16_t* wdeq = i8 ? bc.take<uint16_t>((size_t)D * C) : nullptr;
-    MMDIT_CUDA(launch_ln_modulate(sw.x + (size_t)d.Lt * D, d.L, d.Li, d.B, D, mod_final, mod_final + D, 2 * D,
+    MMDIT_CUDA(launch_ln_modulate(sw.x + (size_t)d.Lt * D, d.L, d.Lg, d.B, D, mod_final, mod_final + D, 2 * D,
                                   shape.eps_ln, y, st));
     GemmParams p = gemm_params(GM_STORE_F32);
     float* v = v_out ? v_out : sw.v;
     p.out = v;
     p.out_ld = C;
-    p.out_seg_rows = d.Li;
-    MMDIT_TRY(run_gemm(y, D, d.Li, d.Li, d.B, D, w.final, C, p, wdeq, st));
-    MMDIT_CUDA(launch_euler(x_lat, v, false, (float)(sigma_next - sigma), (long long)d.B * d.Li * C, st, sig_tab,
+    p.out_seg_rows = d.Lg;
+    MMDIT_TRY(run_gemm(y, D, d.Lg, d.Lg, d.B, D, w.final, C, p, wdeq, st));
+    MMDIT_CUDA(launch_euler(x_lat, v, false, (float)(sigma_next - sigma), (long long)d.B * d.Lg * C, st, sig_tab,
                             sig_idx));
   }
   return MMDIT_OK;
@@ -844,7 +863,8 @@ int mmdit_rope2d_build(const mmdit_shape_t* shape, int32_t* ids, float* cos_, fl
   if (!al16(cos_) || !al16(sin_) || (ids && (reinterpret_cast<uintptr_t>(ids) & 3))) return MMDIT_ERR_ALIGN;
   MMDIT_TRY(check_device());
   return cuda_status(
-      launch_rope_build(d.Lt, shape->grid_w, d.L, shape->rope_axes, shape->rope_theta, ids, cos_, sin_, S(stream)));
+      launch_rope_build(d.Lt, shape->grid_w, d.Lg, shape->ref_w, d.L, shape->rope_axes, shape->rope_theta, ids, cos_,
+                        sin_, S(stream)));
 }
 
 int rope2d_apply(const mmdit_shape_t* shape, const float* cos_, const float* sin_, void* x, int row_stride,
@@ -934,13 +954,16 @@ int mmdit_single_block_fwd(const mmdit_shape_t* shape, const mmdit_single_w_t* w
   return single_block_impl(*shape, d, *w, vec, mod_precomputed, x, cos_, sin_, sw, S(stream));
 }
 
-int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_txt_in,
-                   double sigma, double sigma_next, float* v_out, void* ws, size_t ws_bytes, void* stream) {
+int mmdit_step_i2i_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_ref,
+                       const float* x_txt_in, double sigma, double sigma_next, float* v_out, void* ws,
+                       size_t ws_bytes, void* stream) {
   Dims d;
   MMDIT_TRY(check_shape(shape, &d));
-  if (!w || !x_lat || (d.Lt > 0 && !x_txt_in) || !ws) return MMDIT_ERR_ARG;
+  if (!w || !x_lat || (d.Lt > 0 && !x_txt_in) || !ws || (d.Lr > 0) != (x_ref != nullptr)) return MMDIT_ERR_ARG;
   MMDIT_TRY(step_w_check(*shape, *w));
-  if (!al16(x_lat) || (x_txt_in && !al16(x_txt_in)) || !al16(ws) || (v_out && !al16(v_out))) return MMDIT_ERR_ALIGN;
+  if (!al16(x_lat) || (x_ref && !al16(x_ref)) || (x_txt_in && !al16(x_txt_in)) || !al16(ws) ||
+      (v_out && !al16(v_out)))
+    return MMDIT_ERR_ALIGN;
   size_t need = 0;
   MMDIT_TRY(mmdit_step_workspace_size(shape, w->n_double, w->n_single, &need));
   if (ws_bytes < need) return MMDIT_ERR_WORKSPACE;
@@ -948,8 +971,13 @@ int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x
   Carve c{static_cast<uint8_t*>(ws), 0};
   StepWS sw;
   layout_step(d, *shape, w->n_double, w->n_single, c, sw);
-  return step_impl(*shape, d, *w, x_lat, x_txt_in, sigma, sigma_next, v_out, nullptr, nullptr, nullptr, true, sw,
-                   S(stream));
+  return step_impl(*shape, d, *w, x_lat, x_ref, x_txt_in, sigma, sigma_next, v_out, nullptr, nullptr, nullptr, true,
+                   sw, S(stream));
+}
+
+int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_txt_in,
+                   double sigma, double sigma_next, float* v_out, void* ws, size_t ws_bytes, void* stream) {
+  return mmdit_step_i2i_fwd(shape, w, x_lat, nullptr, x_txt_in, sigma, sigma_next, v_out, ws, ws_bytes, stream);
 }
 
 // Workspace of the sampling loop: the step's, then the conditioning.
@@ -991,6 +1019,7 @@ int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdi
   Dims d;
   MMDIT_TRY(check_shape(shape, &d));
   if (!w || !cond || !x_lat || (d.Lt > 0 && !txt) || !pooled || !sigmas || !ws || n_steps < 1) return MMDIT_ERR_ARG;
+  if (d.Lr > 0) return MMDIT_ERR_ARG;  // reference latents: step by step through mmdit_step_i2i_fwd
   if (flags & ~MMDIT_SAMPLE_GRAPH) return MMDIT_ERR_ARG;
   MMDIT_TRY(step_w_check(*shape, *w));
   const bool i8 = shape->w_dtype == MMDIT_I8W;
@@ -1013,8 +1042,8 @@ int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdi
   layout_sample(d, *shape, C_txt, n_steps, c, sa);
 
   // step-independent work: RoPE tables, the text stream, the conditioning vector
-  MMDIT_CUDA(launch_rope_build(d.Lt, shape->grid_w, d.L, shape->rope_axes, shape->rope_theta, nullptr, sw.cs, sw.sn,
-                               st));
+  MMDIT_CUDA(launch_rope_build(d.Lt, shape->grid_w, d.Lg, shape->ref_w, d.L, shape->rope_axes, shape->rope_theta,
+                               nullptr, sw.cs, sw.sn, st));
   if (d.Lt > 0) {
     GemmParams p = gemm_params(GM_STORE_F32);
     p.out = sa.x_txt;
@@ -1032,13 +1061,13 @@ int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdi
   MMDIT_CUDA(launch_add(sa.vec_cond, sa.ptmp, (long long)d.B * D, st));
 
   // step 0 eagerly (this also performs every one-time kernel set-up before a capture)
-  MMDIT_TRY(step_impl(*shape, d, *w, x_lat, sa.x_txt, sigmas[0], sigmas[1], nullptr, sa.vec_cond, nullptr, nullptr,
-                      false, sw, st));
+  MMDIT_TRY(step_impl(*shape, d, *w, x_lat, nullptr, sa.x_txt, sigmas[0], sigmas[1], nullptr, sa.vec_cond, nullptr,
+                      nullptr, false, sw, st));
   const bool graph = (flags & MMDIT_SAMPLE_GRAPH) && n_steps > 1 && !g_trace.on;
   if (!graph) {
     for (int i = 1; i < n_steps; ++i)
-      MMDIT_TRY(step_impl(*shape, d, *w, x_lat, sa.x_txt, sigmas[i], sigmas[i + 1], nullptr, sa.vec_cond, nullptr,
-                          nullptr, false, sw, st));
+      MMDIT_TRY(step_impl(*shape, d, *w, x_lat, nullptr, sa.x_txt, sigmas[i], sigmas[i + 1], nullptr, sa.vec_cond,
+                          nullptr, nullptr, false, sw, st));
     return MMDIT_OK;
   }
   // Steps 1 .. n - 1: one captured step reading sigma_k, sigma_{k+1} at the
@@ -1053,7 +1082,8 @@ int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdi
   if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
     rc = MMDIT_ERR_CUDA;
   } else {
-    rc = step_impl(*shape, d, *w, x_lat, sa.x_txt, 0.0, 0.0, nullptr, sa.vec_cond, sa.sig, sa.ctr, false, sw, cs);
+    rc = step_impl(*shape, d, *w, x_lat, nullptr, sa.x_txt, 0.0, 0.0, nullptr, sa.vec_cond, sa.sig, sa.ctr, false, sw,
+                   cs);
     if (rc == MMDIT_OK) rc = cuda_status(launch_counter(sa.ctr, 1, true, cs));
     const cudaError_t e = cudaStreamEndCapture(cs, &graph_def);  // always closes the capture
     if (rc == MMDIT_OK && e != cudaSuccess) rc = MMDIT_ERR_CUDA;

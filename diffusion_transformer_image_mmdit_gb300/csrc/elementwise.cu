@@ -286,8 +286,12 @@ __global__ void counter_kernel(int* c, int value, int add) { *c = add ? *c + val
 
 // ------------------------------------------------------------------ RoPE
 // ids [L,3] and cos/sin [L, d/2]: angle = pos_axis * theta^(-2i/d_axis), fp64.
-__global__ void rope_build_kernel(int L_txt, int grid_w, int L, int a0, int a1, int a2, double theta,
-                                  int32_t* __restrict__ ids, float* __restrict__ cs, float* __restrict__ sn) {
+// Tokens: L_txt text at (0, 0, 0), then n_gen target image tokens at
+// (0, h, w) on a grid_w-wide grid, then reference image tokens at (1, h, w)
+// on a ref_w-wide grid.
+__global__ void rope_build_kernel(int L_txt, int grid_w, int n_gen, int ref_w, int L, int a0, int a1, int a2,
+                                  double theta, int32_t* __restrict__ ids, float* __restrict__ cs,
+                                  float* __restrict__ sn) {
   const int npairs = (a0 + a1 + a2) / 2;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)L * npairs) return;
@@ -295,8 +299,15 @@ __global__ void rope_build_kernel(int L_txt, int grid_w, int L, int a0, int a1, 
   int pos[3] = {0, 0, 0};
   if (tok >= L_txt) {
     const int img = tok - L_txt;
-    pos[1] = img / grid_w;
-    pos[2] = img - pos[1] * grid_w;
+    if (img < n_gen) {
+      pos[1] = img / grid_w;
+      pos[2] = img - pos[1] * grid_w;
+    } else {
+      const int r = img - n_gen;
+      pos[0] = 1;
+      pos[1] = r / ref_w;
+      pos[2] = r - pos[1] * ref_w;
+    }
   }
   if (p == 0 && ids) {
     ids[3 * tok + 0] = pos[0];
@@ -767,12 +778,13 @@ cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t s
   return cudaGetLastError();
 }
 
-cudaError_t launch_rope_build(int L_txt, int grid_w, int L, const int axes[3], double theta, int32_t* ids, float* cs,
+cudaError_t launch_rope_build(int L_txt, int grid_w, int n_gen, int ref_w, int L, const int axes[3], double theta,
+                              int32_t* ids, float* cs,
                               float* sn, cudaStream_t st) {
   const long long n = (long long)L * ((axes[0] + axes[1] + axes[2]) / 2);
   launch_begin(KID_ROPE_BUILD, st);
-  rope_build_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(L_txt, grid_w, L, axes[0], axes[1], axes[2], theta,
-                                                                 ids, cs, sn);
+  rope_build_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(L_txt, grid_w, n_gen, ref_w > 0 ? ref_w : 1, L,
+                                                                 axes[0], axes[1], axes[2], theta, ids, cs, sn);
   launch_end(st);
   return cudaGetLastError();
 }

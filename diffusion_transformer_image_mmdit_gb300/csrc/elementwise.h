@@ -47,7 +47,9 @@ cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const 
 // t_tab != null: t = t_scale * t_tab[*t_idx], read on the device.
 cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t st, const double* t_tab = nullptr,
                             const int* t_idx = nullptr, double t_scale = 1.0);
-cudaError_t launch_rope_build(int L_txt, int grid_w, int L, const int axes[3], double theta, int32_t* ids, float* cs,
+// Tokens: L_txt text, n_gen target image tokens on a grid_w-wide grid, then reference tokens on a ref_w-wide grid.
+cudaError_t launch_rope_build(int L_txt, int grid_w, int n_gen, int ref_w, int L, const int axes[3], double theta,
+                              int32_t* ids, float* cs,
                               float* sn, cudaStream_t st);
 cudaError_t launch_rope_apply(uint16_t* x, long long rows, int L, int H, int d, int row_stride, const float* cs,
                               const float* sn, cudaStream_t st);

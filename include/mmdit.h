@@ -85,7 +85,23 @@ typedef struct {
   int C_lat;        /* latent channels per image token (step only) */
   int t_dim;        /* timestep sinusoid width (step only) */
   int mlp_act;      /* MMDIT_MLP_GELU or MMDIT_MLP_SWIGLU (see below) */
+  int ref_h;        /* reference latent grid rows (image-to-image), 0 = none */
+  int ref_w;        /* reference latent grid columns, 0 = none */
 } mmdit_shape_t;
+
+/* Reference latent (image-to-image).  The Luminal blog (section "The AMD
+ * MI300X pipeline") computes the reference image's latent once per run and
+ * appends it to the noise tokens; no page gives its positions.  Reading
+ * taken: per sample the tokens are [text (L_txt); target image (grid_h x
+ * grid_w, row-major); reference image (ref_h x ref_w, row-major)], and the
+ * RoPE position of a token is text (0, 0, 0), target (0, h, w), reference
+ * (1, h, w): the reference sits on its own grid and differs from the target
+ * on the first axis, which text and target leave at 0.  The blocks treat all
+ * image tokens alike: the image stream of a double block holds
+ * L_img = grid_h grid_w + ref_h ref_w tokens per sample, in this order.  The
+ * step (mmdit_step_i2i_fwd) projects both latents with img_in and applies
+ * the final layer and the Euler update to the target tokens only.  ref_h and
+ * ref_w are both 0 or both positive. */
 
 /* MLP activation.  GELU-tanh: mlp_in (double) and the MLP rows of lin1
  * (single) have D_mlp output rows.  SwiGLU (the Flux.2 Klein blocks; the
@@ -180,8 +196,8 @@ int mmdit_step_workspace_size(const mmdit_shape_t* shape, int n_double, int n_si
  * The Luminal blog (section "What the compiler found on its own") describes
  * RoPE as pairing each channel with a partner channel and combining the two
  * with cosine and sine tables; it fixes nothing else.  Reading taken: text
- * token i sits at (0, 0, 0); image
- * token (h, w) at (0, h, w).  Channel pairs are adjacent, (2i, 2i+1); the
+ * token i sits at (0, 0, 0); target image token (h, w) at (0, h, w); a
+ * reference image token (h, w) at (1, h, w).  Channel pairs are adjacent, (2i, 2i+1); the
  * first rope_axes[0]/2 pairs follow axis 0, the next rope_axes[1]/2 axis 1,
  * the rest axis 2.  Pair i of axis a turns by pos_a * theta^(-2i/rope_axes[a]),
  * computed in fp64 and rounded once to fp32.
@@ -263,6 +279,17 @@ int mmdit_single_block_fwd(const mmdit_shape_t* shape, const mmdit_single_w_t* w
  * v_out: device fp32 [B, L_img, C_lat] or NULL. */
 int mmdit_step_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_txt_in,
                    double sigma, double sigma_next, float* v_out, void* ws, size_t ws_bytes, void* stream);
+
+/* The same step with a reference latent (shape->ref_h, ref_w > 0): the image
+ * tokens are img_in([x_lat; x_ref]) per sample, laid out as above.
+ * x_lat: device fp32 [B, grid_h grid_w, C_lat], updated in place (target
+ * tokens only).  x_ref: device fp32 [B, ref_h ref_w, C_lat], read only.
+ * v_out: device fp32 [B, grid_h grid_w, C_lat] or NULL.  mmdit_step_fwd is
+ * this call without a reference (it rejects ref_h > 0 with MMDIT_ERR_ARG;
+ * so does mmdit_sample). */
+int mmdit_step_i2i_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, float* x_lat, const float* x_ref,
+                       const float* x_txt_in, double sigma, double sigma_next, float* v_out, void* ws,
+                       size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------ sigma schedule */
 /* The sampler's noise levels.  The Luminal blog (section "The AMD MI300X

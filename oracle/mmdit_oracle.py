@@ -52,10 +52,22 @@ class Shape:
     n_double: int = 1
     n_single: int = 0
     mlp: str = "gelu"  # "gelu": GELU-tanh MLP; "swiglu": SiLU(gate) * up over [gate; up] projections
+    ref_h: int = 0  # reference latent grid (image-to-image), 0 = none
+    ref_w: int = 0
+
+    @property
+    def L_gen(self) -> int:
+        """Target image tokens (the latent being denoised)."""
+        return self.grid_h * self.grid_w
+
+    @property
+    def L_ref(self) -> int:
+        return self.ref_h * self.ref_w
 
     @property
     def L_img(self) -> int:
-        return self.grid_h * self.grid_w
+        """All image-stream tokens: target, then reference."""
+        return self.L_gen + self.L_ref
 
     @property
     def L(self) -> int:
@@ -118,14 +130,26 @@ def rms_norm(x, g, eps):
 
 # --------------------------------------------------------------------------
 # 2D axial RoPE
-def rope_ids(L_txt: int, grid_h: int, grid_w: int) -> np.ndarray:
+def rope_ids(L_txt: int, grid_h: int, grid_w: int, ref_h: int = 0, ref_w: int = 0) -> np.ndarray:
     """Position ids [L, 3] (int32).  Text tokens sit at (0, 0, 0); the image
     token at latent row h, column w (row-major after the text) sits at
-    (0, h, w)."""
-    ids = np.zeros((L_txt + grid_h * grid_w, 3), dtype=np.int32)
+    (0, h, w).
+
+    Reference latent (image-to-image): the Luminal blog (section "The AMD
+    MI300X pipeline") appends the once-computed reference latent to the noise
+    tokens; no page gives its positions.  Reading taken: its ref_h x ref_w
+    tokens follow the target tokens, row-major, at (1, h, w), so they keep
+    their own 2D grid and differ from the target only on the first axis."""
+    L_gen, L_ref = grid_h * grid_w, ref_h * ref_w
+    ids = np.zeros((L_txt + L_gen + L_ref, 3), dtype=np.int32)
     hh, ww = np.meshgrid(np.arange(grid_h), np.arange(grid_w), indexing="ij")
-    ids[L_txt:, 1] = hh.reshape(-1)
-    ids[L_txt:, 2] = ww.reshape(-1)
+    ids[L_txt:L_txt + L_gen, 1] = hh.reshape(-1)
+    ids[L_txt:L_txt + L_gen, 2] = ww.reshape(-1)
+    if L_ref:
+        rh, rw = np.meshgrid(np.arange(ref_h), np.arange(ref_w), indexing="ij")
+        ids[L_txt + L_gen:, 0] = 1
+        ids[L_txt + L_gen:, 1] = rh.reshape(-1)
+        ids[L_txt + L_gen:, 2] = rw.reshape(-1)
     return ids
 
 
@@ -326,7 +350,7 @@ def euler_step(x, v, sigma, sigma_next):
     return x + (sigma_next - sigma) * v
 
 
-def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape, vec_add=None, rnd=None, qin=None):
+def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape, vec_add=None, rnd=None, qin=None, x_ref=None):
     """One full step: timestep embedding, img_in, the double blocks, the
     single blocks on [text; image], the final layer on the image tokens, the
     Euler update.  vec_add ([B, D] or None) is added to the timestep
@@ -334,20 +358,25 @@ def denoise_step(x_lat, x_txt, sigma, sigma_next, W, sh: Shape, vec_add=None, rn
     rnd and qin are handed to every block unchanged (precision and
     activation-quantisation models, see double_block); None leaves the
     plain definition.
+    x_ref ([B, ref_h ref_w, C_lat], with sh.ref_h, sh.ref_w set): the
+    reference latent, projected by img_in like the noise latent and appended
+    to its tokens (positions: see rope_ids); the final layer and the Euler
+    update see the target tokens only.
     Returns (x_lat_next, v)."""
-    ids = rope_ids(sh.L_txt, sh.grid_h, sh.grid_w)
+    ids = rope_ids(sh.L_txt, sh.grid_h, sh.grid_w, sh.ref_h, sh.ref_w)
     cos, sin = rope_tables(ids, sh.rope_axes, sh.rope_theta)
     vec = time_embed(sigma, W, sh)
     if vec_add is not None:
         vec = vec + vec_add
-    h_img = img_in(x_lat, W)
+    assert (x_ref is None) == (sh.L_ref == 0), "x_ref is given exactly when the shape has a reference grid"
+    h_img = img_in(x_lat if x_ref is None else np.concatenate([x_lat, x_ref], axis=1), W)
     h_txt = x_txt
     for blk in W["double"]:
         h_txt, h_img = double_block(h_txt, h_img, vec, blk, sh, cos, sin, rnd=rnd, qin=qin)
     x = np.concatenate([h_txt, h_img], axis=1)
     for blk in W["single"]:
         x = single_block(x, vec, blk, sh, cos, sin, rnd=rnd, qin=qin)
-    v = final_layer(x[:, sh.L_txt:], vec, W, sh)
+    v = final_layer(x[:, sh.L_txt:sh.L_txt + sh.L_gen], vec, W, sh)
     return euler_step(x_lat, v, sigma, sigma_next), v
 
 

@@ -52,7 +52,8 @@ def api_shape(cfg: dict, **kw) -> api.Shape:
 
 def oracle_shape(cfg: dict) -> O.Shape:
     return O.Shape(B=cfg["B"], L_txt=cfg["L_txt"], grid_h=cfg["grid_h"], grid_w=cfg["grid_w"], D=cfg["D"], H=cfg["H"],
-                   d_head=cfg["d_head"], D_mlp=cfg["D_mlp"], rope_axes=tuple(cfg["rope_axes"]))
+                   d_head=cfg["d_head"], D_mlp=cfg["D_mlp"], rope_axes=tuple(cfg["rope_axes"]),
+                   ref_h=cfg.get("ref_h", 0), ref_w=cfg.get("ref_w", 0))
 
 
 def f32(a) -> torch.Tensor:
@@ -92,7 +93,7 @@ def assert_close(gpu, ref, rel=REL_L2, max_abs=MAX_ABS, what=""):
 
 
 def tables(cfg):
-    ids = O.rope_ids(cfg["L_txt"], cfg["grid_h"], cfg["grid_w"])
+    ids = O.rope_ids(cfg["L_txt"], cfg["grid_h"], cfg["grid_w"], cfg.get("ref_h", 0), cfg.get("ref_w", 0))
     return O.rope_tables(ids, tuple(cfg["rope_axes"]), 10000.0)
 
 

@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from diffusion_transformer_image_mmdit_gb300 import api, synthetic as S, weights as Wt
+from diffusion_transformer_image_mmdit_gb300 import _lib, api, synthetic as S, weights as Wt
 from oracle import mmdit_oracle as O
 from tests.test_gpu_kernels import decode_e4m3
 from tests.gpu_common import (CONFIGS, FULL, MAX_ABS, REL_L2, REL_L2_INT8_SCHEME, api_shape, assert_close, bf16, check_status, f32,
@@ -200,6 +200,47 @@ def test_step_small(i8):
     assert_close(host(xl), ref_x, rel=tol, what="step x_lat")
 
 
+@pytest.mark.parametrize("i8", [False, True])
+def test_step_i2i_small(i8):
+    """A whole image-to-image step (2 double + 2 single blocks, batch 2): the
+    reference latent (a 6 x 5 grid after the 10 x 12 target) is projected with
+    the noise latent, joins every block at positions (1, h, w), and only the
+    target tokens reach the final layer and the Euler update."""
+    cfg = dict(CONFIGS["d128"], B=2, ref_h=6, ref_w=5)
+    sh = oracle_shape(cfg)
+    sh.C_lat, sh.t_dim = 64, 256
+    W = S.embed_params(cfg["D"], sh.C_lat, sh.t_dim, seed=6)
+    W["double"] = [S.double_block_params(f"i2i.d{i}", cfg["D"], cfg["d_head"], cfg["D_mlp"]) for i in range(2)]
+    W["single"] = [S.single_block_params(f"i2i.s{i}", cfg["D"], cfg["d_head"], cfg["D_mlp"]) for i in range(2)]
+    x_lat = S.normal_f32("i2i.lat", (cfg["B"], sh.L_gen, sh.C_lat))
+    x_ref = S.normal_f32("i2i.ref", (cfg["B"], sh.L_ref, sh.C_lat))
+    x_txt = S.normal_f32("i2i.txt", (cfg["B"], cfg["L_txt"], cfg["D"]))
+    sig = O.sigma_schedule(4, O.shift_mu(sh.L_gen))
+    shape = api_shape(cfg, C_lat=sh.C_lat, t_dim=sh.t_dim, w_dtype=api.MMDIT_I8W if i8 else api.MMDIT_BF16)
+    w = Wt.step_from_host(W)
+    if i8:
+        w = w.quantized()
+    ws = api.alloc_workspace(api.step_workspace_size(shape, 2, 2))
+    xl = f32(x_lat)
+    v = torch.empty_like(xl)
+    api.mmdit_step_i2i_fwd(shape, w, xl, f32(x_ref), f32(x_txt), sig[1], sig[2], v, ws)
+    check_status()
+    ref_x, ref_v = O.denoise_step(x_lat, x_txt, sig[1], sig[2], W, sh, x_ref=x_ref)
+    tol = REL_L2_INT8_SCHEME if i8 else 1e-2
+    assert rel_l2(host(v), ref_v) <= tol, rel_l2(host(v), ref_v)
+    assert_close(host(xl), ref_x, rel=tol, what="i2i step x_lat")
+    # the step without a reference is rejected for this shape, and the reference changes the result
+    with pytest.raises(_lib.MMDiTError):
+        api.mmdit_step_fwd(shape, w, xl, f32(x_txt), sig[1], sig[2], v, ws)
+    no_ref, _ = O.denoise_step(x_lat, x_txt, sig[1], sig[2], W, _no_ref_shape(sh))
+    assert rel_l2(ref_x - x_lat, no_ref - x_lat) > 1e-3
+
+
+def _no_ref_shape(sh):
+    import dataclasses
+    return dataclasses.replace(sh, ref_h=0, ref_w=0)
+
+
 def test_step_small_f8():
     """A whole step (2 double + 2 single blocks, batch 2) with the block linears in e4m3, against the
     bf16-weight oracle: the velocity within the e4m3 scheme bar (the blocks themselves are pinned against
@@ -298,6 +339,34 @@ def test_klein_single_block_sampled():
     ref = O.single_block(x, vec, p, sh, c, s, rows=rows)
     emu = O.single_block(x, vec, p, sh, c, s, rows=rows, rnd=S.round_bf16)
     flux_check("klein single rows", g[:, rows], emu, ref, stated=False)
+
+
+def test_klein_i2i_blocks_sampled():
+    """Flux.2 Klein block shapes with image-to-image reference tokens: 512 text
+    + a 32x32 target grid + a 32x32 reference grid (positions (1, h, w)), a
+    double and a single block, sampled rows from the text, target and
+    reference tokens against the oracle."""
+    cfg = dict(B=1, L_txt=512, grid_h=32, grid_w=32, ref_h=32, ref_w=32, **KLEIN)
+    sh = swiglu_shape(cfg)
+    c, s = tables(cfg)
+    p = S.double_block_params("klein.i2i.d", cfg["D"], cfg["d_head"], cfg["D_mlp"], mlp="swiglu")
+    a = S.activations(1, cfg["L_txt"], sh.L_img, cfg["D"])
+    gt, gi, _ = run_double(cfg, p, a)
+    rt_rows = _sample_rows(cfg["L_txt"], 3, 11)
+    ri_rows = np.unique(np.concatenate([_sample_rows(sh.L_gen, 3, 12), sh.L_gen + _sample_rows(sh.L_ref, 3, 13)]))
+    rt, ri = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows)
+    et, ei = O.double_block(a["x_txt"], a["x_img"], a["vec"], p, sh, c, s, rows_txt=rt_rows, rows_img=ri_rows,
+                            rnd=S.round_bf16)
+    flux_check("klein i2i double x_txt rows", gt[:, rt_rows], et, rt, stated=False)
+    flux_check("klein i2i double x_img rows (target and reference)", gi[:, ri_rows], ei, ri, stated=False)
+    q = S.single_block_params("klein.i2i.s", cfg["D"], cfg["d_head"], cfg["D_mlp"], mlp="swiglu")
+    x = S.normal_f32("klein.i2i.x", (1, sh.L, cfg["D"]))
+    vec = S.normal_f32("klein.i2i.vec", (1, cfg["D"]))
+    g, _ = run_single(cfg, q, x, vec)
+    rows = np.unique(np.concatenate([rt_rows, cfg["L_txt"] + ri_rows]))
+    ref = O.single_block(x, vec, q, sh, c, s, rows=rows)
+    emu = O.single_block(x, vec, q, sh, c, s, rows=rows, rnd=S.round_bf16)
+    flux_check("klein i2i single rows", g[:, rows], emu, ref, stated=False)
 
 
 # ------------------------------------------------------------------ FP8 (e4m3) blocks

@@ -25,12 +25,18 @@ def _gpu():
 
 
 # ------------------------------------------------------------------ RoPE
-@pytest.mark.parametrize("cfg", [CONFIGS["c1"], CONFIGS["d128"], CONFIGS["tail"], FULL["c3"], FULL["c4"]])
+# image-to-image: 1200x800 target (75x50 latent grid) plus a reference latent of the same size
+I2I_1200 = dict(B=1, L_txt=512, grid_h=75, grid_w=50, ref_h=75, ref_w=50, D=4096, H=32, d_head=128, D_mlp=12288,
+                rope_axes=(16, 56, 56))
+
+
+@pytest.mark.parametrize("cfg", [CONFIGS["c1"], CONFIGS["d128"], CONFIGS["tail"], FULL["c3"], FULL["c4"],
+                                 dict(CONFIGS["d128"], ref_h=3, ref_w=7), I2I_1200])
 def test_rope_tables_bit_exact(cfg):
     shape = api_shape(cfg)
     ids, cs, sn = gpu_tables(shape)
     torch.cuda.synchronize()
-    ref_ids = O.rope_ids(cfg["L_txt"], cfg["grid_h"], cfg["grid_w"])
+    ref_ids = O.rope_ids(cfg["L_txt"], cfg["grid_h"], cfg["grid_w"], cfg.get("ref_h", 0), cfg.get("ref_w", 0))
     c, s = tables(cfg)
     assert np.array_equal(ids.cpu().numpy(), ref_ids)
     gc, gs = cs.cpu().numpy(), sn.cpu().numpy()

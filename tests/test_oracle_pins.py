@@ -89,6 +89,18 @@ def test_rope_ids_layout():
     assert ids.dtype == np.int32 and ids.tolist() == expect
 
 
+def test_rope_ids_with_reference_layout():
+    """Reference grid 1 x 3 after a 2 x 2 target and 2 text tokens, written out
+    by hand: the reference tokens sit at (1, h, w) on their own grid."""
+    ids = O.rope_ids(2, 2, 2, 1, 3)
+    expect = [[0, 0, 0], [0, 0, 0], [0, 0, 0], [0, 0, 1], [0, 1, 0], [0, 1, 1], [1, 0, 0], [1, 0, 1], [1, 0, 2]]
+    assert ids.dtype == np.int32 and ids.tolist() == expect
+    # a target token and the reference token at the same (h, w) differ only on the axis-0 pairs
+    c, s = O.rope_tables(O.rope_ids(0, 2, 3, 2, 3), (16, 24, 24), 10000.0)
+    assert np.array_equal(c[:6, 8:], c[6:, 8:]) and np.array_equal(s[:6, 8:], s[6:, 8:])
+    assert not np.allclose(c[:6, :8], c[6:, :8])
+
+
 def test_latent_token_counts_golden():
     g = json.load(open(os.path.join(GOLD, "latent_tokens.json")))
     for c in g["cases"]:
@@ -203,8 +215,17 @@ def _tables(sh):
     return O.rope_tables(O.rope_ids(sh.L_txt, sh.grid_h, sh.grid_w), sh.rope_axes, sh.rope_theta)
 
 
+def _torch_ids(sh):
+    """Position ids written out in torch from the reading (independent of the
+    oracle's rope_ids): text (0, 0, 0), target (0, h, w), reference (1, h, w)."""
+    gh, gw, rh, rw = sh.grid_h, sh.grid_w, sh.ref_h, sh.ref_w
+    tgt = torch.stack([torch.zeros(gh * gw), torch.arange(gh).repeat_interleave(gw), torch.arange(gw).repeat(gh)], 1)
+    ref = torch.stack([torch.ones(rh * rw), torch.arange(rh).repeat_interleave(rw), torch.arange(rw).repeat(rh)], 1)
+    return torch.cat([torch.zeros(sh.L_txt, 3), tgt, ref], 0).to(torch.int64).numpy()
+
+
 def _torch_rope(x, sh):
-    ids = O.rope_ids(sh.L_txt, sh.grid_h, sh.grid_w)
+    ids = _torch_ids(sh)
     ang = []
     for a, d_a in enumerate(sh.rope_axes):
         om = torch.tensor(sh.rope_theta) ** (-torch.arange(0, d_a, 2) / d_a)
@@ -698,13 +719,13 @@ def _step_case(sh):
         for k in list(d):
             if k.endswith("_w"):
                 d[k] = d[k] * 10.0
-    x_lat = rnd("stp.lat", (sh.B, sh.L_img, sh.C_lat))
+    x_lat = rnd("stp.lat", (sh.B, sh.L_gen, sh.C_lat))
     x_txt = rnd("stp.txt", (sh.B, sh.L_txt, sh.D))
     vec_add = rnd("stp.add", (sh.B, sh.D))
     return W, x_lat, x_txt, vec_add
 
 
-def _torch_step(x_lat, x_txt, sigma, sigma_next, W, sh, vec_add):
+def _torch_step(x_lat, x_txt, sigma, sigma_next, W, sh, vec_add, x_ref=None):
     T = torch.from_numpy
     w = {k: T(v) for k, v in W.items() if isinstance(v, np.ndarray)}
     half = sh.t_dim // 2
@@ -713,14 +734,15 @@ def _torch_step(x_lat, x_txt, sigma, sigma_next, W, sh, vec_add):
     vec = F.linear(F.silu(F.linear(torch.cat([a.cos(), a.sin()], 1), w["t_w1"], w["t_b1"])), w["t_w2"], w["t_b2"])
     vec = vec + T(vec_add)
     h_txt = x_txt
-    h_img = F.linear(T(x_lat), w["img_in_w"], w["img_in_b"]).numpy()
+    lat = T(x_lat) if x_ref is None else torch.cat([T(x_lat), T(x_ref)], 1)
+    h_img = F.linear(lat, w["img_in_w"], w["img_in_b"]).numpy()
     for blk in W["double"]:
         h_txt, h_img = _torch_double(h_txt, h_img, vec.numpy(), blk, sh)
     x = torch.cat([T(h_txt), T(h_img)], 1)
     for blk in W["single"]:
         x = T(_torch_single(x.numpy(), vec.numpy(), blk, sh))
     m = F.linear(F.silu(vec), w["final_mod_w"], w["final_mod_b"]).unsqueeze(1).chunk(2, -1)
-    y = F.layer_norm(x[:, sh.L_txt:], (sh.D,), eps=sh.eps_ln) * (1 + m[1]) + m[0]
+    y = F.layer_norm(x[:, sh.L_txt:sh.L_txt + sh.grid_h * sh.grid_w], (sh.D,), eps=sh.eps_ln) * (1 + m[1]) + m[0]
     v = F.linear(y, w["final_w"], w["final_b"])
     return (T(x_lat) + (sigma_next - sigma) * v).numpy(), v.numpy()
 
@@ -736,22 +758,27 @@ def test_denoise_step_vs_torch_restatement():
     assert rel(got_x, x_lat) > 1e-3  # the step moves the latent
 
 
-def _step_variant(x_lat, x_txt, sigma, sigma_next, W, sh, vec_add=None, rnd=None, qin=None, *, final_head=False,
-                  skip_img_in=False, img_first=False, drop_vec_add=False):
+def _step_variant(x_lat, x_txt, sigma, sigma_next, W, sh, vec_add=None, rnd=None, qin=None, x_ref=None, *,
+                  final_head=False, skip_img_in=False, img_first=False, drop_vec_add=False, final_on_ref=False):
     """The step composed from the oracle's public pieces, with switches that
     each plant one composition mistake (all off: the oracle's own step)."""
-    cos, sin = O.rope_tables(O.rope_ids(sh.L_txt, sh.grid_h, sh.grid_w), sh.rope_axes, sh.rope_theta)
+    cos, sin = O.rope_tables(O.rope_ids(sh.L_txt, sh.grid_h, sh.grid_w, sh.ref_h, sh.ref_w), sh.rope_axes,
+                             sh.rope_theta)
     vec = O.time_embed(sigma, W, sh)
     if vec_add is not None and not drop_vec_add:
         vec = vec + vec_add
-    h_img = np.asarray(x_lat, np.float64) if skip_img_in else O.img_in(x_lat, W)
+    lat = x_lat if x_ref is None else np.concatenate([x_lat, x_ref], axis=1)
+    h_img = np.asarray(lat, np.float64) if skip_img_in else O.img_in(lat, W)
     h_txt = x_txt
     for blk in W["double"]:
         h_txt, h_img = O.double_block(h_txt, h_img, vec, blk, sh, cos, sin)
     x = np.concatenate([h_img, h_txt] if img_first else [h_txt, h_img], axis=1)
     for blk in W["single"]:
         x = O.single_block(x, vec, blk, sh, cos, sin)
-    img = x[:, :sh.L_img] if (img_first or final_head) else x[:, sh.L_txt:]
+    if final_on_ref:
+        img = x[:, sh.L_txt + sh.L_gen:]
+    else:
+        img = x[:, :sh.L_gen] if (img_first or final_head) else x[:, sh.L_txt:sh.L_txt + sh.L_gen]
     v = O.final_layer(img, vec, W, sh)
     return O.euler_step(x_lat, v, sigma, sigma_next), v
 
@@ -773,6 +800,54 @@ def test_planted_step_composition_mistakes_are_caught(monkeypatch, mistake):
         return _step_variant(*args, **kw, **{mistake: True})
 
     _planted(monkeypatch, "denoise_step", planted, test_denoise_step_vs_torch_restatement)
+
+
+# Image-to-image: the reference latent is projected like the noise latent and
+# appended to its tokens (Luminal blog, "The AMD MI300X pipeline"); positions
+# (1, h, w) per the reading in rope_ids.  The reference grid has the target's
+# size here so that a step reading the wrong image slice still runs.
+SH_I2I = O.Shape(B=2, L_txt=5, grid_h=3, grid_w=4, D=64, H=2, d_head=32, D_mlp=96, rope_axes=(8, 12, 12),
+                 C_lat=64, t_dim=32, n_double=2, n_single=2, ref_h=3, ref_w=4)
+
+
+def test_i2i_step_vs_torch_restatement():
+    sh = SH_I2I
+    W, x_lat, x_txt, vec_add = _step_case(sh)
+    x_ref = rnd("stp.ref", (sh.B, sh.L_ref, sh.C_lat))
+    got_x, got_v = O.denoise_step(x_lat, x_txt, 0.8, 0.7, W, sh, vec_add=vec_add, x_ref=x_ref)
+    ref_x, ref_v = _torch_step(x_lat, x_txt, 0.8, 0.7, W, sh, vec_add, x_ref=x_ref)
+    assert got_v.shape == (sh.B, sh.L_gen, sh.C_lat)
+    assert rel(got_v, ref_v) < 1e-12, rel(got_v, ref_v)
+    assert rel(got_x - x_lat, ref_x - x_lat) < 1e-12
+    # the reference reaches the velocity of the target tokens (through attention)
+    other, _ = O.denoise_step(x_lat, x_txt, 0.8, 0.7, W, sh, vec_add=vec_add, x_ref=x_ref * 0.5)
+    assert rel(other, got_x) > 1e-6
+
+
+def test_planted_reference_mistakes_are_caught(monkeypatch):
+    """Reference tokens at axis-0 index 0 (the target's positions); the final
+    layer applied to the reference tokens instead of the target ones."""
+    orig_ids, orig_step = O.rope_ids, O.denoise_step
+
+    def ids_no_index(L_txt, gh, gw, rh=0, rw=0):
+        ids = orig_ids(L_txt, gh, gw, rh, rw)
+        ids[:, 0] = 0
+        return ids
+
+    _planted(monkeypatch, "rope_ids", ids_no_index, test_i2i_step_vs_torch_restatement)
+    monkeypatch.setattr(O, "rope_ids", orig_ids)
+    sh = SH_I2I
+    W, x_lat, x_txt, vec_add = _step_case(sh)
+    x_ref = rnd("stp.ref", (sh.B, sh.L_ref, sh.C_lat))
+    a = O.denoise_step(x_lat, x_txt, 0.8, 0.7, W, sh, vec_add=vec_add, x_ref=x_ref)
+    b = _step_variant(x_lat, x_txt, 0.8, 0.7, W, sh, vec_add, x_ref=x_ref)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])  # the variant without switches is the step
+
+    def planted(*args, **kw):
+        return _step_variant(*args, **kw, final_on_ref=True)
+
+    _planted(monkeypatch, "denoise_step", planted, test_i2i_step_vs_torch_restatement)
+    monkeypatch.setattr(O, "denoise_step", orig_step)
 
 
 # ------------------------------------------------------------------ int8 quantiser
