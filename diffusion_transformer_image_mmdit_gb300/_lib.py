@@ -97,6 +97,8 @@ SIGNATURES = {
     "mmdit_ln_modulate_f8": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_int64, c_float, c_void_p,
                                      c_void_p, c_void_p, c_void_p]),
     "mmdit_gemv": (c_int, [POINTER(Linear), c_int, c_int, c_int, c_void_p, c_int, c_void_p, c_void_p]),
+    "mmdit_heads_pack": (c_int, [c_void_p, c_int64, c_int, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "mmdit_heads_unpack": (c_int, [c_void_p, c_int64, c_int, c_int, c_void_p, c_int, c_void_p]),
     "mmdit_shift_mu": (c_double, [c_int]),
     "mmdit_sigma_schedule": (c_int, [c_int, c_double, POINTER(c_double)]),
     "mmdit_time_embed": (c_int, [POINTER(Shape), POINTER(Linear), POINTER(Linear), c_double, c_void_p, c_void_p,

@@ -406,6 +406,19 @@ def mmdit_gemv(lin: LinearDev, x: torch.Tensor, act: int, y: torch.Tensor, strea
     call("mmdit_gemv", ctypes.byref(st), B, lin.N, K, ptr(x), act, ptr(y), stream_handle(stream))
 
 
+def mmdit_heads_pack(src: torch.Tensor, sections: int, groups: int, group_cols: int, dst: torch.Tensor,
+                     stream=None):
+    """src [rows, src_ld] bf16 -> dst [groups, rows, sections, group_cols] (see include/mmdit.h)."""
+    rows, ld = src.shape
+    call("mmdit_heads_pack", ptr(src), rows, ld, sections, groups, group_cols, ptr(dst), stream_handle(stream))
+
+
+def mmdit_heads_unpack(src: torch.Tensor, groups: int, group_cols: int, dst: torch.Tensor, stream=None):
+    """src [groups, rows, group_cols] bf16 -> dst [rows, dst_ld] (head group g at columns g * group_cols)."""
+    rows, ld = dst.shape
+    call("mmdit_heads_unpack", ptr(src), rows, groups, group_cols, ptr(dst), ld, stream_handle(stream))
+
+
 def mmdit_time_embed(shape: Shape, time1: LinearDev, time2: LinearDev, sigma: float, vec: torch.Tensor,
                      ws: torch.Tensor, stream=None):
     a, b = time1.struct(), time2.struct()

@@ -773,7 +773,7 @@ const char* mmdit_kernel_name(int kernel_id) {
   static const char* names[KID_COUNT] = {"gemm_bf16_tc", "attn_fwd",   "ln_modulate", "gemv",      "sinusoid",
                                          "rope_build",   "rope_apply", "euler",       "quantize_w8", "dequant_i8",
                                          "cast_bf16",    "attn_prep",  "wait_selftest", "add_f32",
-                                         "step_counter", "quantize_f8"};
+                                         "step_counter", "quantize_f8", "heads_pack",   "heads_unpack"};
   return (kernel_id >= 0 && kernel_id < KID_COUNT) ? names[kernel_id] : "unknown";
 }
 
@@ -1125,6 +1125,30 @@ int euler_step(float* x, const void* v, int v_dtype, double sigma, double sigma_
   if (n == 0) return MMDIT_OK;
   MMDIT_TRY(check_device());
   return cuda_status(launch_euler(x, v, v_dtype == MMDIT_BF16, (float)(sigma_next - sigma), n, S(stream)));
+}
+
+int mmdit_heads_pack(const void* src, int64_t rows, int src_ld, int sections, int groups, int group_cols, void* dst,
+                     void* stream) {
+  if (!src || !dst || rows < 0 || sections < 1 || groups < 1) return MMDIT_ERR_ARG;
+  if (group_cols < 8 || group_cols % 8 || src_ld % 8 || (long long)src_ld < (long long)sections * groups * group_cols)
+    return MMDIT_ERR_SHAPE;
+  if (!al16(src) || !al16(dst)) return MMDIT_ERR_ALIGN;
+  if (rows == 0) return MMDIT_OK;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_heads_pack(static_cast<const uint16_t*>(src), rows, src_ld, sections, groups, group_cols,
+                                       static_cast<uint16_t*>(dst), S(stream)));
+}
+
+int mmdit_heads_unpack(const void* src, int64_t rows, int groups, int group_cols, void* dst, int dst_ld,
+                       void* stream) {
+  if (!src || !dst || rows < 0 || groups < 1) return MMDIT_ERR_ARG;
+  if (group_cols < 8 || group_cols % 8 || dst_ld % 8 || (long long)dst_ld < (long long)groups * group_cols)
+    return MMDIT_ERR_SHAPE;
+  if (!al16(src) || !al16(dst)) return MMDIT_ERR_ALIGN;
+  if (rows == 0) return MMDIT_OK;
+  MMDIT_TRY(check_device());
+  return cuda_status(launch_heads_unpack(static_cast<const uint16_t*>(src), rows, groups, group_cols,
+                                         static_cast<uint16_t*>(dst), dst_ld, S(stream)));
 }
 
 int mmdit_quantize_w8(const void* w, int w_dtype, int N, int K, int8_t* q, float* scale, void* stream) {

@@ -99,6 +99,40 @@ __global__ void __launch_bounds__(128) ln_mod_kernel(const __grid_constant__ LnJ
   }
 }
 
+// ------------------------------------------------------------------ sequence-parallel exchange layouts
+// Ulysses sequence parallelism swaps a token shard with all heads for all
+// tokens with a head group.  pack: src rows [rows][src_ld] hold `sections`
+// consecutive sections (q | k | v) of `groups` head groups of gc columns
+// each; dst [groups][rows][sections][gc], so that the chunk for head group g
+// is contiguous.  unpack: src [groups][rows][gc] -> dst [rows][dst_ld] at
+// columns g * gc + c.  One thread per 16-byte vector (8 bf16).
+__global__ void heads_pack_kernel(const uint16_t* __restrict__ src, long long rows, int src_ld, int sections,
+                                  int groups, int gc, uint16_t* __restrict__ dst) {
+  const int v8 = gc / 8;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long per_group = rows * sections * v8;
+  if (idx >= per_group * groups) return;
+  const int g = (int)(idx / per_group);
+  long long rem = idx - g * per_group;
+  const long long r = rem / (sections * v8);
+  rem -= r * (sections * v8);
+  const int sct = (int)(rem / v8), c = (int)(rem - (long long)sct * v8);
+  const uint4 v = *reinterpret_cast<const uint4*>(src + r * src_ld + ((long long)sct * groups + g) * gc + 8 * c);
+  *reinterpret_cast<uint4*>(dst + idx * 8) = v;
+}
+
+__global__ void heads_unpack_kernel(const uint16_t* __restrict__ src, long long rows, int groups, int gc,
+                                    uint16_t* __restrict__ dst, int dst_ld) {
+  const int v8 = gc / 8;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * groups * v8) return;
+  const long long r = idx / ((long long)groups * v8);
+  const long long rem = idx - r * groups * v8;
+  const int g = (int)(rem / v8), c = (int)(rem - (long long)g * v8);
+  *reinterpret_cast<uint4*>(dst + r * dst_ld + (long long)g * gc + 8 * c) =
+      *reinterpret_cast<const uint4*>(src + ((long long)g * rows + r) * gc + 8 * c);
+}
+
 // ------------------------------------------------------------------ GEMV
 // y[b, n] = sum_k W[n, k] act(x[b, k]) (* scale[n]) + bias[n] for B <= 8 rows
 // of x (K a multiple of 16): one warp per output row, 16-byte weight loads
@@ -785,6 +819,26 @@ cudaError_t launch_rope_build(int L_txt, int grid_w, int n_gen, int ref_w, int L
   launch_begin(KID_ROPE_BUILD, st);
   rope_build_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(L_txt, grid_w, n_gen, ref_w > 0 ? ref_w : 1, L,
                                                                  axes[0], axes[1], axes[2], theta, ids, cs, sn);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_heads_pack(const uint16_t* src, long long rows, int src_ld, int sections, int groups, int gc,
+                              uint16_t* dst, cudaStream_t st) {
+  const long long n = rows * sections * groups * (gc / 8);
+  if (n == 0) return cudaSuccess;
+  launch_begin(KID_HEADS_PACK, st);
+  heads_pack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, rows, src_ld, sections, groups, gc, dst);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_heads_unpack(const uint16_t* src, long long rows, int groups, int gc, uint16_t* dst, int dst_ld,
+                                cudaStream_t st) {
+  const long long n = rows * groups * (gc / 8);
+  if (n == 0) return cudaSuccess;
+  launch_begin(KID_HEADS_UNPACK, st);
+  heads_unpack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, rows, groups, gc, dst, dst_ld);
   launch_end(st);
   return cudaGetLastError();
 }

@@ -67,6 +67,12 @@ cudaError_t launch_dequant_i8(const int8_t* q, uint16_t* out, long long n, cudaS
 cudaError_t launch_quantize_f8(const void* x, bool x_bf16, long long rows, int K, long long ld, uint8_t* q,
                                long long qld, float* scale, cudaStream_t st);
 cudaError_t launch_cast_bf16(const float* x, uint16_t* y, long long n, cudaStream_t st);
+// Ulysses exchange layouts (bf16): pack src [rows][src_ld] (sections x groups x gc columns) into
+// dst [groups][rows][sections][gc]; unpack src [groups][rows][gc] into dst [rows][dst_ld] (gc % 8 == 0).
+cudaError_t launch_heads_pack(const uint16_t* src, long long rows, int src_ld, int sections, int groups, int gc,
+                              uint16_t* dst, cudaStream_t st);
+cudaError_t launch_heads_unpack(const uint16_t* src, long long rows, int groups, int gc, uint16_t* dst, int dst_ld,
+                                cudaStream_t st);
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned* status, cudaStream_t st);
 cudaError_t launch_attn_prep(const uint16_t* qkv, long long qkv_ld, int B, int L, int L_txt, int H, int d,
                              const float* gq0, const float* gq1, const float* gk0, const float* gk1, float eps,

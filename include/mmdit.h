@@ -291,6 +291,30 @@ int mmdit_step_i2i_fwd(const mmdit_shape_t* shape, const mmdit_step_w_t* w, floa
                        const float* x_txt_in, double sigma, double sigma_next, float* v_out, void* ws,
                        size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------ sequence parallelism */
+/* Exchange layouts of Ulysses sequence parallelism.  The SGLang blog
+ * ("Architecture Deep Dive", "SGLang Diffusion Serving") scales the DiT over
+ * several GPUs with USP, hybrid Ulysses sequence parallelism and ring
+ * attention; Ulysses gives each of P ranks a shard of the token sequence for
+ * the linears and, around attention, swaps it for all tokens of H / P heads
+ * with two all-to-all exchanges.  These calls lay the data out for those
+ * exchanges on one device; the exchanges themselves belong to the caller's
+ * collective library.  All data bf16, pointers device and 16-byte aligned,
+ * group_cols and the row strides multiples of 8; no workspace.
+ * mmdit_heads_pack: src [rows][src_ld] whose first sections * groups *
+ * group_cols columns hold `sections` blocks (q | k | v) of `groups` head
+ * groups of group_cols columns each; writes dst [groups][rows][sections]
+ * [group_cols], the chunk for head group g contiguous at g * rows * sections
+ * * group_cols.
+ * mmdit_heads_unpack: src [groups][rows][group_cols] -> dst [rows][dst_ld],
+ * head group g at columns g * group_cols .. (g + 1) * group_cols.
+ * Errors: MMDIT_ERR_ARG (null pointer, counts below 1), MMDIT_ERR_SHAPE
+ * (widths), MMDIT_ERR_ALIGN; nothing is launched then. */
+int mmdit_heads_pack(const void* src, int64_t rows, int src_ld, int sections, int groups, int group_cols, void* dst,
+                     void* stream);
+int mmdit_heads_unpack(const void* src, int64_t rows, int groups, int group_cols, void* dst, int dst_ld,
+                       void* stream);
+
 /* ------------------------------------------------------------ sigma schedule */
 /* The sampler's noise levels.  The Luminal blog (section "The AMD MI300X
  * pipeline") integrates the latent with an Euler sampler, and the flux-amd-rocm
