@@ -35,14 +35,26 @@ constexpr float kRescaleThreshold = 16.0f;
 //   warps 0-3   softmax of tile 0; warps 4-7 softmax of tile 1 (one query
 //               row per thread, 216 registers each after setmaxnreg so a
 //               whole 128-score row stays in registers).
-//   warp 8      TMA: both Q tiles once, then K and V^T tiles, 2-stage ring.
+//   warp 8      TMA: both Q tiles once, then V^T(j) and K(j + 1) tiles (the
+//               order their ring slots free up and the MMAs need them),
+//               2-stage rings.
 //   warp 9      TMEM (S0 | S1 | O0 | O1, 128 columns each) and the MMAs, in
-//               the order S0(j), S1(j), then per j: PV0(j), S0(j+1), PV1(j),
+//               the order S0(0), S1(0), then per j: PV0(j), S0(j+1), PV1(j),
 //               S1(j+1), so the tensor pipe works on one tile while the
 //               other tile's softmax runs.  P(j) is written by the softmax
 //               over the first 64 columns of S(j) as packed bf16 and read by
 //               the P V MMA straight from TMEM; S(j+1) reuses the columns
 //               only after PV(j), which precedes it in the MMA issue order.
+//               The tensor pipe accepts only a few MMAs ahead of the one it
+//               executes, so the issuing warp runs close behind it: every
+//               wait it makes (about 175 cycles even on a completed phase),
+//               every branch around an MMA group and every extra commit
+//               shows up as idle tensor cycles.  The steady-state loop is
+//               therefore straight-line (the last KV tile is peeled off), the
+//               K(j+1) and V(j+1) waits sit inside the preceding MMA group
+//               where queued MMAs cover them, and the K ring slot is released
+//               by the softmax warps of tile 1 (they see S1(j) complete)
+//               instead of by a second commit.
 //   warps 10-11 idle (they complete the third warpgroup, which gives its
 //               registers to the softmax warpgroups).
 // Softmax per KV tile: one TMEM load of the S row, tree max/sum, exp2 on the
@@ -76,7 +88,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
   const uint32_t q_full = smem_u32(bars + 0);
   const uint32_t k_full0 = smem_u32(bars + 1);    // [2] per stage
   const uint32_t v_full0 = smem_u32(bars + 3);    // [2] per stage
-  const uint32_t k_empty0 = smem_u32(bars + 5);   // [2] per stage: freed after both S MMAs of the K tile
+  const uint32_t k_empty0 = smem_u32(bars + 5);   // [2] per stage: freed once S1 of the K tile has completed
   const uint32_t s_full0 = smem_u32(bars + 7);    // [2] per tile
   const uint32_t p_full0 = smem_u32(bars + 9);    // [2] per tile
   const uint32_t pv_done0 = smem_u32(bars + 11);  // [2] per tile
@@ -135,6 +147,8 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
     for (int j = 0; j < nkv; ++j) {
       if (!mbar_wait_warp(s_full, j & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
       tc_fence_after();
+      // S1(j) has completed, and S0(j) before it: the K(j) ring slot is free
+      if (t == 1 && quad == 0 && lane == 0) mbar_arrive(k_empty0 + 8 * (j & 1));
       const int kv0 = j * kAttnBN;
       float sv[kAttnBN];
       {
@@ -150,14 +164,17 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         for (int c = 0; c < kAttnBN; ++c)
           if (kv0 + c >= p.L) sv[c] = -INFINITY;
       }
-      // row max: 8 independent chains of three-input max
+      // row max: 8 independent chains of three-input max over columns
+      // 8..119 in pairs of 8, then columns 120..127
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-      for (int c = 8; c < kAttnBN; c += 16)
+      for (int c = 8; c + 16 <= kAttnBN; c += 16)
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[kAttnBN - 8 + i]);
       const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       const float m_new = fmaxf(m_run, mx * sl2);
       // P V(j - 1) has completed here: S(j) was issued after it and the
@@ -249,9 +266,10 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
 #pragma unroll
           for (int hf = 0; hf < HD / 64; ++hf)
             tma_load_3d(smem_u32(sQ + t * SM::QT + hf * kHalf), &tmQK, q_full, h * HD + hf * 64, q0 + t * kAttnBM, b);
-        // Loads in the order the MMAs need them: K(j + 1) (for S(j + 1)) before
-        // V(j) (for P V(j)).  K and V rings are freed independently, so a K
-        // slot is refilled as soon as both S MMAs that read it complete.
+        // Loads in the order the MMAs need them: V(j) (for P V0(j)) before
+        // K(j + 1) (for S0(j + 1), issued after P V0(j)).  This is also the
+        // order in which their ring slots free up: V(j)'s after P V1(j - 2),
+        // K(j + 1)'s after S1(j - 1), which follows it in the tensor pipe.
         int n_k = 0, n_v = 0;  // tiles whose loads were issued (for the drain after a time-out)
         auto load_k = [&](int j) -> bool {
           const int st = j & 1;
@@ -278,7 +296,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
           return true;
         };
         bool okp = load_k(0);
-        for (int j = 0; okp && j < nkv; ++j) okp = (j + 1 >= nkv || load_k(j + 1)) && load_v(j);
+        for (int j = 0; okp && j < nkv; ++j) okp = load_v(j) && (j + 1 >= nkv || load_k(j + 1));
         if (*abort_flag) {
           // After a time-out anywhere in the CTA: wait (bounded) until every
           // copy still in flight into this CTA's shared memory has landed (Q,
@@ -298,51 +316,82 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       const uint32_t leader = elect_one_sync();
       const uint32_t idesc_s = idesc_bf16(128, kAttnBN);
       const uint32_t idesc_o = idesc_bf16(128, HD);
-      // Descriptors of both Q tiles and both K / V stages are built once;
-      // each MMA adds a compile-time offset in 16-byte units.
-      const uint64_t dQ0 = sdesc_k128(smem_u32(sQ)), dQ1 = sdesc_k128(smem_u32(sQ + SM::QT));
-      const uint64_t dK0 = sdesc_k128(smem_u32(sK)), dK1 = sdesc_k128(smem_u32(sK + SM::K));
-      const uint64_t dV0 = sdesc_k128(smem_u32(sV)), dV1 = sdesc_k128(smem_u32(sV + SM::V));
+      // Descriptors of Q tile 0 and of ring stage 0 are built once; an MMA
+      // adds the tile / stage / K-step offset in 16-byte units to the start
+      // address field (bits 0-13, which holds every shared address < 256 KB).
+      const uint64_t dQ0 = sdesc_k128(smem_u32(sQ));
+      const uint64_t dK0 = sdesc_k128(smem_u32(sK));
+      const uint64_t dV0 = sdesc_k128(smem_u32(sV));
       auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
         return mbar_wait_warp(bar, parity, abort_flag, p.status, ST_TIMEOUT_MMA);
       };
-      auto issue_s = [&](int t, int j) -> bool {
-        const int st = j & 1;
-        if (t == 0 && !wait(k_full0 + 8 * st, (j >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t aQ = t ? dQ1 : dQ0;
-        const uint64_t bK = st ? dK1 : dK0;
+      // S(t, j) = Q_t K(j)^T (kS = d / 16 steps of K = 16) and
+      // O_t += P_t(j) V(j) (8 steps: 128 keys), MMAs k0..k1-1 of those steps.
+      // Operand selection is arithmetic, not a branch.
+      constexpr int kS = HD / 16;
+      auto mma_s = [&](int t, int j, int k0, int k1) {
+        const uint64_t aQ = dQ0 + (uint64_t)(t * (SM::QT >> 4));
+        const uint64_t bK = dK0 + (uint64_t)((j & 1) * (SM::K >> 4));
         const uint32_t dS = tmem + t * 128;
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
+        for (int k = k0; k < k1; ++k) {
           const uint32_t off = ((k >> 2) * kHalf + (k & 3) * 32) >> 4;
           umma_bf16_if(leader, dS, aQ + off, bK + off, idesc_s, k > 0 ? 1u : 0u);
         }
-        umma_commit_if(leader, s_full0 + 8 * t);
-        if (t == 1) umma_commit_if(leader, k_empty0 + 8 * st);
-        return true;
       };
-      auto issue_pv = [&](int t, int j) -> bool {
-        const int st = j & 1;
-        if (!wait(p_full0 + 8 * t, j & 1)) return false;
-        if (t == 0 && !wait(v_full0 + 8 * st, (j >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t bV = st ? dV1 : dV0;
+      auto mma_pv = [&](int t, int j, int k0, int k1) {
+        const uint64_t bV = dV0 + (uint64_t)((j & 1) * (SM::V >> 4));
         const uint32_t dO = tmem + 256 + t * 128, aP = tmem + t * 128;
         const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int k = 0; k < kAttnBN / 16; ++k) {
+        for (int k = k0; k < k1; ++k) {
           const uint32_t off = ((k >> 2) * (HD * 128) + (k & 3) * 32) >> 4;
           umma_bf16_ta_if(leader, dO, aP + k * 8, bV + off, idesc_o, k > 0 ? 1u : acc0);
         }
-        if (j + 1 == nkv) umma_commit_if(leader, pv_done0 + 8 * t);  // for the final O / l
-        if (t == 1) umma_commit_if(leader, v_empty0 + 8 * st);
-        return true;
       };
-      bool ok = wait(q_full, 0) && issue_s(0, 0) && issue_s(1, 0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        ok = issue_pv(0, j) && (j + 1 >= nkv || issue_s(0, j + 1)) && issue_pv(1, j) &&
-             (j + 1 >= nkv || issue_s(1, j + 1));
+      // After a failed wait the loop still issues the MMAs of that step (all
+      // operands lie inside this CTA's shared and tensor memory) and stops at
+      // the next loop test: no branch sits between the waits and the MMAs.
+      bool ok = wait(q_full, 0) && wait(k_full0, 0);
+      tc_fence_after();
+      mma_s(0, 0, 0, kS);
+      umma_commit_if(leader, s_full0);
+      mma_s(1, 0, 0, kS / 2);
+      ok = ok && wait(v_full0, 0);
+      tc_fence_after();
+      mma_s(1, 0, kS / 2, kS);
+      umma_commit_if(leader, s_full0 + 8);
+      int j = 0;
+#pragma unroll 1
+      for (; ok && j + 1 < nkv; ++j) {
+        const uint32_t st1 = (uint32_t)((j + 1) & 1), ph1 = (uint32_t)(((j + 1) >> 1) & 1);
+        ok = wait(p_full0, j & 1);
+        tc_fence_after();
+        mma_pv(0, j, 0, 4);
+        ok = wait(k_full0 + 8 * st1, ph1) && ok;  // K(j + 1), for S0(j + 1) below
+        tc_fence_after();
+        mma_pv(0, j, 4, 8);
+        mma_s(0, j + 1, 0, kS);
+        umma_commit_if(leader, s_full0);
+        ok = wait(p_full0 + 8, j & 1) && ok;
+        tc_fence_after();
+        mma_pv(1, j, 0, 8);
+        umma_commit_if(leader, v_empty0 + 8 * (j & 1));  // P V0(j) and P V1(j) have read V(j)
+        mma_s(1, j + 1, 0, kS / 2);
+        ok = wait(v_full0 + 8 * st1, ph1) && ok;  // V(j + 1), for P V0(j + 1)
+        tc_fence_after();
+        mma_s(1, j + 1, kS / 2, kS);
+        umma_commit_if(leader, s_full0 + 8);
+      }
+      if (ok) {  // the last KV tile
+        ok = wait(p_full0, j & 1);
+        tc_fence_after();
+        mma_pv(0, j, 0, 8);
+        umma_commit_if(leader, pv_done0);  // for the final O / l
+        ok = wait(p_full0 + 8, j & 1) && ok;
+        tc_fence_after();
+        mma_pv(1, j, 0, 8);
+        umma_commit_if(leader, pv_done0 + 8);
       }
       if (*abort_flag) {
         // every MMA this warp issued (they read shared memory and write the
