@@ -58,7 +58,8 @@ constexpr float kRescaleThreshold = 16.0f;
 //   warps 10-11 idle (they complete the third warpgroup, which gives its
 //               registers to the softmax warpgroups).
 // Softmax per KV tile: one TMEM load of the S row, tree max/sum, exp2 on the
-//               MUFU, lazy O rescale in TMEM, final O / l and bf16 store.
+//               MUFU, lazy O rescale in TMEM; at the end O / l as bf16,
+//               staged in shared memory and written with TMA tile stores.
 constexpr int kAttn2Threads = 384;
 // Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512);
 // warpgroup 2 drops to 72 and the two softmax warpgroups rise to 216:
@@ -77,7 +78,7 @@ struct Attn2Smem {
 template <int HD>
 __global__ void __launch_bounds__(kAttn2Threads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ AttnParams p) {
+                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ AttnParams p) {
   using SM = Attn2Smem<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tmQK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -237,24 +239,42 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
     if (ok && mbar_wait_warp(pv_done, 0, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) {  // the last P V only
       tc_fence_after();
       const float inv_l = 1.0f / l_run;
-      const int row = q0 + t * kAttnBM + r;
-      uint16_t* dst = p.out + ((long long)b * p.L + row) * p.out_ld + h * HD;
+      // O / l as bf16 through shared memory.  This warp's 32 rows go to its
+      // own block of the K ring (idle now: every S MMA has completed and no
+      // load is pending) in the 128-byte-swizzled layout of the output
+      // tensor map -- row `lane` at a 128-byte pitch, 16-byte chunk j at
+      // position j ^ (lane % 8), one 4 KB block per 64 columns -- and lane 0
+      // writes them out with TMA tile stores (rows at or beyond L are
+      // clipped by the tensor map).  A warp's 16-byte shared stores then take
+      // 4 wavefronts each, where direct row-per-thread global stores touched
+      // 32 scattered sectors per instruction.
+      uint8_t* stg = sK + (t * 4 + quad) * (HD / 64) * 4096;
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t raw[32];
         MMDIT_TMEM_LD32(tO + c * 32, raw);
         tmem_wait_ld();
-        float v[32];
+        uint8_t* rowp = stg + (c >> 1) * 4096 + lane * 128;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]) * inv_l;
-        if (row < p.L) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                               pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        for (int i = 0; i < 4; ++i) {
+          const int chunk = (c & 1) * 4 + i;
+          const float* v = reinterpret_cast<const float*>(raw + 8 * i);
+          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (lane & 7)) << 4)) =
+              make_uint4(pack_bf16x2(v[0] * inv_l, v[1] * inv_l), pack_bf16x2(v[2] * inv_l, v[3] * inv_l),
+                         pack_bf16x2(v[4] * inv_l, v[5] * inv_l), pack_bf16x2(v[6] * inv_l, v[7] * inv_l));
         }
       }
+      fence_proxy_async_smem();  // the shared stores are visible to the TMA unit
+      __syncwarp();
+      const int row0 = q0 + t * kAttnBM + quad * 32;
+      if (lane == 0 && row0 < p.L) {
+#pragma unroll
+        for (int hf = 0; hf < HD / 64; ++hf)
+          tma_store_3d(&tmO, smem_u32(stg + hf * 4096), h * HD + hf * 64, row0, b);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // the staging block has been read before the CTA exits
+      }
+      __syncwarp();
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
@@ -410,7 +430,8 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
 }
 
 template <int HD>
-cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, cudaStream_t s) {
+cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, const CUtensorMap& tmO, const AttnParams& p,
+                            cudaStream_t s) {
   // shared-memory opt-in once per device, safe under concurrent first calls
   static std::once_flag once[64];
   static cudaError_t setup_err[64];
@@ -423,17 +444,17 @@ cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, con
   if (setup_err[dev] != cudaSuccess) return setup_err[dev];
   dim3 grid((p.n_q_tiles + 1) / 2, p.H, p.B);
   launch_begin(KID_ATTENTION, s);
-  attn_fwd_kernel<HD><<<grid, kAttn2Threads, Attn2Smem<HD>::total, s>>>(tmQK, tmV, p);
+  attn_fwd_kernel<HD><<<grid, kAttn2Threads, Attn2Smem<HD>::total, s>>>(tmQK, tmV, tmO, p);
   launch_end(s);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, int d_head,
-                             cudaStream_t s) {
-  if (d_head == 128) return launch_attn2_hd<128>(tmQK, tmV, p, s);
-  return launch_attn2_hd<64>(tmQK, tmV, p, s);
+cudaError_t launch_attention(const CUtensorMap& tmQK, const CUtensorMap& tmV, const CUtensorMap& tmO,
+                             const AttnParams& p, int d_head, cudaStream_t s) {
+  if (d_head == 128) return launch_attn2_hd<128>(tmQK, tmV, tmO, p, s);
+  return launch_attn2_hd<64>(tmQK, tmV, tmO, p, s);
 }
 
 }  // namespace mmdit

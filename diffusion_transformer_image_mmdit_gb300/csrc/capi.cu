@@ -314,6 +314,12 @@ int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint
   if (!make_tmap_3d(&tv, vT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)L, (uint64_t)D, (uint64_t)B,
                     (uint64_t)Lpad * 2, (uint64_t)Lpad * 2 * D, 64, (uint32_t)d_head, true))
     return MMDIT_ERR_ALIGN;
+  // Output rows of D columns at a pitch of out_ld elements, written by 32-row
+  // TMA tile stores; rows at or beyond L are clipped.
+  CUtensorMap to;
+  if (!make_tmap_3d(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)D, (uint64_t)L, (uint64_t)B,
+                    (uint64_t)out_ld * 2, (uint64_t)out_ld * 2 * L, 64, 32, true))
+    return MMDIT_ERR_ALIGN;
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   p.L = L;
@@ -322,10 +328,8 @@ int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint
   p.n_q_tiles = (L + kAttnBM - 1) / kAttnBM;
   p.n_kv_tiles = (L + kAttnBN - 1) / kAttnBN;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d_head));
-  p.out = out;
-  p.out_ld = out_ld;
   p.status = device_status_ptr();
-  return cuda_status(launch_attention(tq, tv, p, d_head, st));
+  return cuda_status(launch_attention(tq, tv, to, p, d_head, st));
 }
 
 static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, uint16_t* out, long long out_ld,

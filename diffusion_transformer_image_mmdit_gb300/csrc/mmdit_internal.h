@@ -83,8 +83,6 @@ constexpr int kAttnBN = 128;  // keys per KV tile
 struct AttnParams {
   int L, H, B, n_q_tiles, n_kv_tiles;
   float scale_log2;              // log2(e) / sqrt(d_head)
-  uint16_t* out;        // [B][L][out_ld], head h at column h*d
-  long long out_ld;
   unsigned* status;
 };
 
@@ -126,8 +124,10 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_gemm(const GemmGroup& g, cudaStream_t s);
-cudaError_t launch_attention(const CUtensorMap& tmQK, const CUtensorMap& tmV, const AttnParams& p, int d_head,
-                             cudaStream_t s);
+// tmO: bf16 output [B][L][out_ld] (head h at column h*d), box 64 columns x 32
+// rows, 128-byte swizzle.
+cudaError_t launch_attention(const CUtensorMap& tmQK, const CUtensorMap& tmV, const CUtensorMap& tmO,
+                             const AttnParams& p, int d_head, cudaStream_t s);
 int num_sms();
 
 // Status (an MMDIT_* code) of the current device for the kernels: sm_103,
