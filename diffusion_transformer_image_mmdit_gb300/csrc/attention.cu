@@ -33,8 +33,10 @@ constexpr float kRescaleThreshold = 16.0f;
 
 // Two query tiles per CTA (256 rows of one (sample, head)), K/V tiles shared.
 //   warps 0-3   softmax of tile 0; warps 4-7 softmax of tile 1 (one query
-//               row per thread, 216 registers each after setmaxnreg so a
-//               whole 128-score row stays in registers).
+//               row per thread, 208 registers each after setmaxnreg so a
+//               whole 128-score row stays in registers).  P goes back to
+//               TMEM in two halves, each with its own barrier, so P V(j)
+//               starts on keys 0..63 while keys 64..127 are exponentiated.
 //   warp 8      TMA: both Q tiles once, then V^T(j) and K(j + 1) tiles (the
 //               order their ring slots free up and the MMAs need them),
 //               2-stage rings.
@@ -62,10 +64,11 @@ constexpr float kRescaleThreshold = 16.0f;
 //               staged in shared memory and written with TMA tile stores.
 constexpr int kAttn2Threads = 384;
 // Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512);
-// warpgroup 2 drops to 72 and the two softmax warpgroups rise to 216:
-// 128 x 72 + 256 x 216 = 64512.
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsControl = 72;
+// warpgroup 2 drops to 88 and the two softmax warpgroups rise to 208:
+// 128 x 88 + 256 x 208 = 64512.  A softmax thread holds a 128-score row
+// and 64 packed P words; the MMA warp's unrolled issue loop needs about 88.
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsControl = 88;
 
 template <int HD>
 struct Attn2Smem {
@@ -95,7 +98,8 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
   const uint32_t pv_done0 = smem_u32(bars + 11);  // [2] per tile
   const uint32_t v_empty0 = smem_u32(bars + 13);  // [2] per stage: freed after both P V MMAs of the V tile
   const uint32_t mma_done = smem_u32(bars + 15);  // after a time-out: every issued MMA has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  const uint32_t p_half0 = smem_u32(bars + 16);   // [2] per tile: P over keys 0..63 written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -114,6 +118,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       mbar_init(v_empty0 + 8 * i, 1);
       mbar_init(s_full0 + 8 * i, 1);
       mbar_init(p_full0 + 8 * i, 4);
+      mbar_init(p_half0 + 8 * i, 4);
       mbar_init(pv_done0 + 8 * i, 1);
     }
     mbar_init(mma_done, 1);
@@ -141,7 +146,8 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
-    const uint32_t s_full = s_full0 + 8 * t, p_full = p_full0 + 8 * t, pv_done = pv_done0 + 8 * t;
+    const uint32_t s_full = s_full0 + 8 * t, p_full = p_full0 + 8 * t, p_half = p_half0 + 8 * t;
+    const uint32_t pv_done = pv_done0 + 8 * t;
     float m_run = -INFINITY, l_run = 0.f;
     const float sl2 = p.scale_log2;
     bool ok = true;
@@ -224,10 +230,20 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         float p0, p1;
         f2_unpack(p2, p0, p1);
         pk[c] = pack_bf16x2(p0, p1);
+        // P over keys 0..63 is complete after pair 31: it is stored then,
+        // and handed over 8 pairs later (the store's latency overlaps those
+        // pairs), so that P V(j) starts on those keys while the other half
+        // is computed.
+        if (c == kAttnBN / 4 - 1) MMDIT_TMEM_ST32(tS, pk);
+        if (c == kAttnBN / 4 + 7) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_half);
+        }
       }
       float ls[2];
       f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), ls[0], ls[1]);
-      MMDIT_TMEM_ST32(tS, pk);
       MMDIT_TMEM_ST32(tS + 32, (pk + 32));
       l_run += ls[0] + ls[1];
       tmem_wait_st();
@@ -384,17 +400,22 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
 #pragma unroll 1
       for (; ok && j + 1 < nkv; ++j) {
         const uint32_t st1 = (uint32_t)((j + 1) & 1), ph1 = (uint32_t)(((j + 1) >> 1) & 1);
-        ok = wait(p_full0, j & 1);
+        ok = wait(p_half0, j & 1);  // P0(j) over keys 0..63
         tc_fence_after();
         mma_pv(0, j, 0, 4);
-        ok = wait(k_full0 + 8 * st1, ph1) && ok;  // K(j + 1), for S0(j + 1) below
+        ok = wait(p_full0, j & 1) && ok;  // P0(j) over keys 64..127
         tc_fence_after();
         mma_pv(0, j, 4, 8);
+        ok = wait(k_full0 + 8 * st1, ph1) && ok;  // K(j + 1), for S0(j + 1)
+        tc_fence_after();
         mma_s(0, j + 1, 0, kS);
         umma_commit_if(leader, s_full0);
+        ok = wait(p_half0 + 8, j & 1) && ok;
+        tc_fence_after();
+        mma_pv(1, j, 0, 4);
         ok = wait(p_full0 + 8, j & 1) && ok;
         tc_fence_after();
-        mma_pv(1, j, 0, 8);
+        mma_pv(1, j, 4, 8);
         umma_commit_if(leader, v_empty0 + 8 * (j & 1));  // P V0(j) and P V1(j) have read V(j)
         mma_s(1, j + 1, 0, kS / 2);
         ok = wait(v_full0 + 8 * st1, ph1) && ok;  // V(j + 1), for P V0(j + 1)
@@ -403,13 +424,19 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         umma_commit_if(leader, s_full0 + 8);
       }
       if (ok) {  // the last KV tile
-        ok = wait(p_full0, j & 1);
+        ok = wait(p_half0, j & 1);
         tc_fence_after();
-        mma_pv(0, j, 0, 8);
+        mma_pv(0, j, 0, 4);
+        ok = wait(p_full0, j & 1) && ok;
+        tc_fence_after();
+        mma_pv(0, j, 4, 8);
         umma_commit_if(leader, pv_done0);  // for the final O / l
+        ok = wait(p_half0 + 8, j & 1) && ok;
+        tc_fence_after();
+        mma_pv(1, j, 0, 4);
         ok = wait(p_full0 + 8, j & 1) && ok;
         tc_fence_after();
-        mma_pv(1, j, 0, 8);
+        mma_pv(1, j, 4, 8);
         umma_commit_if(leader, pv_done0 + 8);
       }
       if (*abort_flag) {
