@@ -52,11 +52,11 @@ constexpr float kRescaleThreshold = 16.0f;
 //               wait it makes (about 175 cycles even on a completed phase),
 //               every branch around an MMA group and every extra commit
 //               shows up as idle tensor cycles.  The steady-state loop is
-//               therefore straight-line (the last KV tile is peeled off), the
-//               K(j+1) and V(j+1) waits sit inside the preceding MMA group
-//               where queued MMAs cover them, and the K ring slot is released
-//               by the softmax warps of tile 1 (they see S1(j) complete)
-//               instead of by a second commit.
+//               therefore straight-line (the last KV tile is peeled off), each
+//               wait (P halves, K(j+1), V(j+1)) sits behind at least four
+//               queued MMAs that cover it, and the K ring slot is released by
+//               the softmax warps of tile 1 (they see S1(j) complete) instead
+//               of by a second commit.
 //   warps 10-11 idle (they complete the third warpgroup, which gives its
 //               registers to the softmax warpgroups).
 // Softmax per KV tile: one TMEM load of the S row, tree max/sum, exp2 on the
