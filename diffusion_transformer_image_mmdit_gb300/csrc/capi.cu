@@ -777,7 +777,8 @@ const char* mmdit_kernel_name(int kernel_id) {
   static const char* names[KID_COUNT] = {"gemm_bf16_tc", "attn_fwd",   "ln_modulate", "gemv",      "sinusoid",
                                          "rope_build",   "rope_apply", "euler",       "quantize_w8", "dequant_i8",
                                          "cast_bf16",    "attn_prep",  "wait_selftest", "add_f32",
-                                         "step_counter", "quantize_f8", "heads_pack",   "heads_unpack"};
+                                         "step_counter", "quantize_f8", "heads_pack",   "heads_unpack",
+                                         "vT_transpose"};
   return (kernel_id >= 0 && kernel_id < KID_COUNT) ? names[kernel_id] : "unknown";
 }
 

@@ -568,12 +568,12 @@ __global__ void cast_f32_bf16_kernel(const float* __restrict__ x, uint16_t* __re
 
 // ------------------------------------------------------------------ attention prep
 // One warp per (sample, token, head): q and k get RMSNorm (gain by stream)
-// and RoPE, written to qk [B][L][2D]; v is written transposed to vT [B][D][Lpad].
+// and RoPE, written to qk [B][L][2D].  v goes transposed to vT [B][D][Lpad]
+// through vT_transpose_kernel below.
 template <int HD>
 __global__ void attn_prep_kernel(const uint16_t* __restrict__ qkv, long long qkv_ld, int B, int L, int L_txt, int H,
                                  const float* gq0, const float* gq1, const float* gk0, const float* gk1, float eps,
-                                 const float* __restrict__ cs, const float* __restrict__ sn, uint16_t* __restrict__ qk,
-                                 uint16_t* __restrict__ vT, long long vT_ld) {
+                                 const float* __restrict__ cs, const float* __restrict__ sn, uint16_t* __restrict__ qk) {
   constexpr int PER = HD / 32;  // channels per lane (2 or 4), consecutive
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -581,7 +581,6 @@ __global__ void attn_prep_kernel(const uint16_t* __restrict__ qkv, long long qkv
   const int h = (int)(gw % H);
   const long long bt = gw / H;
   const int tok = (int)(bt % L);
-  const int b = (int)(bt / L);
   const int D = H * HD;
   const uint16_t* row = qkv + bt * qkv_ld;
   const bool txt = tok < L_txt;
@@ -614,9 +613,38 @@ __global__ void attn_prep_kernel(const uint16_t* __restrict__ qkv, long long qkv
 #pragma unroll
     for (int j = 0; j < PER; j += 2) *reinterpret_cast<uint32_t*>(dst + j) = pack_bf16x2(v[j], v[j + 1]);
   }
-  const uint16_t* vs = row + 2 * D + h * HD + lane * PER;
+}
+
+// V^T for the standalone attention: v[b][tok][c] (columns 2D + c of a qkv
+// row) -> vT[b][c][tok].  A CTA moves a 64-token x 64-channel tile through
+// shared memory, so that the loads (8 channels of one token) and the stores
+// (8 tokens of one channel) are 16-byte vectors along contiguous memory.
+// In the tile, the 16-byte chunk j of token row r sits at chunk position
+// j ^ ((r >> 3) & 7): the 8-token chunks one warp reads for a channel are
+// 8 rows apart, and the swizzle puts them in 8 different bank groups.
+// Tokens at or beyond L load as zeros and are stored only up to the 8-token
+// chunk holding token L - 1 (vT rows are padded to a multiple of 8).
+__global__ void __launch_bounds__(256) vT_transpose_kernel(const uint16_t* __restrict__ qkv, long long qkv_ld, int L,
+                                                           int D, uint16_t* __restrict__ vT, long long vT_ld) {
+  __shared__ __align__(16) uint16_t tile[64][64];  // [token][channel], swizzled 16-byte chunks
+  const int t0 = blockIdx.x * 64, c0 = blockIdx.y * 64, b = blockIdx.z;
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int t = i >> 3, k = i & 7;  // token of the tile, 8-channel chunk
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (t0 + t < L)
+      v = *reinterpret_cast<const uint4*>(qkv + ((long long)b * L + t0 + t) * qkv_ld + 2LL * D + c0 + 8 * k);
+    *reinterpret_cast<uint4*>(&tile[t][8 * (k ^ ((t >> 3) & 7))]) = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int c = i >> 3, t = 8 * (i & 7);  // channel of the tile, first token of an 8-token chunk
+    if (t0 + t >= L) continue;
+    const int col = 8 * ((c >> 3) ^ ((t >> 3) & 7)) + (c & 7);  // rows t .. t + 7 share t >> 3
+    uint32_t w[4];
 #pragma unroll
-  for (int j = 0; j < PER; ++j) vT[((long long)b * D + h * HD + lane * PER + j) * vT_ld + tok] = vs[j];
+    for (int q = 0; q < 4; ++q) w[q] = (uint32_t)tile[t + 2 * q][col] | ((uint32_t)tile[t + 2 * q + 1][col] << 16);
+    *reinterpret_cast<uint4*>(vT + ((long long)b * D + c0 + c) * vT_ld + t0 + t) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 // ------------------------------------------------------------------ wait self-test
@@ -939,11 +967,16 @@ cudaError_t launch_attn_prep(const uint16_t* qkv, long long qkv_ld, int B, int L
   const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
   launch_begin(KID_ATTN_PREP, st);
   if (d == 128)
-    attn_prep_kernel<128><<<blocks, 256, 0, st>>>(qkv, qkv_ld, B, L, L_txt, H, gq0, gq1, gk0, gk1, eps, cs, sn, qk,
-                                                  vT, vT_ld);
+    attn_prep_kernel<128><<<blocks, 256, 0, st>>>(qkv, qkv_ld, B, L, L_txt, H, gq0, gq1, gk0, gk1, eps, cs, sn, qk);
   else
-    attn_prep_kernel<64><<<blocks, 256, 0, st>>>(qkv, qkv_ld, B, L, L_txt, H, gq0, gq1, gk0, gk1, eps, cs, sn, qk, vT,
-                                                 vT_ld);
+    attn_prep_kernel<64><<<blocks, 256, 0, st>>>(qkv, qkv_ld, B, L, L_txt, H, gq0, gq1, gk0, gk1, eps, cs, sn, qk);
+  launch_end(st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int D = H * d;
+  launch_begin(KID_VT_TRANSPOSE, st);
+  vT_transpose_kernel<<<dim3((unsigned)((L + 63) / 64), (unsigned)(D / 64), (unsigned)B), 256, 0, st>>>(qkv, qkv_ld, L,
+                                                                                                    D, vT, vT_ld);
   launch_end(st);
   return cudaGetLastError();
 }

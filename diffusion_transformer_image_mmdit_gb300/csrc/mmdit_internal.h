@@ -109,6 +109,7 @@ enum KernelId : int {
   KID_QUANTIZE_F8,
   KID_HEADS_PACK,
   KID_HEADS_UNPACK,
+  KID_VT_TRANSPOSE,
   KID_COUNT
 };
 // Bracket every kernel launch: counts launches and, while a trace is on,
