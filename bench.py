@@ -173,6 +173,8 @@ def gemm_traffic_scaled(c: dict):
     processes (block launches: all tokens, embedder / final launches: image
     tokens), then the launches are weighted by the workload's block counts.
     Returns (bytes per launch, description) or (None, reason)."""
+    if c.get("f8"):
+        return None, "no capture of the e4m3 GEMM (the committed capture is of the bf16 block-pair workload)"
     rows = gemm_launch_table("c3pair")
     if rows is None:
         return None, "no capture of the current GEMM sources"
