@@ -389,23 +389,31 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int, full: bool =
         dist.barrier()
     torch.cuda.synchronize()
     n0 = api.launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event before the first step and one after each step, all on the
+    # launch stream: the first and last bound the timed region, the ones in
+    # between give the per-step distribution
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with ClockSampler(local_rank) as clk:
-        e0.record(stream)
+        ev[0].record(stream)
         for i in range(args.steps):
             step(args.warmup + i)
-        e1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     launches = api.launch_count() - n0
-    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
     ms_step = ms / args.steps
+    step_ms = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
     st = api.sync_status()
     if st != 0:
         raise RuntimeError(f"device status {st} after timed region")
+    import numpy as np
+    dist_ms = {"median": round(float(np.median(step_ms)), 3), "p10": round(float(np.percentile(step_ms, 10)), 3),
+               "p90": round(float(np.percentile(step_ms, 90)), 3), "rank": "0"}
     if not full:
-        res = {"ms_step": ms_step, "clocks": clk.summary(), "launches_per_step": launches / args.steps}
+        res = {"ms_step": ms_step, "clocks": clk.summary(), "launches_per_step": launches / args.steps,
+               "step_ms": dist_ms}
         del w, wstruct, ws
         torch.cuda.empty_cache()
         return res
@@ -446,7 +454,7 @@ def run_ours(args, c: dict, rank: int, world: int, local_rank: int, full: bool =
     e2e_ms = max_over_ranks(f0.elapsed_time(f1) / args.steps, dev)
 
     res = {
-        "ms_step": ms_step, "launches_per_step": launches / args.steps, "clocks": clk.summary(),
+        "ms_step": ms_step, "step_ms": dist_ms, "launches_per_step": launches / args.steps, "clocks": clk.summary(),
         "e2e_ms": e2e_ms, "h2d": xl_h.numel() * 4 + xt_h.numel() * 4, "d2h": out_h.numel() * 4,
         "per_kernel": {k: {"launches": a[0], "ms": round(a[1], 4), "share": round(a[1] / traced_total, 4)}
                        for k, a in sorted(per.items(), key=lambda kv: -kv[1][1])},
@@ -525,8 +533,8 @@ def run_sample(args, c: dict):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="c4", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -595,7 +603,8 @@ def main():
             extras[key] = {"workload": WORKLOAD_NAME[name], "ms_per_step": round(rx["ms_step"], 3),
                            "ms_per_image": round(rx["ms_step"] / cx["B"], 3),
                            "tflops": round(fx["total"] / (rx["ms_step"] * 1e-3) / 1e12, 1),
-                           "steps": args.steps, "warmup": args.warmup, "clocks": rx["clocks"]}
+                           "step_ms": rx["step_ms"], "steps": args.steps, "warmup": args.warmup,
+                           "clocks": rx["clocks"]}
     if rank != 0:
         return
     pk = r["peaks"]
@@ -615,7 +624,8 @@ def main():
     traffic, traffic_src = gemm_traffic_scaled(c)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 3), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(r["ms_step"], 3), "step_ms": r["step_ms"],
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8w-bf16" if c["int8"] else "e4m3-bf16" if c.get("f8") else "bf16",
         "data": "synthetic: seeded GPU draws, weights N(0,0.02), latents and text tokens N(0,1); random init",
         "config": cfg_json,
