@@ -555,7 +555,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     fl = step_flops(c)
     cfg_json = {"workload": WORKLOAD_NAME[args.config], "model": "flux-shaped MMDiT (random init)",
-                "global_batch": c["B"] * max(world, args.gpus if world == 1 else world), "seq_len": fl["L"],
+                "global_batch": c["B"] * world, "seq_len": fl["L"],
                 "parallelism": f"replicas x{world}",
                 "l2": f"inputs larger than L2: {step_weight_bytes(c) / 1e9:.2f} GB of weights read per step"}
 
