@@ -135,8 +135,9 @@ __global__ void heads_unpack_kernel(const uint16_t* __restrict__ src, long long 
 
 // ------------------------------------------------------------------ GEMV
 // y[b, n] = sum_k W[n, k] act(x[b, k]) (* scale[n]) + bias[n] for B <= 8 rows
-// of x (K a multiple of 16): one warp per output row, 16-byte weight loads
-// along K, x staged in shared memory after the activation once per CTA.  The grid is a few CTAs
+// of x (K a multiple of 16): one warp per output row (for B > 1, per group of
+// kGemvRowsPerWarp rows handled together), 16-byte weight loads along K, x
+// staged in shared memory after the activation once per CTA.  The grid is a few CTAs
 // per SM striding over the rows, so the staging is paid once per CTA rather
 // than once per 32 rows.
 constexpr int kGemvRowsPerWarp = 4;
@@ -199,6 +200,80 @@ __device__ __forceinline__ void gemv_row(const uint8_t* __restrict__ wrow, const
             t = fmaf(w[4 * j + 3], xj.w, fmaf(w[4 * j + 2], xj.z, fmaf(w[4 * j + 1], xj.y, fmaf(w[4 * j], xj.x, t))));
           }
           acc[b] = t;
+        }
+      }
+    }
+  }
+}
+
+// Four int8 values (one 32-bit word) to fp32, exactly, on the FMA pipe
+// instead of four int-to-float conversions: with its sign bit flipped the
+// byte b becomes q + 128 in 0..255; placed as the low mantissa byte of the
+// float 2^23 it gives 2^23 + q + 128, from which 2^23 + 128 is subtracted.
+__device__ __forceinline__ void i8x4_to_f32(uint32_t q, float* w) {
+  const uint32_t u = q ^ 0x80808080u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540u | i)) - 8388736.0f;
+}
+
+// The NR rows of one warp at once, for batches B > 1: the weight vectors at
+// one K position are loaded for all NR rows, and the x values there (all B
+// rows of x) are read from shared memory once for the NR rows.  One row at a
+// time reads B * 4 float4s of x per 16-byte weight vector -- 256 bytes per 16
+// weight bytes with B = 4 and int8 weights, which made the kernel bound by
+// shared memory; sharing them cuts that NR-fold.  wrow[r] is null for rows
+// past the end.
+template <bool I8, int BM, int NR>
+__device__ __forceinline__ void gemv_rows(const uint8_t* const* wrow, const float* xs, int B, int K, int lane,
+                                          float (&acc)[NR][BM]) {
+  constexpr int EPV = I8 ? 16 : 8;
+  constexpr int U = kGemvVecBatch / NR;  // vectors per row in flight: kGemvVecBatch loads per lane
+  const int nvec = K / EPV;
+#pragma unroll 1
+  for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+    uint4 wv[NR][U];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (wrow[r] && v0 + 32 * u < nvec) wv[r][u] = __ldg(reinterpret_cast<const uint4*>(wrow[r]) + v0 + 32 * u);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= nvec) break;
+      const int sw = I8 ? ((v >> 1) & 3) : ((v >> 2) & 1);
+      // the vector in two halves of EPV / 2 elements, so that only half of
+      // its x values (for all B rows) are held at a time
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        constexpr int Q = EPV / 8;  // float4s of x per half vector and row
+        float4 xv[BM][Q];
+#pragma unroll
+        for (int b = 0; b < BM; ++b)
+#pragma unroll
+          for (int j = 0; j < Q; ++j)
+            xv[b][j] = b < B ? reinterpret_cast<const float4*>(xs + b * K + v * EPV)[(hv * Q + j) ^ sw]
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          if (!wrow[r]) continue;
+          float w[EPV / 2];
+          const uint32_t q0 = hv ? wv[r][u].z : wv[r][u].x, q1 = hv ? wv[r][u].w : wv[r][u].y;
+          if (I8) {
+            i8x4_to_f32(q0, w);
+            i8x4_to_f32(q1, w + 4);
+          } else {
+            w[0] = bf16_lo(q0), w[1] = bf16_hi(q0), w[2] = bf16_lo(q1), w[3] = bf16_hi(q1);
+          }
+#pragma unroll
+          for (int b = 0; b < BM; ++b) {
+            float t = acc[r][b];
+#pragma unroll
+            for (int j = 0; j < Q; ++j)
+              t = fmaf(w[4 * j + 3], xv[b][j].w, fmaf(w[4 * j + 2], xv[b][j].z,
+                       fmaf(w[4 * j + 1], xv[b][j].y, fmaf(w[4 * j], xv[b][j].x, t))));
+            acc[r][b] = t;
+          }
         }
       }
     }
@@ -285,6 +360,97 @@ __global__ void __launch_bounds__(256) gemv_batched_kernel(const __grid_constant
       for (int b = 0; b < BM; ++b) {
         if (b < B) {
           const float t = warp_sum(acc[b]);
+          if (lane == 0) job.out[(long long)b * job.N + n] = t * sc + bi;
+        }
+      }
+    }
+  }
+}
+
+
+// B > 1: the same two kernels with the kGemvRowsPerWarp rows of a warp
+// handled together (gemv_rows); two CTAs per SM keep enough loads in flight.
+template <bool I8, int BM>
+__global__ void __launch_bounds__(256, 2) gemv_rows_kernel(const void* __restrict__ W, const float* __restrict__ wscale,
+                                                           const float* __restrict__ bias, const float* __restrict__ x,
+                                                           int B, int N, int K, int act, float* __restrict__ y) {
+  extern __shared__ float xs[];
+  gemv_stage_x<I8>(x, B, K, act, xs);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int stride = gridDim.x * kGemvWarps * kGemvRowsPerWarp;
+#pragma unroll 1
+  for (int row0 = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp; row0 < N; row0 += stride) {
+    const uint8_t* wrow[kGemvRowsPerWarp];
+#pragma unroll
+    for (int rr = 0; rr < kGemvRowsPerWarp; ++rr)
+      wrow[rr] = row0 + rr < N ? reinterpret_cast<const uint8_t*>(W) + (long long)(row0 + rr) * K * (I8 ? 1 : 2)
+                               : nullptr;
+    float acc[kGemvRowsPerWarp][BM];
+#pragma unroll
+    for (int rr = 0; rr < kGemvRowsPerWarp; ++rr)
+#pragma unroll
+      for (int b = 0; b < BM; ++b) acc[rr][b] = 0.f;
+    gemv_rows<I8, BM, kGemvRowsPerWarp>(wrow, xs, B, K, lane, acc);
+#pragma unroll
+    for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
+      const int n = row0 + rr;
+      if (n >= N) break;
+      const float sc = wscale ? wscale[n] : 1.0f;
+      const float bi = bias ? bias[n] : 0.0f;
+#pragma unroll
+      for (int b = 0; b < BM; ++b) {
+        if (b < B) {
+          const float t = warp_sum(acc[rr][b]);
+          if (lane == 0) y[(long long)b * N + n] = t * sc + bi;
+        }
+      }
+    }
+  }
+}
+
+template <bool I8, int BM>
+__global__ void __launch_bounds__(256, 2) gemv_rows_batched_kernel(const __grid_constant__ GemvBatch jb,
+                                                                   const float* __restrict__ x, int B, int K, int act) {
+  extern __shared__ float xs[];
+  gemv_stage_x<I8>(x, B, K, act, xs);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = jb.row0[jb.n_jobs];
+  const int stride = gridDim.x * kGemvWarps * kGemvRowsPerWarp;
+  int j = 0;
+#pragma unroll 1
+  for (int row_base = (blockIdx.x * kGemvWarps + warp) * kGemvRowsPerWarp; row_base < total; row_base += stride) {
+    const uint8_t* wrow[kGemvRowsPerWarp];
+    int jr[kGemvRowsPerWarp], nr[kGemvRowsPerWarp];
+#pragma unroll
+    for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
+      const int R = row_base + rr;
+      wrow[rr] = nullptr;
+      jr[rr] = j;
+      nr[rr] = 0;
+      if (R < total) {
+        while (R >= jb.row0[j + 1]) ++j;
+        jr[rr] = j;
+        nr[rr] = R - jb.row0[j];
+        wrow[rr] = reinterpret_cast<const uint8_t*>(jb.job[j].W) + (long long)nr[rr] * K * (I8 ? 1 : 2);
+      }
+    }
+    float acc[kGemvRowsPerWarp][BM];
+#pragma unroll
+    for (int rr = 0; rr < kGemvRowsPerWarp; ++rr)
+#pragma unroll
+      for (int b = 0; b < BM; ++b) acc[rr][b] = 0.f;
+    gemv_rows<I8, BM, kGemvRowsPerWarp>(wrow, xs, B, K, lane, acc);
+#pragma unroll
+    for (int rr = 0; rr < kGemvRowsPerWarp; ++rr) {
+      if (!wrow[rr]) break;
+      const GemvJob& job = jb.job[jr[rr]];
+      const int n = nr[rr];
+      const float sc = job.scale ? job.scale[n] : 1.0f;
+      const float bi = job.bias ? job.bias[n] : 0.0f;
+#pragma unroll
+      for (int b = 0; b < BM; ++b) {
+        if (b < B) {
+          const float t = warp_sum(acc[rr][b]);
           if (lane == 0) job.out[(long long)b * job.N + n] = t * sc + bi;
         }
       }
@@ -752,36 +918,38 @@ using GemvFn = void (*)(const void*, const float*, const float*, const float*, i
 using GemvBatchedFn = void (*)(const GemvBatch, const float*, int, int, int);
 template <bool I8>
 static GemvFn gemv_fn(int B) {
-  return B <= 1 ? gemv_kernel<I8, 1> : B <= 2 ? gemv_kernel<I8, 2> : B <= 4 ? gemv_kernel<I8, 4> : gemv_kernel<I8, 8>;
+  return B <= 1   ? gemv_kernel<I8, 1>
+         : B <= 2 ? gemv_rows_kernel<I8, 2>
+         : B <= 4 ? gemv_rows_kernel<I8, 4>
+                  : gemv_rows_kernel<I8, 8>;
 }
 template <bool I8>
 static GemvBatchedFn gemv_batched_fn(int B) {
-  return B <= 1 ? gemv_batched_kernel<I8, 1>
-                : B <= 2 ? gemv_batched_kernel<I8, 2> : B <= 4 ? gemv_batched_kernel<I8, 4> : gemv_batched_kernel<I8, 8>;
+  return B <= 1   ? gemv_batched_kernel<I8, 1>
+         : B <= 2 ? gemv_rows_batched_kernel<I8, 2>
+         : B <= 4 ? gemv_rows_batched_kernel<I8, 4>
+                  : gemv_rows_batched_kernel<I8, 8>;
 }
 
 // Lets every GEMV instance use up to 200 KB of dynamic shared memory (x of up
-// to 8 rows); once per device.
+// to 8 rows); once per device, safe under concurrent first calls.
 static cudaError_t gemv_attributes() {
-  static bool done[64] = {};
+  static std::once_flag once[64];
+  static cudaError_t err[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 64) return cudaErrorInvalidDevice;
-  if (done[dev]) return cudaSuccess;
-  const void* fns[16];
-  int n = 0;
-  for (int B : {1, 2, 4, 8}) {
-    fns[n++] = (const void*)gemv_fn<false>(B);
-    fns[n++] = (const void*)gemv_fn<true>(B);
-    fns[n++] = (const void*)gemv_batched_fn<false>(B);
-    fns[n++] = (const void*)gemv_batched_fn<true>(B);
-  }
-  for (int i = 0; i < n; ++i) {
-    const cudaError_t e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-  }
-  done[dev] = true;
-  return cudaSuccess;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    err[dev] = cudaSuccess;
+    for (int B : {1, 2, 4, 8}) {
+      const void* fns[4] = {(const void*)gemv_fn<false>(B), (const void*)gemv_fn<true>(B),
+                            (const void*)gemv_batched_fn<false>(B), (const void*)gemv_batched_fn<true>(B)};
+      for (const void* f : fns) {
+        const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess && err[dev] == cudaSuccess) err[dev] = e;
+      }
+    }
+  });
+  return err[dev];
 }
 
 cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
