@@ -23,6 +23,8 @@
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (with that device current) and caches it; make
 //    that first call before any stream capture.
+#include <atomic>
+
 #include "elementwise.h"
 #include "mmdit.h"
 #include "mmdit_internal.h"
@@ -35,16 +37,17 @@ constexpr size_t kNoallocScratchBytes = 48ull << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// Device address of g_noalloc_scratch, per device, filled by the first call.
+// Device address of g_noalloc_scratch, per device, filled by the first call
+// (threads racing on it compute the same address; the atomic publishes it).
 void* scratch_address(int dev) {
-  static void* addr[64] = {};
+  static std::atomic<void*> addr[64] = {};
   if (dev < 0 || dev >= 64) return nullptr;
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
+  void* q = addr[dev].load(std::memory_order_acquire);
+  if (!q) {
+    if (cudaGetSymbolAddress(&q, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev].store(q, std::memory_order_release);
   }
-  return addr[dev];
+  return q;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

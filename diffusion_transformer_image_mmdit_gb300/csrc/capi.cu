@@ -55,39 +55,50 @@ static int current_device() {
   return dev < 0 ? 0 : (dev > 63 ? 63 : dev);
 }
 
+// Per-device values looked up once.  Several host threads may race on the
+// first lookup; each computes the same value, and the atomics make the
+// publication well defined.
 unsigned* device_status_ptr() {
-  static unsigned* ptrs[64] = {};
+  static std::atomic<unsigned*> ptrs[64] = {};
   const int dev = current_device();
-  if (!ptrs[dev]) {
+  unsigned* q = ptrs[dev].load(std::memory_order_acquire);
+  if (!q) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptrs[dev] = static_cast<unsigned*>(p);
+    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) {
+      q = static_cast<unsigned*>(p);
+      ptrs[dev].store(q, std::memory_order_release);
+    }
   }
-  return ptrs[dev];
+  return q;
 }
 
 int num_sms() {
-  static int sms[64] = {};
+  static std::atomic<int> sms[64] = {};
   const int dev = current_device();
-  if (!sms[dev]) {
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (!n) {
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    sms[dev] = v > 0 ? v : 1;
+    n = v > 0 ? v : 1;
+    sms[dev].store(n, std::memory_order_relaxed);
   }
-  return sms[dev];
+  return n;
 }
 
 // 1 = sm_103, -1 = other device, 0 = unknown yet.
 static int device_ok() {
-  static int ok[64] = {};
+  static std::atomic<int> ok[64] = {};
   const int dev = current_device();
-  if (!ok[dev]) {
+  int k = ok[dev].load(std::memory_order_relaxed);
+  if (!k) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return 0;
-    ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    k = (major == 10 && minor == 3) ? 1 : -1;
+    ok[dev].store(k, std::memory_order_relaxed);
   }
-  return ok[dev] > 0;
+  return k > 0;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
