@@ -34,6 +34,8 @@ CONFIGS = {
     "step1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=False, n_steps=50, **FLUX),
     # one double + one single block at 1024^2 (the block-pair workload; small case for full profiles)
     "c3pair": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=1, n_single=1, int8=False, n_steps=50, **FLUX),
+    # one double + one single block at 1328^2 (the block launches of the full 1328^2 step, at its token count)
+    "c4pair": dict(B=1, L_txt=512, grid_h=83, grid_w=83, n_double=1, n_single=1, int8=False, n_steps=50, **FLUX),
     # one double block at 512^2 (512 + 1024 tokens)
     "c2": dict(B=1, L_txt=512, grid_h=32, grid_w=32, n_double=1, n_single=0, int8=False, n_steps=50, **FLUX),
     # Flux.2 Klein 9B block shapes (D 4096, 32 heads, SwiGLU MLP 12288, 8 double + 24 single) at 1024^2
@@ -64,6 +66,8 @@ WORKLOAD_NAME = {
     "step1024": "bf16 denoising step, 19 double + 38 single blocks, 512 text + 64x64 image tokens (1024^2), batch 1",
     "c3pair": "one double + one single block (with embedding, img_in, final layer, Euler) at 512 text + 64x64 image "
               "tokens, batch 1, bf16",
+    "c4pair": "one double + one single block (with embedding, img_in, final layer, Euler) at 512 text + 83x83 image "
+              "tokens (1328^2), batch 1, bf16",
     "c2": "one double block (with embedding, img_in, final layer, Euler) at 512 text + 32x32 image tokens, batch 1",
     "klein1024": "Flux.2 Klein-shaped denoising step: 8 double + 24 single blocks, D=4096, 32x128 heads, SwiGLU "
                  "MLP 12288, 512 text + 64x64 image tokens (1024^2), batch 1, bf16, step 0 of a 4-step schedule",
@@ -167,28 +171,36 @@ def gemm_launch_table(config: str):
 
 
 def gemm_traffic_scaled(c: dict):
-    """DRAM bytes per GEMM launch of workload c, from the ncu capture of the
-    block-pair workload (one double + one single block at 512 + 64x64 tokens):
-    each captured launch's traffic is scaled by the ratio of the token rows it
-    processes (block launches: all tokens, embedder / final launches: image
-    tokens), then the launches are weighted by the workload's block counts.
-    Returns (bytes per launch, description) or (None, reason)."""
+    """DRAM bytes per GEMM launch of workload c, from an ncu capture of a
+    block-pair workload (one double + one single block). A capture at the
+    workload's own token count (512 + 83x83 or 512 + 64x64, batch 1) has the
+    same launches as the full step, so only its block counts weight them.
+    Otherwise each launch of the 512 + 64x64 capture is scaled by the ratio of
+    the token rows it processes (block launches: all tokens, embedder / final
+    launches: image tokens). Returns (bytes per launch, description) or
+    (None, reason)."""
     if c.get("f8"):
-        return None, "no capture of the e4m3 GEMM (the committed capture is of the bf16 block-pair workload)"
-    rows = gemm_launch_table("c3pair")
+        return None, "no capture of the e4m3 GEMM (the committed captures are of the bf16 block-pair workloads)"
+    if c.get("swiglu") or (c["D"], c["D_mlp"]) != (CONFIGS["c3pair"]["D"], CONFIGS["c3pair"]["D_mlp"]) \
+            or c.get("ref_h"):
+        return None, "no capture of this model's GEMM shapes (the committed captures are of the D=3072 blocks)"
+    L, Li = c["L_txt"] + c["grid_h"] * c["grid_w"], c["grid_h"] * c["grid_w"]
+    exact = [k for k in ("c4pair", "c3pair") if c["B"] == 1 and CONFIGS[k]["L_txt"] == c["L_txt"]
+             and (CONFIGS[k]["grid_h"], CONFIGS[k]["grid_w"]) == (c["grid_h"], c["grid_w"])]
+    name = exact[0] if exact and gemm_launch_table(exact[0]) is not None else "c3pair"
+    rows = gemm_launch_table(name)
     if rows is None:
         return None, "no capture of the current GEMM sources"
-    cap = CONFIGS["c3pair"]
+    cap = CONFIGS[name]
     L_cap, Li_cap = cap["L_txt"] + cap["grid_h"] * cap["grid_w"], cap["grid_h"] * cap["grid_w"]
-    L, Li = c["L_txt"] + c["grid_h"] * c["grid_w"], c["grid_h"] * c["grid_w"]
     dbl = sng = io = 0.0
     n_dbl = n_sng = n_io = 0
-    for name, m, n, k, rd, wr in rows:
+    for lname, m, n, k, rd, wr in rows:
         b = (rd + wr) * 1e6
-        if name in ("img_in", "final"):
+        if lname in ("img_in", "final"):
             io += b * (c["B"] * Li) / Li_cap
             n_io += 1
-        elif name in ("lin1", "lin2"):
+        elif lname in ("lin1", "lin2"):
             sng += b * (c["B"] * L) / L_cap
             n_sng += 1
         else:
@@ -196,6 +208,10 @@ def gemm_traffic_scaled(c: dict):
             n_dbl += 1
     total = c["n_double"] * dbl + c["n_single"] * sng + io
     launches = c["n_double"] * n_dbl + c["n_single"] * n_sng + n_io
+    if c["B"] * L == L_cap and Li == Li_cap:
+        return total / launches, (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of the {len(rows)} GEMM launches "
+                                  f"of the block-pair workload at this token count ({L_cap} tokens), weighted by "
+                                  f"this workload's block counts")
     return total / launches, (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of the {len(rows)} GEMM launches of "
                               f"the block-pair workload ({L_cap} tokens), each scaled by the token rows of this "
                               f"workload ({c['B']} x {L}); the W share does not grow with tokens, so this "
@@ -204,17 +220,18 @@ def gemm_traffic_scaled(c: dict):
 
 def gemm_algorithmic_bytes(c: dict) -> float:
     """Operand and result bytes of the step's GEMM launches, averaged per
-    launch: A and W read once (bf16), bf16 results written once, fp32
-    residual tiles read and written once."""
+    launch: A and each problem's W read once (bf16), bf16 results written
+    once, fp32 residual tiles read and written once."""
     B, D, Dm, C = c["B"], c["D"], c["D_mlp"], c["C_lat"]
     L, Li = c["L_txt"] + c["grid_h"] * c["grid_w"], c["grid_h"] * c["grid_w"]
     M = B * L
     m_in = 2 * Dm if c.get("swiglu") else Dm
     out_in = Dm
-    dbl = ((M * D + 3 * D * D) * 2 + M * 3 * D * 2            # qkv: q, k, v^T
-           + (M * D + D * D) * 2 + M * D * 8                  # proj + gated residual
-           + (M * D + m_in * D) * 2 + M * out_in * 2          # mlp in
-           + (M * Dm + D * Dm) * 2 + M * D * 8)               # mlp out + gated residual
+    # the text and image streams of a double block have their own weights: W counted twice
+    dbl = ((M * D + 2 * 3 * D * D) * 2 + M * 3 * D * 2        # qkv: q, k, v^T
+           + (M * D + 2 * D * D) * 2 + M * D * 8              # proj + gated residual
+           + (M * D + 2 * m_in * D) * 2 + M * out_in * 2      # mlp in
+           + (M * Dm + 2 * D * Dm) * 2 + M * D * 8)           # mlp out + gated residual
     sng = ((M * D + (3 * D + m_in) * D) * 2 + M * (3 * D + Dm) * 2
            + (M * (D + Dm) + D * (D + Dm)) * 2 + M * D * 8)
     io = (B * Li * C + D * C) * 2 + B * Li * D * 4 + (B * Li * D + C * D) * 2 + B * Li * C * 4
