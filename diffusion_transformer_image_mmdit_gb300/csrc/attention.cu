@@ -20,6 +20,25 @@
 // than 16 (a factor 2^16), which stays exact because the same reference is
 // used for the numerator and the row sum: P entries stay below 2^16 (bf16
 // keeps its relative precision there) and the fp32 sums far from overflow.
+//
+// Work schedule (persistent, one CTA per SM).  A work unit is a pair of
+// query tiles (256 rows) of one (sample, head) over all n_kv KV tiles.  CTA
+// c of G runs whole units c, c + G, ... for `dp_rounds` rounds; the units
+// left after those rounds (between G and 2G of them) form the tail, whose KV
+// steps (numbered unit by unit) are cut into G equal contiguous ranges, one
+// per CTA.  Every CTA thus does the same number of KV steps to within one,
+// where one unit per CTA launched as a grid left the SMs of the last partial
+// wave idle.  A range is at least n_kv steps long, so a tail unit is split
+// at most once, at the boundary between CTAs c and c + 1: part A (its first
+// KV tiles) is the last item of CTA c, part B (the rest) the first tail item
+// of CTA c + 1.  Each part writes its unnormalised O rows with their running
+// max and sum (fp32) to its slot in global memory and counts itself on the
+// unit's counter; the part that arrives second reads the other slot, merges
+// the two with the usual rescaling, O = (2^(m_A - m) O_A + 2^(m_B - m) O_B) /
+// (2^(m_A - m) l_A + 2^(m_B - m) l_B) with m = max(m_A, m_B), and stores the
+// result.  Neither part waits for the other.  Consecutive items of a CTA
+// overlap: the next item's K tile and Q tiles load while the current item's
+// last P V MMAs and epilogue run.
 #include <mutex>
 
 #include "common.cuh"
@@ -31,15 +50,20 @@ namespace {
 constexpr uint32_t kHalf = 128 * 128;  // one 128-row x 128-byte swizzled half tile
 constexpr float kRescaleThreshold = 16.0f;
 
-// Two query tiles per CTA (256 rows of one (sample, head)), K/V tiles shared.
+// Roles (two query tiles per CTA, K/V tiles shared):
 //   warps 0-3   softmax of tile 0; warps 4-7 softmax of tile 1 (one query
 //               row per thread, 208 registers each after setmaxnreg so a
 //               whole 128-score row stays in registers).  P goes back to
 //               TMEM in two halves, each with its own barrier, so P V(j)
 //               starts on keys 0..63 while keys 64..127 are exponentiated.
-//   warp 8      TMA: both Q tiles once, then V^T(j) and K(j + 1) tiles (the
-//               order their ring slots free up and the MMAs need them),
-//               2-stage rings.
+//               At the end of an item the warps read O out of TMEM (then
+//               hand the columns back), and store O / l through their own
+//               4 KB of shared memory with TMA tile stores, or write and
+//               merge the partial result of a split unit.
+//   warp 8      TMA: per item its first K tile, the two Q tiles (each once
+//               the previous item's last S MMA of that tile has completed),
+//               then V^T(j) and K(j + 1) tiles (the order their ring slots
+//               free up and the MMAs need them), 2-stage rings.
 //   warp 9      TMEM (S0 | S1 | O0 | O1, 128 columns each) and the MMAs, in
 //               the order S0(0), S1(0), then per j: PV0(j), S0(j+1), PV1(j),
 //               S1(j+1), so the tensor pipe works on one tile while the
@@ -52,16 +76,16 @@ constexpr float kRescaleThreshold = 16.0f;
 //               wait it makes (about 175 cycles even on a completed phase),
 //               every branch around an MMA group and every extra commit
 //               shows up as idle tensor cycles.  The steady-state loop is
-//               therefore straight-line (the last KV tile is peeled off), each
-//               wait (P halves, K(j+1), V(j+1)) sits behind at least four
-//               queued MMAs that cover it, and the K ring slot is released by
-//               the softmax warps of tile 1 (they see S1(j) complete) instead
-//               of by a second commit.
+//               therefore straight-line (the last KV tile of an item is
+//               peeled off), each wait (P halves, K(j+1), V(j+1)) sits
+//               behind at least four queued MMAs that cover it, and the K
+//               ring slot is released by the softmax warps of tile 1 (they
+//               see S1(j) complete) instead of by a second commit.
 //   warps 10-11 idle (they complete the third warpgroup, which gives its
 //               registers to the softmax warpgroups).
-// Softmax per KV tile: one TMEM load of the S row, tree max/sum, exp2 on the
-//               MUFU, lazy O rescale in TMEM; at the end O / l as bf16,
-//               staged in shared memory and written with TMA tile stores.
+// Barrier phases run on across items: ring stages and the per-step
+// barriers follow a KV-step count kept by every role, the per-item barriers
+// (Q tiles, P V done, O drained) the item count.
 constexpr int kAttn2Threads = 384;
 // Register split (setmaxnreg): launched at 168 per thread (384 x 168 = 64512);
 // warpgroup 2 drops to 88 and the two softmax warpgroups rise to 208:
@@ -69,13 +93,54 @@ constexpr int kAttn2Threads = 384;
 // and 64 packed P words; the MMA warp's unrolled issue loop needs about 88.
 constexpr uint32_t kRegsSoftmax = 208;
 constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kStageO = 4096;  // a softmax warp's O staging block: 32 rows x 64 columns bf16
 
 template <int HD>
 struct Attn2Smem {
   static constexpr uint32_t QT = (HD / 64) * kHalf;  // one 128-row Q tile
   static constexpr uint32_t K = (HD / 64) * kHalf;
   static constexpr uint32_t V = 2 * HD * 128;
-  static constexpr uint32_t total = 1024 + 2 * QT + 2 * K + 2 * V + 256;
+  static constexpr uint32_t total = 1024 + 2 * QT + 2 * K + 2 * V + 8 * kStageO + 256;
+};
+static_assert(Attn2Smem<128>::total <= 232448, "attention shared memory above the 227 KB a CTA can have");
+
+struct AttnItem {
+  int u, jb, je;  // unit, KV tiles [jb, je)
+};
+
+// The items of this CTA, in order (identical in every role).
+struct AttnWork {
+  int c, G, nkv, round, rounds, units, base;
+  long long s, s1;  // this CTA's range of tail KV steps
+  __device__ explicit AttnWork(const AttnParams& p) {
+    c = (int)blockIdx.x;
+    G = (int)gridDim.x;
+    nkv = p.n_kv_tiles;
+    round = 0;
+    rounds = p.dp_rounds;
+    units = p.n_units;
+    base = rounds * G;
+    const long long T = (long long)p.tail_units * nkv;
+    s = T * c / G;
+    s1 = T * (c + 1) / G;
+  }
+  __device__ bool next(AttnItem& it) {
+    while (round < rounds) {
+      const int u = round++ * G + c;
+      if (u < units) {
+        it.u = u, it.jb = 0, it.je = nkv;
+        return true;
+      }
+    }
+    if (s >= s1) return false;
+    const long long uo = s / nkv;
+    const int jb = (int)(s - uo * nkv);
+    const long long left = s1 - s;
+    const int je = left < (long long)(nkv - jb) ? jb + (int)left : nkv;
+    it.u = base + (int)uo, it.jb = jb, it.je = je;
+    s += je - jb;
+    return true;
+  }
 };
 
 template <int HD>
@@ -88,30 +153,32 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + 2 * SM::QT;
   uint8_t* sV = sK + 2 * SM::K;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * SM::V);
-  const uint32_t q_full = smem_u32(bars + 0);
-  const uint32_t k_full0 = smem_u32(bars + 1);    // [2] per stage
-  const uint32_t v_full0 = smem_u32(bars + 3);    // [2] per stage
-  const uint32_t k_empty0 = smem_u32(bars + 5);   // [2] per stage: freed once S1 of the K tile has completed
-  const uint32_t s_full0 = smem_u32(bars + 7);    // [2] per tile
-  const uint32_t p_full0 = smem_u32(bars + 9);    // [2] per tile
-  const uint32_t pv_done0 = smem_u32(bars + 11);  // [2] per tile
-  const uint32_t v_empty0 = smem_u32(bars + 13);  // [2] per stage: freed after both P V MMAs of the V tile
-  const uint32_t mma_done = smem_u32(bars + 15);  // after a time-out: every issued MMA has completed
-  const uint32_t p_half0 = smem_u32(bars + 16);   // [2] per tile: P over keys 0..63 written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  uint8_t* sO = sV + 2 * SM::V;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sO + 8 * kStageO);
+  const uint32_t q_full0 = smem_u32(bars + 0);    // [2] per tile: Q tile loaded (once per item)
+  const uint32_t k_full0 = smem_u32(bars + 2);    // [2] per stage
+  const uint32_t v_full0 = smem_u32(bars + 4);    // [2] per stage
+  const uint32_t k_empty0 = smem_u32(bars + 6);   // [2] per stage: freed once S1 of the K tile has completed
+  const uint32_t s_full0 = smem_u32(bars + 8);    // [2] per tile
+  const uint32_t p_full0 = smem_u32(bars + 10);   // [2] per tile
+  const uint32_t pv_done0 = smem_u32(bars + 12);  // [2] per tile: the item's last P V has completed
+  const uint32_t v_empty0 = smem_u32(bars + 14);  // [2] per stage: freed after both P V MMAs of the V tile
+  const uint32_t mma_done = smem_u32(bars + 16);  // after a time-out: every issued MMA has completed
+  const uint32_t p_half0 = smem_u32(bars + 17);   // [2] per tile: P over keys 0..63 written
+  const uint32_t q_empty0 = smem_u32(bars + 19);  // [2] per tile: the item's last S MMA of the tile has completed
+  const uint32_t o_free0 = smem_u32(bars + 21);   // [2] per tile: O read out of TMEM by the tile's softmax warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int q0 = blockIdx.x * (2 * kAttnBM);
   const int D = p.H * HD;
   const int nkv = p.n_kv_tiles;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full0 + 8 * i, 1);
+      mbar_init(q_empty0 + 8 * i, 1);
       mbar_init(k_full0 + 8 * i, 1);
       mbar_init(v_full0 + 8 * i, 1);
       mbar_init(k_empty0 + 8 * i, 1);
@@ -120,6 +187,7 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       mbar_init(p_full0 + 8 * i, 4);
       mbar_init(p_half0 + 8 * i, 4);
       mbar_init(pv_done0 + 8 * i, 1);
+      mbar_init(o_free0 + 8 * i, 4);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -143,172 +211,239 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     const int t = warp >> 2;
     const int quad = warp & 3;
+    const int wid = warp;  // t * 4 + quad
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
     const uint32_t s_full = s_full0 + 8 * t, p_full = p_full0 + 8 * t, p_half = p_half0 + 8 * t;
-    const uint32_t pv_done = pv_done0 + 8 * t;
-    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t pv_done = pv_done0 + 8 * t, o_free = o_free0 + 8 * t;
+    uint8_t* stg = sO + wid * kStageO;
     const float sl2 = p.scale_log2;
+    AttnWork work(p);
+    AttnItem I;
+    uint32_t g = 0, it = 0;  // KV steps and items done
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait_warp(s_full, j & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
-      tc_fence_after();
-      // S1(j) has completed, and S0(j) before it: the K(j) ring slot is free
-      if (t == 1 && quad == 0 && lane == 0) mbar_arrive(k_empty0 + 8 * (j & 1));
-      const int kv0 = j * kAttnBN;
-      float sv[kAttnBN];
-      {
-        uint32_t raw[kAttnBN];
+    while (ok && work.next(I)) {
+      const int n = I.je - I.jb;
+      float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll 1
+      for (int jj = 0; jj < n; ++jj) {
+        const uint32_t gj = g + (uint32_t)jj;
+        if (!mbar_wait_warp(s_full, gj & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) { ok = false; break; }
+        tc_fence_after();
+        // S1(j) has completed, and S0(j) before it: the K(j) ring slot is free
+        if (t == 1 && quad == 0 && lane == 0) mbar_arrive(k_empty0 + 8 * (gj & 1));
+        const int kv0 = (I.jb + jj) * kAttnBN;
+        float sv[kAttnBN];
+        {
+          uint32_t raw[kAttnBN];
 #pragma unroll
-        for (int c = 0; c < kAttnBN / 32; ++c) MMDIT_TMEM_LD32(tS + c * 32, (raw + c * 32));
+          for (int c = 0; c < kAttnBN / 32; ++c) MMDIT_TMEM_LD32(tS + c * 32, (raw + c * 32));
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < kAttnBN; ++c) sv[c] = __uint_as_float(raw[c]);
+        }
+        if (kv0 + kAttnBN > p.L) {
+#pragma unroll
+          for (int c = 0; c < kAttnBN; ++c)
+            if (kv0 + c >= p.L) sv[c] = -INFINITY;
+        }
+        // row max: 8 independent chains of three-input max over columns
+        // 8..119 in pairs of 8, then columns 120..127
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+        for (int c = 8; c + 16 <= kAttnBN; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[kAttnBN - 8 + i]);
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        const float m_new = fmaxf(m_run, mx * sl2);
+        // P V(j - 1) has completed here: S(j) was issued after it and the
+        // commit behind s_full covers every earlier MMA of the issuing thread.
+        // So O may be rescaled, and P(j) may overwrite P(j - 1), without a
+        // further wait.
+        // Lazy rescale: the TMEM accesses are warp-wide, so the warp rescales
+        // when any of its rows needs it (alpha = 1, an exact no-op, for the
+        // others).  The item's first P V overwrites O, so its first step has
+        // nothing to rescale.
+        const bool grow = m_new > m_run + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float alpha = grow ? ex2_approx(m_run - m_new) : 1.0f;
+          if (jj > 0) {
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+              uint32_t raw[32];
+              MMDIT_TMEM_LD32(tO + c * 32, raw);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
+              MMDIT_TMEM_ST32(tO + c * 32, raw);
+            }
+            tmem_wait_st();
+          }
+          if (grow) {
+            l_run *= alpha;
+            m_run = m_new;
+          }
+        }
+        // exponentials on column pairs (f32x2 arithmetic for the argument and the
+        // sums), row sum in 4 packed partial sums, bf16 P over the first 64
+        // columns of S.  Every exponential is a MUFU ex2: at 32 results per
+        // cycle per SM it takes fewer issue slots than a polynomial on the FMA
+        // pipe, and the softmax is issue-bound.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_run, -m_run);
+        uint64_t ls2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ls2[i] = f2_pack(0.f, 0.f);
+        uint32_t pk[kAttnBN / 2];
+#pragma unroll
+        for (int c = 0; c < kAttnBN / 2; ++c) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sl2x2, negm2), x0, x1);
+          const uint64_t p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
+          ls2[c & 3] = f2_add(ls2[c & 3], p2);
+          float p0, p1;
+          f2_unpack(p2, p0, p1);
+          pk[c] = pack_bf16x2(p0, p1);
+          // P over keys 0..63 is complete after pair 31: it is stored then,
+          // and handed over 8 pairs later (the store's latency overlaps those
+          // pairs), so that P V(j) starts on those keys while the other half
+          // is computed.
+          if (c == kAttnBN / 4 - 1) MMDIT_TMEM_ST32(tS, pk);
+          if (c == kAttnBN / 4 + 7) {
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_half);
+          }
+        }
+        float ls[2];
+        f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), ls[0], ls[1]);
+        MMDIT_TMEM_ST32(tS + 32, (pk + 32));
+        l_run += ls[0] + ls[1];
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      if (!ok || !mbar_wait_warp(pv_done, it & 1, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // O of this warp's 32 rows into registers; the columns go back to the
+      // MMA warp at once (the next item's first P V overwrites them).
+      float o[HD];
+      {
+        uint32_t raw[HD];
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) MMDIT_TMEM_LD32(tO + c * 32, (raw + c * 32));
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < kAttnBN; ++c) sv[c] = __uint_as_float(raw[c]);
+        for (int c = 0; c < HD; ++c) o[c] = __uint_as_float(raw[c]);
       }
-      if (kv0 + kAttnBN > p.L) {
-#pragma unroll
-        for (int c = 0; c < kAttnBN; ++c)
-          if (kv0 + c >= p.L) sv[c] = -INFINITY;
-      }
-      // row max: 8 independent chains of three-input max over columns
-      // 8..119 in pairs of 8, then columns 120..127
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
-#pragma unroll
-      for (int c = 8; c + 16 <= kAttnBN; c += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[kAttnBN - 8 + i]);
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      const float m_new = fmaxf(m_run, mx * sl2);
-      // P V(j - 1) has completed here: S(j) was issued after it and the
-      // commit behind s_full covers every earlier MMA of the issuing thread.
-      // So O may be rescaled, and P(j) may overwrite P(j - 1), without a
-      // further wait.
-      // Lazy rescale: the TMEM accesses are warp-wide, so the warp rescales
-      // when any of its rows needs it (alpha = 1, an exact no-op, for the
-      // others).
-      const bool grow = m_new > m_run + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float alpha = grow ? ex2_approx(m_run - m_new) : 1.0f;
-        if (j > 0) {
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t raw[32];
-            MMDIT_TMEM_LD32(tO + c * 32, raw);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
-            MMDIT_TMEM_ST32(tO + c * 32, raw);
-          }
-          tmem_wait_st();
-        }
-        if (grow) {
-          l_run *= alpha;
-          m_run = m_new;
-        }
-      }
-      // exponentials on column pairs (f32x2 arithmetic for the argument and the
-      // sums), row sum in 4 packed partial sums, bf16 P over the first 64
-      // columns of S.  Every exponential is a MUFU ex2: at 32 results per
-      // cycle per SM it takes fewer issue slots than a polynomial on the FMA
-      // pipe, and the softmax is issue-bound.
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_run, -m_run);
-      uint64_t ls2[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ls2[i] = f2_pack(0.f, 0.f);
-      uint32_t pk[kAttnBN / 2];
-#pragma unroll
-      for (int c = 0; c < kAttnBN / 2; ++c) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(sv[2 * c], sv[2 * c + 1]), sl2x2, negm2), x0, x1);
-        const uint64_t p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
-        ls2[c & 3] = f2_add(ls2[c & 3], p2);
-        float p0, p1;
-        f2_unpack(p2, p0, p1);
-        pk[c] = pack_bf16x2(p0, p1);
-        // P over keys 0..63 is complete after pair 31: it is stored then,
-        // and handed over 8 pairs later (the store's latency overlaps those
-        // pairs), so that P V(j) starts on those keys while the other half
-        // is computed.
-        if (c == kAttnBN / 4 - 1) MMDIT_TMEM_ST32(tS, pk);
-        if (c == kAttnBN / 4 + 7) {
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(p_half);
-        }
-      }
-      float ls[2];
-      f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), ls[0], ls[1]);
-      MMDIT_TMEM_ST32(tS + 32, (pk + 32));
-      l_run += ls[0] + ls[1];
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok && mbar_wait_warp(pv_done, 0, abort_flag, p.status, ST_TIMEOUT_SOFTMAX)) {  // the last P V only
-      tc_fence_after();
-      const float inv_l = 1.0f / l_run;
-      // O / l as bf16 through shared memory.  This warp's 32 rows go to its
-      // own block of the K ring (idle now: every S MMA has completed and no
-      // load is pending) in the 128-byte-swizzled layout of the output
-      // tensor map -- row `lane` at a 128-byte pitch, 16-byte chunk j at
-      // position j ^ (lane % 8), one 4 KB block per 64 columns -- and lane 0
-      // writes them out with TMA tile stores (rows at or beyond L are
-      // clipped by the tensor map).  A warp's 16-byte shared stores then take
-      // 4 wavefronts each, where direct row-per-thread global stores touched
-      // 32 scattered sectors per instruction.
-      uint8_t* stg = sK + (t * 4 + quad) * (HD / 64) * 4096;
+      if (lane == 0) mbar_arrive(o_free);
+
+      const int pair = I.u % p.n_pairs;
+      const int bh = I.u / p.n_pairs;
+      const int h = bh % p.H, b = bh / p.H;
+      bool store = true;
+      if (I.jb > 0 || I.je < nkv) {
+        // Part of a split unit: A (keys from 0) is the last item of CTA c,
+        // B (keys up to the end) the first tail item of CTA c + 1; boundary c
+        // names the unit.  Slot layout per warp: O as [HD / 4][32 lanes]
+        // float4 (coalesced rows of 512 bytes), then m[32], l[32].
+        const int part = I.jb > 0 ? 1 : 0;
+        const int bound = (int)blockIdx.x - part;
+        constexpr int kSlot = 32 * HD + 64;
+        float* own = p.part + (size_t)((bound * 2 + part) * 8 + wid) * kSlot;
+        const float* oth = p.part + (size_t)((bound * 2 + (part ^ 1)) * 8 + wid) * kSlot;
+        float4* own4 = reinterpret_cast<float4*>(own);
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t raw[32];
-        MMDIT_TMEM_LD32(tO + c * 32, raw);
-        tmem_wait_ld();
-        uint8_t* rowp = stg + (c >> 1) * 4096 + lane * 128;
+        for (int k = 0; k < HD / 4; ++k)
+          __stcg(own4 + k * 32 + lane, make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]));
+        __stcg(own + 32 * HD + lane, m_run);
+        __stcg(own + 32 * HD + 32 + lane, l_run);
+        __threadfence();
+        __syncwarp();
+        int second = 0;
+        if (lane == 0) second = atomicAdd(p.cnt + bound * 8 + wid, 1) != 0;
+        second = __shfl_sync(0xffffffffu, second, 0);
+        if (!second) {
+          store = false;  // the other part, still running, merges and stores
+        } else {
+          __threadfence();
+          const float m_o = __ldcg(oth + 32 * HD + lane);
+          const float l_o = __ldcg(oth + 32 * HD + 32 + lane);
+          const float m = fmaxf(m_run, m_o);
+          const float a = ex2_approx(m_run - m), c = ex2_approx(m_o - m);
+          l_run = a * l_run + c * l_o;
+          const float4* oth4 = reinterpret_cast<const float4*>(oth);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int chunk = (c & 1) * 4 + i;
-          const float* v = reinterpret_cast<const float*>(raw + 8 * i);
-          *reinterpret_cast<uint4*>(rowp + ((chunk ^ (lane & 7)) << 4)) =
-              make_uint4(pack_bf16x2(v[0] * inv_l, v[1] * inv_l), pack_bf16x2(v[2] * inv_l, v[3] * inv_l),
-                         pack_bf16x2(v[4] * inv_l, v[5] * inv_l), pack_bf16x2(v[6] * inv_l, v[7] * inv_l));
+          for (int k = 0; k < HD / 4; ++k) {
+            const float4 w = __ldcg(oth4 + k * 32 + lane);
+            o[4 * k] = fmaf(a, o[4 * k], c * w.x);
+            o[4 * k + 1] = fmaf(a, o[4 * k + 1], c * w.y);
+            o[4 * k + 2] = fmaf(a, o[4 * k + 2], c * w.z);
+            o[4 * k + 3] = fmaf(a, o[4 * k + 3], c * w.w);
+          }
         }
       }
-      fence_proxy_async_smem();  // the shared stores are visible to the TMA unit
-      __syncwarp();
-      const int row0 = q0 + t * kAttnBM + quad * 32;
-      if (lane == 0 && row0 < p.L) {
+      if (store) {
+        // O / l as bf16 through this warp's staging block, 64 columns at a
+        // time, in the 128-byte-swizzled layout of the output tensor map --
+        // row `lane` at a 128-byte pitch, 16-byte chunk i at position
+        // i ^ (lane % 8) -- written out by lane 0 with TMA tile stores (rows
+        // at or beyond L are clipped by the tensor map).  A warp's 16-byte
+        // shared stores take 4 wavefronts each, where direct row-per-thread
+        // global stores touched 32 scattered sectors per instruction.
+        const float inv_l = 1.0f / l_run;
+        const int row0 = pair * (2 * kAttnBM) + t * kAttnBM + quad * 32;
+        uint8_t* rowp = stg + lane * 128;
 #pragma unroll
-        for (int hf = 0; hf < HD / 64; ++hf)
-          tma_store_3d(&tmO, smem_u32(stg + hf * 4096), h * HD + hf * 64, row0, b);
-        bulk_commit_group();
-        bulk_wait_group_read0();  // the staging block has been read before the CTA exits
+        for (int hf = 0; hf < HD / 64; ++hf) {
+          if (lane == 0) bulk_wait_group_read0();  // the previous store has read the block
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float* v = o + hf * 64 + 8 * i;
+            *reinterpret_cast<uint4*>(rowp + ((i ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16x2(v[0] * inv_l, v[1] * inv_l), pack_bf16x2(v[2] * inv_l, v[3] * inv_l),
+                           pack_bf16x2(v[4] * inv_l, v[5] * inv_l), pack_bf16x2(v[6] * inv_l, v[7] * inv_l));
+          }
+          fence_proxy_async_smem();  // the shared stores are visible to the TMA unit
+          __syncwarp();
+          if (lane == 0 && row0 < p.L) {
+            tma_store_3d(&tmO, smem_u32(stg), h * HD + hf * 64, row0, b);
+            bulk_commit_group();
+          }
+        }
       }
-      __syncwarp();
+      g += (uint32_t)n;
+      ++it;
     }
+    if (lane == 0) bulk_wait_group_read0();  // the staging block has been read before the CTA exits
+    __syncwarp();
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (warp == 8) {
       if (lane == 0) {
-        mbar_expect_tx(q_full, 2 * SM::QT);
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int hf = 0; hf < HD / 64; ++hf)
-            tma_load_3d(smem_u32(sQ + t * SM::QT + hf * kHalf), &tmQK, q_full, h * HD + hf * 64, q0 + t * kAttnBM, b);
-        // Loads in the order the MMAs need them: V(j) (for P V0(j)) before
-        // K(j + 1) (for S0(j + 1), issued after P V0(j)).  This is also the
-        // order in which their ring slots free up: V(j)'s after P V1(j - 2),
-        // K(j + 1)'s after S1(j - 1), which follows it in the tensor pipe.
-        int n_k = 0, n_v = 0;  // tiles whose loads were issued (for the drain after a time-out)
+        // Loads in the order the MMAs need them: per item K(first), the Q
+        // tiles, then V(j) (for P V0(j)) before K(j + 1) (for S0(j + 1),
+        // issued after P V0(j)).  This is also the order in which their slots
+        // free up: V(j)'s after P V1(j - 2), K(j + 1)'s after S1(j - 1), Q
+        // tile t's after the previous item's last S MMA of tile t.
+        uint32_t n_k = 0, n_v = 0, n_item = 0;  // loads issued (ring counters, and for the drain after a time-out)
+        uint32_t n_q[2] = {0, 0};
+        int h = 0, b = 0;
         auto load_k = [&](int j) -> bool {
-          const int st = j & 1;
-          if (!mbar_wait(k_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER))
+          const uint32_t st = n_k & 1;
+          if (!mbar_wait(k_empty0 + 8 * st, ((n_k >> 1) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER))
             return false;
           ++n_k;
           mbar_expect_tx(k_full0 + 8 * st, SM::K);
@@ -319,8 +454,8 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
           return true;
         };
         auto load_v = [&](int j) -> bool {
-          const int st = j & 1;
-          if (!mbar_wait(v_empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER))
+          const uint32_t st = n_v & 1;
+          if (!mbar_wait(v_empty0 + 8 * st, ((n_v >> 1) & 1) ^ 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER))
             return false;
           ++n_v;
           mbar_expect_tx(v_full0 + 8 * st, SM::V);
@@ -330,18 +465,41 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
                         h * HD, b);
           return true;
         };
-        bool okp = load_k(0);
-        for (int j = 0; okp && j < nkv; ++j) okp = load_v(j) && (j + 1 >= nkv || load_k(j + 1));
+        AttnWork work(p);
+        AttnItem I;
+        bool okp = true;
+        while (okp && work.next(I)) {
+          const int pair = I.u % p.n_pairs;
+          const int bh = I.u / p.n_pairs;
+          h = bh % p.H, b = bh / p.H;
+          okp = load_k(I.jb);
+          for (int t = 0; okp && t < 2; ++t) {
+            if (n_item > 0 &&
+                !mbar_wait(q_empty0 + 8 * t, (n_item - 1) & 1, abort_flag, p.status, ST_TIMEOUT_PRODUCER)) {
+              okp = false;
+              break;
+            }
+            ++n_q[t];
+            mbar_expect_tx(q_full0 + 8 * t, SM::QT);
+#pragma unroll
+            for (int hf = 0; hf < HD / 64; ++hf)
+              tma_load_3d(smem_u32(sQ + t * SM::QT + hf * kHalf), &tmQK, q_full0 + 8 * t, h * HD + hf * 64,
+                          pair * (2 * kAttnBM) + t * kAttnBM, b);
+          }
+          for (int j = I.jb; okp && j < I.je; ++j) okp = load_v(j) && (j + 1 >= I.je || load_k(j + 1));
+          ++n_item;
+        }
         if (*abort_flag) {
           // After a time-out anywhere in the CTA: wait (bounded) until every
-          // copy still in flight into this CTA's shared memory has landed (Q,
-          // and the last two K and V tiles, one per ring stage) before the CTA
-          // frees its resources and exits.
+          // copy still in flight into this CTA's shared memory has landed
+          // (the last Q load of each tile, and the last two K and V tiles,
+          // one per ring stage) before the CTA frees its resources and exits.
           constexpr unsigned long long kDrainNs = 100000000ull;
-          mbar_wait(q_full, 0, nullptr, nullptr, 0, kDrainNs);
-          for (int j = max(0, n_k - 2); j < n_k; ++j)
+          for (int t = 0; t < 2; ++t)
+            if (n_q[t] > 0) mbar_wait(q_full0 + 8 * t, (n_q[t] - 1) & 1, nullptr, nullptr, 0, kDrainNs);
+          for (uint32_t j = n_k > 2 ? n_k - 2 : 0; j < n_k; ++j)
             mbar_wait(k_full0 + 8 * (j & 1), (j >> 1) & 1, nullptr, nullptr, 0, kDrainNs);
-          for (int j = max(0, n_v - 2); j < n_v; ++j)
+          for (uint32_t j = n_v > 2 ? n_v - 2 : 0; j < n_v; ++j)
             mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, nullptr, nullptr, 0, kDrainNs);
         }
       }
@@ -360,13 +518,14 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
         return mbar_wait_warp(bar, parity, abort_flag, p.status, ST_TIMEOUT_MMA);
       };
-      // S(t, j) = Q_t K(j)^T (kS = d / 16 steps of K = 16) and
-      // O_t += P_t(j) V(j) (8 steps: 128 keys), MMAs k0..k1-1 of those steps.
+      // S(t, g) = Q_t K(g)^T (kS = d / 16 steps of K = 16) and
+      // O_t (+)= P_t(g) V(g) (8 steps: 128 keys), MMAs k0..k1-1 of those
+      // steps; g counts KV steps over all items (it selects the ring stage).
       // Operand selection is arithmetic, not a branch.
       constexpr int kS = HD / 16;
-      auto mma_s = [&](int t, int j, int k0, int k1) {
+      auto mma_s = [&](int t, uint32_t g, int k0, int k1) {
         const uint64_t aQ = dQ0 + (uint64_t)(t * (SM::QT >> 4));
-        const uint64_t bK = dK0 + (uint64_t)((j & 1) * (SM::K >> 4));
+        const uint64_t bK = dK0 + (uint64_t)((g & 1) * (SM::K >> 4));
         const uint32_t dS = tmem + t * 128;
 #pragma unroll
         for (int k = k0; k < k1; ++k) {
@@ -374,10 +533,9 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
           umma_bf16_if(leader, dS, aQ + off, bK + off, idesc_s, k > 0 ? 1u : 0u);
         }
       };
-      auto mma_pv = [&](int t, int j, int k0, int k1) {
-        const uint64_t bV = dV0 + (uint64_t)((j & 1) * (SM::V >> 4));
+      auto mma_pv = [&](int t, uint32_t g, uint32_t acc0, int k0, int k1) {
+        const uint64_t bV = dV0 + (uint64_t)((g & 1) * (SM::V >> 4));
         const uint32_t dO = tmem + 256 + t * 128, aP = tmem + t * 128;
-        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int k = k0; k < k1; ++k) {
           const uint32_t off = ((k >> 2) * (HD * 128) + (k & 3) * 32) >> 4;
@@ -387,57 +545,85 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
       // After a failed wait the loop still issues the MMAs of that step (all
       // operands lie inside this CTA's shared and tensor memory) and stops at
       // the next loop test: no branch sits between the waits and the MMAs.
-      bool ok = wait(q_full, 0) && wait(k_full0, 0);
-      tc_fence_after();
-      mma_s(0, 0, 0, kS);
-      umma_commit_if(leader, s_full0);
-      mma_s(1, 0, 0, kS / 2);
-      ok = ok && wait(v_full0, 0);
-      tc_fence_after();
-      mma_s(1, 0, kS / 2, kS);
-      umma_commit_if(leader, s_full0 + 8);
-      int j = 0;
-#pragma unroll 1
-      for (; ok && j + 1 < nkv; ++j) {
-        const uint32_t st1 = (uint32_t)((j + 1) & 1), ph1 = (uint32_t)(((j + 1) >> 1) & 1);
-        ok = wait(p_half0, j & 1);  // P0(j) over keys 0..63
+      AttnWork work(p);
+      AttnItem I;
+      uint32_t g = 0, it = 0;
+      bool ok = true;
+      while (ok && work.next(I)) {
+        const int n = I.je - I.jb;
+        const uint32_t ph_it = it & 1;
+        ok = wait(q_full0, ph_it) && wait(k_full0 + 8 * (g & 1), (g >> 1) & 1);
         tc_fence_after();
-        mma_pv(0, j, 0, 4);
-        ok = wait(p_full0, j & 1) && ok;  // P0(j) over keys 64..127
-        tc_fence_after();
-        mma_pv(0, j, 4, 8);
-        ok = wait(k_full0 + 8 * st1, ph1) && ok;  // K(j + 1), for S0(j + 1)
-        tc_fence_after();
-        mma_s(0, j + 1, 0, kS);
+        mma_s(0, g, 0, kS);
         umma_commit_if(leader, s_full0);
-        ok = wait(p_half0 + 8, j & 1) && ok;
+        if (n == 1) umma_commit_if(leader, q_empty0);
+        ok = wait(q_full0 + 8, ph_it) && ok;
         tc_fence_after();
-        mma_pv(1, j, 0, 4);
-        ok = wait(p_full0 + 8, j & 1) && ok;
+        mma_s(1, g, 0, kS / 2);
+        ok = wait(v_full0 + 8 * (g & 1), (g >> 1) & 1) && ok;
         tc_fence_after();
-        mma_pv(1, j, 4, 8);
-        umma_commit_if(leader, v_empty0 + 8 * (j & 1));  // P V0(j) and P V1(j) have read V(j)
-        mma_s(1, j + 1, 0, kS / 2);
-        ok = wait(v_full0 + 8 * st1, ph1) && ok;  // V(j + 1), for P V0(j + 1)
-        tc_fence_after();
-        mma_s(1, j + 1, kS / 2, kS);
+        mma_s(1, g, kS / 2, kS);
         umma_commit_if(leader, s_full0 + 8);
-      }
-      if (ok) {  // the last KV tile
-        ok = wait(p_half0, j & 1);
-        tc_fence_after();
-        mma_pv(0, j, 0, 4);
-        ok = wait(p_full0, j & 1) && ok;
-        tc_fence_after();
-        mma_pv(0, j, 4, 8);
-        umma_commit_if(leader, pv_done0);  // for the final O / l
-        ok = wait(p_half0 + 8, j & 1) && ok;
-        tc_fence_after();
-        mma_pv(1, j, 0, 4);
-        ok = wait(p_full0 + 8, j & 1) && ok;
-        tc_fence_after();
-        mma_pv(1, j, 4, 8);
-        umma_commit_if(leader, pv_done0 + 8);
+        if (n == 1) umma_commit_if(leader, q_empty0 + 8);
+        if (it > 0) {
+          // the previous item's O columns have been read out (the first P V
+          // of this item overwrites them)
+          ok = wait(o_free0, ph_it ^ 1) && ok;
+          ok = wait(o_free0 + 8, ph_it ^ 1) && ok;
+          tc_fence_after();
+        }
+        int jj = 0;
+#pragma unroll 1
+        for (; ok && jj + 1 < n; ++jj) {
+          const uint32_t gj = g + (uint32_t)jj, gn = gj + 1;
+          const uint32_t st1 = gn & 1, ph1 = (gn >> 1) & 1;
+          const uint32_t acc0 = jj > 0 ? 1u : 0u;
+          ok = wait(p_half0, gj & 1);  // P0(j) over keys 0..63
+          tc_fence_after();
+          mma_pv(0, gj, acc0, 0, 4);
+          ok = wait(p_full0, gj & 1) && ok;  // P0(j) over keys 64..127
+          tc_fence_after();
+          mma_pv(0, gj, acc0, 4, 8);
+          ok = wait(k_full0 + 8 * st1, ph1) && ok;  // K(j + 1), for S0(j + 1)
+          tc_fence_after();
+          mma_s(0, gn, 0, kS);
+          umma_commit_if(leader, s_full0);
+          if (jj + 2 == n) umma_commit_if(leader, q_empty0);  // the item's last S0
+          ok = wait(p_half0 + 8, gj & 1) && ok;
+          tc_fence_after();
+          mma_pv(1, gj, acc0, 0, 4);
+          ok = wait(p_full0 + 8, gj & 1) && ok;
+          tc_fence_after();
+          mma_pv(1, gj, acc0, 4, 8);
+          umma_commit_if(leader, v_empty0 + 8 * (gj & 1));  // P V0(j) and P V1(j) have read V(j)
+          mma_s(1, gn, 0, kS / 2);
+          ok = wait(v_full0 + 8 * st1, ph1) && ok;  // V(j + 1), for P V0(j + 1)
+          tc_fence_after();
+          mma_s(1, gn, kS / 2, kS);
+          umma_commit_if(leader, s_full0 + 8);
+          if (jj + 2 == n) umma_commit_if(leader, q_empty0 + 8);  // the item's last S1
+        }
+        if (ok) {  // the item's last KV tile
+          const uint32_t gj = g + (uint32_t)jj;
+          const uint32_t acc0 = jj > 0 ? 1u : 0u;
+          ok = wait(p_half0, gj & 1);
+          tc_fence_after();
+          mma_pv(0, gj, acc0, 0, 4);
+          ok = wait(p_full0, gj & 1) && ok;
+          tc_fence_after();
+          mma_pv(0, gj, acc0, 4, 8);
+          umma_commit_if(leader, pv_done0);  // for the final O / l
+          ok = wait(p_half0 + 8, gj & 1) && ok;
+          tc_fence_after();
+          mma_pv(1, gj, acc0, 0, 4);
+          ok = wait(p_full0 + 8, gj & 1) && ok;
+          tc_fence_after();
+          mma_pv(1, gj, acc0, 4, 8);
+          umma_commit_if(leader, v_empty0 + 8 * (gj & 1));
+          umma_commit_if(leader, pv_done0 + 8);
+        }
+        g += (uint32_t)n;
+        ++it;
       }
       if (*abort_flag) {
         // every MMA this warp issued (they read shared memory and write the
@@ -456,8 +642,8 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
 }
 
 template <int HD>
-cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, const CUtensorMap& tmO, const AttnParams& p,
-                            cudaStream_t s) {
+cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, const CUtensorMap& tmO,
+                            const AttnParams& p_in, cudaStream_t s) {
   // shared-memory opt-in once per device, safe under concurrent first calls
   static std::once_flag once[64];
   static cudaError_t setup_err[64];
@@ -468,9 +654,26 @@ cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, con
                                           (int)Attn2Smem<HD>::total);
   });
   if (setup_err[dev] != cudaSuccess) return setup_err[dev];
-  dim3 grid((p.n_q_tiles + 1) / 2, p.H, p.B);
+  AttnParams p = p_in;
+  p.n_pairs = (p.n_q_tiles + 1) / 2;
+  p.n_units = p.n_pairs * p.H * p.B;
+  if (p.n_units <= 0) return cudaSuccess;
+  int G = num_sms();
+  if (G > kAttnMaxCtas) G = kAttnMaxCtas;
+  if (G > p.n_units) G = p.n_units;
+  if (G < 1) return cudaErrorInvalidConfiguration;
+  if (p.part && p.cnt && p.n_units > G) {
+    // whole rounds, then the last one to two rounds' worth of units balanced
+    p.dp_rounds = p.n_units / G - 1;
+    p.tail_units = p.n_units - p.dp_rounds * G;
+    cudaError_t e = cudaMemsetAsync(p.cnt, 0, sizeof(int) * 8 * (size_t)G, s);
+    if (e != cudaSuccess) return e;
+  } else {
+    p.dp_rounds = (p.n_units + G - 1) / G;
+    p.tail_units = 0;
+  }
   launch_begin(KID_ATTENTION, s);
-  attn_fwd_kernel<HD><<<grid, kAttn2Threads, Attn2Smem<HD>::total, s>>>(tmQK, tmV, tmO, p);
+  attn_fwd_kernel<HD><<<G, kAttn2Threads, Attn2Smem<HD>::total, s>>>(tmQK, tmV, tmO, p);
   launch_end(s);
   return cudaGetLastError();
 }

@@ -97,5 +97,7 @@ extern "C" int joint_attention_fwd_noalloc(const mmdit_shape_t* shape, const voi
   if (launch_attn_prep(static_cast<const uint16_t*>(qkv), qkv_row_stride, B, L, Lt, H, d, gq0, gq1, gk0, gk1,
                        shape->eps_rms, cos_, sin_, qk, vT, Lpad, s) != cudaSuccess)
     return MMDIT_ERR_CUDA;
-  return run_attention_prepared(B, L, H, d, Lpad, qk, vT, static_cast<uint16_t*>(out), out_row_stride, s);
+  // No merge area in the static scratch: the schedule runs whole units only.
+  return run_attention_prepared(B, L, H, d, Lpad, qk, vT, static_cast<uint16_t*>(out), out_row_stride, nullptr,
+                                nullptr, s);
 }

@@ -314,7 +314,7 @@ static GemmParams gemm_params(int mode) {
 
 // ----------------------------------------------------------------- attention
 int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint16_t* qk, const uint16_t* vT,
-                           uint16_t* out, long long out_ld, cudaStream_t st) {
+                           uint16_t* out, long long out_ld, int* merge_cnt, float* merge_part, cudaStream_t st) {
   CUtensorMap tq, tv;
   const int D = H * d_head;
   const uint64_t D2 = 2ull * D;
@@ -340,12 +340,25 @@ int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint
   p.n_kv_tiles = (L + kAttnBN - 1) / kAttnBN;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d_head));
   p.status = device_status_ptr();
+  p.cnt = merge_cnt;
+  p.part = merge_part;
   return cuda_status(launch_attention(tq, tv, to, p, d_head, st));
 }
 
+// Merge area of the persistent attention's split tail units (counters, then
+// partial-result slots), carved from a workspace.
+struct AttnMerge {
+  int* cnt;
+  float* part;
+};
+static void take_attn_merge(const Dims& d, Carve& c, AttnMerge& m) {
+  m.cnt = c.take<int>((size_t)kAttnMaxCtas * 8);
+  m.part = c.take<float>(attn_merge_floats(d.d));
+}
+
 static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, uint16_t* out, long long out_ld,
-                         cudaStream_t st) {
-  return run_attention_prepared(d.B, d.L, d.H, d.d, d.Lpad, qk, vT, out, out_ld, st);
+                         const AttnMerge& m, cudaStream_t st) {
+  return run_attention_prepared(d.B, d.L, d.H, d.d, d.Lpad, qk, vT, out, out_ld, m.cnt, m.part, st);
 }
 
 // ----------------------------------------------------------------- workspace layouts
@@ -354,6 +367,7 @@ struct DoubleWS {
   uint16_t *y, *qk, *vT, *O, *h, *wdeq[2];
   uint8_t* a8;  // FP8: e4m3 copy of the current GEMM input (all rows), and its row scales
   float* as;
+  AttnMerge am;
 };
 // y and h hold both streams at once (text rows first), so that each linear
 // of the two streams runs as one grouped launch; int8 weights need one
@@ -371,6 +385,7 @@ static void layout_double(const Dims& d, bool i8, bool need_mod, Carve& c, Doubl
   w.wdeq[1] = i8 ? c.take<uint16_t>(wmax) : nullptr;
   w.a8 = d.f8 ? c.take<uint8_t>((size_t)d.B * d.L * (d.D > d.Dm ? d.D : d.Dm)) : nullptr;
   w.as = d.f8 ? c.take<float>((size_t)d.B * d.L) : nullptr;
+  take_attn_merge(d, c, w.am);
 }
 
 struct SingleWS {
@@ -378,6 +393,7 @@ struct SingleWS {
   uint16_t *y, *qk, *vT, *cat, *wdeq;
   uint8_t* a8;
   float* as;
+  AttnMerge am;
 };
 static void layout_single(const Dims& d, bool i8, bool need_mod, Carve& c, SingleWS& w) {
   w.mod = need_mod ? c.take<float>((size_t)d.B * 3 * d.D) : nullptr;
@@ -388,6 +404,7 @@ static void layout_single(const Dims& d, bool i8, bool need_mod, Carve& c, Singl
   w.wdeq = i8 ? c.take<uint16_t>(((size_t)3 * d.D + (size_t)(d.swiglu ? 2 : 1) * d.Dm) * d.D) : nullptr;
   w.a8 = d.f8 ? c.take<uint8_t>((size_t)d.B * d.L * (d.D + d.Dm)) : nullptr;
   w.as = d.f8 ? c.take<float>((size_t)d.B * d.L) : nullptr;
+  take_attn_merge(d, c, w.am);
 }
 
 struct StepWS {
@@ -489,7 +506,7 @@ static int double_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
     MMDIT_TRY(prepare_gemm(A, D, Ls[i], Ls[i], d.B, D, w.qkv[i], 3 * D, p, ws.wdeq[i], st, pr[i]));
   }
   MMDIT_TRY(grouped(pr));
-  MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.O, D, st));
+  MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.O, D, ws.am, st));
   if (d.f8) MMDIT_TRY(quant(ws.O, D));
   // x += gate1 * (o Wp^T + bp)
   for (int i = first; i < 2; ++i) {
@@ -587,7 +604,7 @@ static int single_block_impl(const mmdit_shape_t& s, const Dims& d, const mmdit_
                            st, pr[1]));
     MMDIT_TRY(launch_problems(&pr[0], &pr[1], st));
   }
-  MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.cat, cat_ld, st));
+  MMDIT_TRY(run_attention(d, ws.qk, ws.vT, ws.cat, cat_ld, ws.am, st));
   if (d.f8) MMDIT_CUDA(launch_quantize_f8(ws.cat, true, rows, (int)cat_ld, cat_ld, ws.a8, cat_ld, ws.as, st));
   GemmParams p2 = gemm_params(GM_RESID);
   p2.ascale = d.f8 ? ws.as : nullptr;
@@ -849,10 +866,13 @@ int mmdit_workspace_size(const mmdit_shape_t* shape, int op, size_t* bytes) {
       layout_single(d, i8, true, c, w);
       break;
     }
-    case MMDIT_OP_ATTENTION:
+    case MMDIT_OP_ATTENTION: {
       c.take<uint16_t>((size_t)d.B * d.L * 2 * d.D);
       c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
+      AttnMerge m;
+      take_attn_merge(d, c, m);
       break;
+    }
     default:
       return MMDIT_ERR_ARG;
   }
@@ -917,9 +937,11 @@ int joint_attention_fwd(const mmdit_shape_t* shape, const void* qkv, int qkv_row
   Carve c{static_cast<uint8_t*>(ws), 0};
   uint16_t* qk = c.take<uint16_t>((size_t)d.B * d.L * 2 * d.D);
   uint16_t* vT = c.take<uint16_t>((size_t)d.B * d.D * d.Lpad);
+  AttnMerge am;
+  take_attn_merge(d, c, am);
   MMDIT_CUDA(launch_attn_prep(static_cast<const uint16_t*>(qkv), qkv_row_stride, d.B, d.L, d.Lt, d.H, d.d, gq0, gq1,
                               gk0, gk1, shape->eps_rms, cos_, sin_, qk, vT, d.Lpad, S(stream)));
-  return run_attention(d, qk, vT, static_cast<uint16_t*>(out), out_row_stride, S(stream));
+  return run_attention(d, qk, vT, static_cast<uint16_t*>(out), out_row_stride, am, S(stream));
 }
 
 int mmdit_double_block_fwd(const mmdit_shape_t* shape, const mmdit_double_w_t* w, const float* vec,

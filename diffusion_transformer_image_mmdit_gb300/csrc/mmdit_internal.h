@@ -80,11 +80,22 @@ struct GemmGroup {
 constexpr int kAttnBM = 128;  // queries per CTA
 constexpr int kAttnBN = 128;  // keys per KV tile
 
+constexpr int kAttnMaxCtas = 160;  // bound on the persistent attention grid (one CTA per SM)
+
 struct AttnParams {
   int L, H, B, n_q_tiles, n_kv_tiles;
   float scale_log2;              // log2(e) / sqrt(d_head)
   unsigned* status;
+  // Split-tail merge area (both null: whole units only, no split): per
+  // boundary between consecutive CTAs, 8 counters (one per softmax warp) and
+  // 2 x 8 slots of 32 x d_head + 64 floats (attn_merge_floats).
+  int* cnt;
+  float* part;
+  // Set by the launcher: units (query-tile pairs x heads x samples), whole
+  // rounds, and the tail units balanced over the grid.
+  int n_pairs, n_units, dp_rounds, tail_units;
 };
+inline size_t attn_merge_floats(int d_head) { return (size_t)kAttnMaxCtas * 2 * 8 * (32 * (size_t)d_head + 64); }
 
 // ----------------------------------------------------------------- host helpers
 unsigned* device_status_ptr();  // device address of the status word (current device)
@@ -137,8 +148,10 @@ int device_check();
 
 // Joint attention over prepared operands: q and k rows in qk [B][L][2D]
 // (normalised and rotated), v transposed in vT [B][D][Lpad]; writes out
-// [B][L][out_ld] bf16.  Returns an MMDIT_* status.
+// [B][L][out_ld] bf16.  merge_cnt / merge_part: the split-tail merge area
+// (kAttnMaxCtas * 8 ints, attn_merge_floats(d_head) floats), or both null
+// for a schedule of whole units only.  Returns an MMDIT_* status.
 int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint16_t* qk, const uint16_t* vT,
-                           uint16_t* out, long long out_ld, cudaStream_t st);
+                           uint16_t* out, long long out_ld, int* merge_cnt, float* merge_part, cudaStream_t st);
 
 }  // namespace mmdit
