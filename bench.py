@@ -131,21 +131,30 @@ def peaks() -> dict:
 
 # ------------------------------------------------------------------ ncu traffic of the GEMM
 GEMM_SOURCES = ["diffusion_transformer_image_mmdit_gb300/csrc/gemm.cu",
-                "diffusion_transformer_image_mmdit_gb300/csrc/common.cuh",
-                "diffusion_transformer_image_mmdit_gb300/csrc/mmdit_internal.h"]
+                "diffusion_transformer_image_mmdit_gb300/csrc/common.cuh"]
+# (file, start marker, end marker): the GEMM sections of shared files
+GEMM_SECTIONS = [("diffusion_transformer_image_mmdit_gb300/csrc/mmdit_internal.h",
+                  "// ----------------------------------------------------------------- GEMM",
+                  "// ----------------------------------------------------------------- attention"),
+                 ("diffusion_transformer_image_mmdit_gb300/csrc/capi.cu",
+                  "// ----------------------------------------------------------------- GEMM",
+                  "static GemmParams gemm_params(int mode)")]
 
 
 def gemm_sources_sha256() -> str:
-    """Hash of the GEMM kernel's sources and of the host code that shapes its
-    launches (tile counts, raster, grouping) in capi.cu."""
+    """Hash of the GEMM kernel's sources: gemm.cu, the device helpers, the
+    GEMM parameter structs, and the host code that shapes its launches (tile
+    counts, raster, grouping) in capi.cu."""
     import hashlib
     h = hashlib.sha256()
     for rel in GEMM_SOURCES:
         h.update(open(os.path.join(ROOT, rel), "rb").read())
-    capi = open(os.path.join(ROOT, "diffusion_transformer_image_mmdit_gb300/csrc/capi.cu")).read()
-    a = capi.find("// ----------------------------------------------------------------- GEMM")
-    b = capi.find("static GemmParams gemm_params(int mode)")
-    h.update(capi[a:b].encode())
+    for rel, start, end in GEMM_SECTIONS:
+        text = open(os.path.join(ROOT, rel)).read()
+        a, b = text.find(start), text.find(end)
+        if a < 0 or b < a:
+            return "missing section in " + rel
+        h.update(text[a:b].encode())
     return h.hexdigest()
 
 
