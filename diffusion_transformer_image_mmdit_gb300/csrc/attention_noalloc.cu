@@ -61,14 +61,23 @@ extern "C" int joint_attention_fwd_noalloc(const mmdit_shape_t* shape, const voi
                                            const float* cos_, const float* sin_, void* out, int out_row_stride,
                                            void* stream) {
   using namespace mmdit;
-  // The public size query validates the shape and gives the scratch it needs.
+  // The public size query validates the shape; the scratch holds qk and vT
+  // only (no merge area: the schedule here runs whole units).
   size_t need = 0;
   const int st = mmdit_workspace_size(shape, MMDIT_OP_ATTENTION, &need);
   if (st != MMDIT_OK) return st;
+  {
+    const size_t B = (size_t)shape->B;
+    const size_t L = (size_t)shape->L_txt + (size_t)shape->grid_h * shape->grid_w + (size_t)shape->ref_h * shape->ref_w;
+    const size_t D = (size_t)shape->D, Lp = (L + 7) / 8 * 8;
+    need = ((B * L * 2 * D * 2 + 255) & ~size_t(255)) + B * D * Lp * 2;
+  }
   if (need > kNoallocScratchBytes) return MMDIT_ERR_WORKSPACE;
   if (!qkv || !out) return MMDIT_ERR_ARG;
   if ((cos_ == nullptr) != (sin_ == nullptr)) return MMDIT_ERR_ARG;
-  const int B = shape->B, Lt = shape->L_txt, L = shape->L_txt + shape->grid_h * shape->grid_w;
+  // the sequence is [text; target image; reference image] tokens, as in the workspace variant
+  const int B = shape->B, Lt = shape->L_txt;
+  const int L = shape->L_txt + shape->grid_h * shape->grid_w + shape->ref_h * shape->ref_w;
   const int D = shape->D, H = shape->H, d = shape->d_head;
   const int Lpad = (L + 7) / 8 * 8;
   if (qkv_row_stride < 3 * D || qkv_row_stride % 8 || out_row_stride < D || out_row_stride % 8)

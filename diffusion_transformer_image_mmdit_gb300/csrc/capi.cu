@@ -352,8 +352,9 @@ struct AttnMerge {
   float* part;
 };
 static void take_attn_merge(const Dims& d, Carve& c, AttnMerge& m) {
-  m.cnt = c.take<int>((size_t)kAttnMaxCtas * 8);
-  m.part = c.take<float>(attn_merge_floats(d.d));
+  const long long units = attn_units(d.B, d.L, d.H);
+  m.cnt = c.take<int>(attn_merge_ctas(units) * 8);
+  m.part = c.take<float>(attn_merge_floats(d.d, units));
 }
 
 static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, uint16_t* out, long long out_ld,

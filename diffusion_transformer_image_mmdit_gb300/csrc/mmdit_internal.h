@@ -88,14 +88,21 @@ struct AttnParams {
   unsigned* status;
   // Split-tail merge area (both null: whole units only, no split): per
   // boundary between consecutive CTAs, 8 counters (one per softmax warp) and
-  // 2 x 8 slots of 32 x d_head + 64 floats (attn_merge_floats).
+  // 2 x 8 slots of 32 x d_head + 64 floats; attn_merge_ctas(units)
+  // boundaries at most.
   int* cnt;
   float* part;
   // Set by the launcher: units (query-tile pairs x heads x samples), whole
   // rounds, and the tail units balanced over the grid.
   int n_pairs, n_units, dp_rounds, tail_units;
 };
-inline size_t attn_merge_floats(int d_head) { return (size_t)kAttnMaxCtas * 2 * 8 * (32 * (size_t)d_head + 64); }
+// Units of an attention launch: pairs of 128-row query tiles x heads x samples.
+inline long long attn_units(int B, int L, int H) { return (long long)((L + 2 * kAttnBM - 1) / (2 * kAttnBM)) * H * B; }
+// The persistent grid never exceeds the unit count, so neither do the boundaries.
+inline size_t attn_merge_ctas(long long units) { return (size_t)(units < kAttnMaxCtas ? units : kAttnMaxCtas); }
+inline size_t attn_merge_floats(int d_head, long long units) {
+  return attn_merge_ctas(units) * 2 * 8 * (32 * (size_t)d_head + 64);
+}
 
 // ----------------------------------------------------------------- host helpers
 unsigned* device_status_ptr();  // device address of the status word (current device)

@@ -288,10 +288,32 @@ def test_gemm_large_tiles_and_ragged():
 
 
 # ------------------------------------------------------------------ attention
-@pytest.mark.parametrize("name", ["c1", "d128", "ragged", "tail"])
+# The persistent attention runs one CTA per SM over units (pairs of 128-row
+# query tiles x heads x samples).  With more units than SMs it runs whole
+# rounds, then splits the remaining units' KV tiles evenly over the CTAs:
+# units cut at a CTA boundary are computed in two parts and merged.  These
+# cases (152 SMs) exercise that tail, all rows compared with the oracle.
+SPLIT_CASES = {
+    # 168 units of 13 KV tiles: no whole round; every CTA takes 14-15 KV steps
+    "split13": dict(B=2, L_txt=64, grid_h=40, grid_w=40, D=1536, H=12, d_head=128, D_mlp=1536,
+                    rope_axes=(16, 56, 56)),
+    # 192 units of 2 KV tiles: parts a single KV tile long
+    "split2": dict(B=8, L_txt=56, grid_h=12, grid_w=12, D=3072, H=24, d_head=128, D_mlp=3072,
+                   rope_axes=(16, 56, 56)),
+    # 384 units of 8 KV tiles (ragged last tile): one whole round, then a tail of 232 units
+    "round_tail": dict(B=4, L_txt=40, grid_h=30, grid_w=32, D=3072, H=24, d_head=128, D_mlp=3072,
+                       rope_axes=(16, 56, 56)),
+    # head width 64: 240 units of 5 KV tiles
+    "split_d64": dict(B=2, L_txt=32, grid_h=24, grid_w=24, D=2560, H=40, d_head=64, D_mlp=2560,
+                      rope_axes=(16, 24, 24)),
+}
+ATTN_CASES = {**{k: CONFIGS[k] for k in ("c1", "d128", "ragged", "tail")}, **SPLIT_CASES}
+
+
+@pytest.mark.parametrize("name", list(ATTN_CASES))
 @pytest.mark.parametrize("norm", [True, False])
 def test_joint_attention(name, norm):
-    cfg = CONFIGS[name]
+    cfg = ATTN_CASES[name]
     shape = api_shape(cfg)
     B, L, H, d, D = cfg["B"], api.seq_len(shape), cfg["H"], cfg["d_head"], cfg["D"]
     Lt = cfg["L_txt"]
