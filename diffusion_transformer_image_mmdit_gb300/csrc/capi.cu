@@ -213,7 +213,7 @@ static bool lin_ok(const mmdit_linear_t& l, bool want_i8) {
 // ----------------------------------------------------------------- GEMM
 // One problem of a GEMM launch: its tensor maps and epilogue parameters.
 struct GemmProblem {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tr;
   GemmParams p;
   bool f8;
 };
@@ -252,6 +252,14 @@ static int prepare_gemm(const void* A, long long a_ld, long long a_seg_rows, int
   if (!make_tmap_3d(&out.tb, W, dt, eb, (uint64_t)K, (uint64_t)N, 1, (uint64_t)K * eb, (uint64_t)N * K * eb, kb,
                     kBN / 2, true))
     return MMDIT_ERR_ALIGN;
+  // GM_RESID: the epilogue adds gate * value into the fp32 residual with TMA
+  // reduce-adds of 32-row x 32-column boxes (rows at or beyond M_seg clipped).
+  std::memset(&out.tr, 0, sizeof(out.tr));
+  if (p.mode == GM_RESID &&
+      (!p.resid || !make_tmap_3d(&out.tr, p.resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)N, (uint64_t)M_seg,
+                                 (uint64_t)n_seg, (uint64_t)p.resid_ld * 4, (uint64_t)p.resid_seg_rows * p.resid_ld * 4,
+                                 32, 32, true)))
+    return MMDIT_ERR_ALIGN;
   out.f8 = f8;
   p.M_seg = M_seg;
   p.n_seg = n_seg;
@@ -281,6 +289,7 @@ static int launch_problems(const GemmProblem* a, const GemmProblem* b, cudaStrea
   std::memset(&g, 0, sizeof(g));
   g.tmA[0] = a->ta;
   g.tmB[0] = a->tb;
+  g.tmR[0] = a->tr;
   g.p[0] = a->p;
   g.n_prob = 1;
   g.f8 = a->f8 ? 1 : 0;
@@ -290,6 +299,7 @@ static int launch_problems(const GemmProblem* a, const GemmProblem* b, cudaStrea
   if (b) {
     g.tmA[1] = b->ta;
     g.tmB[1] = b->tb;
+    g.tmR[1] = b->tr;
     g.p[1] = b->p;
     g.n_prob = 2;
     g.total_tiles += b->p.num_tiles;

@@ -119,7 +119,21 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int 
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// TMA tile reduce-add from this CTA's shared memory into global memory:
+// each element of the box is added (in L2, in the element type of the tensor
+// map) to the global element it maps to; elements outside the tensor are
+// skipped.  Coordinates as for tma_store_3d.  Tracked by the issuing
+// thread's bulk group.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk operation of this thread has completed,
+// its global writes included.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Waits until every committed bulk store of this thread has finished reading
 // its shared-memory source (the global writes may still be in flight; they
 // complete before the grid does).

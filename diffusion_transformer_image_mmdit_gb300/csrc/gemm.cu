@@ -29,7 +29,10 @@
 //               128-column half), fused bias / per-channel scale / GELU-tanh
 //               / SwiGLU / gated fp32 residual / q-k RMSNorm + RoPE /
 //               transposed V store, overlapping the next tile's MMAs; the
-//               drained accumulator is handed back on CTA 0's barrier.
+//               drained accumulator is handed back on CTA 0's barrier.  The
+//               gated residual x += gate * value is a TMA reduce-add of the
+//               staged products into x (the addition happens in L2), so the
+//               epilogue never reads the residual.
 #include <mutex>
 
 #include "common.cuh"
@@ -45,7 +48,7 @@ constexpr uint32_t kStageA = kBM * kBK * 2;       // 16 KB: this CTA's 128 rows 
 constexpr uint32_t kStageB = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128-row half of the W tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiStageBytes = 4096;  // staging area of one epilogue warp
-constexpr size_t kGemmSmem = 1024 + kRing * (kStageA + kStageB) + 256 + kEpiWarps * kEpiStageBytes;
+constexpr size_t kGemmSmem = 1024 + kRing * (kStageA + kStageB) + kEpiWarps * kEpiStageBytes + 256;
 static_assert(kGemmSmem <= 232448, "GEMM shared memory above the 227 KB a CTA can have");
 
 struct TileCoord {
@@ -155,25 +158,6 @@ __device__ __forceinline__ void warp_store_f32x32(uint8_t* stg, int lane, const 
   __syncwarp();
 }
 
-// The transpose of warp_store_f32x32: coalesced loads of 32 rows x 32 fp32,
-// each thread gets its own row (zeros for rows at or beyond nrows).
-__device__ __forceinline__ void warp_load_f32x32(uint8_t* stg, int lane, float* v, const float* row0, long long ld,
-                                                 int nrows) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rr = i * 4 + (lane >> 3), c = lane & 7;
-    const float4 w = rr < nrows ? *reinterpret_cast<const float4*>(row0 + rr * ld + c * 4) : make_float4(0, 0, 0, 0);
-    *reinterpret_cast<float4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4)) = w;
-  }
-  __syncwarp();
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const float4 w = *reinterpret_cast<const float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4));
-    v[4 * c] = w.x, v[4 * c + 1] = w.y, v[4 * c + 2] = w.z, v[4 * c + 3] = w.w;
-  }
-  __syncwarp();
-}
-
 // q/k head of HD columns: bias, RMSNorm with gain g, adjacent-pair RoPE at
 // table row `tok`, bf16 store of the whole head row.  Two passes over the
 // accumulator (TMEM reads are cheap): the first sums squares, the second
@@ -225,8 +209,8 @@ __device__ __forceinline__ void epi_qk_head(uint32_t taddr, const GemmParams& p,
 // of its TMEM lane quadrant (thread = row r of the tile) and the 128 columns
 // of column half `half`.  `tbase` addresses the quadrant's lanes at column 0
 // of the accumulator.
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& c, uint32_t tbase, int r,
-                                              int half, uint8_t* stg) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tmR, const TileCoord& c,
+                                              uint32_t tbase, int r, int half, uint8_t* stg) {
   constexpr int kHalf = kBN / 2;
   const int lane = r & 31;
   const int m = c.tm * kBM + r;
@@ -318,35 +302,31 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       warp_store_bf16x32(stg, lane, v, reinterpret_cast<uint16_t*>(p.out) + orow0 * p.out_ld + n, p.out_ld, nrows);
     } else if (p.mode == GM_STORE_F32) {
       warp_store_f32x32(stg, lane, v, reinterpret_cast<float*>(p.out) + orow0 * p.out_ld + n, p.out_ld, nrows);
-    } else {  // GM_RESID: x += gate * v
-      float gt[32];
+    } else {  // GM_RESID: x += gate * v, added in L2 by a TMA reduce-add
       if (p.gate) {
+        float gt[32];
         load_vec32(p.gate + (long long)c.seg * p.gate_seg_stride + n, gt);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) gt[i] = 1.0f;
+        for (int i = 0; i < 32; ++i) v[i] *= gt[i];
       }
-      float* x0 = p.resid + ((long long)c.seg * p.resid_seg_rows + wm0) * p.resid_ld + n;
-      float x[32];
-      warp_load_f32x32(stg, lane, x, x0, p.resid_ld, nrows);
+      // The warp's 32 rows x 32 columns in the 128-byte-swizzled box layout
+      // of the residual's tensor map: row `lane` at a 128-byte pitch, 16-byte
+      // chunk j at position j ^ (lane % 8).  The block is reused once the
+      // previous reduce has read it.
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = fmaf(gt[i], v[i], x[i]);
-      warp_store_f32x32(stg, lane, x, x0, p.resid_ld, nrows);
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && nrows > 0) {
+        tma_reduce_add_3d(tmR, smem_u32(stg), n, wm0, c.seg);
+        bulk_commit_group();
+      }
     }
   }
-}
-
-// GM_RESID reads this thread's row of the fp32 residual tile in its
-// epilogue.  Issued before the wait for the accumulator, the prefetch runs
-// while the tile's MMAs do, so the epilogue's loads hit L2 instead of
-// waiting on DRAM one 32-column chunk at a time.
-__device__ __forceinline__ void prefetch_resid_row(const GemmParams& p, const TileCoord& c, int r, int half) {
-  const int m = c.tm * kBM + r;
-  const int n0 = c.tn * kBN + half * (kBN / 2);
-  if (m >= p.M_seg || n0 >= p.N) return;
-  const uint32_t bytes = (uint32_t)(min(kBN / 2, p.N - n0) * 4) & ~15u;
-  const float* row = p.resid + ((long long)c.seg * p.resid_seg_rows + m) * p.resid_ld + n0;
-  if (bytes && (reinterpret_cast<uintptr_t>(row) & 15) == 0) prefetch_l2_bulk(row, bytes);
 }
 
 // F8: A and W are e4m3 (one byte per element, 128 elements per 128-byte
@@ -360,7 +340,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kRing * kStageA;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kRing * kStageB);
+  // epilogue staging blocks, 4 KB per epilogue warp, on 1024-byte boundaries
+  // (the 128-byte swizzle of a TMA copy follows the shared-memory address)
+  uint8_t* sE = sB + kRing * kStageB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + kEpiWarps * kEpiStageBytes);
   // full[kRing], tempty[2], mma_done: used in CTA 0 only; empty[kRing], tfull[2]: in both CTAs
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + kRing);
@@ -490,7 +473,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
-    uint8_t* stg = reinterpret_cast<uint8_t*>(bars) + 256 + (warp - 2) * kEpiStageBytes;
+    uint8_t* stg = sE + (warp - 2) * kEpiStageBytes;
     const uint32_t tempty_c0 = mapa_shared(tempty0, 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -498,15 +481,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
       const int q = t < g.tiles0 ? 0 : 1;
       const GemmParams& p = g.p[q];
       const TileCoord c = tile_coord(p, t - (q ? g.tiles0 : 0), rank);
-      if (p.mode == GM_RESID && c.valid) prefetch_resid_row(p, c, r, half);
       if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, status, ST_TIMEOUT_EPILOGUE)) break;
       tc_fence_after();
-      if (c.valid) epilogue_tile(p, c, tmem + ((uint32_t)(quad * 32) << 16) + acc * kBN, r, half, stg);
+      if (c.valid) epilogue_tile(p, &g.tmR[q], c, tmem + ((uint32_t)(quad * 32) << 16) + acc * kBN, r, half, stg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_c0 + 8 * acc);
       if (++acc == 2) acc = 0, acc_phase ^= 1;
     }
+    // this warp's residual reduce-adds have completed (their staging block
+    // read, their sums in global memory) before the CTA moves on
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 done:
   __syncwarp();

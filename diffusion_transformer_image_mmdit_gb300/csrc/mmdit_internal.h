@@ -39,7 +39,7 @@ struct GemmParams {
   long long out_ld;
   long long out_seg_rows;
   int out_row_off;
-  // GM_RESID
+  // GM_RESID (the update goes through GemmGroup::tmR; resid is its base)
   float* resid;
   long long resid_ld;
   long long resid_seg_rows;
@@ -69,6 +69,7 @@ struct GemmParams {
 struct GemmGroup {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
+  CUtensorMap tmR[2];  // GM_RESID: the fp32 residual (cols N, rows M_seg, n_seg), 32 x 32 boxes, 128-byte swizzle
   GemmParams p[2];
   int n_prob;
   int tiles0;
