@@ -485,47 +485,86 @@ __global__ void add_f32_kernel(float* __restrict__ y, const float* __restrict__ 
 __global__ void counter_kernel(int* c, int value, int add) { *c = add ? *c + value : value; }
 
 // ------------------------------------------------------------------ RoPE
-// ids [L,3] and cos/sin [L, d/2]: angle = pos_axis * theta^(-2i/d_axis), fp64.
-// Tokens: L_txt text at (0, 0, 0), then n_gen target image tokens at
-// (0, h, w) on a grid_w-wide grid, then reference image tokens at (1, h, w)
-// on a ref_w-wide grid.
-__global__ void rope_build_kernel(int L_txt, int grid_w, int n_gen, int ref_w, int L, int a0, int a1, int a2,
-                                  double theta, int32_t* __restrict__ ids, float* __restrict__ cs,
-                                  float* __restrict__ sn) {
+// ids [L,3] and cos/sin [L, d/2]: angle = pos_axis * theta^(-2i/d_axis), fp64,
+// rounded once to fp32.  Tokens: L_txt text at (0, 0, 0), then n_gen target
+// image tokens at (0, h, w) on a grid_w-wide grid, then reference image
+// tokens at (1, h, w) on a ref_w-wide grid.  Pair p belongs to axis 0 for
+// p < a0/2, to axis 1 for p < (a0 + a1)/2, to axis 2 otherwise.
+//
+// A value depends only on (position along its axis, pair), so a CTA takes a
+// kRopeTH x kRopeTW tile of one image grid, evaluates the distinct values of
+// the tile once in fp64 (rows x axis-1 pairs, columns x axis-2 pairs, and
+// the axis-0 pairs) into shared memory, and writes the tile's rows from
+// there; text CTAs write the position-0 values (cos 1, sin 0) directly.
+// FP64 is the slow unit of this GPU, and per-element evaluation cost about
+// 13 times the evaluations.
+constexpr int kRopeTH = 8, kRopeTW = 16, kRopeMaxAxisPairs = 64, kRopeTxtTok = 32;
+
+__global__ void __launch_bounds__(256) rope_build_kernel(int L_txt, int grid_h, int grid_w, int ref_h, int ref_w,
+                                                         int a0, int a1, int a2, double theta, int nb_txt,
+                                                         int nt_gen_w, int nb_gen, int nt_ref_w,
+                                                         int32_t* __restrict__ ids, float* __restrict__ cs,
+                                                         float* __restrict__ sn) {
+  __shared__ double om[3][kRopeMaxAxisPairs];
+  __shared__ float tc[kRopeTH + kRopeTW + 1][kRopeMaxAxisPairs];
+  __shared__ float ts[kRopeTH + kRopeTW + 1][kRopeMaxAxisPairs];
   const int npairs = (a0 + a1 + a2) / 2;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)L * npairs) return;
-  const int tok = (int)(idx / npairs), p = (int)(idx - (long long)tok * npairs);
-  int pos[3] = {0, 0, 0};
-  if (tok >= L_txt) {
-    const int img = tok - L_txt;
-    if (img < n_gen) {
-      pos[1] = img / grid_w;
-      pos[2] = img - pos[1] * grid_w;
-    } else {
-      const int r = img - n_gen;
-      pos[0] = 1;
-      pos[1] = r / ref_w;
-      pos[2] = r - pos[1] * ref_w;
+  const int e1 = a0 / 2, e2 = (a0 + a1) / 2;  // first pair of axis 1, of axis 2
+  const int np0 = e1, np1 = e2 - e1, np2 = npairs - e2;
+  int blk = (int)blockIdx.x;
+  if (blk < nb_txt) {
+    const long long tok0 = (long long)blk * kRopeTxtTok;
+    for (int e = threadIdx.x; e < kRopeTxtTok * npairs; e += blockDim.x) {
+      const long long tok = tok0 + e / npairs;
+      const int p = e % npairs;
+      if (tok >= L_txt) break;
+      cs[tok * npairs + p] = 1.0f;  // cos(0), sin(0)
+      sn[tok * npairs + p] = 0.0f;
+      if (p == 0 && ids) ids[3 * tok] = 0, ids[3 * tok + 1] = 0, ids[3 * tok + 2] = 0;
     }
+    return;
   }
-  if (p == 0 && ids) {
-    ids[3 * tok + 0] = pos[0];
-    ids[3 * tok + 1] = pos[1];
-    ids[3 * tok + 2] = pos[2];
+  blk -= nb_txt;
+  const int ref = blk >= nb_gen ? 1 : 0;
+  if (ref) blk -= nb_gen;
+  const int W = ref ? ref_w : grid_w, Hg = ref ? ref_h : grid_h, ntw = ref ? nt_ref_w : nt_gen_w;
+  const long long base = (long long)L_txt + (ref ? (long long)grid_h * grid_w : 0);
+  const int r0 = (blk / ntw) * kRopeTH, c0 = (blk % ntw) * kRopeTW;
+  // frequencies of every pair, then the tile's distinct values
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    const int ax = p < e1 ? 0 : p < e2 ? 1 : 2;
+    const int i = p - (ax == 0 ? 0 : ax == 1 ? e1 : e2);
+    const int da = ax == 0 ? a0 : ax == 1 ? a1 : a2;
+    om[ax][i] = pow(theta, (-2.0 * (double)i) / (double)da);
   }
-  int axis, i, da;
-  if (p < a0 / 2) {
-    axis = 0, i = p, da = a0;
-  } else if (p < (a0 + a1) / 2) {
-    axis = 1, i = p - a0 / 2, da = a1;
-  } else {
-    axis = 2, i = p - (a0 + a1) / 2, da = a2;
+  __syncthreads();
+  const int n1 = kRopeTH * np1, n2 = kRopeTW * np2;
+  for (int e = threadIdx.x; e < n1 + n2 + np0; e += blockDim.x) {
+    int slot, i, ax, pos;
+    if (e < n1) {
+      slot = e / np1, i = e - slot * np1, ax = 1, pos = r0 + slot;
+    } else if (e < n1 + n2) {
+      const int f = e - n1, k = f / np2;
+      slot = kRopeTH + k, i = f - k * np2, ax = 2, pos = c0 + k;
+    } else {
+      slot = kRopeTH + kRopeTW, i = e - n1 - n2, ax = 0, pos = ref;
+    }
+    const double ang = (double)pos * om[ax][i];
+    tc[slot][i] = (float)cos(ang);
+    ts[slot][i] = (float)sin(ang);
   }
-  const double omega = pow(theta, (-2.0 * (double)i) / (double)da);
-  const double ang = (double)pos[axis] * omega;
-  cs[idx] = (float)cos(ang);
-  sn[idx] = (float)sin(ang);
+  __syncthreads();
+  for (int e = threadIdx.x; e < kRopeTH * kRopeTW * npairs; e += blockDim.x) {
+    const int t = e / npairs, p = e - t * npairs;
+    const int r = r0 + t / kRopeTW, c = c0 + t % kRopeTW;
+    if (r >= Hg || c >= W) continue;
+    const long long tok = base + (long long)r * W + c;
+    const int slot = p < e1 ? kRopeTH + kRopeTW : p < e2 ? r - r0 : kRopeTH + (c - c0);
+    const int i = p < e1 ? p : p < e2 ? p - e1 : p - e2;
+    cs[tok * npairs + p] = tc[slot][i];
+    sn[tok * npairs + p] = ts[slot][i];
+    if (p == 0 && ids) ids[3 * tok] = ref, ids[3 * tok + 1] = r, ids[3 * tok + 2] = c;
+  }
 }
 
 // x [rows][row_stride] bf16, each row H*d channels; one thread per 8 channels.
@@ -1011,10 +1050,22 @@ cudaError_t launch_sinusoid(double t, int B, int dim, float* out, cudaStream_t s
 cudaError_t launch_rope_build(int L_txt, int grid_w, int n_gen, int ref_w, int L, const int axes[3], double theta,
                               int32_t* ids, float* cs,
                               float* sn, cudaStream_t st) {
-  const long long n = (long long)L * ((axes[0] + axes[1] + axes[2]) / 2);
+  const int npairs = (axes[0] + axes[1] + axes[2]) / 2;
+  if (axes[0] / 2 > kRopeMaxAxisPairs || (axes[0] + axes[1]) / 2 - axes[0] / 2 > kRopeMaxAxisPairs ||
+      npairs - (axes[0] + axes[1]) / 2 > kRopeMaxAxisPairs || grid_w < 1)
+    return cudaErrorInvalidValue;
+  const int grid_h = n_gen / grid_w;
+  const int n_ref = L - L_txt - n_gen;
+  const int rw = ref_w > 0 ? ref_w : 1, rh = n_ref > 0 ? n_ref / rw : 0;
+  const int nb_txt = (L_txt + kRopeTxtTok - 1) / kRopeTxtTok;
+  const int nt_gen_w = (grid_w + kRopeTW - 1) / kRopeTW, nt_ref_w = (rw + kRopeTW - 1) / kRopeTW;
+  const int nb_gen = ((grid_h + kRopeTH - 1) / kRopeTH) * nt_gen_w;
+  const int nb_ref = rh > 0 ? ((rh + kRopeTH - 1) / kRopeTH) * nt_ref_w : 0;
+  const int blocks = nb_txt + nb_gen + nb_ref;
+  if (blocks == 0) return cudaSuccess;
   launch_begin(KID_ROPE_BUILD, st);
-  rope_build_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(L_txt, grid_w, n_gen, ref_w > 0 ? ref_w : 1, L,
-                                                                 axes[0], axes[1], axes[2], theta, ids, cs, sn);
+  rope_build_kernel<<<blocks, 256, 0, st>>>(L_txt, grid_h, grid_w, rh, rw, axes[0], axes[1], axes[2], theta, nb_txt,
+                                            nt_gen_w, nb_gen, nt_ref_w, ids, cs, sn);
   launch_end(st);
   return cudaGetLastError();
 }
