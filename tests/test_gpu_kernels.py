@@ -306,6 +306,9 @@ SPLIT_CASES = {
     # head width 64: 240 units of 5 KV tiles
     "split_d64": dict(B=2, L_txt=32, grid_h=24, grid_w=24, D=2560, H=40, d_head=64, D_mlp=2560,
                       rope_axes=(16, 24, 24)),
+    # 192 units of a single (ragged) KV tile: more units than SMs, none of them splittable
+    "one_kv_tile": dict(B=8, L_txt=19, grid_h=9, grid_w=9, D=3072, H=24, d_head=128, D_mlp=3072,
+                        rope_axes=(16, 56, 56)),
 }
 ATTN_CASES = {**{k: CONFIGS[k] for k in ("c1", "d128", "ragged", "tail")}, **SPLIT_CASES}
 

@@ -75,6 +75,21 @@ def test_no_alloc_matches_workspace_variant_on_consecutive_calls(name):
     check_status()
 
 
+def test_no_alloc_more_units_than_sms():
+    """160 attention units (pairs of query tiles x heads), more than the
+    152 SMs: the no-alloc variant runs them as whole units in two rounds,
+    the workspace variant balances them by splitting units, so the two are
+    each checked against the oracle rather than against one another."""
+    need_gpu()
+    cfg = dict(B=1, L_txt=64, grid_h=32, grid_w=32, D=4096, H=32, d_head=128, D_mlp=4096, rope_axes=(16, 56, 56))
+    shape, qkv, qn, kn, qkv_h, g_h = _inputs(cfg, "units160")
+    _, cs, sn = gpu_tables(shape)
+    ref = _oracle(cfg, qkv_h, g_h)
+    assert_close(host(_no_alloc(shape, qkv, qn, kn, cs, sn)), ref, what="no-alloc attention, 160 units")
+    assert_close(host(_with_workspace(shape, qkv, qn, kn, cs, sn)), ref, what="workspace attention, 160 units")
+    check_status()
+
+
 def test_no_alloc_rejects_shapes_beyond_its_scratch():
     need_gpu()
     shape = api_shape(FULL["c3"])  # needs about 85 MB of scratch, more than the fixed 48 MiB
