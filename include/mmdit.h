@@ -230,13 +230,19 @@ int joint_attention_fwd(const mmdit_shape_t* shape, const void* qkv, int qkv_row
  * No counterpart on the pages: this is a deployment variant.  A caller such
  * as a plugin inside a host application that owns every device allocation,
  * or code that must avoid the implicit synchronisation cudaMalloc/cudaFree
- * can cause, may have no workspace to pass.  This call computes exactly what
- * joint_attention_fwd computes (same arguments minus ws/ws_bytes) and
- * allocates nothing: its scratch is a fixed 48 MiB device array inside the
- * library, reserved on every GPU that loads it until the process exits.
- *  - Shapes needing more scratch than 48 MiB (the ws size that
- *    mmdit_workspace_size(MMDIT_OP_ATTENTION) reports) return
+ * can cause, may have no workspace to pass.  This call computes the
+ * attention joint_attention_fwd computes (same arguments minus ws/ws_bytes)
+ * and allocates nothing: its scratch is a fixed 48 MiB device array inside
+ * the library, reserved on every GPU that loads it until the process exits.
+ *  - The scratch holds the normalised, rotated q and k (B*L*2*D bf16) and
+ *    the transposed v (B*D*Lpad bf16, Lpad = L rounded up to 8), each
+ *    256-byte aligned.  Shapes needing more than 48 MiB return
  *    MMDIT_ERR_WORKSPACE and launch nothing.
+ *  - With at most one work unit (a pair of 128-row query tiles of one
+ *    sample and head) per SM the result is bit-identical to
+ *    joint_attention_fwd's.  Above that, joint_attention_fwd balances its
+ *    last rounds by splitting units in two and merging the parts, which
+ *    this call (no merge area) does not, so the two may differ by rounding.
  *  - The array is shared by all calls on a device: calls that overlap on
  *    the GPU (e.g. on two streams) race.  It keeps the last call's contents;
  *    nothing in it needs clearing, since each call writes every byte it reads.
