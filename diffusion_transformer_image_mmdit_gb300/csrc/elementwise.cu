@@ -668,9 +668,6 @@ __global__ void __launch_bounds__(256) quantize_kernel(const T* __restrict__ w, 
   }
 }
 
-// Two fp32 values to packed e4m3 (lo in the low byte), round to nearest
-// even, saturating at +-448.
-
 // One CTA per row of x (row stride ld): s = max|x| / 448 (fp32, 1 for a zero
 // row), q = e4m3(x / s) with the quotient rounded once in fp32.  K even.
 template <typename T>

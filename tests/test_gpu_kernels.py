@@ -239,6 +239,45 @@ def test_quantize_f8_bit_exact():
     assert np.array_equal(decode_e4m3(qw.cpu().numpy()), rqw)
 
 
+def _e4m3_midpoints():
+    """Every point where e4m3 rounding changes below 448: the midpoints between
+    adjacent e4m3 values, normal binades 2^-6 .. 2^8 and the subnormal range."""
+    mids = [(2 * k + 1) * 2.0 ** -10 for k in range(8)]
+    for e in range(-6, 9):
+        mids += [2.0 ** e * (1 + (2 * j + 1) / 16) for j in range(8)]
+    return np.array([m for m in mids if m < 448.0])
+
+
+@pytest.mark.parametrize("sv,inputs", [(1.75, ("bf16", "f32")), (1.875, ("f32",))])
+def test_quantize_f8_ties(sv, inputs):
+    """Rows whose scale is s = sv (max |x| = 448 sv) and whose entries are sv * m
+    for every e4m3 midpoint m: each quotient x / s is exactly a tie, which
+    e4m3 rounds to even.  For these two scales, a quotient formed as
+    x * RN(1/s) lands an ulp off the tie for 78 and 109 of the 126 midpoints,
+    and would round 30 and 46 of them to the wrong side, so the test tells a
+    correctly rounded quotient from a reciprocal multiply.  The kernels must
+    give the oracle's codes bit for bit (bf16 rows through the row kernel, fp32
+    rows through the general kernel), alongside random entries."""
+    mids = _e4m3_midpoints()
+    K = 384
+    rows = []
+    for r in range(4):
+        row = S.normal_f32(f"q8t.{sv}.{r}", (K,), 20.0)
+        row[0] = 448.0 * sv
+        row[1:1 + len(mids)] = sv * mids * (1 if r % 2 == 0 else -1)
+        rows.append(np.clip(row, -448.0 * sv, 448.0 * sv))
+    x = np.stack(rows).astype(np.float32)
+    if "bf16" in inputs:
+        x = S.round_bf16(x)
+        assert np.all(x[0, 1:1 + len(mids)] == sv * mids), "tie inputs must be bf16-exact"
+    rq, rs = O.quantize_f8_rows(x)
+    assert np.all(rs == np.float32(sv))
+    for kind in inputs:
+        q, s_ = api.quantize_f8(bf16(x) if kind == "bf16" else f32(x))
+        assert np.array_equal(host(s_).astype(np.float32), rs)
+        assert np.array_equal(decode_e4m3(q.cpu().numpy()), rq), f"e4m3 ties differ ({kind} rows, s = {sv})"
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 512, 256), (1, 256, 128), (270, 384, 384)])
 @pytest.mark.parametrize("epi", ["f32", "bf16", "gelu", "swiglu", "resid"])
 def test_linear_f8(M, N, K, epi):
