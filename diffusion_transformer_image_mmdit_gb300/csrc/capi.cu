@@ -673,40 +673,61 @@ static int step_w_check(const mmdit_shape_t& shape, const mmdit_step_w_t& w) {
 // sigma_next are read on the device as sig_tab[k], sig_tab[k + 1] with
 // k = *sig_idx (the host values are ignored), so one captured step replays
 // for every step of a schedule.
+// The modulation linears of every block and of the final layer, in the
+// order of their vectors in a step's modulation buffer `base`: a double
+// block's two streams ([B][6D] each), a single block's [B][3D], the final
+// layer's [B][2D].  Output row b of a job goes to out + b * ldo (ldo 0: N).
+static std::vector<GemvJob> mod_jobs(const Dims& d, const mmdit_step_w_t& w, float* base, long long ldo) {
+  const int D = d.D;
+  std::vector<GemvJob> jobs;
+  float* mp = base;
+  const size_t rows = ldo ? 1 : (size_t)d.B;  // with a row stride, one row's outputs per job slot
+  for (int i = 0; i < w.n_double; ++i)
+    for (int s = 0; s < 2; ++s) {
+      const mmdit_linear_t& l = w.doubles[i].mod[s];
+      jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 6 * D, ldo});
+      mp += rows * 6 * D;
+    }
+  for (int i = 0; i < w.n_single; ++i) {
+    const mmdit_linear_t& l = w.singles[i].mod;
+    jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 3 * D, ldo});
+    mp += rows * 3 * D;
+  }
+  jobs.push_back(GemvJob{w.final_mod.w, w.final_mod.scale, w.final_mod.b, mp, 2 * D, ldo});
+  return jobs;
+}
+
+// mods_all: the modulation buffers of every step of a sampling run, computed
+// beforehand (step k's at mods_all + k * mods_floats); step_impl then copies
+// step k's (k = *sig_idx on the device, or step_k) instead of evaluating the
+// timestep embedding and the modulation linears.
 static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step_w_t& w, float* x_lat,
                      const float* x_ref, const float* x_txt_in, double sigma, double sigma_next, float* v_out,
                      const float* vec_add,
-                     const double* sig_tab, const int* sig_idx, bool build_rope, const StepWS& sw, cudaStream_t st) {
+                     const double* sig_tab, const int* sig_idx, bool build_rope, const StepWS& sw, cudaStream_t st,
+                     const float* mods_all = nullptr, int step_k = 0) {
   const bool i8 = shape.w_dtype == MMDIT_I8W;
   const int D = d.D, C = shape.C_lat;
   if (build_rope)
     MMDIT_CUDA(launch_rope_build(d.Lt, shape.grid_w, d.Lg, shape.ref_w, d.L, shape.rope_axes, shape.rope_theta,
                                  nullptr, sw.cs, sw.sn, st));
-  // timestep embedding: vec = time2 SiLU(time1 sinusoid(1000 sigma))
-  MMDIT_CUDA(launch_sinusoid(1000.0 * sigma, d.B, shape.t_dim, sw.temb, st, sig_tab, sig_idx, 1000.0));
-  float* th = sw.temb + (size_t)d.B * shape.t_dim;
-  MMDIT_CUDA(launch_gemv(w.time1.w, w.time1.scale != nullptr, w.time1.scale, w.time1.b, sw.temb, d.B, D,
-                         shape.t_dim, 0, th, st));
-  MMDIT_CUDA(launch_gemv(w.time2.w, w.time2.scale != nullptr, w.time2.scale, w.time2.b, th, d.B, D, D, 1,
-                         sw.vec, st));
-  if (vec_add) MMDIT_CUDA(launch_add(sw.vec, vec_add, (long long)d.B * D, st));
-  // modulation vectors of every block and of the final layer (they depend on vec only): one batched launch
-  std::vector<GemvJob> jobs;
-  float* mp = sw.mods;
-  for (int i = 0; i < w.n_double; ++i)
-    for (int s = 0; s < 2; ++s) {
-      const mmdit_linear_t& l = w.doubles[i].mod[s];
-      jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 6 * D});
-      mp += (size_t)d.B * 6 * D;
-    }
-  for (int i = 0; i < w.n_single; ++i) {
-    const mmdit_linear_t& l = w.singles[i].mod;
-    jobs.push_back(GemvJob{l.w, l.scale, l.b, mp, 3 * D});
-    mp += (size_t)d.B * 3 * D;
+  const long long mods_n = (long long)mods_floats(d, w.n_double, w.n_single);
+  if (mods_all) {
+    MMDIT_CUDA(launch_select_step(mods_all, mods_n, mods_n, sig_idx, step_k, sw.mods, st));
+  } else {
+    // timestep embedding: vec = time2 SiLU(time1 sinusoid(1000 sigma))
+    MMDIT_CUDA(launch_sinusoid(1000.0 * sigma, d.B, shape.t_dim, sw.temb, st, sig_tab, sig_idx, 1000.0));
+    float* th = sw.temb + (size_t)d.B * shape.t_dim;
+    MMDIT_CUDA(launch_gemv(w.time1.w, w.time1.scale != nullptr, w.time1.scale, w.time1.b, sw.temb, d.B, D,
+                           shape.t_dim, 0, th, st));
+    MMDIT_CUDA(launch_gemv(w.time2.w, w.time2.scale != nullptr, w.time2.scale, w.time2.b, th, d.B, D, D, 1,
+                           sw.vec, st));
+    if (vec_add) MMDIT_CUDA(launch_add(sw.vec, vec_add, (long long)d.B * D, st));
+    // modulation vectors of every block and of the final layer (they depend on vec only): one batched launch
+    const std::vector<GemvJob> jobs = mod_jobs(d, w, sw.mods, 0);
+    MMDIT_CUDA(launch_gemv_batched(jobs.data(), (int)jobs.size(), i8, sw.vec, d.B, D, 1, st));
   }
-  float* mod_final = mp;
-  jobs.push_back(GemvJob{w.final_mod.w, w.final_mod.scale, w.final_mod.b, mod_final, 2 * D});
-  MMDIT_CUDA(launch_gemv_batched(jobs.data(), (int)jobs.size(), i8, sw.vec, d.B, D, 1, st));
+  float* const mod_final = sw.mods + mods_n - (size_t)d.B * 2 * D;
   // residual stream x = [text; image] per sample: text copied in, image from img_in
   if (d.Lt > 0)
     MMDIT_CUDA(cudaMemcpy2DAsync(sw.x, (size_t)d.L * D * 4, x_txt_in, (size_t)d.Lt * D * 4, (size_t)d.Lt * D * 4, d.B,
@@ -737,7 +758,7 @@ static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step
     MMDIT_TRY(launch_problems(&pr[0], d.Lr > 0 ? &pr[1] : nullptr, st));
   }
   // blocks
-  mp = sw.mods;
+  float* mp = sw.mods;
   {
     Carve bc{sw.block, 0};
     DoubleWS dw;
@@ -817,7 +838,7 @@ const char* mmdit_kernel_name(int kernel_id) {
                                          "rope_build",   "rope_apply", "euler",       "quantize_w8", "dequant_i8",
                                          "cast_bf16",    "attn_prep",  "wait_selftest", "add_f32",
                                          "step_counter", "quantize_f8", "heads_pack",   "heads_unpack",
-                                         "vT_transpose"};
+                                         "vT_transpose", "select_step"};
   return (kernel_id >= 0 && kernel_id < KID_COUNT) ? names[kernel_id] : "unknown";
 }
 
@@ -1035,9 +1056,14 @@ struct SampleWS {
   double* sig;
   int* ctr;
   uint16_t* wdeq;
+  float* vec_all;   // [B][n_steps][D]: every step's conditioning vector
+  float* mods_all;  // [n_steps][mods_floats]: every step's modulation buffer
 };
-static void layout_sample(const Dims& d, const mmdit_shape_t& s, int C_txt, int n_steps, Carve& c, SampleWS& w) {
+static void layout_sample(const Dims& d, const mmdit_shape_t& s, int n_double, int n_single, int C_txt, int n_steps,
+                          Carve& c, SampleWS& w) {
   const bool i8 = s.w_dtype == MMDIT_I8W;
+  w.vec_all = c.take<float>((size_t)d.B * n_steps * d.D);
+  w.mods_all = c.take<float>((size_t)n_steps * mods_floats(d, n_double, n_single));
   w.x_txt = c.take<float>((size_t)d.B * d.Lt * d.D);
   w.vec_cond = c.take<float>((size_t)d.B * d.D);
   w.ctemb = c.take<float>((size_t)d.B * (s.t_dim + d.D));
@@ -1057,7 +1083,7 @@ int mmdit_sample_workspace_size(const mmdit_shape_t* shape, int n_double, int n_
   MMDIT_TRY(check_shape(shape, &d));
   Carve c{nullptr, step};
   SampleWS w;
-  layout_sample(d, *shape, C_txt, n_steps, c, w);
+  layout_sample(d, *shape, n_double, n_single, C_txt, n_steps, c, w);
   *bytes = c.off + 256;
   return MMDIT_OK;
 }
@@ -1088,7 +1114,7 @@ int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdi
   StepWS sw;
   layout_step(d, *shape, w->n_double, w->n_single, c, sw);
   SampleWS sa;
-  layout_sample(d, *shape, C_txt, n_steps, c, sa);
+  layout_sample(d, *shape, w->n_double, w->n_single, C_txt, n_steps, c, sa);
 
   // step-independent work: RoPE tables, the text stream, the conditioning vector
   MMDIT_CUDA(launch_rope_build(d.Lt, shape->grid_w, d.Lg, shape->ref_w, d.L, shape->rope_axes, shape->rope_theta,
@@ -1109,14 +1135,43 @@ int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdi
   MMDIT_CUDA(launch_gemv(cond->vec2.w, i8, cond->vec2.scale, cond->vec2.b, sa.phid, d.B, D, D, 1, sa.ptmp, st));
   MMDIT_CUDA(launch_add(sa.vec_cond, sa.ptmp, (long long)d.B * D, st));
 
+  // Every step's conditioning vector vec_k = time2 SiLU(time1 sinusoid(1000 sigma_k)) + vec_cond, then the
+  // modulation vectors of every step in one pass per sample: the modulation weights (the largest read of a
+  // step after the block weights) are read once per 8 steps instead of once per step.
+  {
+    float* th = sw.temb + (size_t)d.B * shape->t_dim;
+    for (int k = 0; k < n_steps; ++k) {
+      MMDIT_CUDA(launch_sinusoid(1000.0 * sigmas[k], d.B, shape->t_dim, sw.temb, st));
+      MMDIT_CUDA(launch_gemv(w->time1.w, w->time1.scale != nullptr, w->time1.scale, w->time1.b, sw.temb, d.B, D,
+                             shape->t_dim, 0, th, st));
+      MMDIT_CUDA(launch_gemv(w->time2.w, w->time2.scale != nullptr, w->time2.scale, w->time2.b, th, d.B, D, D, 1,
+                             sw.vec, st));
+      MMDIT_CUDA(launch_add(sw.vec, sa.vec_cond, (long long)d.B * D, st));
+      MMDIT_CUDA(cudaMemcpy2DAsync(sa.vec_all + (size_t)k * D, (size_t)n_steps * D * 4, sw.vec, (size_t)D * 4,
+                                   (size_t)D * 4, d.B, cudaMemcpyDeviceToDevice, st));
+    }
+    const long long mods_n = (long long)mods_floats(d, w->n_double, w->n_single);
+    for (int b = 0; b < d.B; ++b) {
+      // rows k of sample b: outputs at mods_all + k * mods_n, in the step buffer's layout at sample b
+      std::vector<GemvJob> jobs = mod_jobs(d, *w, sa.mods_all, mods_n);
+      size_t off = 0;
+      for (GemvJob& j : jobs) {
+        j.out = sa.mods_all + off + (size_t)b * j.N;
+        off += (size_t)d.B * j.N;
+      }
+      MMDIT_CUDA(launch_gemv_batched(jobs.data(), (int)jobs.size(), i8, sa.vec_all + (size_t)b * n_steps * D,
+                                     n_steps, D, 1, st));
+    }
+  }
+
   // step 0 eagerly (this also performs every one-time kernel set-up before a capture)
   MMDIT_TRY(step_impl(*shape, d, *w, x_lat, nullptr, sa.x_txt, sigmas[0], sigmas[1], nullptr, sa.vec_cond, nullptr,
-                      nullptr, false, sw, st));
+                      nullptr, false, sw, st, sa.mods_all, 0));
   const bool graph = (flags & MMDIT_SAMPLE_GRAPH) && n_steps > 1 && !g_trace.on;
   if (!graph) {
     for (int i = 1; i < n_steps; ++i)
       MMDIT_TRY(step_impl(*shape, d, *w, x_lat, nullptr, sa.x_txt, sigmas[i], sigmas[i + 1], nullptr, sa.vec_cond,
-                          nullptr, nullptr, false, sw, st));
+                          nullptr, nullptr, false, sw, st, sa.mods_all, i));
     return MMDIT_OK;
   }
   // Steps 1 .. n - 1: one captured step reading sigma_k, sigma_{k+1} at the
@@ -1132,7 +1187,7 @@ int mmdit_sample(const mmdit_shape_t* shape, const mmdit_step_w_t* w, const mmdi
     rc = MMDIT_ERR_CUDA;
   } else {
     rc = step_impl(*shape, d, *w, x_lat, nullptr, sa.x_txt, 0.0, 0.0, nullptr, sa.vec_cond, sa.sig, sa.ctr, false, sw,
-                   cs);
+                   cs, sa.mods_all, 0);
     if (rc == MMDIT_OK) rc = cuda_status(launch_counter(sa.ctr, 1, true, cs));
     const cudaError_t e = cudaStreamEndCapture(cs, &graph_def);  // always closes the capture
     if (rc == MMDIT_OK && e != cudaSuccess) rc = MMDIT_ERR_CUDA;
@@ -1311,8 +1366,8 @@ int mmdit_ln_modulate_f8(const float* x, int B, int rows, int D, const float* sh
 int mmdit_gemv(const mmdit_linear_t* lin, int B, int N, int K, const float* x, int act, float* y, void* stream) {
   if (!lin || !x || !y || (act != 0 && act != 1)) return MMDIT_ERR_ARG;
   if (!lin_ok(*lin, lin->scale != nullptr)) return MMDIT_ERR_ARG;
-  if (B < 1 || B > 8 || N < 1 || K < 16 || K % 16) return MMDIT_ERR_SHAPE;
-  if ((size_t)B * K * 4 > 200 * 1024) return MMDIT_ERR_SHAPE;
+  if (B < 1 || B > 16 || N < 1 || K < 16 || K % 16) return MMDIT_ERR_SHAPE;
+  if ((size_t)8 * K * 4 > 200 * 1024) return MMDIT_ERR_SHAPE;  // 8 rows of x in shared memory
   MMDIT_TRY(check_device());
   return cuda_status(launch_gemv(lin->w, lin->scale != nullptr, lin->scale, lin->b, x, B, N, K, act, y, S(stream)));
 }

@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(256) gemv_batched_kernel(const __grid_constant
       for (int b = 0; b < BM; ++b) {
         if (b < B) {
           const float t = warp_sum(acc[b]);
-          if (lane == 0) job.out[(long long)b * job.N + n] = t * sc + bi;
+          if (lane == 0) job.out[(long long)b * (job.ldo ? job.ldo : job.N) + n] = t * sc + bi;
         }
       }
     }
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(256, 2) gemv_rows_batched_kernel(const __grid_
       for (int b = 0; b < BM; ++b) {
         if (b < B) {
           const float t = warp_sum(acc[rr][b]);
-          if (lane == 0) job.out[(long long)b * job.N + n] = t * sc + bi;
+          if (lane == 0) job.out[(long long)b * (job.ldo ? job.ldo : job.N) + n] = t * sc + bi;
         }
       }
     }
@@ -479,6 +479,16 @@ __global__ void sinusoid_kernel(double t, const double* __restrict__ t_tab, cons
 __global__ void add_f32_kernel(float* __restrict__ y, const float* __restrict__ x, long long n) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) y[i] += x[i];
+}
+
+// dst[i] = src[k * stride + i] for i < n (n, stride multiples of 4, 16-byte
+// aligned), with k = *k_dev when given (the device step counter of a replayed
+// step), else k_host: one step's slice of buffers computed for every step.
+__global__ void select_step_kernel(const float4* __restrict__ src, long long stride4, long long n4,
+                                   const int* __restrict__ k_dev, int k_host, float4* __restrict__ dst) {
+  const long long k = k_dev ? *k_dev : k_host;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x)
+    dst[i] = src[k * stride4 + i];
 }
 
 // The device step counter of a replayed step: set once, advanced at the end of each step.
@@ -988,26 +998,49 @@ static cudaError_t gemv_attributes() {
   return err[dev];
 }
 
+static cudaError_t launch_gemv_batched_rows(const GemvJob* jobs, int n_jobs, bool i8, const float* x, int r0, int B,
+                                           int K, int act, cudaStream_t st);
+
+// The kernels take at most kGemvMaxRows rows of x (their compile-time batch
+// bound); more rows go in consecutive launches of up to that many.
+constexpr int kGemvMaxRows = 8;
+
 cudaError_t launch_gemv(const void* W, bool i8, const float* wscale, const float* bias, const float* x, int B, int N,
                         int K, int act, float* y, cudaStream_t st) {
   const cudaError_t ea = gemv_attributes();
   if (ea != cudaSuccess) return ea;
-  const size_t smem = (size_t)B * K * sizeof(float);
-  const GemvFn fn = i8 ? gemv_fn<true>(B) : gemv_fn<false>(B);
-  const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
-  int blocks = (N + rows_per_cta - 1) / rows_per_cta;
-  const int resident = gemv_resident_ctas((const void*)fn, smem);
-  if (blocks > resident) blocks = resident;
-  launch_begin(KID_GEMV, st);
-  fn<<<blocks, 256, smem, st>>>(W, wscale, bias, x, B, N, K, act, y);
-  launch_end(st);
-  return cudaGetLastError();
+  for (int r0 = 0; r0 < B; r0 += kGemvMaxRows) {
+    const int nb = B - r0 < kGemvMaxRows ? B - r0 : kGemvMaxRows;
+    const size_t smem = (size_t)nb * K * sizeof(float);
+    const GemvFn fn = i8 ? gemv_fn<true>(nb) : gemv_fn<false>(nb);
+    const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
+    int blocks = (N + rows_per_cta - 1) / rows_per_cta;
+    const int resident = gemv_resident_ctas((const void*)fn, smem);
+    if (blocks > resident) blocks = resident;
+    launch_begin(KID_GEMV, st);
+    fn<<<blocks, 256, smem, st>>>(W, wscale, bias, x + (size_t)r0 * K, nb, N, K, act, y + (size_t)r0 * N);
+    launch_end(st);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const float* x, int B, int K, int act,
                                 cudaStream_t st) {
   const cudaError_t ea = gemv_attributes();
   if (ea != cudaSuccess) return ea;
+  for (int r0 = 0; r0 < B; r0 += kGemvMaxRows) {
+    const int nb = B - r0 < kGemvMaxRows ? B - r0 : kGemvMaxRows;
+    const cudaError_t e = launch_gemv_batched_rows(jobs, n_jobs, i8, x + (size_t)r0 * K, r0, nb, K, act, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Rows r0 .. r0 + B - 1 of x (x points at row r0), B <= kGemvMaxRows.
+static cudaError_t launch_gemv_batched_rows(const GemvJob* jobs, int n_jobs, bool i8, const float* x, int r0, int B,
+                                           int K, int act, cudaStream_t st) {
   const size_t smem = (size_t)B * K * sizeof(float);
   const GemvBatchedFn fn = i8 ? gemv_batched_fn<true>(B) : gemv_batched_fn<false>(B);
   for (int first = 0; first < n_jobs; first += kMaxGemvJobs) {
@@ -1016,10 +1049,12 @@ cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const 
     jb.row0[0] = 0;
     for (int i = 0; i < jb.n_jobs; ++i) {
       jb.job[i] = jobs[first + i];
+      const long long ldo = jb.job[i].ldo ? jb.job[i].ldo : jb.job[i].N;
+      jb.job[i].out += (size_t)r0 * ldo;
       jb.row0[i + 1] = jb.row0[i] + jobs[first + i].N;
     }
     for (int i = jb.n_jobs; i < kMaxGemvJobs; ++i) {
-      jb.job[i] = GemvJob{nullptr, nullptr, nullptr, nullptr, 0};
+      jb.job[i] = GemvJob{nullptr, nullptr, nullptr, nullptr, 0, 0};
       jb.row0[i + 1] = jb.row0[jb.n_jobs];
     }
     const int rows_per_cta = kGemvWarps * kGemvRowsPerWarp;
@@ -1112,6 +1147,21 @@ cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long lo
 cudaError_t launch_add(float* y, const float* x, long long n, cudaStream_t st) {
   launch_begin(KID_ADD, st);
   add_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, x, n);
+  launch_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_step(const float* src, long long stride, long long n, const int* k_dev, int k_host,
+                               float* dst, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (n % 4 || stride % 4 || (reinterpret_cast<uintptr_t>(src) & 15) || (reinterpret_cast<uintptr_t>(dst) & 15))
+    return cudaErrorInvalidValue;
+  const long long n4 = n / 4;
+  long long blocks = (n4 + 255) / 256;
+  if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+  launch_begin(KID_SELECT_STEP, st);
+  select_step_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(src), stride / 4, n4, k_dev,
+                                                        k_host, reinterpret_cast<float4*>(dst));
   launch_end(st);
   return cudaGetLastError();
 }

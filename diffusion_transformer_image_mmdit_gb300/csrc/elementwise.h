@@ -41,6 +41,7 @@ struct GemvJob {
   const float* bias;
   float* out;
   int N;
+  long long ldo;  // elements between the outputs of consecutive x rows (0: N)
 };
 cudaError_t launch_gemv_batched(const GemvJob* jobs, int n_jobs, bool i8, const float* x, int B, int K, int act,
                                 cudaStream_t st);
@@ -58,6 +59,10 @@ cudaError_t launch_euler(float* x, const void* v, bool v_bf16, float dt, long lo
                          const double* sig_tab = nullptr, const int* sig_idx = nullptr);
 // y += x (n floats).
 cudaError_t launch_add(float* y, const float* x, long long n, cudaStream_t st);
+// dst[i] = src[k * stride + i], i < n: step k's slice of a buffer computed for
+// every step, k = *k_dev (device counter) when k_dev is given, else k_host.
+cudaError_t launch_select_step(const float* src, long long stride, long long n, const int* k_dev, int k_host,
+                               float* dst, cudaStream_t st);
 // *c = value (add = false) or *c += value (add = true), one thread.
 cudaError_t launch_counter(int* c, int value, bool add, cudaStream_t st);
 cudaError_t launch_quantize(const void* w, bool w_bf16, int N, int K, int8_t* q, float* scale, cudaStream_t st);

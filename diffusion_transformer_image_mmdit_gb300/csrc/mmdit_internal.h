@@ -129,6 +129,7 @@ enum KernelId : int {
   KID_HEADS_PACK,
   KID_HEADS_UNPACK,
   KID_VT_TRANSPOSE,
+  KID_SELECT_STEP,
   KID_COUNT
 };
 // Bracket every kernel launch: counts launches and, while a trace is on,

@@ -449,8 +449,9 @@ int mmdit_ln_modulate(const float* x, int B, int rows, int D, const float* shift
 int mmdit_ln_modulate_f8(const float* x, int B, int rows, int D, const float* shift, const float* scale,
                          int64_t mod_stride, float eps, void* y, uint8_t* q, float* s, void* stream);
 
-/* y[b, n] = W act(x[b, :]) + bias, x device fp32 [B, K] (B <= 8),
- * act 0 = identity, 1 = SiLU; y device fp32 [B, N]. */
+/* y[b, n] = W act(x[b, :]) + bias, x device fp32 [B, K] (1 <= B <= 16,
+ * K <= 6400), act 0 = identity, 1 = SiLU; y device fp32 [B, N].  Rows of x
+ * go through the weights 8 at a time. */
 int mmdit_gemv(const mmdit_linear_t* lin, int B, int N, int K, const float* x, int act, float* y, void* stream);
 
 /* vec = time2(SiLU(time1(sinusoid(1000 sigma)))) for all B samples:

@@ -134,10 +134,12 @@ def test_ln_modulate_f8_fused(D):
 
 @pytest.mark.parametrize("i8", [False, True])
 @pytest.mark.parametrize("act", [0, 1])
-def test_gemv(i8, act):
-    B, N, K = 3, 1000, 3072
+@pytest.mark.parametrize("B", [3, 12])
+def test_gemv(i8, act, B):
+    """B = 12 runs as two launches of 8 and 4 rows."""
+    N, K = 1000, 3072
     w, b = S.linear_params("gv", N, K)
-    x = S.normal_f32("gv.x", (B, K))
+    x = S.normal_f32(f"gv.x{B}", (B, K))
     lin = LinearDev(bf16(w), f32(b))
     wref = w
     if i8:
