@@ -455,9 +455,11 @@ def _run_sample(case, graph):
     return host(xl)
 
 
-@pytest.mark.parametrize("graph,i8", [(False, False), (True, False), (True, True)])
-def test_sample_loop_small(graph, i8):
-    case = _sample_case(3, i8)
+@pytest.mark.parametrize("graph,i8,n_steps", [(False, False, 3), (True, False, 3), (True, True, 3), (True, False, 10)])
+def test_sample_loop_small(graph, i8, n_steps):
+    """n_steps = 10: the modulation vectors of all steps are computed before
+    the loop 8 steps per weight pass, so this case takes two passes."""
+    case = _sample_case(n_steps, i8)
     cfg, sh, W, x_lat, txt, pooled, sig = case[:7]
     got = _run_sample(case, graph)
     ref = O.sample(x_lat, txt, pooled, 3.5, sig, W, sh)
