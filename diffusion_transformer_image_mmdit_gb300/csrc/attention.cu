@@ -36,9 +36,11 @@
 // unit's counter; the part that arrives second reads the other slot, merges
 // the two with the usual rescaling, O = (2^(m_A - m) O_A + 2^(m_B - m) O_B) /
 // (2^(m_A - m) l_A + 2^(m_B - m) l_B) with m = max(m_A, m_B), and stores the
-// result.  Neither part waits for the other.  Consecutive items of a CTA
-// overlap: the next item's K tile and Q tiles load while the current item's
-// last P V MMAs and epilogue run.
+// result.  Neither part waits for the other.  With no more units than SMs
+// each CTA runs one unit, and a launch given no merge area runs every unit
+// whole, round-robin.  Consecutive items of a CTA overlap: the next item's K
+// tile and Q tiles load while the current item's last P V MMAs and epilogue
+// run.
 #include <mutex>
 
 #include "common.cuh"
