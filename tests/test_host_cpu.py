@@ -67,3 +67,36 @@ def test_clock_sampler_summary():
     assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1371.0
     cs.rows.append([x.strip() for x in line.format(sm=1200, pw=800, act="8", hw="Active", cap="Not Active").split(",")])
     assert bench.ClockSampler.summary(cs)["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_bench_gemm_bytes_and_traffic_source():
+    """Algorithmic GEMM bytes count each problem's weights once (the two streams of a double block have
+    their own), and the bench's per-launch DRAM traffic comes from the capture at the workload's own token
+    count when one exists (no scaling), from the 512 + 64x64 capture scaled by token rows otherwise, and is
+    absent for shapes or precisions no committed capture covers."""
+    import bench
+    c = dict(bench.CONFIGS["c4pair"])
+    B, D, Dm, C = c["B"], c["D"], c["D_mlp"], c["C_lat"]
+    L, Li = c["L_txt"] + c["grid_h"] * c["grid_w"], c["grid_h"] * c["grid_w"]
+    M = B * L
+    w_double = 2 * (3 * D * D + D * D + Dm * D + D * Dm) * 2  # both streams' weights, bf16
+    w_single = ((3 * D + Dm) * D + D * (D + Dm)) * 2
+    w_io = (D * C + C * D) * 2
+    acts = ((M * D + M * 3 * D + M * D + M * D * 4 + M * D + M * Dm + M * Dm + M * D * 4)  # double: A, outputs, resid
+            + (M * D + M * (3 * D + Dm) + M * (D + Dm) + M * D * 4)) * 2                    # single
+    io_acts = (B * Li * C * 2 + B * Li * D * 4) + (B * Li * D * 2 + B * Li * C * 4)
+    total = w_double + w_single + w_io + acts + io_acts
+    assert abs(bench.gemm_algorithmic_bytes(c) * 8 - total) / total < 1e-12
+    t, src = bench.gemm_traffic_scaled(bench.CONFIGS["c4"])
+    if t is not None:  # the committed captures match the current GEMM sources
+        assert "at this token count (7401 tokens)" in src
+        rows = bench.gemm_launch_table("c4pair")
+        dbl = sum((r[4] + r[5]) * 1e6 for r in rows if r[0] in ("qkv", "proj", "mlp_in", "mlp_out"))
+        sng = sum((r[4] + r[5]) * 1e6 for r in rows if r[0] in ("lin1", "lin2"))
+        io = sum((r[4] + r[5]) * 1e6 for r in rows if r[0] in ("img_in", "final"))
+        assert abs(t - (19 * dbl + 38 * sng + io) / 154) < 1.0
+        t5, src5 = bench.gemm_traffic_scaled(bench.CONFIGS["c5"])
+        assert t5 is not None and "scaled by the token rows" in src5
+    for name in ("klein1024", "klein_i2i", "c4_f8"):
+        t, src = bench.gemm_traffic_scaled(bench.CONFIGS[name])
+        assert t is None and src
