@@ -13,9 +13,10 @@
 //   the 256-row W tile into its own shared memory (plain TMA tile loads),
 //   and the MMA reads both CTAs' halves, so W crosses L2 -> SM once per pair
 //   and the pair issues half the MMAs two independent CTAs would.
-//   warp 0      TMA producer (both CTAs): its A tile 128x64 and its W half
-//               128x64 per K block into a 6-stage ring (128-byte swizzle,
-//               32 KB per stage).  Both CTAs' loads complete on CTA 0's
+//   warp 0      TMA producer (both CTAs): its A tile 128x128 and its W half
+//               128x128 per K block (two 128-byte-swizzled K slices each)
+//               into a 3-stage ring (64 KB per stage; a K that ends in one
+//               slice ends in a one-slice stage).  Both CTAs' loads complete on CTA 0's
 //               full barrier (two arrivals with their byte counts).  CTA 0's
 //               MMAs release a stage on CTA 0's empty barrier; CTA 0's
 //               producer passes each release on to CTA 1's empty barrier.
@@ -43,9 +44,17 @@ namespace {
 
 constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, one per 128-column half
 constexpr int kGemmThreads = 32 * (2 + kEpiWarps);
-constexpr int kRing = 6;                          // stages of the TMA ring
-constexpr uint32_t kStageA = kBM * kBK * 2;       // 16 KB: this CTA's 128 rows of A
-constexpr uint32_t kStageB = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128-row half of the W tile
+// A stage holds two K slices of one 128-byte swizzle row each (128 bf16 or
+// 256 e4m3 K elements): per stage one full-barrier wait, eight pair MMAs
+// and one release, where one-slice stages made the barrier round trips
+// (wait, commit, the release forwarded to CTA 1) cost up to 8 % of the
+// K = 3072 launches.  The last stage of a K not a multiple of two slices
+// holds one.
+constexpr int kRing = 3;                           // stages of the TMA ring (192 KB)
+constexpr uint32_t kHalfA = kBM * kBK * 2;         // 16 KB: one K slice of this CTA's 128 rows of A
+constexpr uint32_t kHalfB = (kBN / 2) * kBK * 2;   // 16 KB: one K slice of this CTA's half of the W tile
+constexpr uint32_t kStageA = 2 * kHalfA;
+constexpr uint32_t kStageB = 2 * kHalfB;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiStageBytes = 4096;  // staging area of one epilogue warp
 constexpr size_t kGemmSmem = 1024 + kRing * (kStageA + kStageB) + kEpiWarps * kEpiStageBytes + 256;
@@ -335,7 +344,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
 // of W per CTA and takes four pair MMAs.
 template <bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmGroup g) {
-  constexpr int kKB = F8 ? 128 : kBK;  // K elements per stage
+  constexpr int kSL = F8 ? 128 : kBK;  // K elements per slice (one 128-byte row)
+  constexpr int kKB = 2 * kSL;         // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -409,8 +419,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         // W rows of this CTA's half of the 256-row tile: rows n0 + 128 rank, or
         // for SwiGLU the matching 128 gate rows (rank 0) and up rows (rank 1)
         const int brow = p.mode == GM_SWIGLU ? c.tn * (kBN / 2) + rank * p.swiglu_up : n0 + rank * (kBN / 2);
-        const int nk = p.K / kKB;
+        const int nk = (p.K + kKB - 1) / kKB;
         for (int kb = 0; kb < nk; ++kb) {
+          const int ns = p.K - kb * kKB >= kKB ? 2 : 1;  // K slices in this stage
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, status, ST_TIMEOUT_PRODUCER)) goto done;
           // CTA 0's MMAs commit to CTA 0's empty barrier only (one commit per
           // stage keeps the MMA warp's issue free for MMAs); CTA 0's producer
@@ -418,11 +429,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
           if (rank == 0 && n_fill >= kRing) mbar_arrive_cluster(empty_c1 + 8 * stage);
           const uint32_t fb = full_c0 + 8 * stage;
           if (rank == 0)
-            mbar_expect_tx(full0 + 8 * stage, kStageA + kStageB);
+            mbar_expect_tx(full0 + 8 * stage, ns * (kHalfA + kHalfB));
           else
-            mbar_arrive_expect_tx_cluster(fb, kStageA + kStageB);
-          tma_load_3d_pair(smem_u32(sA + stage * kStageA), &g.tmA[q], fb, kb * kKB, m0, c.seg);
-          tma_load_3d_pair(smem_u32(sB + stage * kStageB), &g.tmB[q], fb, kb * kKB, brow, 0);
+            mbar_arrive_expect_tx_cluster(fb, ns * (kHalfA + kHalfB));
+          for (int sl = 0; sl < ns; ++sl) {
+            tma_load_3d_pair(smem_u32(sA + stage * kStageA + sl * kHalfA), &g.tmA[q], fb, kb * kKB + sl * kSL, m0,
+                             c.seg);
+            tma_load_3d_pair(smem_u32(sB + stage * kStageB + sl * kHalfB), &g.tmB[q], fb, kb * kKB + sl * kSL, brow, 0);
+          }
           ++n_fill;
           if (++stage == kRing) stage = 0, phase ^= 1;
         }
@@ -443,21 +457,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int t = cluster; t < g.total_tiles; t += n_clusters) {
-        const int nk = g.p[t < g.tiles0 ? 0 : 1].K / kKB;
+        const int K = g.p[t < g.tiles0 ? 0 : 1].K;
+        const int nk = (K + kKB - 1) / kKB;
         if (!mbar_wait_warp(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
         tc_fence_after();
         const uint32_t d = tmem + acc * kBN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_warp(full0 + 8 * stage, phase, abort_flag, status, ST_TIMEOUT_MMA)) goto done;
           tc_fence_after();
-          const uint64_t da = dA0 + (uint64_t)(stage * (kStageA >> 4));
-          const uint64_t db = dB0 + (uint64_t)(stage * (kStageB >> 4));
+          const int ns = K - kb * kKB >= kKB ? 2 : 1;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // 32 bytes of K per MMA
-            if (F8)
-              umma_f8_pair_if(elected, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-            else
-              umma_bf16_pair_if(elected, d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+          for (int sl = 0; sl < 2; ++sl) {
+            if (sl < ns) {
+              const uint64_t da = dA0 + (uint64_t)((stage * kStageA + sl * kHalfA) >> 4);
+              const uint64_t db = dB0 + (uint64_t)((stage * kStageB + sl * kHalfB) >> 4);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {  // 32 bytes of K per MMA
+                if (F8)
+                  umma_f8_pair_if(elected, d, da + 2 * k, db + 2 * k, idesc, (kb | sl | k) != 0);
+                else
+                  umma_bf16_pair_if(elected, d, da + 2 * k, db + 2 * k, idesc, (kb | sl | k) != 0);
+              }
+            }
           }
           umma_commit_pair_if(elected, empty0 + 8 * stage);  // frees the stage (CTA 1 via CTA 0's producer)
           if (++stage == kRing) stage = 0, phase ^= 1;
