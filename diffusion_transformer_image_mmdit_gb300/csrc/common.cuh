@@ -340,6 +340,16 @@ __device__ __forceinline__ void umma_commit_pair_if(uint32_t issue, uint32_t bar
       : "memory");
 }
 
+// Arrive on the mbarrier at the same shared-memory offset in each CTA of
+// cta_mask once every pair MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit_pair_mc_if(uint32_t issue, uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %2;\n\t}"
+      ::"r"(bar), "r"(issue), "h"(cta_mask)
+      : "memory");
+}
+
 // mbar_wait by every lane of a converged warp; true in all lanes only if
 // every lane saw the phase complete (a time-out in any lane fails them all).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status,

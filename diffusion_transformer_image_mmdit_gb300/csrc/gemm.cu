@@ -18,8 +18,8 @@
 //               into a 3-stage ring (64 KB per stage; a K that ends in one
 //               slice ends in a one-slice stage).  Both CTAs' loads complete on CTA 0's
 //               full barrier (two arrivals with their byte counts).  CTA 0's
-//               MMAs release a stage on CTA 0's empty barrier; CTA 0's
-//               producer passes each release on to CTA 1's empty barrier.
+//               MMAs release a stage with one commit multicast to both CTAs'
+//               empty barriers.
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
 //               in both CTAs (one collective pair allocation); in CTA 0 it
 //               issues the pair MMAs (M=256, N=256, K=16) from one elected
@@ -408,7 +408,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
   if (warp == 0) {
     if (lane == 0) {
       const uint32_t full_c0 = mapa_shared(full0, 0);    // CTA 0's full barriers, as seen from this CTA
-      const uint32_t empty_c1 = mapa_shared(empty0, 1);  // CTA 1's empty barriers
       int stage = 0;
       uint32_t phase = 0;
       for (int t = cluster; t < g.total_tiles; t += n_clusters) {
@@ -423,10 +422,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
         for (int kb = 0; kb < nk; ++kb) {
           const int ns = p.K - kb * kKB >= kKB ? 2 : 1;  // K slices in this stage
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, status, ST_TIMEOUT_PRODUCER)) goto done;
-          // CTA 0's MMAs commit to CTA 0's empty barrier only (one commit per
-          // stage keeps the MMA warp's issue free for MMAs); CTA 0's producer
-          // passes the release on to CTA 1 once it has seen it.
-          if (rank == 0 && n_fill >= kRing) mbar_arrive_cluster(empty_c1 + 8 * stage);
           const uint32_t fb = full_c0 + 8 * stage;
           if (rank == 0)
             mbar_expect_tx(full0 + 8 * stage, ns * (kHalfA + kHalfB));
@@ -456,6 +451,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      // Stages this CTA pair fills in all (n_total) and has consumed (n_cons).
+      int n_total = 0, n_cons = 0;
+      for (int t = cluster; t < g.total_tiles; t += n_clusters) n_total += (g.p[t < g.tiles0 ? 0 : 1].K + kKB - 1) / kKB;
       for (int t = cluster; t < g.total_tiles; t += n_clusters) {
         const int K = g.p[t < g.tiles0 ? 0 : 1].K;
         const int nk = (K + kKB - 1) / kKB;
@@ -480,7 +478,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __g
               }
             }
           }
-          umma_commit_pair_if(elected, empty0 + 8 * stage);  // frees the stage (CTA 1 via CTA 0's producer)
+          // One commit frees the stage in both CTAs (multicast to the empty
+          // barrier at the same offset in each).  The releases of the last
+          // ring round, which no fill waits for, go to CTA 0 only: every
+          // arrival that reaches CTA 1 is then one its producer waits for
+          // before it leaves the loop, so none can land after CTA 1 exits.
+          // (Forwarding each release to CTA 1 through CTA 0's producer made
+          // CTA 1's refills later and the K-heavy launches 1.5-2 % slower.)
+          if (n_cons + kRing < n_total)
+            umma_commit_pair_mc_if(elected, empty0 + 8 * stage, 3);
+          else
+            umma_commit_pair_if(elected, empty0 + 8 * stage);
+          ++n_cons;
           if (++stage == kRing) stage = 0, phase ^= 1;
         }
         umma_commit_pair_if(elected, tfull0 + 8 * acc);
