@@ -141,20 +141,29 @@ GEMM_SECTIONS = [("diffusion_transformer_image_mmdit_gb300/csrc/mmdit_internal.h
                   "static GemmParams gemm_params(int mode)")]
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and blank lines (string literals kept),
+    so that an edit of comments alone leaves the hash below unchanged."""
+    import re
+    tok = re.compile(r'"(?:\\.|[^"\\\n])*"|//[^\n]*|/\*.*?\*/', re.S)
+    out = tok.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", text)
+    return "\n".join(line.rstrip() for line in out.splitlines() if line.strip())
+
+
 def gemm_sources_sha256() -> str:
-    """Hash of the GEMM kernel's sources: gemm.cu, the device helpers, the
-    GEMM parameter structs, and the host code that shapes its launches (tile
-    counts, raster, grouping) in capi.cu."""
+    """Hash of the GEMM kernel's code (comments left out): gemm.cu, the device
+    helpers, the GEMM parameter structs, and the host code that shapes its
+    launches (tile counts, raster, grouping) in capi.cu."""
     import hashlib
     h = hashlib.sha256()
     for rel in GEMM_SOURCES:
-        h.update(open(os.path.join(ROOT, rel), "rb").read())
+        h.update(_code_only(open(os.path.join(ROOT, rel)).read()).encode())
     for rel, start, end in GEMM_SECTIONS:
         text = open(os.path.join(ROOT, rel)).read()
         a, b = text.find(start), text.find(end)
         if a < 0 or b < a:
             return "missing section in " + rel
-        h.update(text[a:b].encode())
+        h.update(_code_only(text[a:b]).encode())
     return h.hexdigest()
 
 

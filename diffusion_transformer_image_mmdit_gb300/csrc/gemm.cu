@@ -339,9 +339,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
 }
 
 // F8: A and W are e4m3 (one byte per element, 128 elements per 128-byte
-// K block, kind::f8f6f4 MMAs of K = 32); otherwise bf16 (64 per K block,
-// kind::f16 MMAs of K = 16).  Either way a stage holds 16 KB of A and 16 KB
-// of W per CTA and takes four pair MMAs.
+// K slice, kind::f8f6f4 MMAs of K = 32); otherwise bf16 (64 per K slice,
+// kind::f16 MMAs of K = 16).  Either way a K slice holds 16 KB of A and
+// 16 KB of W per CTA and takes four pair MMAs; a stage holds two slices.
 template <bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_tc_kernel(const __grid_constant__ GemmGroup g) {
   constexpr int kSL = F8 ? 128 : kBK;  // K elements per slice (one 128-byte row)

@@ -69,6 +69,19 @@ def test_clock_sampler_summary():
     assert bench.ClockSampler.summary(cs)["reasons"] == ["hw_slowdown", "sw_power_cap"]
 
 
+def test_bench_gemm_hash_ignores_comments_only():
+    """The hash that ties a committed ncu capture to the GEMM sources covers the code, not its comments:
+    an edit of a comment keeps it, an edit of code (or of a string literal, which may be PTX) changes it."""
+    import bench
+    src = 'int a = 1; // note\n/* block\n comment */\nasm("x // y");\n\nint b = 2;\n'
+    ref = bench._code_only(src)
+    assert ref == 'int a = 1;\nasm("x // y");\nint b = 2;'
+    assert bench._code_only(src.replace("// note", "// another note")) == ref
+    assert bench._code_only(src.replace("block", "longer block")) == ref
+    assert bench._code_only(src.replace("int b = 2", "int b = 3")) != ref
+    assert bench._code_only(src.replace('"x // y"', '"x // z"')) != ref
+
+
 def test_bench_gemm_bytes_and_traffic_source():
     """Algorithmic GEMM bytes count each problem's weights once (the two streams of a double block have
     their own), and the bench's per-launch DRAM traffic comes from the capture at the workload's own token
