@@ -318,6 +318,44 @@ def test_linear_f8(M, N, K, epi):
         assert_close(host(y), r, max_abs=2.0 ** -8 * max(1.0, np.abs(r).max()) + 1e-4, what=f"fp8 gemm {epi}")
 
 
+@pytest.mark.parametrize("K", [192, 320])
+def test_gemm_many_tiles_k_tail(K):
+    """Several tiles per CTA pair with a K that ends in a one-slice stage (K = 192: one full stage and
+    a half; K = 320: two and a half), so the ring stages and their barrier phases wrap across tiles,
+    and the stage releases reach both CTAs except in each pair's last ring round; M tail of 77 rows."""
+    M, N = 256 * 30 + 77, 2048  # 31 pair-rows x 8 N tiles = 248 tiles over at most 76 CTA pairs
+    w, b = S.linear_params(f"gtail{K}", N, K)
+    x = S.normal_bf16(f"gtail{K}.x", (M, K))
+    lin = LinearDev(bf16(w), f32(b))
+    ref = O.linear(x, w, b)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_F32)
+    assert_close(host(y), ref, rel=1e-4, max_abs=1e-2, what=f"gemm K={K} f32")
+    r0 = S.normal_f32(f"gtail{K}.r", (M, N))
+    gate = S.normal_f32(f"gtail{K}.g", (N,))
+    y = f32(r0)
+    api.mmdit_linear_fwd(lin, bf16(x), y, api.MMDIT_EPI_RESID, gate=f32(gate))
+    assert_close(host(y), r0 + gate * ref, rel=1e-4, max_abs=1e-2, what=f"gemm K={K} resid")
+
+
+def test_linear_f8_many_tiles_k_tail():
+    """e4m3 GEMM with several tiles per CTA pair and K = 384: one stage of 256 K elements and one of
+    128 per tile, gated-residual epilogue, M tail of 33 rows."""
+    M, N, K = 4096 + 33, 2048, 384
+    w, b = S.linear_params("l8tail", N, K)
+    x = S.normal_bf16("l8tail.x", (M, K))
+    lin8 = api.quantize_linear_f8(LinearDev(bf16(w), f32(b)))
+    x8, xs = api.quantize_f8(bf16(x))
+    xd = decode_e4m3(x8.cpu().numpy()) * host(xs)[:, None]
+    wd = decode_e4m3(lin8.w.cpu().numpy()) * host(lin8.scale)[:, None]
+    ref = O.linear(xd, wd, b)
+    r0 = S.normal_f32("l8tail.r", (M, N))
+    gate = S.normal_f32("l8tail.g", (N,))
+    y = f32(r0)
+    api.mmdit_linear_f8_fwd(lin8, x8, xs, y, api.MMDIT_EPI_RESID, gate=f32(gate))
+    assert_close(host(y), r0 + gate * ref, rel=1e-4, max_abs=1e-4, what="fp8 gemm many tiles resid")
+
+
 def test_gemm_large_tiles_and_ragged():
     """Several waves of persistent tiles, M tail of 9 rows, K = 3072."""
     M, N, K = 128 * 20 + 9, 1024, 3072
