@@ -36,7 +36,9 @@
 // unit's counter; the part that arrives second reads the other slot, merges
 // the two with the usual rescaling, O = (2^(m_A - m) O_A + 2^(m_B - m) O_B) /
 // (2^(m_A - m) l_A + 2^(m_B - m) l_B) with m = max(m_A, m_B), and stores the
-// result.  Neither part waits for the other.  With no more units than SMs
+// result, then sets the counter back to zero, so the counters need clearing
+// only before the first launch over a merge area.  Neither part waits for the
+// other.  With no more units than SMs
 // each CTA runs one unit, and a launch given no merge area runs every unit
 // whole, round-robin.  Consecutive items of a CTA overlap: the next item's K
 // tile and Q tiles load while the current item's last P V MMAs and epilogue
@@ -379,6 +381,9 @@ __global__ void __launch_bounds__(kAttn2Threads, 1)
         if (!second) {
           store = false;  // the other part, still running, merges and stores
         } else {
+          // both parts have counted: the counter goes back to zero for the
+          // next launch that uses this merge area
+          if (lane == 0) p.cnt[bound * 8 + wid] = 0;
           __threadfence();
           const float m_o = __ldcg(oth + 32 * HD + lane);
           const float l_o = __ldcg(oth + 32 * HD + 32 + lane);
@@ -668,8 +673,10 @@ cudaError_t launch_attn2_hd(const CUtensorMap& tmQK, const CUtensorMap& tmV, con
     // whole rounds, then the last one to two rounds' worth of units balanced
     p.dp_rounds = p.n_units / G - 1;
     p.tail_units = p.n_units - p.dp_rounds * G;
-    cudaError_t e = cudaMemsetAsync(p.cnt, 0, sizeof(int) * 8 * (size_t)G, s);
-    if (e != cudaSuccess) return e;
+    if (!p.cnt_zero) {
+      cudaError_t e = cudaMemsetAsync(p.cnt, 0, sizeof(int) * 8 * (size_t)G, s);
+      if (e != cudaSuccess) return e;
+    }
   } else {
     p.dp_rounds = (p.n_units + G - 1) / G;
     p.tail_units = 0;

@@ -324,7 +324,8 @@ static GemmParams gemm_params(int mode) {
 
 // ----------------------------------------------------------------- attention
 int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint16_t* qk, const uint16_t* vT,
-                           uint16_t* out, long long out_ld, int* merge_cnt, float* merge_part, cudaStream_t st) {
+                           uint16_t* out, long long out_ld, int* merge_cnt, float* merge_part, cudaStream_t st,
+                           bool merge_cnt_zero) {
   CUtensorMap tq, tv;
   const int D = H * d_head;
   const uint64_t D2 = 2ull * D;
@@ -352,6 +353,7 @@ int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint
   p.status = device_status_ptr();
   p.cnt = merge_cnt;
   p.part = merge_part;
+  p.cnt_zero = merge_cnt_zero ? 1 : 0;
   return cuda_status(launch_attention(tq, tv, to, p, d_head, st));
 }
 
@@ -360,16 +362,26 @@ int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint
 struct AttnMerge {
   int* cnt;
   float* part;
+  size_t cnt_bytes;
+  bool zeroed;  // cnt cleared by the caller (then every launch leaves it zero)
 };
 static void take_attn_merge(const Dims& d, Carve& c, AttnMerge& m) {
   const long long units = attn_units(d.B, d.L, d.H);
+  m.cnt_bytes = attn_merge_ctas(units) * 8 * sizeof(int);
   m.cnt = c.take<int>(attn_merge_ctas(units) * 8);
   m.part = c.take<float>(attn_merge_floats(d.d, units));
+  m.zeroed = false;
+}
+// One clear of the merge counters before a loop of blocks that share them.
+static int clear_attn_merge(AttnMerge& m, cudaStream_t st) {
+  const int rc = cuda_status(cudaMemsetAsync(m.cnt, 0, m.cnt_bytes, st));
+  m.zeroed = rc == MMDIT_OK;
+  return rc;
 }
 
 static int run_attention(const Dims& d, const uint16_t* qk, const uint16_t* vT, uint16_t* out, long long out_ld,
                          const AttnMerge& m, cudaStream_t st) {
-  return run_attention_prepared(d.B, d.L, d.H, d.d, d.Lpad, qk, vT, out, out_ld, m.cnt, m.part, st);
+  return run_attention_prepared(d.B, d.L, d.H, d.d, d.Lpad, qk, vT, out, out_ld, m.cnt, m.part, st, m.zeroed);
 }
 
 // ----------------------------------------------------------------- workspace layouts
@@ -763,6 +775,7 @@ static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step
     Carve bc{sw.block, 0};
     DoubleWS dw;
     layout_double(d, i8, false, bc, dw);
+    if (w.n_double > 0) MMDIT_TRY(clear_attn_merge(dw.am, st));
     for (int i = 0; i < w.n_double; ++i) {
       MMDIT_TRY(double_block_impl(shape, d, w.doubles[i], nullptr, mp, sw.x, d.L, sw.x + (size_t)d.Lt * D, d.L,
                                   sw.cs, sw.sn, dw, st));
@@ -773,6 +786,7 @@ static int step_impl(const mmdit_shape_t& shape, const Dims& d, const mmdit_step
     Carve bc{sw.block, 0};
     SingleWS ssw;
     layout_single(d, i8, false, bc, ssw);
+    if (w.n_single > 0) MMDIT_TRY(clear_attn_merge(ssw.am, st));
     for (int i = 0; i < w.n_single; ++i) {
       MMDIT_TRY(single_block_impl(shape, d, w.singles[i], nullptr, mp, sw.x, sw.cs, sw.sn, ssw, st));
       mp += (size_t)d.B * 3 * D;

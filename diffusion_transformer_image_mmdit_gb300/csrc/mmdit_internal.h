@@ -93,6 +93,10 @@ struct AttnParams {
   // boundaries at most.
   int* cnt;
   float* part;
+  // Nonzero: the counters are known to be zero (the caller cleared them, and
+  // every launch leaves them zero: the part that merges a split unit resets
+  // the unit's counter), so the launcher does not clear them.
+  int cnt_zero;
   // Set by the launcher: units (query-tile pairs x heads x samples), whole
   // rounds, and the tail units balanced over the grid.
   int n_pairs, n_units, dp_rounds, tail_units;
@@ -161,6 +165,7 @@ int device_check();
 // (kAttnMaxCtas * 8 ints, attn_merge_floats(d_head) floats), or both null
 // for a schedule of whole units only.  Returns an MMDIT_* status.
 int run_attention_prepared(int B, int L, int H, int d_head, int Lpad, const uint16_t* qk, const uint16_t* vT,
-                           uint16_t* out, long long out_ld, int* merge_cnt, float* merge_part, cudaStream_t st);
+                           uint16_t* out, long long out_ld, int* merge_cnt, float* merge_part, cudaStream_t st,
+                           bool merge_cnt_zero = false);
 
 }  // namespace mmdit

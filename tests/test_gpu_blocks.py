@@ -200,6 +200,34 @@ def test_step_small(i8):
     assert_close(host(xl), ref_x, rel=tol, what="step x_lat")
 
 
+def test_step_split_attention_units():
+    """A step whose attention launches have more units than the GPU has SMs (4 samples x 8 heads x 5
+    query-tile pairs = 160 units), so every launch splits tail units between CTAs and merges them through
+    the shared counter area: the step clears the counters once per block loop and each launch leaves them
+    zero for the next (two double and two single blocks)."""
+    cfg = dict(B=4, L_txt=48, grid_h=24, grid_w=48, D=1024, H=8, d_head=128, D_mlp=2048, rope_axes=(16, 56, 56))
+    sh = oracle_shape(cfg)
+    sh.C_lat, sh.t_dim = 64, 256
+    units = ((cfg["L_txt"] + sh.L_img + 255) // 256) * cfg["H"] * cfg["B"]
+    assert units > torch.cuda.get_device_properties(0).multi_processor_count
+    W = S.embed_params(cfg["D"], sh.C_lat, sh.t_dim, seed=5)
+    W["double"] = [S.double_block_params(f"sp.d{i}", cfg["D"], cfg["d_head"], cfg["D_mlp"]) for i in range(2)]
+    W["single"] = [S.single_block_params(f"sp.s{i}", cfg["D"], cfg["d_head"], cfg["D_mlp"]) for i in range(2)]
+    x_lat = S.normal_f32("sp.lat", (cfg["B"], sh.L_img, sh.C_lat))
+    x_txt = S.normal_f32("sp.txt", (cfg["B"], cfg["L_txt"], cfg["D"]))
+    sig = O.sigma_schedule(50, O.shift_mu(sh.L_img))
+    shape = api_shape(cfg, C_lat=sh.C_lat, t_dim=sh.t_dim)
+    w = Wt.step_from_host(W)
+    ws = api.alloc_workspace(api.step_workspace_size(shape, 2, 2))
+    ref_x, ref_v = O.denoise_step(x_lat, x_txt, sig[0], sig[1], W, sh)
+    for _ in range(2):  # the second call finds the counters the first one left
+        xl = f32(x_lat)
+        v = torch.empty_like(xl)
+        api.mmdit_step_fwd(shape, w, xl, f32(x_txt), sig[0], sig[1], v, ws)
+        assert rel_l2(host(v), ref_v) <= 1e-2, rel_l2(host(v), ref_v)
+        assert_close(host(xl), ref_x, rel=1e-2, what="step x_lat (split attention units)")
+
+
 @pytest.mark.parametrize("i8", [False, True])
 def test_step_i2i_small(i8):
     """A whole image-to-image step (2 double + 2 single blocks, batch 2): the
