@@ -57,6 +57,10 @@ CONFIGS = {
     # the whole sampling loop at 1024^2: 28 steps, guidance 3.5, text encoder width 4096, pooled width 768
     "sample1024": dict(B=1, L_txt=512, grid_h=64, grid_w=64, n_double=19, n_single=38, int8=False, n_steps=28,
                        C_txt=4096, C_pool=768, guidance=3.5, **FLUX),
+    # the layout kernels of Ulysses sequence parallelism over P = 8 ranks at the 1328^2 sequence, every
+    # rank's pack and unpack of one block run one after the other on this GPU
+    "ulysses_layout": dict(B=1, L_txt=512, grid_h=83, grid_w=83, n_double=19, n_single=38, int8=False, n_steps=50,
+                           P=8, **FLUX),
 }
 WORKLOAD_NAME = {
     "c4": "full denoising step, 19 double + 38 single blocks, D=3072, 24x128 heads, MLP 12288, 512 text + 83x83 "
@@ -82,6 +86,10 @@ WORKLOAD_NAME = {
     "sample1024": "sampling loop, 28 Euler steps of the 57-block bf16 model at 512 text + 64x64 image tokens "
                   "(1024^2), batch 1, guidance 3.5, text projection 4096 -> 3072, pooled vector 768; steps 1.. "
                   "replayed from one captured CUDA graph",
+    "ulysses_layout": "Ulysses layout kernels of the 57 blocks of a step at 512 text + 83x83 image tokens (7401), "
+                      "D=3072, over P = 8 sequence shards: per block and shard, q|k|v rows [rows, 3D] packed to "
+                      "[P][rows][3][D/P] before the exchange and the attention output [P][rows][D/P] unpacked to "
+                      "[rows, D] after it, all shards on this GPU in turn (the exchanges themselves need P GPUs)",
 }
 
 
@@ -565,6 +573,83 @@ def run_sample(args, c: dict):
     print(json.dumps(out))
 
 
+def run_ulysses_layout(args, c: dict):
+    """One 'step' is the pack and unpack launches of every shard for every
+    block of a denoising step (HBM-bound: each moves its bytes once in and
+    once out).  At least 100 steps are timed, so that the clock sampler sees
+    the timed region."""
+    import torch
+    from diffusion_transformer_image_mmdit_gb300 import api, build
+    from diffusion_transformer_image_mmdit_gb300.ulysses import ShardPlan
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build.build()
+    api._lib.load()
+    P, D = c["P"], c["D"]
+    plan = ShardPlan(c["L_txt"], c["grid_h"] * c["grid_w"], P)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    qkv = [torch.randn((n, 3 * D), generator=gen, device=dev).to(torch.bfloat16) for n in plan.sizes()]
+    send = [torch.empty((P, n, 3, D // P), dtype=torch.bfloat16, device=dev) for n in plan.sizes()]
+    back = [torch.randn((P, n, D // P), generator=gen, device=dev).to(torch.bfloat16) for n in plan.sizes()]
+    out = [torch.empty((n, D), dtype=torch.bfloat16, device=dev) for n in plan.sizes()]
+    stream = torch.cuda.current_stream()
+
+    n_blocks = c["n_double"] + c["n_single"]
+
+    def launches():
+        st = torch.cuda.current_stream()
+        for _ in range(n_blocks):
+            for r in range(P):
+                api.mmdit_heads_pack(qkv[r], 3, P, D // P, send[r], stream=st)
+                api.mmdit_heads_unpack(back[r], P, D // P, out[r], stream=st)
+
+    # the step's launches replayed from one CUDA graph, so that the host's
+    # per-call cost does not pace these short kernels
+    launches()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launches()
+    torch.cuda.synchronize()
+
+    def step():
+        graph.replay()
+
+    args.steps = max(args.steps, 100)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        time.sleep(0.5)  # the sampler's first reading comes before the timed region ends
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if api.sync_status() != 0:
+        raise RuntimeError("device status after timed region")
+    ms = e0.elapsed_time(e1) / args.steps
+    L = plan.L
+    # pack and unpack of every block: every bf16 element read once and written once
+    moved = n_blocks * (2 * (L * 3 * D * 2) + 2 * (L * D * 2))
+    pk = peaks()
+    gbs = moved / ms / 1e6
+    outj = {"metric": "Ulysses layout kernels, GB/s moved (read + written)", "value": round(gbs, 1), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (N(0,1) bf16 rows); the step's launches replayed from one CUDA graph",
+            "config": {"workload": WORKLOAD_NAME[args.config], "seq_len": L, "P": P,
+                       "l2": f"inputs larger than L2: {moved / n_blocks / 1e6:.0f} MB touched per block"},
+            "roofline": {"kernel": "heads_pack + heads_unpack", "bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 3),
+                         "traffic": None, "peak_source": pk["source"] + " copy bandwidth"},
+            "gpu_launches": 2 * P * n_blocks * args.steps, "clocks": clk.summary()}
+    print(json.dumps(outj))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -584,6 +669,13 @@ def main():
                               "denoising step; a sampling loop is only measured for this implementation"}))
             return
         run_sample(args, c)
+        return
+    if args.config == "ulysses_layout":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the oracle on one "
+                              "denoising step; the layout kernels are only measured for this implementation"}))
+            return
+        run_ulysses_layout(args, c)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

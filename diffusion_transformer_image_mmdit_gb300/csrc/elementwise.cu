@@ -105,32 +105,38 @@ __global__ void __launch_bounds__(128) ln_mod_kernel(const __grid_constant__ LnJ
 // consecutive sections (q | k | v) of `groups` head groups of gc columns
 // each; dst [groups][rows][sections][gc], so that the chunk for head group g
 // is contiguous.  unpack: src [groups][rows][gc] -> dst [rows][dst_ld] at
-// columns g * gc + c.  One thread per 16-byte vector (8 bf16).
-__global__ void heads_pack_kernel(const uint16_t* __restrict__ src, long long rows, int src_ld, int sections,
-                                  int groups, int gc, uint16_t* __restrict__ dst) {
+// columns g * gc + c.  A CTA moves whole rows (grid-stride over rows), its
+// threads striding over the row's 16-byte vectors (8 bf16): the source row
+// is read contiguously, and every run of gc / 8 vectors lands contiguously.
+// Index arithmetic in 32 bits per row (one row holds at most 2^31 vectors).
+__global__ void __launch_bounds__(256) heads_pack_kernel(const uint16_t* __restrict__ src, long long rows, int src_ld,
+                                                         int sections, int groups, int gc,
+                                                         uint16_t* __restrict__ dst) {
   const int v8 = gc / 8;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long per_group = rows * sections * v8;
-  if (idx >= per_group * groups) return;
-  const int g = (int)(idx / per_group);
-  long long rem = idx - g * per_group;
-  const long long r = rem / (sections * v8);
-  rem -= r * (sections * v8);
-  const int sct = (int)(rem / v8), c = (int)(rem - (long long)sct * v8);
-  const uint4 v = *reinterpret_cast<const uint4*>(src + r * src_ld + ((long long)sct * groups + g) * gc + 8 * c);
-  *reinterpret_cast<uint4*>(dst + idx * 8) = v;
+  const int per_row = sections * groups * v8;
+  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + r * src_ld);
+    for (int j = threadIdx.x; j < per_row; j += blockDim.x) {
+      const int sg = j / v8, c = j - sg * v8;  // source column block sg = sct * groups + g
+      const int sct = sg / groups, g = sg - sct * groups;
+      const uint4 v = s4[j];
+      *reinterpret_cast<uint4*>(dst + (((long long)g * rows + r) * sections + sct) * gc + 8 * c) = v;
+    }
+  }
 }
 
-__global__ void heads_unpack_kernel(const uint16_t* __restrict__ src, long long rows, int groups, int gc,
-                                    uint16_t* __restrict__ dst, int dst_ld) {
+__global__ void __launch_bounds__(256) heads_unpack_kernel(const uint16_t* __restrict__ src, long long rows,
+                                                           int groups, int gc, uint16_t* __restrict__ dst,
+                                                           int dst_ld) {
   const int v8 = gc / 8;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= rows * groups * v8) return;
-  const long long r = idx / ((long long)groups * v8);
-  const long long rem = idx - r * groups * v8;
-  const int g = (int)(rem / v8), c = (int)(rem - (long long)g * v8);
-  *reinterpret_cast<uint4*>(dst + r * dst_ld + (long long)g * gc + 8 * c) =
-      *reinterpret_cast<const uint4*>(src + ((long long)g * rows + r) * gc + 8 * c);
+  const int per_row = groups * v8;
+  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst + r * dst_ld);
+    for (int j = threadIdx.x; j < per_row; j += blockDim.x) {
+      const int g = j / v8, c = j - g * v8;
+      d4[j] = *reinterpret_cast<const uint4*>(src + ((long long)g * rows + r) * gc + 8 * c);
+    }
+  }
 }
 
 // ------------------------------------------------------------------ GEMV
@@ -1107,7 +1113,8 @@ cudaError_t launch_heads_pack(const uint16_t* src, long long rows, int src_ld, i
   const long long n = rows * sections * groups * (gc / 8);
   if (n == 0) return cudaSuccess;
   launch_begin(KID_HEADS_PACK, st);
-  heads_pack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, rows, src_ld, sections, groups, gc, dst);
+  const unsigned grid = (unsigned)std::min<long long>(rows, (long long)num_sms() * 8);
+  heads_pack_kernel<<<grid, 256, 0, st>>>(src, rows, src_ld, sections, groups, gc, dst);
   launch_end(st);
   return cudaGetLastError();
 }
@@ -1117,7 +1124,8 @@ cudaError_t launch_heads_unpack(const uint16_t* src, long long rows, int groups,
   const long long n = rows * groups * (gc / 8);
   if (n == 0) return cudaSuccess;
   launch_begin(KID_HEADS_UNPACK, st);
-  heads_unpack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, rows, groups, gc, dst, dst_ld);
+  const unsigned grid = (unsigned)std::min<long long>(rows, (long long)num_sms() * 8);
+  heads_unpack_kernel<<<grid, 256, 0, st>>>(src, rows, groups, gc, dst, dst_ld);
   launch_end(st);
   return cudaGetLastError();
 }
