@@ -1,6 +1,7 @@
 """Host logic of the product path checked against the oracle on CPU: the
 library's sigma schedule (host code behind the C ABI, no GPU needed), and the
 benchmark's FLOP accounting against the per-block formula 24 L D^2 + 4 L^2 D."""
+import json
 import numpy as np
 import pytest
 
@@ -67,6 +68,23 @@ def test_clock_sampler_summary():
     assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1371.0
     cs.rows.append([x.strip() for x in line.format(sm=1200, pw=800, act="8", hw="Active", cap="Not Active").split(",")])
     assert bench.ClockSampler.summary(cs)["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_bench_configs_are_named_and_reference_arm_declines_gpu_only_ones(capsys):
+    """Every bench workload has its name for the JSON line, and the reference arm (the oracle on the host)
+    prints an 'unavailable' line for the workloads it does not time instead of running anything."""
+    import sys
+    import bench
+    assert set(bench.WORKLOAD_NAME) == set(bench.CONFIGS)
+    for name in ("sample1024", "ulysses_layout"):
+        argv = sys.argv
+        sys.argv = ["bench.py", "--impl", "reference", "--config", name]
+        try:
+            bench.main()
+        finally:
+            sys.argv = argv
+        line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["unavailable"]
 
 
 def test_bench_gemm_hash_ignores_comments_only():
